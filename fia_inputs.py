@@ -1,0 +1,260 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/bench and the CPU oracle.
+
+This module only draws random numbers and arranges them into tensors of the
+shapes the FusedInferAttentionScore / PromptFlashAttention / BlockSparseAttention
+pages describe.  It holds none of the attention arithmetic.
+
+Every tensor comes from numpy's PCG64 seeded with (BASE_SEED, workload id,
+tensor id), is drawn in float32 and cast to fp16/bf16 with round-to-nearest-even
+by torch.  All tensors are returned on the CPU; callers move them where needed.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+BASE_SEED = 20261202
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def rng(workload: int, tensor: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([BASE_SEED, workload, tensor])))
+
+
+def normal(shape, dtype: str, workload: int, tensor: int) -> torch.Tensor:
+    x = rng(workload, tensor).standard_normal(size=tuple(shape), dtype=np.float32)
+    return torch.from_numpy(x).to(DTYPES[dtype])
+
+
+def uniform_ints(lo: int, hi: int, n: int, workload: int, tensor: int) -> list[int]:
+    """n integers uniform on [lo, hi] (inclusive)."""
+    return [int(v) for v in rng(workload, tensor).integers(lo, hi + 1, size=n)]
+
+
+def cumsum_no_leading_zero(lengths):
+    out, acc = [], 0
+    for n in lengths:
+        acc += int(n)
+        out.append(acc)
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# Dense prefill (BNSD / BSND / BSH / TND)
+# --------------------------------------------------------------------------------------
+@dataclass
+class PrefillCase:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    num_heads: int
+    num_key_value_heads: int
+    scale: float
+    layout: str
+    sparse_mode: int
+    actual_seq_qlen: list | None = None
+    actual_seq_kvlen: list | None = None
+    atten_mask: torch.Tensor | None = None
+    lse: bool = True
+    meta: dict = field(default_factory=dict)
+
+
+def prefill_case(B, N1, N2, Sq, Skv, D, dtype="bf16", layout="BNSD", sparse_mode=0,
+                 actual_seq_qlen=None, actual_seq_kvlen=None, workload=100, Dv=None,
+                 poison_padding=False) -> PrefillCase:
+    """Dense q/k/v with iid N(0,1) entries in the given layout.
+
+    With poison_padding, key/value rows past each batch's actual kv length are
+    set to NaN: a correct implementation never lets them reach the output."""
+    Dv = D if Dv is None else Dv
+    if layout == "BNSD":
+        qs, ks, vs = (B, N1, Sq, D), (B, N2, Skv, D), (B, N2, Skv, Dv)
+    elif layout == "BSND":
+        qs, ks, vs = (B, Sq, N1, D), (B, Skv, N2, D), (B, Skv, N2, Dv)
+    elif layout == "BSH":
+        qs, ks, vs = (B, Sq, N1 * D), (B, Skv, N2 * D), (B, Skv, N2 * Dv)
+    else:
+        raise ValueError(layout)
+    q = normal(qs, dtype, workload, 1)
+    k = normal(ks, dtype, workload, 2)
+    v = normal(vs, dtype, workload, 3)
+    if poison_padding and actual_seq_kvlen is not None:
+        for b in range(B):
+            L = actual_seq_kvlen[0] if len(actual_seq_kvlen) == 1 else actual_seq_kvlen[b]
+            if layout == "BNSD":
+                k[b, :, L:] = float("nan"); v[b, :, L:] = float("nan")
+            else:
+                k[b, L:] = float("nan"); v[b, L:] = float("nan")
+    return PrefillCase(q, k, v, N1, N2, 1.0 / math.sqrt(D), layout, sparse_mode,
+                       actual_seq_qlen, actual_seq_kvlen)
+
+
+def tnd_case(lengths_q, lengths_kv, N1, N2, D, dtype="bf16", sparse_mode=3, workload=300) -> PrefillCase:
+    Tq, Tkv = sum(lengths_q), sum(lengths_kv)
+    q = normal((Tq, N1, D), dtype, workload, 1)
+    k = normal((Tkv, N2, D), dtype, workload, 2)
+    v = normal((Tkv, N2, D), dtype, workload, 3)
+    return PrefillCase(q, k, v, N1, N2, 1.0 / math.sqrt(D), "TND", sparse_mode,
+                       cumsum_no_leading_zero(lengths_q), cumsum_no_leading_zero(lengths_kv))
+
+
+# The five workloads the pages' operator is exercised on (sizes fixed here).
+def workload_prefill_bnsd_f16_small() -> PrefillCase:
+    """Prefill BNSD fp16: B=1, Q_N=KV_N=2, S=128, D=64, causal, LSE on."""
+    return prefill_case(1, 2, 2, 128, 128, 64, dtype="f16", layout="BNSD", sparse_mode=2, workload=1)
+
+
+def workload_tnd_varlen(n_seq=8, lo=256, hi=4096, N1=32, N2=8, D=128, workload=3) -> PrefillCase:
+    """Varlen TND bf16 prefill: n_seq lengths uniform on [lo, hi], causal, GQA 32/8."""
+    lens = uniform_ints(lo, hi, n_seq, workload, 0)
+    return tnd_case(lens, lens, N1, N2, D, "bf16", sparse_mode=3, workload=workload)
+
+
+# --------------------------------------------------------------------------------------
+# Paged decode
+# --------------------------------------------------------------------------------------
+@dataclass
+class DecodeCase:
+    q: torch.Tensor               # BNSD (B, N1, 1, D)
+    k_pool: torch.Tensor          # (nblk, N2, bs, D)
+    v_pool: torch.Tensor
+    block_table: torch.Tensor     # int32 (B, max_blocks)
+    kv_lens: list
+    block_size: int
+    num_heads: int
+    num_key_value_heads: int
+    scale: float
+    meta: dict = field(default_factory=dict)
+
+
+def paged_decode_case(B, N1, N2, D, kv_lens, block_size=128, dtype="bf16", workload=200,
+                      extra_table_cols=1, poison=True, layout_kv="BNBD") -> DecodeCase:
+    """Paged KV cache: each sequence's logical blocks map to a random permutation of
+    a shared physical pool.  One extra pool block is filled with NaN; unused
+    block_table entries point at it, as do the unused tail rows of each sequence's
+    last block, so any read past a sequence's length poisons the output."""
+    nb = [(L + block_size - 1) // block_size for L in kv_lens]
+    total = sum(nb)
+    nblk = total + 1
+    poison_id = total
+    perm = rng(workload, 10).permutation(total)
+    max_blocks = max(max(nb), 1) + extra_table_cols
+    table = np.full((B, max_blocks), poison_id, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        for i in range(nb[b]):
+            table[b, i] = perm[pos]
+            pos += 1
+    if layout_kv == "BNBD":
+        shape = (nblk, N2, block_size, D)
+    else:  # (blocknum, blocksize, H)
+        shape = (nblk, block_size, N2 * D)
+    k = normal(shape, dtype, workload, 2)
+    v = normal(shape, dtype, workload, 3)
+    if poison:
+        k[poison_id] = float("nan")
+        v[poison_id] = float("nan")
+        for b in range(B):
+            tail = kv_lens[b] % block_size
+            if nb[b] and tail:
+                last = int(table[b, nb[b] - 1])
+                if layout_kv == "BNBD":
+                    k[last, :, tail:] = float("nan"); v[last, :, tail:] = float("nan")
+                else:
+                    k[last, tail:] = float("nan"); v[last, tail:] = float("nan")
+    q = normal((B, N1, 1, D), dtype, workload, 1)
+    return DecodeCase(q, k, v, torch.from_numpy(table), list(kv_lens), block_size, N1, N2,
+                      1.0 / math.sqrt(D), {"poison_block": poison_id, "layout_kv": layout_kv})
+
+
+def workload_paged_gqa_decode(B=16, N1=32, N2=8, D=128, max_len=4096, workload=2) -> DecodeCase:
+    """Decode GQA bf16 with paged KV: lengths uniform on [1, max_len], block 128."""
+    lens = uniform_ints(1, max_len, B, workload, 0)
+    return paged_decode_case(B, N1, N2, D, lens, 128, "bf16", workload)
+
+
+# --------------------------------------------------------------------------------------
+# MLA decode
+# --------------------------------------------------------------------------------------
+@dataclass
+class MLACase:
+    q: torch.Tensor            # BSND (B, 1, N1, 512)
+    q_rope: torch.Tensor       # (B, 1, N1, 64)
+    latent: torch.Tensor       # (nblk, bs, 512)  -- key and value
+    rope: torch.Tensor         # (nblk, bs, 64)
+    block_table: torch.Tensor  # int32 (B, max_blocks)
+    kv_lens: list
+    block_size: int
+    num_heads: int
+    scale: float
+
+
+def mla_decode_case(B, N1, kv_lens, block_size=128, Dl=512, Dr=64, workload=400, extra_blocks=0) -> MLACase:
+    nb = [(L + block_size - 1) // block_size for L in kv_lens]
+    total = sum(nb) + extra_blocks
+    perm = rng(workload, 10).permutation(total)
+    max_blocks = max(nb)
+    table = np.zeros((B, max_blocks), dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        for i in range(max_blocks):
+            if i < nb[b]:
+                table[b, i] = perm[pos]; pos += 1
+            else:
+                table[b, i] = perm[-1]
+    latent = normal((total, block_size, Dl), "bf16", workload, 2)
+    rope = normal((total, block_size, Dr), "bf16", workload, 3)
+    q = normal((B, 1, N1, Dl), "bf16", workload, 1)
+    qr = normal((B, 1, N1, Dr), "bf16", workload, 4)
+    return MLACase(q, qr, latent, rope, torch.from_numpy(table), list(kv_lens), block_size, N1,
+                   1.0 / math.sqrt(Dl + Dr))
+
+
+def workload_mla_decode(B=32, N1=128, L=8192, workload=4) -> MLACase:
+    """MLA decode bf16: 128 heads, 512-d latent + 64-d rope, kv length L, block 128."""
+    return mla_decode_case(B, N1, [L] * B, 128, workload=workload)
+
+
+# --------------------------------------------------------------------------------------
+# Block-sparse prefill
+# --------------------------------------------------------------------------------------
+@dataclass
+class BSACase:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    mask: torch.Tensor         # uint8 (B, N1, ceil(Sq/X), ceil(Skv/Y)), nonzero = keep
+    block_shape: tuple
+    num_heads: int
+    num_key_value_heads: int
+    scale: float
+    layout: str
+    actual_seq_qlen: list | None = None
+    actual_seq_kvlen: list | None = None
+
+
+def bsa_case(B, N1, N2, Sq, Skv, D, X=128, Y=128, keep=0.25, dtype="bf16", workload=500,
+             diagonal=True) -> BSACase:
+    """BNSD q/k/v and a block mask keeping the diagonal block plus each other
+    block with probability `keep` (seeded Bernoulli)."""
+    q = normal((B, N1, Sq, D), dtype, workload, 1)
+    k = normal((B, N2, Skv, D), dtype, workload, 2)
+    v = normal((B, N2, Skv, D), dtype, workload, 3)
+    nq, nk = -(-Sq // X), -(-Skv // Y)
+    u = rng(workload, 5).random(size=(B, N1, nq, nk))
+    m = (u < keep).astype(np.uint8)
+    if diagonal:
+        for i in range(nq):
+            # the KV block holding the same token positions as query block i
+            j = min((i * X) // Y, nk - 1)
+            m[:, :, i, j] = 1
+    return BSACase(q, k, v, torch.from_numpy(m), (X, Y), N1, N2, 1.0 / math.sqrt(D), "BNSD")
+
+
+def workload_bsa(B=2, N1=32, N2=8, S=16384, D=128, workload=5) -> BSACase:
+    """Block-sparse prefill bf16: 128x128 blocks, diagonal + ~25% of the rest."""
+    return bsa_case(B, N1, N2, S, S, D, 128, 128, 0.25, "bf16", workload)
