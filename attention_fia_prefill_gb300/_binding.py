@@ -1,0 +1,292 @@
+"""ctypes binding of libfia (include/fia.h): argument marshalling only.
+
+Every step of the attention runs in the library's CUDA kernels.  The functions
+here turn torch tensors into fia_tensor descriptors, allocate outputs and the
+workspace with torch on the tensors' device, and pass the current CUDA stream.
+There is no fallback: a missing library or a failing call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+INT32_MAX = 2147483647
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libfia.so")
+
+FIA_OK = 0
+STATUS_NAMES = {
+    0: "FIA_OK", 1: "FIA_ERR_NULL", 2: "FIA_ERR_DTYPE", 3: "FIA_ERR_SHAPE", 4: "FIA_ERR_LAYOUT",
+    5: "FIA_ERR_UNSUPPORTED", 6: "FIA_ERR_SEQLEN", 7: "FIA_ERR_BLOCK_TABLE", 8: "FIA_ERR_WORKSPACE",
+    9: "FIA_ERR_CUDA", 10: "FIA_ERR_TIMEOUT", 11: "FIA_ERR_HEADS", 12: "FIA_ERR_SPARSE_MODE",
+    13: "FIA_ERR_ALIGNMENT",
+}
+DTYPE_F16, DTYPE_BF16, DTYPE_F32, DTYPE_I32, DTYPE_I64, DTYPE_U8, DTYPE_BOOL, DTYPE_I8 = range(8)
+
+# Every symbol include/fia.h declares.
+EXPORTS = [
+    "fia_params_init", "fia_prefill_get_workspace_size", "fia_prefill", "fia_decode_get_workspace_size",
+    "fia_decode", "bsa_get_workspace_size", "bsa_forward", "fia_device_status", "fia_status_string",
+    "fia_last_error", "fia_profile_next_call",
+]
+
+
+class FIAError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {detail}")
+
+
+class FiaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 5)]
+
+
+class FiaParams(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int64), ("num_key_value_heads", ctypes.c_int64), ("scale_value", ctypes.c_double),
+        ("input_layout", ctypes.c_char_p), ("sparse_mode", ctypes.c_int64), ("pre_tokens", ctypes.c_int64),
+        ("next_tokens", ctypes.c_int64), ("actual_seq_qlen", ctypes.POINTER(ctypes.c_int64)),
+        ("n_actual_seq_qlen", ctypes.c_int64), ("actual_seq_kvlen", ctypes.POINTER(ctypes.c_int64)),
+        ("n_actual_seq_kvlen", ctypes.c_int64), ("block_size", ctypes.c_int64),
+        ("softmax_lse_flag", ctypes.c_int32), ("inner_precise", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Loads libfia.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"libfia.so not built at {p}; run attention_fia_prefill_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    T = ctypes.POINTER(FiaTensor)
+    P = ctypes.POINTER(FiaParams)
+    st = ctypes.c_int
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    vp = ctypes.c_void_p
+    lib.fia_params_init.argtypes = [P]
+    lib.fia_params_init.restype = None
+    lib.fia_prefill_get_workspace_size.argtypes = [T, T, T, T, P, T, T, sz]
+    lib.fia_prefill_get_workspace_size.restype = st
+    lib.fia_prefill.argtypes = [T, T, T, T, P, T, T, vp, ctypes.c_size_t, vp]
+    lib.fia_prefill.restype = st
+    lib.fia_decode_get_workspace_size.argtypes = [T, T, T, T, T, T, T, P, T, T, sz]
+    lib.fia_decode_get_workspace_size.restype = st
+    lib.fia_decode.argtypes = [T, T, T, T, T, T, T, P, T, T, vp, ctypes.c_size_t, vp]
+    lib.fia_decode.restype = st
+    lib.bsa_get_workspace_size.argtypes = [T, T, T, T, ctypes.POINTER(ctypes.c_int64), P, T, T, sz]
+    lib.bsa_get_workspace_size.restype = st
+    lib.bsa_forward.argtypes = [T, T, T, T, ctypes.POINTER(ctypes.c_int64), P, T, T, vp, ctypes.c_size_t, vp]
+    lib.bsa_forward.restype = st
+    lib.fia_device_status.argtypes = [vp, vp]
+    lib.fia_device_status.restype = st
+    lib.fia_status_string.argtypes = [st]
+    lib.fia_status_string.restype = ctypes.c_char_p
+    lib.fia_last_error.argtypes = []
+    lib.fia_last_error.restype = ctypes.c_char_p
+    lib.fia_profile_next_call.argtypes = [vp, vp]
+    lib.fia_profile_next_call.restype = None
+    if path is None:
+        _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------------ marshalling
+def _dtype_code(t) -> int:
+    import torch
+    m = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.int32: DTYPE_I32,
+         torch.int64: DTYPE_I64, torch.uint8: DTYPE_U8, torch.bool: DTYPE_BOOL, torch.int8: DTYPE_I8}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def tensor_desc(t) -> FiaTensor | None:
+    """fia_tensor for a contiguous torch tensor (None stays None)."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    if t.dim() > 5:
+        raise ValueError("at most 5 dims")
+    d = FiaTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    for i, s in enumerate(t.shape):
+        d.shape[i] = int(s)
+    return d
+
+
+def raw_desc(ptr: int | None, dtype: int, shape) -> FiaTensor:
+    """fia_tensor from a raw pointer (used by host-only validation tests)."""
+    d = FiaTensor()
+    d.data = ptr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    for i, s in enumerate(shape):
+        d.shape[i] = int(s)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+class Params:
+    """Builds an fia_params struct; keeps the host length arrays alive."""
+
+    def __init__(self, *, num_heads, num_key_value_heads=0, scale_value=1.0, input_layout="BSH", sparse_mode=0,
+                 pre_tokens=INT32_MAX, next_tokens=INT32_MAX, actual_seq_qlen=None, actual_seq_kvlen=None,
+                 block_size=0, softmax_lse_flag=False, inner_precise=0):
+        lib = load_library()
+        self.p = FiaParams()
+        lib.fia_params_init(ctypes.byref(self.p))
+        self._layout = input_layout.encode()
+        self.p.num_heads = int(num_heads)
+        self.p.num_key_value_heads = int(num_key_value_heads)
+        self.p.scale_value = float(scale_value)
+        self.p.input_layout = self._layout
+        self.p.sparse_mode = int(sparse_mode)
+        self.p.pre_tokens = int(pre_tokens)
+        self.p.next_tokens = int(next_tokens)
+        self._q = self._kv = None
+        if actual_seq_qlen is not None:
+            self._q = (ctypes.c_int64 * len(actual_seq_qlen))(*[int(x) for x in actual_seq_qlen])
+            self.p.actual_seq_qlen = self._q
+            self.p.n_actual_seq_qlen = len(actual_seq_qlen)
+        if actual_seq_kvlen is not None:
+            self._kv = (ctypes.c_int64 * len(actual_seq_kvlen))(*[int(x) for x in actual_seq_kvlen])
+            self.p.actual_seq_kvlen = self._kv
+            self.p.n_actual_seq_kvlen = len(actual_seq_kvlen)
+        self.p.block_size = int(block_size)
+        self.p.softmax_lse_flag = 1 if softmax_lse_flag else 0
+        self.p.inner_precise = int(inner_precise)
+
+
+def check(status: int):
+    if status != FIA_OK:
+        lib = load_library()
+        raise FIAError(status, lib.fia_last_error().decode(errors="replace"))
+
+
+def _stream_ptr(device):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _lse_shape(q, layout, num_heads):
+    if layout == "TND":
+        return (q.shape[0], num_heads, 1)
+    if layout == "BNSD":
+        return (q.shape[0], num_heads, q.shape[2], 1)
+    return (q.shape[0], num_heads, q.shape[1], 1)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("fia kernels take CUDA tensors")
+
+
+# ------------------------------------------------------------------ public API
+def fia_prefill(query, key, value, *, atten_mask=None, actual_seq_qlen=None, actual_seq_kvlen=None, num_heads=1,
+                num_key_value_heads=0, scale_value=1.0, input_layout="BSH", sparse_mode=0, pre_tokens=INT32_MAX,
+                next_tokens=INT32_MAX, softmax_lse_flag=False, inner_precise=0, out=None, softmax_lse=None,
+                workspace=None):
+    """Full attention (Q_S >= 1).  Returns (attention_out, softmax_lse or None)."""
+    import torch
+    _require_cuda(query, key, value, atten_mask)
+    lib = load_library()
+    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+                 input_layout=input_layout, sparse_mode=sparse_mode, pre_tokens=pre_tokens, next_tokens=next_tokens,
+                 actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen,
+                 softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
+    if out is None:
+        out = torch.empty_like(query)
+    if softmax_lse_flag and softmax_lse is None:
+        softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
+    dq, dk, dv, dm, do, dl = (tensor_desc(t) for t in (query, key, value, atten_mask, out, softmax_lse))
+    ws = ctypes.c_size_t(0)
+    check(lib.fia_prefill_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dm), ctypes.byref(prm.p), _ref(do),
+                                             _ref(dl), ctypes.byref(ws)))
+    if workspace is None or workspace.numel() < ws.value:
+        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
+    check(lib.fia_prefill(_ref(dq), _ref(dk), _ref(dv), _ref(dm), ctypes.byref(prm.p), _ref(do), _ref(dl),
+                          ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
+                          _stream_ptr(query.device)))
+    return out, softmax_lse
+
+
+def fia_decode(query, key, value, *, query_rope=None, key_rope=None, block_table=None, block_size=0,
+               actual_seq_kvlen=None, atten_mask=None, num_heads=1, num_key_value_heads=0, scale_value=1.0,
+               input_layout="BSH", softmax_lse_flag=False, inner_precise=0, out=None, softmax_lse=None,
+               workspace=None):
+    """Incremental attention (Q_S = 1), paged or contiguous, optionally MLA."""
+    import torch
+    _require_cuda(query, key, value, query_rope, key_rope, block_table)
+    lib = load_library()
+    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+                 input_layout=input_layout, actual_seq_kvlen=actual_seq_kvlen, block_size=block_size,
+                 softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
+    if out is None:
+        out = torch.empty_like(query)
+    if softmax_lse_flag and softmax_lse is None:
+        softmax_lse = torch.empty((query.shape[0], num_heads, 1, 1), dtype=torch.float32, device=query.device)
+    descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, block_table, atten_mask, out,
+                                      softmax_lse)]
+    dq, dk, dv, dqr, dkr, dbt, dm, do, dl = descs
+    ws = ctypes.c_size_t(0)
+    check(lib.fia_decode_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dqr), _ref(dkr), _ref(dbt), _ref(dm),
+                                            ctypes.byref(prm.p), _ref(do), _ref(dl), ctypes.byref(ws)))
+    if workspace is None or workspace.numel() < ws.value:
+        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
+    check(lib.fia_decode(_ref(dq), _ref(dk), _ref(dv), _ref(dqr), _ref(dkr), _ref(dbt), _ref(dm), ctypes.byref(prm.p),
+                         _ref(do), _ref(dl), ctypes.c_void_p(workspace.data_ptr()),
+                         ctypes.c_size_t(workspace.numel()), _stream_ptr(query.device)))
+    return out, softmax_lse
+
+
+def bsa_forward(query, key, value, block_sparse_mask, block_shape, *, actual_seq_qlen=None, actual_seq_kvlen=None,
+                num_heads=1, num_key_value_heads=0, scale_value=1.0, input_layout="BNSD", softmax_lse_flag=False,
+                out=None, softmax_lse=None, workspace=None):
+    """Block-sparse attention: each query block attends to the KV blocks its mask row keeps."""
+    import torch
+    _require_cuda(query, key, value, block_sparse_mask)
+    lib = load_library()
+    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+                 input_layout=input_layout, actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen,
+                 softmax_lse_flag=softmax_lse_flag)
+    if out is None:
+        out = torch.empty_like(query)
+    if softmax_lse_flag and softmax_lse is None:
+        softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
+    shape = (ctypes.c_int64 * 2)(int(block_shape[0]), int(block_shape[1]))
+    dq, dk, dv, dmask, do, dl = (tensor_desc(t) for t in (query, key, value, block_sparse_mask, out, softmax_lse))
+    ws = ctypes.c_size_t(0)
+    check(lib.bsa_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do),
+                                     _ref(dl), ctypes.byref(ws)))
+    if workspace is None or workspace.numel() < ws.value:
+        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
+    check(lib.bsa_forward(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do), _ref(dl),
+                          ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
+                          _stream_ptr(query.device)))
+    return out, softmax_lse
+
+
+def profile_next_call(start_event, stop_event):
+    """Record two torch.cuda.Event objects around the main kernel of the next call."""
+    lib = load_library()
+    lib.fia_profile_next_call(ctypes.c_void_p(start_event.cuda_event), ctypes.c_void_p(stop_event.cuda_event))
+
+
+def fia_device_status(workspace) -> int:
+    """Device-side status recorded in a workspace (synchronises the current stream)."""
+    lib = load_library()
+    return lib.fia_device_status(ctypes.c_void_p(workspace.data_ptr()), _stream_ptr(workspace.device))

@@ -1,0 +1,900 @@
+// Host side of the C ABI declared in include/fia.h: argument validation,
+// per-batch length resolution, work planning, TMA descriptor encoding, and the
+// kernel launches.  Nothing here allocates device memory: plans and partial
+// results live in the caller's workspace.
+#include "../../include/fia.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using namespace fia;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Events the caller asked to have recorded around the main kernel of its next
+// call on this thread (fia_profile_next_call).
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+template <typename F>
+cudaError_t profiled(cudaStream_t s, F&& launch) {
+  cudaEvent_t a = g_prof_start, b = g_prof_stop;
+  g_prof_start = g_prof_stop = nullptr;
+  if (a != nullptr) {
+    cudaError_t e = cudaEventRecord(a, s);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess) return e;
+  if (b != nullptr) return cudaEventRecord(b, s);
+  return cudaSuccess;
+}
+
+fia_status fail(fia_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+constexpr int64_t kInt32Max = 2147483647;
+constexpr size_t kHeader = 256;   // workspace bytes [0, 256): device status word + padding
+constexpr int kMaxDecodeCtas = 1024;
+
+bool present(const fia_tensor* t) { return t != nullptr && t->data != nullptr && t->ndim > 0; }
+
+int64_t numel(const fia_tensor* t) {
+  if (t == nullptr || t->ndim <= 0) return 0;
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+bool is_half(int32_t dt) { return dt == FIA_DTYPE_F16 || dt == FIA_DTYPE_BF16; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+enum Layout { L_BSH, L_BSND, L_BNSD, L_TND, L_BAD };
+
+Layout parse_layout(const char* s) {
+  if (s == nullptr) return L_BSH;
+  if (!strcmp(s, "BSH")) return L_BSH;
+  if (!strcmp(s, "BSND")) return L_BSND;
+  if (!strcmp(s, "BNSD")) return L_BNSD;
+  if (!strcmp(s, "TND")) return L_TND;
+  return L_BAD;
+}
+
+// --------------------------------------------------------------- TMA encode
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// rank-d tiled map of 16-bit elements, 128-byte swizzle, box {64, box_rows, 1, ...}
+fia_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                    uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(FIA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t box[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    box[i] = i == 0 ? 64 : (i == 1 ? box_rows : 1);
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, rank, const_cast<void*>(base), gd, gs, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FIA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return FIA_OK;
+}
+
+fia_status cuda_check(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(FIA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return FIA_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+// ------------------------------------------------------ length resolution
+// actual_seq_* rules (npu_fused_infer_attention_score_v2, actual_seq_qlen /
+// actual_seq_kvlen): absent -> the tensor's S; one entry -> every batch; >= B
+// entries -> the first B; other counts are errors; entries in [0, S].
+fia_status resolve_lengths(const int64_t* lst, int64_t n, int64_t B, int64_t S, std::vector<int32_t>& out,
+                           const char* name) {
+  out.assign(size_t(B), int32_t(S));
+  if (lst == nullptr) {
+    if (n != 0) return fail(FIA_ERR_SEQLEN, "%s: NULL list with nonzero count", name);
+    return FIA_OK;
+  }
+  if (n != 1 && n < B) return fail(FIA_ERR_SEQLEN, "%s: %lld entries for B=%lld", name, (long long)n, (long long)B);
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t v = lst[n == 1 ? 0 : b];
+    if (v < 0 || v > S) return fail(FIA_ERR_SEQLEN, "%s[%lld]=%lld outside [0,%lld]", name, (long long)b, (long long)v, (long long)S);
+    out[size_t(b)] = int32_t(v);
+  }
+  return FIA_OK;
+}
+
+// TND: cumulative lengths without a leading 0; B = list length (<= 4096),
+// non-decreasing, non-negative, last entry <= T.
+fia_status resolve_tnd(const int64_t* lst, int64_t n, int64_t T, std::vector<int32_t>& start,
+                       std::vector<int32_t>& len, const char* name) {
+  if (lst == nullptr || n <= 0) return fail(FIA_ERR_SEQLEN, "%s is required for TND", name);
+  if (n > 4096) return fail(FIA_ERR_SEQLEN, "%s has %lld entries (> 4096)", name, (long long)n);
+  start.resize(size_t(n));
+  len.resize(size_t(n));
+  int64_t prev = 0;
+  for (int64_t b = 0; b < n; ++b) {
+    if (lst[b] < prev) return fail(FIA_ERR_SEQLEN, "%s must be non-decreasing and non-negative", name);
+    start[size_t(b)] = int32_t(prev);
+    len[size_t(b)] = int32_t(lst[b] - prev);
+    prev = lst[b];
+  }
+  if (prev > T) return fail(FIA_ERR_SEQLEN, "%s total %lld exceeds T=%lld", name, (long long)prev, (long long)T);
+  return FIA_OK;
+}
+
+// GQA rules (num_key_value_heads): Q_N a multiple of KV_N, Q_N / KV_N <= 64.
+// The MLA case (query_rope/key_rope given) takes Q_N up to 128 over KV_N = 1.
+fia_status resolve_heads(const fia_params* p, int64_t& N1, int64_t& N2, int64_t max_ratio = 64) {
+  N1 = p->num_heads;
+  N2 = p->num_key_value_heads == 0 ? p->num_heads : p->num_key_value_heads;
+  if (N1 <= 0 || N2 <= 0) return fail(FIA_ERR_HEADS, "num_heads=%lld num_key_value_heads=%lld", (long long)N1, (long long)N2);
+  if (N1 % N2 != 0) return fail(FIA_ERR_HEADS, "num_heads %lld not a multiple of num_key_value_heads %lld", (long long)N1, (long long)N2);
+  if (N1 / N2 > max_ratio)
+    return fail(FIA_ERR_HEADS, "num_heads / num_key_value_heads = %lld > %lld", (long long)(N1 / N2), (long long)max_ratio);
+  return FIA_OK;
+}
+
+// ------------------------------------------------------------ prefill plan
+struct Geometry {
+  Layout layout;
+  int64_t B, N1, N2, S1, S2, D, T1, T2;
+  bool bf16;
+  std::vector<BatchInfo> batches;
+};
+
+// Shapes of q/k/v in a dense layout -> (B, N, S, D).  BSH splits H by heads.
+fia_status dense_dims(const fia_tensor* t, Layout L, int64_t N, int64_t& B, int64_t& S, int64_t& D, const char* name) {
+  if (L == L_BNSD || L == L_BSND) {
+    if (t->ndim != 4) return fail(FIA_ERR_SHAPE, "%s must be 4-D for %s", name, L == L_BNSD ? "BNSD" : "BSND");
+    B = t->shape[0];
+    const int64_t n = L == L_BNSD ? t->shape[1] : t->shape[2];
+    S = L == L_BNSD ? t->shape[2] : t->shape[1];
+    D = t->shape[3];
+    if (n != N) return fail(FIA_ERR_HEADS, "%s has %lld heads, expected %lld", name, (long long)n, (long long)N);
+  } else if (L == L_BSH) {
+    if (t->ndim != 3) return fail(FIA_ERR_SHAPE, "%s must be 3-D for BSH", name);
+    B = t->shape[0];
+    S = t->shape[1];
+    if (t->shape[2] % N != 0) return fail(FIA_ERR_SHAPE, "%s H=%lld not divisible by %lld heads", name, (long long)t->shape[2], (long long)N);
+    D = t->shape[2] / N;
+  } else {
+    if (t->ndim != 3) return fail(FIA_ERR_SHAPE, "%s must be 3-D for TND", name);
+    B = -1;
+    S = t->shape[0];
+    if (t->shape[1] != N) return fail(FIA_ERR_HEADS, "%s has %lld heads, expected %lld", name, (long long)t->shape[1], (long long)N);
+    D = t->shape[2];
+  }
+  return FIA_OK;
+}
+
+bool same_shape(const fia_tensor* a, const fia_tensor* b) {
+  if (a->ndim != b->ndim) return false;
+  for (int i = 0; i < a->ndim; ++i)
+    if (a->shape[i] != b->shape[i]) return false;
+  return true;
+}
+
+// Strides (elements) of (b, n, s) for a dense layout with N heads of D.
+void bns_strides(Layout L, int64_t N, int64_t S, int64_t D, int64_t* st) {
+  if (L == L_BNSD) { st[0] = N * S * D; st[1] = S * D; st[2] = D; }
+  else if (L == L_TND) { st[0] = 0; st[1] = D; st[2] = N * D; }
+  else { st[0] = S * N * D; st[1] = D; st[2] = N * D; }
+}
+
+fia_status check_lse(const fia_tensor* lse, const fia_params* p, Layout L, int64_t B, int64_t N1, int64_t S1, int64_t T1) {
+  if (p->softmax_lse_flag == 0) return FIA_OK;
+  if (!present(lse)) return fail(FIA_ERR_NULL, "softmax_lse_flag set but softmax_lse absent");
+  if (lse->dtype != FIA_DTYPE_F32) return fail(FIA_ERR_DTYPE, "softmax_lse must be fp32");
+  if (L == L_TND) {
+    if (!(lse->ndim == 3 && lse->shape[0] == T1 && lse->shape[1] == N1 && lse->shape[2] == 1))
+      return fail(FIA_ERR_SHAPE, "softmax_lse must be (T, N1, 1)");
+  } else if (!(lse->ndim == 4 && lse->shape[0] == B && lse->shape[1] == N1 && lse->shape[2] == S1 && lse->shape[3] == 1)) {
+    return fail(FIA_ERR_SHAPE, "softmax_lse must be (B, N1, S1, 1)");
+  }
+  if (!aligned16(lse->data)) return fail(FIA_ERR_ALIGNMENT, "softmax_lse not 16-byte aligned");
+  return FIA_OK;
+}
+
+// Common validation of q/k/v/out for the dense prefill and block-sparse calls.
+fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_params* p,
+                            const fia_tensor* out, bool bsa, Geometry& g) {
+  if (p == nullptr) return fail(FIA_ERR_NULL, "params is NULL");
+  if (!present(q) || !present(k) || !present(v) || !present(out))
+    return fail(FIA_ERR_NULL, "query/key/value/attention_out required");
+  g.layout = parse_layout(p->input_layout);
+  if (g.layout == L_BAD) return fail(FIA_ERR_LAYOUT, "input_layout '%s' not supported", p->input_layout);
+  if (bsa && g.layout == L_BSH) return fail(FIA_ERR_LAYOUT, "block-sparse attention takes TND, BNSD or BSND");
+  if (!is_half(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype)
+    return fail(FIA_ERR_DTYPE, "query/key/value must share fp16 or bf16");
+  if (out->dtype != q->dtype) return fail(FIA_ERR_DTYPE, "attention_out must have the query's dtype");
+  fia_status st = resolve_heads(p, g.N1, g.N2);
+  if (st != FIA_OK) return st;
+  if (!same_shape(k, v)) return fail(FIA_ERR_SHAPE, "key and value shapes differ");
+  if (!same_shape(q, out)) return fail(FIA_ERR_SHAPE, "attention_out must have the query's shape");
+  int64_t Bq, Bk, Dk;
+  st = dense_dims(q, g.layout, g.N1, Bq, g.S1, g.D, "query");
+  if (st != FIA_OK) return st;
+  st = dense_dims(k, g.layout, g.N2, Bk, g.S2, Dk, "key");
+  if (st != FIA_OK) return st;
+  if (Dk != g.D) return fail(FIA_ERR_SHAPE, "query D=%lld, key D=%lld", (long long)g.D, (long long)Dk);
+  if (g.D != 64 && g.D != 128) return fail(FIA_ERR_UNSUPPORTED, "head dim %lld (kernels take 64 or 128)", (long long)g.D);
+  if (!(p->scale_value > 0.0) || !std::isfinite(p->scale_value))
+    return fail(FIA_ERR_UNSUPPORTED, "scale_value must be finite and > 0");
+  if (p->inner_precise < 0 || p->inner_precise > 4) return fail(FIA_ERR_UNSUPPORTED, "inner_precise %d", p->inner_precise);
+  g.bf16 = q->dtype == FIA_DTYPE_BF16;
+  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data))
+    return fail(FIA_ERR_ALIGNMENT, "query/key/value/attention_out must be 16-byte aligned");
+  if (g.layout == L_TND) {
+    g.T1 = g.S1;
+    g.T2 = g.S2;
+    std::vector<int32_t> qs, ql, ks, kl;
+    st = resolve_tnd(p->actual_seq_qlen, p->n_actual_seq_qlen, g.T1, qs, ql, "actual_seq_qlen");
+    if (st != FIA_OK) return st;
+    st = resolve_tnd(p->actual_seq_kvlen, p->n_actual_seq_kvlen, g.T2, ks, kl, "actual_seq_kvlen");
+    if (st != FIA_OK) return st;
+    if (ql.size() != kl.size()) return fail(FIA_ERR_SEQLEN, "TND lists must have the same number of entries");
+    g.B = int64_t(ql.size());
+    g.batches.resize(ql.size());
+    for (size_t b = 0; b < ql.size(); ++b) g.batches[b] = BatchInfo{qs[b], ql[b], ks[b], kl[b]};
+  } else {
+    if (Bq != Bk) return fail(FIA_ERR_SHAPE, "query B=%lld, key B=%lld", (long long)Bq, (long long)Bk);
+    g.B = Bq;
+    g.T1 = g.T2 = 0;
+    if (bsa && ((p->actual_seq_qlen == nullptr) != (p->actual_seq_kvlen == nullptr)))
+      return fail(FIA_ERR_SEQLEN, "actual_seq_qlen and actual_seq_kvlen must be given together");
+    std::vector<int32_t> ql, kl;
+    st = resolve_lengths(p->actual_seq_qlen, p->n_actual_seq_qlen, g.B, g.S1, ql, "actual_seq_qlen");
+    if (st != FIA_OK) return st;
+    st = resolve_lengths(p->actual_seq_kvlen, p->n_actual_seq_kvlen, g.B, g.S2, kl, "actual_seq_kvlen");
+    if (st != FIA_OK) return st;
+    g.batches.resize(size_t(g.B));
+    for (int64_t b = 0; b < g.B; ++b) g.batches[size_t(b)] = BatchInfo{0, ql[size_t(b)], 0, kl[size_t(b)]};
+  }
+  return FIA_OK;
+}
+
+int causal_tiles(const BatchInfo& bi, int q_tile, int mode) {
+  const int q0 = q_tile * kTileM;
+  const int off = mode == 3 ? bi.kv_len - bi.q_len : 0;
+  const int last_row = std::min(q0 + kTileM - 1, bi.q_len - 1);
+  const int maxkey = std::min(bi.kv_len - 1, last_row + off);
+  return maxkey >= 0 ? maxkey / kTileN + 1 : 0;
+}
+
+void build_items(const Geometry& g, int prefill_mode, int causal_mode, std::vector<WorkItem>& items) {
+  items.clear();
+  for (int64_t b = 0; b < g.B; ++b) {
+    const BatchInfo& bi = g.batches[size_t(b)];
+    const int nqt = (bi.q_len + kTileM - 1) / kTileM;
+    for (int64_t h = 0; h < g.N1; ++h)
+      for (int qt = 0; qt < nqt; ++qt) {
+        const int cost = prefill_mode == kCausal ? causal_tiles(bi, qt, causal_mode) : (bi.kv_len + kTileN - 1) / kTileN;
+        items.push_back(WorkItem{int32_t(b), int32_t(h), qt, cost});
+      }
+  }
+  // Longest first (an LPT order for the hardware block scheduler); ties keep
+  // the heads of one GQA group next to each other for L2 reuse of K/V.
+  std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) { return a.cost > b.cost; });
+}
+
+size_t prefill_ws_bytes(size_t n_batches, size_t n_items) {
+  return kHeader + align_up(n_batches * sizeof(BatchInfo), 256) + align_up(n_items * sizeof(WorkItem), 256);
+}
+
+size_t count_items(const Geometry& g) {
+  size_t n = 0;
+  for (const auto& bi : g.batches) n += size_t((bi.q_len + kTileM - 1) / kTileM) * size_t(g.N1);
+  return n;
+}
+
+fia_status check_ws(void* ws, size_t have, size_t need) {
+  if (ws == nullptr) return fail(FIA_ERR_WORKSPACE, "workspace is NULL");
+  if (have < need) return fail(FIA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", have, need);
+  if (!aligned16(ws)) return fail(FIA_ERR_ALIGNMENT, "workspace not 16-byte aligned");
+  return FIA_OK;
+}
+
+// Encode the (D, S, N, B) maps of a dense tensor (TND: (D, T, N, 1)).
+fia_status dense_map(CUtensorMap* m, const fia_tensor* t, Layout L, int64_t B, int64_t N, int64_t S, int64_t D) {
+  uint64_t dims[4], st[3];
+  const uint64_t e = 2;
+  if (L == L_BNSD) {
+    dims[0] = D; dims[1] = S; dims[2] = N; dims[3] = B;
+    st[0] = D * e; st[1] = S * D * e; st[2] = N * S * D * e;
+  } else if (L == L_TND) {
+    dims[0] = D; dims[1] = S; dims[2] = N; dims[3] = 1;
+    st[0] = N * D * e; st[1] = D * e; st[2] = S * N * D * e;
+  } else {
+    dims[0] = D; dims[1] = S; dims[2] = N; dims[3] = B;
+    st[0] = N * D * e; st[1] = D * e; st[2] = S * N * D * e;
+  }
+  return make_map(m, t->data, 4, dims, st, 128);
+}
+
+// Launch the prefill (dense/causal) or block-sparse kernels for a validated geometry.
+fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_tensor* q, const fia_tensor* k,
+                       const fia_tensor* v, const fia_tensor* out, const fia_tensor* lse_t, const fia_params* prm,
+                       const uint8_t* bsa_mask, int nqb, int nkb, int bx, int by, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  std::vector<WorkItem> items;
+  build_items(g, mode, causal_mode, items);
+  const size_t need = prefill_ws_bytes(g.batches.size(), items.size());
+  fia_status st = check_ws(ws, ws_bytes, need);
+  if (st != FIA_OK) return st;
+  float* lse = (prm->softmax_lse_flag && present(lse_t)) ? static_cast<float*>(lse_t->data) : nullptr;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  st = cuda_check(cudaMemsetAsync(base, 0, kHeader, stream), "status reset");
+  if (st != FIA_OK) return st;
+  if (g.B == 0) return FIA_OK;
+
+  int64_t os[3], ls[3] = {0, 0, 0};
+  bns_strides(g.layout, g.N1, g.S1, g.D, os);
+  if (g.layout == L_TND) { ls[0] = 0; ls[1] = 1; ls[2] = g.N1; }
+  else { ls[0] = g.N1 * g.S1; ls[1] = g.S1; ls[2] = 1; }
+
+  // upload the plan
+  std::vector<uint8_t> plan(need - kHeader, 0);
+  const size_t off_items = align_up(g.batches.size() * sizeof(BatchInfo), 256);
+  memcpy(plan.data(), g.batches.data(), g.batches.size() * sizeof(BatchInfo));
+  if (!items.empty()) memcpy(plan.data() + off_items, items.data(), items.size() * sizeof(WorkItem));
+  st = cuda_check(cudaMemcpyAsync(base + kHeader, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream), "plan upload");
+  if (st != FIA_OK) return st;
+  const BatchInfo* d_batches = reinterpret_cast<const BatchInfo*>(base + kHeader);
+  const WorkItem* d_items = reinterpret_cast<const WorkItem*>(base + kHeader + off_items);
+
+  // rows that no CTA writes: padding rows of the padded layouts
+  if (g.layout != L_TND) {
+    bool padded = false;
+    for (const auto& bi : g.batches) padded |= bi.q_len < g.S1;
+    if (padded) {
+      const int64_t dims[4] = {g.B, g.N1, g.S1, g.D};
+      st = cuda_check(launch_fill_rows(out->data, true, lse, dims, os, ls, d_batches, 0, stream), "fill rows");
+      if (st != FIA_OK) return st;
+    }
+  }
+  if (items.empty()) return FIA_OK;
+  if (g.S2 == 0) {
+    // K/V with S2 = 0: every query row is empty (out = 0, lse = +inf).
+    const int64_t dims[4] = {g.layout == L_TND ? 1 : g.B, g.N1, g.layout == L_TND ? g.T1 : g.S1, g.D};
+    int64_t os2[3] = {os[0], os[1], os[2]}, ls2[3] = {ls[0], ls[1], ls[2]};
+    return cuda_check(launch_fill_rows(out->data, true, lse, dims, os2, ls2, d_batches, 1, stream), "fill rows");
+  }
+
+  PrefillParams pp;
+  memset(&pp, 0, sizeof(pp));
+  const int64_t Bmap = g.layout == L_TND ? 1 : g.B;
+  st = dense_map(&pp.tm_q, q, g.layout, Bmap, g.N1, g.S1, g.D);
+  if (st != FIA_OK) return st;
+  st = dense_map(&pp.tm_k, k, g.layout, Bmap, g.N2, g.S2, g.D);
+  if (st != FIA_OK) return st;
+  st = dense_map(&pp.tm_v, v, g.layout, Bmap, g.N2, g.S2, g.D);
+  if (st != FIA_OK) return st;
+  pp.out = out->data;
+  pp.lse = lse;
+  pp.out_sb = os[0]; pp.out_sn = os[1]; pp.out_ss = os[2];
+  pp.lse_sb = ls[0]; pp.lse_sn = ls[1]; pp.lse_ss = ls[2];
+  pp.batches = d_batches;
+  pp.items = d_items;
+  pp.n_items = int(items.size());
+  pp.num_heads = int(g.N1);
+  pp.num_kv_heads = int(g.N2);
+  pp.group = int(g.N1 / g.N2);
+  pp.is_tnd = g.layout == L_TND;
+  pp.causal_offset_mode = causal_mode;
+  pp.scale_log2 = float(prm->scale_value * 1.4426950408889634);
+  pp.bsa_mask = bsa_mask;
+  pp.bsa_nqb = nqb; pp.bsa_nkb = nkb; pp.bsa_x = bx; pp.bsa_y = by;
+  pp.status = reinterpret_cast<uint32_t*>(base);
+  return cuda_check(profiled(stream, [&] { return launch_prefill(pp, int(g.D), g.bf16, mode, stream); }),
+                    "prefill launch");
+}
+
+// Mask semantics accepted by the prefill kernels.
+fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, int& mode, int& causal_mode) {
+  const int64_t sm = p->sparse_mode;
+  if (sm < 0 || sm > 8) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode %lld not in 0..4", (long long)sm);
+  if (sm >= 5) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode %lld (prefix/global/dilated/block_local) is not supported", (long long)sm);
+  if (sm == 0) {
+    if (present(mask)) return fail(FIA_ERR_UNSUPPORTED, "explicit atten_mask (sparse_mode 0) is not implemented");
+    mode = kDense;
+    causal_mode = 0;
+    return FIA_OK;
+  }
+  if (sm == 1) {
+    if (!present(mask)) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode 1 needs atten_mask");
+    return fail(FIA_ERR_UNSUPPORTED, "sparse_mode 1 (allMask) is not implemented");
+  }
+  if (sm == 4) return fail(FIA_ERR_UNSUPPORTED, "sparse_mode 4 (band) is not implemented");
+  if (present(mask)) {
+    // The 2048 x 2048 lower-triangular mask the pages ask for in modes 2/3 is
+    // only a compressed form of the pattern; the kernels derive it from indices.
+    const int64_t n = mask->ndim;
+    const bool ok = (n >= 2 && n <= 4 && mask->shape[n - 1] == 2048 && mask->shape[n - 2] == 2048 &&
+                     (n < 3 || mask->shape[0] == 1) && (n < 4 || mask->shape[1] == 1));
+    if (!ok) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode %lld mask must be (2048,2048)", (long long)sm);
+  }
+  mode = kCausal;
+  causal_mode = int(sm);
+  return FIA_OK;
+}
+
+}  // namespace
+
+// ======================================================================= ABI
+extern "C" {
+
+void fia_params_init(fia_params* p) {
+  if (p == nullptr) return;
+  memset(p, 0, sizeof(*p));
+  p->num_heads = 1;
+  p->num_key_value_heads = 0;
+  p->scale_value = 1.0;
+  p->input_layout = "BSH";
+  p->sparse_mode = 0;
+  p->pre_tokens = kInt32Max;
+  p->next_tokens = kInt32Max;
+}
+
+const char* fia_status_string(fia_status s) {
+  switch (s) {
+    case FIA_OK: return "FIA_OK";
+    case FIA_ERR_NULL: return "FIA_ERR_NULL: required pointer missing";
+    case FIA_ERR_DTYPE: return "FIA_ERR_DTYPE: unsupported or mismatched element type";
+    case FIA_ERR_SHAPE: return "FIA_ERR_SHAPE: inconsistent shapes";
+    case FIA_ERR_LAYOUT: return "FIA_ERR_LAYOUT: unknown input_layout";
+    case FIA_ERR_UNSUPPORTED: return "FIA_ERR_UNSUPPORTED: not implemented by this library";
+    case FIA_ERR_SEQLEN: return "FIA_ERR_SEQLEN: invalid actual_seq list";
+    case FIA_ERR_BLOCK_TABLE: return "FIA_ERR_BLOCK_TABLE: invalid block_table / block_size";
+    case FIA_ERR_WORKSPACE: return "FIA_ERR_WORKSPACE: workspace missing or too small";
+    case FIA_ERR_CUDA: return "FIA_ERR_CUDA: CUDA call failed";
+    case FIA_ERR_TIMEOUT: return "FIA_ERR_TIMEOUT: a bounded device wait ran out";
+    case FIA_ERR_HEADS: return "FIA_ERR_HEADS: invalid num_heads / num_key_value_heads";
+    case FIA_ERR_SPARSE_MODE: return "FIA_ERR_SPARSE_MODE: invalid sparse_mode or mask";
+    case FIA_ERR_ALIGNMENT: return "FIA_ERR_ALIGNMENT: pointer not 16-byte aligned";
+  }
+  return "unknown fia_status";
+}
+
+const char* fia_last_error(void) { return g_last_error.c_str(); }
+
+void fia_profile_next_call(void* start_event, void* stop_event) {
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+}
+
+fia_status fia_device_status(const void* workspace, void* stream) {
+  if (workspace == nullptr) return fail(FIA_ERR_NULL, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fia_status st = cuda_check(cudaStreamSynchronize(s), "stream sync");
+  if (st != FIA_OK) return st;
+  uint32_t word = 0;
+  st = cuda_check(cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost), "status read");
+  if (st != FIA_OK) return st;
+  return static_cast<fia_status>(word);
+}
+
+// ---------------------------------------------------------------- prefill
+fia_status fia_prefill_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                          const fia_tensor* atten_mask, const fia_params* params,
+                                          const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                                          size_t* workspace_bytes) {
+  if (workspace_bytes == nullptr) return fail(FIA_ERR_NULL, "workspace_bytes is NULL");
+  *workspace_bytes = kHeader;
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;   // empty query
+  Geometry g;
+  fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g);
+  if (st != FIA_OK) return st;
+  int mode, cm;
+  st = prefill_mask_mode(params, atten_mask, mode, cm);
+  if (st != FIA_OK) return st;
+  st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
+  if (st != FIA_OK) return st;
+  *workspace_bytes = prefill_ws_bytes(g.batches.size(), count_items(g));
+  return FIA_OK;
+}
+
+fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                       const fia_tensor* atten_mask, const fia_params* params, const fia_tensor* attention_out,
+                       const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  Geometry g;
+  fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g);
+  if (st != FIA_OK) return st;
+  int mode, cm;
+  st = prefill_mask_mode(params, atten_mask, mode, cm);
+  if (st != FIA_OK) return st;
+  st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
+  if (st != FIA_OK) return st;
+  return run_prefill(g, mode, cm, query, key, value, attention_out, softmax_lse, params, nullptr, 0, 0, 0, 0, workspace,
+                     workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------ block-sparse
+static fia_status bsa_validate(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                               const fia_tensor* mask, const int64_t* block_shape, const fia_params* params,
+                               const fia_tensor* out, const fia_tensor* lse, Geometry& g, int& nqb, int& nkb) {
+  fia_status st = prefill_geometry(query, key, value, params, out, true, g);
+  if (st != FIA_OK) return st;
+  if (block_shape == nullptr) return fail(FIA_ERR_NULL, "block_shape is required");
+  const int64_t X = block_shape[0], Y = block_shape[1];
+  if (X <= 0 || Y <= 0 || Y % 128 != 0) return fail(FIA_ERR_SHAPE, "block_shape [%lld,%lld]: X > 0 and Y a multiple of 128", (long long)X, (long long)Y);
+  if (X % 128 != 0) return fail(FIA_ERR_UNSUPPORTED, "block_shape X=%lld: this library needs a multiple of 128", (long long)X);
+  if (!present(mask)) return fail(FIA_ERR_NULL, "block_sparse_mask is required");
+  if (mask->dtype != FIA_DTYPE_U8 && mask->dtype != FIA_DTYPE_BOOL) return fail(FIA_ERR_DTYPE, "block_sparse_mask must be uint8/bool");
+  int64_t maxq = 0, maxk = 0;
+  for (const auto& bi : g.batches) { maxq = std::max<int64_t>(maxq, bi.q_len); maxk = std::max<int64_t>(maxk, bi.kv_len); }
+  if (g.layout != L_TND && params->actual_seq_qlen == nullptr) { maxq = g.S1; maxk = g.S2; }
+  nqb = int((maxq + X - 1) / X);
+  nkb = int((maxk + Y - 1) / Y);
+  if (!(mask->ndim == 4 && mask->shape[0] == g.B && mask->shape[1] == g.N1 && mask->shape[2] == nqb && mask->shape[3] == nkb))
+    return fail(FIA_ERR_SHAPE, "block_sparse_mask must be (B, N1, %d, %d)", nqb, nkb);
+  if (params->sparse_mode != 0) return fail(FIA_ERR_SPARSE_MODE, "block-sparse attention takes no sparse_mode");
+  return check_lse(lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
+}
+
+fia_status bsa_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                  const fia_tensor* block_sparse_mask, const int64_t* block_shape,
+                                  const fia_params* params, const fia_tensor* attention_out,
+                                  const fia_tensor* softmax_lse, size_t* workspace_bytes) {
+  if (workspace_bytes == nullptr) return fail(FIA_ERR_NULL, "workspace_bytes is NULL");
+  *workspace_bytes = kHeader;
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  Geometry g;
+  int nqb, nkb;
+  fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse, g, nqb, nkb);
+  if (st != FIA_OK) return st;
+  *workspace_bytes = prefill_ws_bytes(g.batches.size(), count_items(g));
+  return FIA_OK;
+}
+
+fia_status bsa_forward(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                       const fia_tensor* block_sparse_mask, const int64_t* block_shape, const fia_params* params,
+                       const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  Geometry g;
+  int nqb, nkb;
+  fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse, g, nqb, nkb);
+  if (st != FIA_OK) return st;
+  return run_prefill(g, kBlockSparse, 0, query, key, value, attention_out, softmax_lse, params,
+                     static_cast<const uint8_t*>(block_sparse_mask->data), nqb, nkb, int(block_shape[0]),
+                     int(block_shape[1]), workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+// ================================================================== decode
+namespace {
+
+struct DecodeGeometry {
+  Layout layout;
+  int64_t B, N1, N2, D, Dv;
+  bool bf16, paged, mla, kv_bnbd;
+  int64_t bs, nblk, S2;
+  std::vector<int32_t> kv_len;
+  int64_t q_sb, q_sn, o_sb, o_sn;
+};
+
+fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_tensor* qr,
+                           const fia_tensor* kr, const fia_tensor* table, const fia_tensor* mask, const fia_params* p,
+                           const fia_tensor* out, DecodeGeometry& g) {
+  if (p == nullptr) return fail(FIA_ERR_NULL, "params is NULL");
+  if (!present(q) || !present(k) || !present(v) || !present(out))
+    return fail(FIA_ERR_NULL, "query/key/value/attention_out required");
+  g.layout = parse_layout(p->input_layout);
+  if (g.layout == L_BAD) return fail(FIA_ERR_LAYOUT, "input_layout '%s' not supported", p->input_layout);
+  if (g.layout == L_TND) return fail(FIA_ERR_UNSUPPORTED, "TND decode is not implemented");
+  if (!is_half(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype || out->dtype != q->dtype)
+    return fail(FIA_ERR_DTYPE, "query/key/value/attention_out must share fp16 or bf16");
+  if (present(qr) != present(kr)) return fail(FIA_ERR_SHAPE, "query_rope and key_rope must be given together");
+  g.mla = present(qr);
+  fia_status st = resolve_heads(p, g.N1, g.N2, g.mla ? 128 : 64);
+  if (st != FIA_OK) return st;
+  if (present(mask)) return fail(FIA_ERR_UNSUPPORTED, "atten_mask in decode is not implemented");
+  if (!same_shape(q, out)) return fail(FIA_ERR_SHAPE, "attention_out must have the query's shape");
+  int64_t Bq, Sq, D;
+  st = dense_dims(q, g.layout, g.N1, Bq, Sq, D, "query");
+  if (st != FIA_OK) return st;
+  if (Sq != 1) return fail(FIA_ERR_UNSUPPORTED, "fia_decode takes Q_S = 1 (got %lld)", (long long)Sq);
+  g.B = Bq;
+  g.D = D;
+  g.bf16 = q->dtype == FIA_DTYPE_BF16;
+  if (!(p->scale_value > 0.0) || !std::isfinite(p->scale_value))
+    return fail(FIA_ERR_UNSUPPORTED, "scale_value must be finite and > 0");
+  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data))
+    return fail(FIA_ERR_ALIGNMENT, "query/key/value/attention_out must be 16-byte aligned");
+  int64_t qs[3];
+  bns_strides(g.layout, g.N1, 1, D, qs);
+  g.q_sb = qs[0]; g.q_sn = qs[1];
+  g.o_sb = qs[0]; g.o_sn = qs[1];
+  g.paged = present(table);
+  if (g.paged) {
+    if (table->dtype != FIA_DTYPE_I32 || table->ndim != 2 || table->shape[0] != g.B)
+      return fail(FIA_ERR_BLOCK_TABLE, "block_table must be int32 (B, maxBlocksPerSeq)");
+    if (!aligned16(table->data)) return fail(FIA_ERR_ALIGNMENT, "block_table not 16-byte aligned");
+    if (p->actual_seq_kvlen == nullptr) return fail(FIA_ERR_SEQLEN, "page attention needs actual_seq_kvlen");
+    g.bs = p->block_size;
+    if (g.bs <= 0 || g.bs % 16 != 0 || !(128 % g.bs == 0 || g.bs % 128 == 0))
+      return fail(FIA_ERR_BLOCK_TABLE, "block_size %lld: multiple of 16 dividing 128, or multiple of 128", (long long)g.bs);
+    if (!same_shape(k, v)) return fail(FIA_ERR_SHAPE, "key and value shapes differ");
+    if (k->ndim == 4) {
+      g.kv_bnbd = true;
+      if (k->shape[1] != g.N2 || k->shape[2] != g.bs || k->shape[3] != D)
+        return fail(FIA_ERR_SHAPE, "paged key must be (blocknum, KV_N, block_size, D)");
+    } else if (k->ndim == 3) {
+      g.kv_bnbd = false;
+      if (k->shape[1] != g.bs || k->shape[2] != g.N2 * D)
+        return fail(FIA_ERR_SHAPE, "paged key must be (blocknum, block_size, KV_N*D)");
+      if (g.layout == L_BNSD && false) return FIA_OK;
+    } else {
+      return fail(FIA_ERR_SHAPE, "paged key must be 3-D or 4-D");
+    }
+    g.nblk = k->shape[0];
+    g.S2 = table->shape[1] * g.bs;
+    st = resolve_lengths(p->actual_seq_kvlen, p->n_actual_seq_kvlen, g.B, g.S2, g.kv_len, "actual_seq_kvlen");
+    if (st != FIA_OK) return st;
+    int64_t need_blocks = 0, max_blocks = 0;
+    for (auto L : g.kv_len) {
+      need_blocks += (L + g.bs - 1) / g.bs;
+      max_blocks = std::max<int64_t>(max_blocks, (L + g.bs - 1) / g.bs);
+    }
+    if (table->shape[1] < max_blocks) return fail(FIA_ERR_BLOCK_TABLE, "block_table has fewer columns than maxBlocksPerSeq");
+    if (g.nblk < need_blocks && !g.mla) return fail(FIA_ERR_BLOCK_TABLE, "blocknum %lld below the %lld blocks the lengths need", (long long)g.nblk, (long long)need_blocks);
+  } else {
+    if (!same_shape(k, v)) return fail(FIA_ERR_SHAPE, "key and value shapes differ");
+    int64_t Bk, Dk;
+    st = dense_dims(k, g.layout, g.N2, Bk, g.S2, Dk, "key");
+    if (st != FIA_OK) return st;
+    if (Bk != g.B || Dk != D) return fail(FIA_ERR_SHAPE, "key must be (B, ..., D) like the query");
+    st = resolve_lengths(p->actual_seq_kvlen, p->n_actual_seq_kvlen, g.B, g.S2, g.kv_len, "actual_seq_kvlen");
+    if (st != FIA_OK) return st;
+    g.bs = 0;
+  }
+  if (g.mla) return fail(FIA_ERR_UNSUPPORTED, "MLA decode is not implemented yet");
+  if (D != 64 && D != 128) return fail(FIA_ERR_UNSUPPORTED, "decode head dim %lld (kernels take 64 or 128)", (long long)D);
+  g.Dv = D;
+  return FIA_OK;
+}
+
+int heads_per_unit(int64_t group) {
+  if (group >= 8) return 8;
+  if (group >= 4) return group == 4 ? 4 : 8;
+  if (group == 3) return 4;
+  return int(group);
+}
+
+struct DecodePlan {
+  std::vector<DecodeSeg> segs;
+  std::vector<int32_t> cta_seg;
+  std::vector<int2> unit_parts;
+  int n_cta = 0, n_units = 0, G = 1, HB = 1;
+};
+
+void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl) {
+  pl.G = heads_per_unit(g.N1 / g.N2);
+  pl.HB = int((g.N1 / g.N2 + pl.G - 1) / pl.G);
+  pl.n_units = int(g.B * g.N2 * pl.HB);
+  std::vector<int32_t> nst(size_t(pl.n_units));
+  int64_t T = 0;
+  for (int u = 0; u < pl.n_units; ++u) {
+    const int b = u / int(g.N2 * pl.HB);
+    nst[size_t(u)] = (g.kv_len[size_t(b)] + 127) / 128;
+    T += nst[size_t(u)];
+  }
+  pl.n_cta = int(std::min<int64_t>(std::min<int64_t>(n_sm, kMaxDecodeCtas), T));
+  pl.segs.clear();
+  pl.cta_seg.assign(size_t(pl.n_cta) + 1, 0);
+  pl.unit_parts.assign(size_t(pl.n_units), int2{0, 0});
+  // unit u occupies global stages [ustart[u], ustart[u] + nst[u])
+  std::vector<int64_t> ustart(size_t(pl.n_units) + 1, 0);
+  for (int u = 0; u < pl.n_units; ++u) ustart[size_t(u) + 1] = ustart[size_t(u)] + nst[size_t(u)];
+  int u = 0;
+  for (int c = 0; c < pl.n_cta; ++c) {
+    pl.cta_seg[size_t(c)] = int32_t(pl.segs.size());
+    int64_t lo = T * c / pl.n_cta, hi = T * (c + 1) / pl.n_cta;
+    while (lo < hi) {
+      while (ustart[size_t(u) + 1] <= lo) ++u;
+      const int64_t e = std::min<int64_t>(hi, ustart[size_t(u) + 1]);
+      DecodeSeg s{u, int32_t(lo - ustart[size_t(u)]), int32_t(e - ustart[size_t(u)]), int32_t(pl.segs.size())};
+      if (pl.unit_parts[size_t(u)].y == 0) pl.unit_parts[size_t(u)].x = s.part;
+      pl.unit_parts[size_t(u)].y += 1;
+      pl.segs.push_back(s);
+      lo = e;
+    }
+  }
+  pl.cta_seg[size_t(pl.n_cta)] = int32_t(pl.segs.size());
+}
+
+struct DecodeWsLayout {
+  size_t off_segs, off_cta, off_units, off_len, off_po, off_pl, total;
+};
+
+DecodeWsLayout decode_ws_layout(size_t n_segs, size_t n_cta, size_t n_units, size_t B, size_t G, size_t D) {
+  DecodeWsLayout w;
+  size_t o = kHeader;
+  w.off_segs = o; o += align_up(n_segs * sizeof(DecodeSeg), 256);
+  w.off_cta = o; o += align_up((n_cta + 1) * sizeof(int32_t), 256);
+  w.off_units = o; o += align_up(n_units * sizeof(int2), 256);
+  w.off_len = o; o += align_up(B * sizeof(int32_t), 256);
+  w.off_po = o; o += align_up(n_segs * G * D * sizeof(float), 256);
+  w.off_pl = o; o += align_up(n_segs * G * sizeof(float), 256);
+  w.total = o;
+  return w;
+}
+
+size_t decode_ws_bound(const DecodeGeometry& g) {
+  const int G = heads_per_unit(g.N1 / g.N2);
+  const int HB = int((g.N1 / g.N2 + G - 1) / G);
+  const size_t n_units = size_t(g.B * g.N2 * HB);
+  const size_t n_segs = n_units + kMaxDecodeCtas;
+  return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), size_t(G), size_t(g.D)).total;
+}
+
+fia_status check_decode_lse(const fia_tensor* lse, const fia_params* p, int64_t B, int64_t N1) {
+  if (p->softmax_lse_flag == 0) return FIA_OK;
+  if (!present(lse)) return fail(FIA_ERR_NULL, "softmax_lse_flag set but softmax_lse absent");
+  if (lse->dtype != FIA_DTYPE_F32) return fail(FIA_ERR_DTYPE, "softmax_lse must be fp32");
+  if (!(lse->ndim == 4 && lse->shape[0] == B && lse->shape[1] == N1 && lse->shape[2] == 1 && lse->shape[3] == 1))
+    return fail(FIA_ERR_SHAPE, "softmax_lse must be (B, N1, 1, 1)");
+  return FIA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fia_status fia_decode_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                         const fia_tensor* query_rope, const fia_tensor* key_rope,
+                                         const fia_tensor* block_table, const fia_tensor* atten_mask,
+                                         const fia_params* params, const fia_tensor* attention_out,
+                                         const fia_tensor* softmax_lse, size_t* workspace_bytes) {
+  if (workspace_bytes == nullptr) return fail(FIA_ERR_NULL, "workspace_bytes is NULL");
+  *workspace_bytes = kHeader;
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  DecodeGeometry g;
+  fia_status st = decode_geometry(query, key, value, query_rope, key_rope, block_table, atten_mask, params, attention_out, g);
+  if (st != FIA_OK) return st;
+  st = check_decode_lse(softmax_lse, params, g.B, g.N1);
+  if (st != FIA_OK) return st;
+  *workspace_bytes = decode_ws_bound(g);
+  return FIA_OK;
+}
+
+fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                      const fia_tensor* query_rope, const fia_tensor* key_rope, const fia_tensor* block_table,
+                      const fia_tensor* atten_mask, const fia_params* params, const fia_tensor* attention_out,
+                      const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  DecodeGeometry g;
+  fia_status st = decode_geometry(query, key, value, query_rope, key_rope, block_table, atten_mask, params, attention_out, g);
+  if (st != FIA_OK) return st;
+  st = check_decode_lse(softmax_lse, params, g.B, g.N1);
+  if (st != FIA_OK) return st;
+  cudaStream_t stream_t = static_cast<cudaStream_t>(stream);
+  DecodePlan pl;
+  plan_decode(g, sm_count(), pl);
+  const DecodeWsLayout w = decode_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B),
+                                            size_t(pl.G), size_t(g.D));
+  st = check_ws(workspace, workspace_bytes, w.total);
+  if (st != FIA_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  st = cuda_check(cudaMemsetAsync(base, 0, kHeader, stream_t), "status reset");
+  if (st != FIA_OK) return st;
+  std::vector<uint8_t> plan(w.off_po - kHeader, 0);
+  memcpy(plan.data() + (w.off_segs - kHeader), pl.segs.data(), pl.segs.size() * sizeof(DecodeSeg));
+  memcpy(plan.data() + (w.off_cta - kHeader), pl.cta_seg.data(), pl.cta_seg.size() * sizeof(int32_t));
+  memcpy(plan.data() + (w.off_units - kHeader), pl.unit_parts.data(), pl.unit_parts.size() * sizeof(int2));
+  memcpy(plan.data() + (w.off_len - kHeader), g.kv_len.data(), g.kv_len.size() * sizeof(int32_t));
+  st = cuda_check(cudaMemcpyAsync(base + kHeader, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream_t), "plan upload");
+  if (st != FIA_OK) return st;
+
+  DecodeParams dp;
+  memset(&dp, 0, sizeof(dp));
+  if (pl.n_cta > 0) {
+    uint64_t dims[2], strides[1];
+    if (g.paged) {
+      if (g.kv_bnbd) {
+        dims[0] = uint64_t(g.D); dims[1] = uint64_t(g.nblk * g.N2 * g.bs);
+        dp.row_per_blk = g.N2 * g.bs; dp.row_per_head = g.bs; dp.col_per_head = 0;
+      } else {
+        dims[0] = uint64_t(g.N2 * g.D); dims[1] = uint64_t(g.nblk * g.bs);
+        dp.row_per_blk = g.bs; dp.row_per_head = 0; dp.col_per_head = int32_t(g.D);
+      }
+      dp.block_size = int(g.bs);
+      dp.box_rows = int(std::min<int64_t>(g.bs, 128));
+      dp.block_table = static_cast<const int32_t*>(block_table->data);
+      dp.table_stride = block_table->shape[1];
+    } else {
+      if (g.layout == L_BNSD) {
+        dims[0] = uint64_t(g.D); dims[1] = uint64_t(g.B * g.N2 * g.S2);
+        dp.row_per_blk = g.N2 * g.S2; dp.row_per_head = g.S2; dp.col_per_head = 0;
+      } else {
+        dims[0] = uint64_t(g.N2 * g.D); dims[1] = uint64_t(g.B * g.S2);
+        dp.row_per_blk = g.S2; dp.row_per_head = 0; dp.col_per_head = int32_t(g.D);
+      }
+      dp.block_size = 1 << 30;
+      dp.box_rows = 128;
+      dp.block_table = nullptr;
+    }
+    strides[0] = dims[0] * 2;
+    st = make_map(&dp.tm_k, key->data, 2, dims, strides, uint32_t(dp.box_rows));
+    if (st != FIA_OK) return st;
+    st = make_map(&dp.tm_v, value->data, 2, dims, strides, uint32_t(dp.box_rows));
+    if (st != FIA_OK) return st;
+  }
+  dp.q = query->data;
+  dp.q_sb = g.q_sb; dp.q_sn = g.q_sn;
+  dp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
+  dp.out = attention_out->data;
+  dp.out_sb = g.o_sb; dp.out_sn = g.o_sn;
+  dp.lse = (params->softmax_lse_flag && present(softmax_lse)) ? static_cast<float*>(softmax_lse->data) : nullptr;
+  dp.lse_sb = g.N1; dp.lse_sn = 1;
+  dp.part_o = reinterpret_cast<float*>(base + w.off_po);
+  dp.part_lse = reinterpret_cast<float*>(base + w.off_pl);
+  dp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
+  dp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
+  dp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
+  dp.n_cta = pl.n_cta;
+  dp.n_units = pl.n_units;
+  dp.batch = int(g.B);
+  dp.num_heads = int(g.N1);
+  dp.num_kv_heads = int(g.N2);
+  dp.group = int(g.N1 / g.N2);
+  dp.heads_per_unit = pl.G;
+  dp.head_blocks = pl.HB;
+  dp.scale_log2 = float(params->scale_value * 1.4426950408889634);
+  dp.status = reinterpret_cast<uint32_t*>(base);
+  st = cuda_check(profiled(stream_t, [&] { return launch_decode(dp, int(g.D), g.bf16, 0, stream_t); }),
+                  "decode launch");
+  if (st != FIA_OK) return st;
+  return cuda_check(launch_decode(dp, int(g.D), g.bf16, 1, stream_t), "decode combine launch");
+}
+
+}  // extern "C"

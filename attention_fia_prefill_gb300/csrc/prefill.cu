@@ -1,0 +1,446 @@
+// Prefill attention on sm_103a: out = softmax(scale * Q K^T + mask) V, plus LSE.
+//
+// Operation: torch_npu.npu_prompt_flash_attention ("功能说明", formula) and
+// npu_fused_infer_attention_score_v2 (Q_S > 1 path, softmax_lse output); the
+// block-sparse variant is aclnnBlockSparseAttentionV2 ("计算公式"), where each
+// 128-row query tile only visits the KV tiles that blockSparseMask selects.
+//
+// One CTA owns 128 query rows of one (batch, query head).  Roles:
+//   warp 0      TMA producer: Q once, then K/V tiles through a ring of stages
+//   warp 1      MMA issuer (one thread) and TMEM owner:
+//                 S_j = Q K_j^T   (tcgen05, SS, fp32 accumulator in TMEM)
+//                 O  += P_j V_j   (tcgen05, P read from TMEM or shared memory)
+//   warps 2..5  softmax: one thread per query row (= TMEM lane); reads S_j from
+//               TMEM, masks, keeps the running max/sum in registers, writes P_j
+//               (bf16/f16), rescales O in TMEM when the max grows by more than
+//               2^8, and runs the epilogue (O / l, LSE).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256 + D).
+// Shared memory tiles are 128 rows x 128 bytes boxes with the 128-byte swizzle
+// that both TMA and the tcgen05 shared-memory descriptors understand.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fia {
+
+template <int D, bool P_TMEM>
+struct PrefillCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kBoxBytes = 128 * 128;
+  static constexpr int kTileBytes = kChunks * kBoxBytes;
+  static constexpr int kStages = (D == 128 && !P_TMEM) ? 2 : 3;
+  static constexpr int kPBytes = P_TMEM ? 0 : 2 * kBoxBytes;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffP = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemUsed = kOffBar + kBarBytes + 1024;
+  // at least ~120 KB so that a second CTA never shares the SM (and its TMEM)
+  static constexpr int kSmem = kSmemUsed < 122880 ? 122880 : kSmemUsed;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;
+};
+
+// Iterates the KV tiles one query tile visits, in ascending order.
+struct TileIter {
+  int n;                       // tiles [0, n) are candidates
+  const uint8_t* mrow;         // block-sparse: mask row, else nullptr
+  int y;                       // block-sparse: keys per mask column
+  __device__ __forceinline__ int next(int t) const {
+    for (int u = t + 1; u < n; ++u)
+      if (mrow == nullptr || mrow[(u * kTileN) / y] != 0) return u;
+    return -1;
+  }
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return reinterpret_cast<uint8_t*>((a + 1023) & ~uintptr_t(1023));
+}
+
+template <int D, bool BF16, int MODE, bool P_TMEM>
+__global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using C = PrefillCfg<D, P_TMEM>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = bars + 4;
+  uint64_t* kv_empty = bars + 7;
+  uint64_t* s_full = bars + 10;
+  uint64_t* p_full = bars + 12;
+  uint64_t* o_done = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 15);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[blockIdx.x];
+  const BatchInfo bi = p.batches[it.b];
+  const int q0 = it.q_tile * kTileM;
+  const int kvh = it.h / p.group;
+  const int diag_off = (MODE == kCausal && p.causal_offset_mode == 3) ? (bi.kv_len - bi.q_len) : 0;
+
+  TileIter iter;
+  iter.mrow = nullptr;
+  iter.y = kTileN;
+  if (MODE == kCausal) {
+    const int last_row = min(q0 + kTileM - 1, bi.q_len - 1);
+    const int maxkey = min(bi.kv_len - 1, last_row + diag_off);
+    iter.n = maxkey >= 0 ? maxkey / kTileN + 1 : 0;
+  } else {
+    iter.n = (bi.kv_len + kTileN - 1) / kTileN;
+  }
+  if (MODE == kBlockSparse) {
+    const int qb = q0 / p.bsa_x;
+    iter.mrow = p.bsa_mask + ((int64_t(it.b) * p.num_heads + it.h) * p.bsa_nqb + qb) * p.bsa_nkb;
+    iter.y = p.bsa_y;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const bool is_tnd = p.is_tnd != 0;
+  const int q_row0 = is_tnd ? bi.q_start + q0 : q0;
+  const int kv_row0 = is_tnd ? bi.kv_start : 0;
+  const int b_coord = is_tnd ? 0 : it.b;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(q_full, C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_4d(smem + C::kOffQ + c * C::kBoxBytes, &p.tm_q, q_full, c * 64, q_row0, it.h, b_coord);
+      int j = 0;
+      for (int t = iter.next(-1); t >= 0; t = iter.next(t), ++j) {
+        const int s = j % S;
+        if (j >= S && !mbar_wait(&kv_empty[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
+        uint8_t* ks = smem + C::kOffK + s * C::kTileBytes;
+        uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
+        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(ks + c * C::kBoxBytes, &p.tm_k, &k_full[s], c * 64, kv_row0 + t * kTileN, kvh, b_coord);
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[s], c * 64, kv_row0 + t * kTileN, kvh, b_coord);
+      }
+      // On an abort, let every copy already issued land before the CTA exits.
+      if (*abort_flag) {
+        for (int s = 0; s < S && s < j; ++s) {
+          const int last = j - 1 - ((j - 1 - s) % S);   // last tile issued into stage s
+          mbar_wait(&k_full[s], (last / S) & 1, nullptr, p.status);
+          mbar_wait(&v_full[s], (last / S) & 1, nullptr, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      int j = 0;
+      auto issue_pv = [&](int jj) -> bool {
+        const int s = jj % S;
+        if (!mbar_wait(p_full, jj & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&v_full[s], (jj / S) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(smem + C::kOffV + s * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          // V is [keys x D] with D contiguous: an MN-major B operand.  A K-step
+          // of 16 keys is 16 rows = 2048 bytes; the next 64 columns of D sit
+          // one 16 KB box further (leading byte offset).
+          const uint64_t bdesc = smem_desc_sw128(v_base + kk * 2048, C::kBoxBytes, 1024);
+          if constexpr (P_TMEM) {
+            mma_ts(tmem + C::kColO, tmem + (jj & 1) * 128 + kk * 8, bdesc, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            const uint32_t p_base = smem_u32(smem + C::kOffP);
+            const uint64_t adesc = smem_desc_sw128(p_base + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
+            mma_ss(tmem + C::kColO, adesc, bdesc, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&kv_empty[s]);
+        mma_commit(o_done);
+        return true;
+      };
+      if (ok) {
+        for (int t = iter.next(-1); t >= 0; t = iter.next(t), ++j) {
+          const int s = j % S;
+          const int sb = j & 1;
+          if (!mbar_wait(&k_full[s], (j / S) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(smem + C::kOffK + s * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            const uint64_t adesc = smem_desc_sw128(q_base + off, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(k_base + off, 16, 1024);
+            mma_ss(tmem + sb * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[sb]);
+          if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        }
+        if (ok && j >= 1) issue_pv(j - 1);
+      }
+      // Wait until every MMA this thread issued has finished before TMEM goes.
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+    const int i = q0 + r;
+    const int diag = i + diag_off;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    int j = 0;
+    for (int t = iter.next(-1); t >= 0; t = iter.next(t), ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_off + sb * 128 + c * 32, u);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      tmem_wait_ld();
+      const int kv0 = t * kTileN;
+      const bool ragged = kv0 + kTileN > bi.kv_len;
+      const bool need_mask = ragged || (MODE == kCausal && kv0 + kTileN - 1 > q0 + diag_off);
+      if (need_mask) {
+        const int lim = (MODE == kCausal) ? min(bi.kv_len - 1, diag) : bi.kv_len - 1;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kv0 + c > lim) x[c] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      const float m_tile = mx * sl2;
+      const float m_new = fmaxf(m, m_tile);
+      // Keep a stale max unless it grows by more than 8 (log2 units): p <= 2^8
+      // stays exact in fp32 and representable in bf16/f16.
+      const float m_use = (m == -INFINITY || m_new > m + 8.f) ? m_new : m;
+      const float alpha = (m_use == m) ? 1.f : fast_exp2(m - m_use);
+      const float mo = (m_use == -INFINITY) ? 0.f : m_use;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float pv = fast_exp2(fmaf(x[c], sl2, -mo));
+        x[c] = pv;
+        sum += pv;
+      }
+      l = l * alpha + sum;
+      if (j > 0) {
+        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            tmem_st32(tmem + lane_off + C::kColO + c * 32, u);
+          }
+        }
+      }
+      if constexpr (P_TMEM) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t u[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = pack2(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1], BF16);
+          tmem_st32(tmem + lane_off + sb * 128 + c * 32, u);
+        }
+      } else {
+        uint8_t* pb = smem + C::kOffP;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          uint4 w;
+          w.x = pack2(x[8 * q + 0], x[8 * q + 1], BF16);
+          w.y = pack2(x[8 * q + 2], x[8 * q + 3], BF16);
+          w.z = pack2(x[8 * q + 4], x[8 * q + 5], BF16);
+          w.w = pack2(x[8 * q + 6], x[8 * q + 7], BF16);
+          const int box = q >> 3, qq = q & 7;
+          *reinterpret_cast<uint4*>(pb + box * C::kBoxBytes + r * 128 + ((qq ^ (r & 7)) << 4)) = w;
+        }
+      }
+      if (ragged) {
+        // Rows of V past the batch's keys may hold anything (even NaN); P is 0
+        // there but 0 * NaN is not, so clear them before the PV product.
+        const int s = j % S;
+        if (!mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (r >= bi.kv_len - kv0) {
+          uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if constexpr (P_TMEM) tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      m = m_use;
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && j > 0) {
+      ok = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status);
+      tc_fence_after();
+    }
+    if (ok) {
+      const bool row_valid = i < bi.q_len;
+      const bool has = l > 0.f;
+      const float inv_l = has ? 1.f / l : 0.f;
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      T* orow = reinterpret_cast<T*>(p.out) + (is_tnd ? int64_t(bi.q_start + i) * p.out_ss
+                                                       : int64_t(it.b) * p.out_sb + int64_t(i) * p.out_ss) +
+                int64_t(it.h) * p.out_sn;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (j > 0) {
+          tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = 0u;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(u[8 * q + 0]) * inv_l, __uint_as_float(u[8 * q + 1]) * inv_l, BF16);
+            w.y = pack2(__uint_as_float(u[8 * q + 2]) * inv_l, __uint_as_float(u[8 * q + 3]) * inv_l, BF16);
+            w.z = pack2(__uint_as_float(u[8 * q + 4]) * inv_l, __uint_as_float(u[8 * q + 5]) * inv_l, BF16);
+            w.w = pack2(__uint_as_float(u[8 * q + 6]) * inv_l, __uint_as_float(u[8 * q + 7]) * inv_l, BF16);
+            if (!has) w = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+          }
+        }
+      }
+      if (row_valid && p.lse != nullptr) {
+        const float lse = has ? (m + __log2f(l)) * 0.69314718055994531f : INFINITY;
+        float* lp = p.lse + (is_tnd ? int64_t(bi.q_start + i) * p.lse_ss
+                                    : int64_t(it.b) * p.lse_sb + int64_t(i) * p.lse_ss) +
+                    int64_t(it.h) * p.lse_sn;
+        *lp = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool BF16, int MODE, bool P_TMEM>
+static cudaError_t launch_one(const PrefillParams& p, cudaStream_t s) {
+  using C = PrefillCfg<D, P_TMEM>;
+  auto k = prefill_kernel<D, BF16, MODE, P_TMEM>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  k<<<p.n_items, C::kThreads, C::kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+#ifndef FIA_P_IN_SMEM
+constexpr bool kPInTmem = true;
+#else
+constexpr bool kPInTmem = false;
+#endif
+
+cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s) {
+  if (p.n_items == 0) return cudaSuccess;
+#define FIA_DISPATCH_MODE(DD, BB)                                                            \
+  switch (mode) {                                                                          \
+    case kDense: return launch_one<DD, BB, kDense, kPInTmem>(p, s);                        \
+    case kCausal: return launch_one<DD, BB, kCausal, kPInTmem>(p, s);                      \
+    case kBlockSparse: return launch_one<DD, BB, kBlockSparse, kPInTmem>(p, s);            \
+    default: return cudaErrorInvalidValue;                                                 \
+  }
+  if (head_dim == 128) {
+    if (bf16) { FIA_DISPATCH_MODE(128, true) } else { FIA_DISPATCH_MODE(128, false) }
+  } else if (head_dim == 64) {
+    if (bf16) { FIA_DISPATCH_MODE(64, true) } else { FIA_DISPATCH_MODE(64, false) }
+  }
+#undef FIA_DISPATCH_MODE
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------------
+// Rows that no prefill CTA writes: padding rows past a batch's actual query
+// length (mode 0) or every row (mode 1, e.g. K/V with S2 = 0).  They receive
+// attention_out = 0 and softmax_lse = +inf.
+// dims = {B, N, S, D}; out_strides/lse_strides = (b, n, s) element strides.
+// ------------------------------------------------------------------------
+__global__ void fill_rows_kernel(uint16_t* out, float* lse, int64_t B, int64_t N, int64_t Sq, int64_t D,
+                                 int64_t osb, int64_t osn, int64_t oss, int64_t lsb, int64_t lsn, int64_t lss,
+                                 const BatchInfo* batches, int mode) {
+  const int64_t row = int64_t(blockIdx.x) * blockDim.y + threadIdx.y;
+  if (row >= B * N * Sq) return;
+  const int64_t s = row % Sq, n = (row / Sq) % N, b = row / (Sq * N);
+  if (mode == 0 && s < batches[b].q_len) return;
+  for (int64_t d = threadIdx.x; d < D; d += blockDim.x) out[b * osb + n * osn + s * oss + d] = 0;
+  if (lse != nullptr && threadIdx.x == 0) lse[b * lsb + n * lsn + s * lss] = INFINITY;
+}
+
+cudaError_t launch_fill_rows(void* out, bool /*half_type*/, float* lse, const int64_t* dims,
+                             const int64_t* os, const int64_t* ls, const BatchInfo* batches, int mode,
+                             cudaStream_t st) {
+  const int64_t rows = dims[0] * dims[1] * dims[2];
+  if (rows == 0) return cudaSuccess;
+  dim3 block(32, 8);
+  const int64_t grid = (rows + 7) / 8;
+  fill_rows_kernel<<<(unsigned)grid, block, 0, st>>>(static_cast<uint16_t*>(out), lse, dims[0], dims[1], dims[2],
+                                                    dims[3], os[0], os[1], os[2], ls ? ls[0] : 0, ls ? ls[1] : 0,
+                                                    ls ? ls[2] : 0, batches, mode);
+  return cudaGetLastError();
+}
+
+}  // namespace fia

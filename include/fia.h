@@ -1,0 +1,205 @@
+/*
+ * fia.h -- C ABI of the fused inference attention library (sm_103a).
+ *
+ * The operator, as the FusedInferAttentionScore pages define it
+ * (torch_npu.npu_fused_infer_attention_score_v2, "计算公式";
+ * torch_npu.npu_prompt_flash_attention, "功能说明"):
+ *
+ *     attention_out = softmax(scale_value * query . key^T + atten_mask) . value
+ *     softmax_lse   = log(sum(exp(s - max(s)))) + max(s)     (fp32, optional)
+ *
+ * Three entry points cover the pages' cases:
+ *   fia_prefill  -- full attention, Q_S >= 1 (PromptFlashAttention)
+ *   fia_decode   -- incremental attention, Q_S = 1, paged or contiguous KV cache,
+ *                   optionally MLA (query_rope / key_rope) (IncreFlashAttention)
+ *   bsa_forward  -- block-sparse attention selected by blockSparseMask
+ *                   (aclnnBlockSparseAttentionV2)
+ * Each has a first phase that validates the arguments and reports the scratch
+ * ("workspace") size, mirroring aclnn's two-phase GetWorkspaceSize + execute
+ * calls (aclnnFusedInferAttentionScoreV5, "函数原型").
+ *
+ * Conventions shared by every call:
+ *   - Tensors are described by fia_tensor: a data pointer, an element type and a
+ *     row-major, contiguous shape (the pages accept contiguous tensors only).
+ *     Data pointers of execute calls are DEVICE pointers, 16-byte aligned.
+ *   - Host arrays (actual_seq_qlen / actual_seq_kvlen) are read during the call
+ *     and not kept.
+ *   - Ownership: the caller owns every buffer (inputs, outputs, workspace).  The
+ *     library allocates no device memory, keeps no pointer after returning, and
+ *     launches its kernels asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).
+ *   - The return value covers argument validation and kernel launch only.  Errors
+ *     found on the device (a bounded wait that ran out) are recorded in the
+ *     workspace and read with fia_device_status().
+ *   - Rows with no key to attend to (K/V with S2 = 0, a fully masked row, a
+ *     padding row past a batch's actual query length) give attention_out = 0 and
+ *     softmax_lse = +inf, extending the pages' empty-tensor rule
+ *     (npu_fused_infer_attention_score_v2, "入参为空的处理").
+ *   - A query with zero elements returns FIA_OK without launching anything.
+ */
+#ifndef FIA_H_
+#define FIA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FIA_API __attribute__((visibility("default")))
+#else
+#define FIA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fia_status {
+  FIA_OK = 0,
+  FIA_ERR_NULL = 1,          /* a required pointer is NULL                                  */
+  FIA_ERR_DTYPE = 2,         /* element types disagree or are not supported                 */
+  FIA_ERR_SHAPE = 3,         /* ranks/dims inconsistent (e.g. key != value shape)           */
+  FIA_ERR_LAYOUT = 4,        /* unknown input_layout                                        */
+  FIA_ERR_UNSUPPORTED = 5,   /* valid on the pages but not implemented by this library     */
+  FIA_ERR_SEQLEN = 6,        /* actual_seq_* list length or values invalid                  */
+  FIA_ERR_BLOCK_TABLE = 7,   /* block_table / block_size invalid                            */
+  FIA_ERR_WORKSPACE = 8,     /* workspace NULL or smaller than the reported size            */
+  FIA_ERR_CUDA = 9,          /* a CUDA runtime call or kernel launch failed                 */
+  FIA_ERR_TIMEOUT = 10,      /* device: a bounded wait inside a kernel ran out              */
+  FIA_ERR_HEADS = 11,        /* num_heads / num_key_value_heads invalid (GQA rules)         */
+  FIA_ERR_SPARSE_MODE = 12,  /* sparse_mode outside 0..4 or its mask requirements unmet     */
+  FIA_ERR_ALIGNMENT = 13     /* a device pointer is not 16-byte aligned                     */
+} fia_status;
+
+typedef enum fia_dtype {
+  FIA_DTYPE_F16 = 0,
+  FIA_DTYPE_BF16 = 1,
+  FIA_DTYPE_F32 = 2,
+  FIA_DTYPE_I32 = 3,
+  FIA_DTYPE_I64 = 4,
+  FIA_DTYPE_U8 = 5,
+  FIA_DTYPE_BOOL = 6,
+  FIA_DTYPE_I8 = 7
+} fia_dtype;
+
+/* A contiguous row-major tensor.  ndim == 0 or data == NULL means "absent"
+ * for optional arguments. */
+typedef struct fia_tensor {
+  void* data;
+  int32_t dtype;       /* fia_dtype */
+  int32_t ndim;        /* 0..5 */
+  int64_t shape[5];
+} fia_tensor;
+
+/* Keyword arguments of the pages' Python API (npu_fused_infer_attention_score_v2
+ * parameter list; npu_prompt_flash_attention prototype).  Fill with
+ * fia_params_init() and override what is needed. */
+typedef struct fia_params {
+  int64_t num_heads;              /* Q_N (num_query_heads / num_heads)                         */
+  int64_t num_key_value_heads;    /* KV_N; 0 means equal to num_heads; Q_N % KV_N == 0,
+                                     Q_N / KV_N <= 64                                          */
+  double scale_value;             /* softmax_scale / scale_value; default 1.0; must be > 0     */
+  const char* input_layout;       /* "BSH", "BSND", "BNSD" or "TND"; default "BSH"             */
+  int64_t sparse_mode;            /* 0..4; 2 = leftUpCausal, 3 = rightDownCausal              */
+  int64_t pre_tokens;             /* default 2147483647                                        */
+  int64_t next_tokens;            /* default 2147483647                                        */
+  const int64_t* actual_seq_qlen;   /* host array or NULL; TND: cumulative, no leading 0       */
+  int64_t n_actual_seq_qlen;
+  const int64_t* actual_seq_kvlen;  /* host array or NULL; TND: cumulative, no leading 0       */
+  int64_t n_actual_seq_kvlen;
+  int64_t block_size;             /* PageAttention tokens per block (0 = no paging)           */
+  int32_t softmax_lse_flag;       /* return_softmax_lse: 1 = write softmax_lse                 */
+  int32_t inner_precise;          /* accepted (0..3); the kernels always keep fp32 softmax    */
+} fia_params;
+
+/* Fills *p with the pages' defaults. */
+FIA_API void fia_params_init(fia_params* p);
+
+/* ------------------------------------------------------------------------
+ * fia_prefill: full attention with Q_S >= 1 over contiguous key/value.
+ *   query  (B,S1,H) BSH | (B,S1,N1,D) BSND | (B,N1,S1,D) BNSD | (T1,N1,D) TND;
+ *          f16 or bf16.  D is 64 or 128.
+ *   key, value: same layout and element type, N2 heads, identical shapes.
+ *   atten_mask: optional.  sparse_mode 2/3 compute the causal pattern from
+ *          indices; a mask given there must be (2048,2048) / (1,2048,2048) /
+ *          (1,1,2048,2048) and is not read.  Modes 0 (with a mask), 1 and 4
+ *          return FIA_ERR_UNSUPPORTED.
+ *   attention_out: the query's shape and element type.
+ *   softmax_lse: fp32 (B,N1,S1,1), or (T1,N1,1) for TND; used when
+ *          params->softmax_lse_flag != 0 (may be absent otherwise).
+ * ------------------------------------------------------------------------ */
+FIA_API fia_status fia_prefill_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                          const fia_tensor* atten_mask, const fia_params* params,
+                                          const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                                          size_t* workspace_bytes);
+FIA_API fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                       const fia_tensor* atten_mask, const fia_params* params, const fia_tensor* attention_out,
+                       const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * fia_decode: incremental attention, one query token per batch (Q_S = 1).
+ *   query  (B,N1,1,D) BNSD | (B,1,N1,D) BSND | (B,1,H) BSH; f16 or bf16.
+ *   key/value, contiguous (block_table absent): the query's layout with N2 heads.
+ *   key/value, paged (block_table present, PageAttention):
+ *          (blocknum, N2, block_size, D)  or  (blocknum, block_size, N2*D);
+ *          block_table int32 (B, >= max blocks per sequence); block ids are not
+ *          validated (as on the pages); actual_seq_kvlen is required.
+ *          block_size: a multiple of 16 that divides 128 or a multiple of 128.
+ *   query_rope / key_rope (MLA): both or neither.  Then D = 512, D_rope = 64,
+ *          N2 = 1, N1 in {1..128}, key = value = the 512-d latent cache
+ *          (blocknum, block_size, 512), key_rope (blocknum, block_size, 64).
+ *          scores = scale * (q . k + q_rope . k_rope).
+ *   atten_mask: must be absent (masked decode is not implemented).
+ *   attention_out: the query's shape; softmax_lse fp32 (B,N1,1,1) if flagged.
+ * ------------------------------------------------------------------------ */
+FIA_API fia_status fia_decode_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                         const fia_tensor* query_rope, const fia_tensor* key_rope,
+                                         const fia_tensor* block_table, const fia_tensor* atten_mask,
+                                         const fia_params* params, const fia_tensor* attention_out,
+                                         const fia_tensor* softmax_lse, size_t* workspace_bytes);
+FIA_API fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                      const fia_tensor* query_rope, const fia_tensor* key_rope, const fia_tensor* block_table,
+                      const fia_tensor* atten_mask, const fia_params* params, const fia_tensor* attention_out,
+                      const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * bsa_forward: block-sparse attention (aclnnBlockSparseAttentionV2).
+ *   query/key/value: BNSD, BSND or TND (one layout for all three); f16/bf16;
+ *          D in {64, 128}; N1 % N2 == 0.
+ *   block_sparse_mask: u8/bool (B, N1, ceil(maxQS/X), ceil(maxKVS/Y));
+ *          nonzero keeps the X x Y block.
+ *   block_shape: {X, Y}; X > 0, Y a multiple of 128 (this library: X also a
+ *          multiple of 128).
+ *   actual_seq_qlen / actual_seq_kvlen: both or neither (TND: both).
+ *   attention_out, softmax_lse: as for fia_prefill.
+ * ------------------------------------------------------------------------ */
+FIA_API fia_status bsa_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                  const fia_tensor* block_sparse_mask, const int64_t* block_shape,
+                                  const fia_params* params, const fia_tensor* attention_out,
+                                  const fia_tensor* softmax_lse, size_t* workspace_bytes);
+FIA_API fia_status bsa_forward(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                       const fia_tensor* block_sparse_mask, const int64_t* block_shape, const fia_params* params,
+                       const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Waits for `stream`, then returns the device-side status recorded in a
+ * workspace by the last call that used it (FIA_OK or FIA_ERR_TIMEOUT). */
+FIA_API fia_status fia_device_status(const void* workspace, void* stream);
+
+/* Static description of a status code. */
+FIA_API const char* fia_status_string(fia_status s);
+
+/* Human-readable detail of the last error returned on the calling thread. */
+FIA_API const char* fia_last_error(void);
+
+/* Profiling aid: the next fia_prefill / fia_decode / bsa_forward call made on
+ * this thread records `start_event` just before its main attention kernel and
+ * `stop_event` just after it, on that call's stream, so the caller can time the
+ * kernel alone with cudaEventElapsedTime.  Both are cudaEvent_t created by the
+ * caller (either may be NULL); the request is consumed by that one call. */
+FIA_API void fia_profile_next_call(void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FIA_H_ */

@@ -1,0 +1,223 @@
+"""The C-ABI library on the host, without a GPU: it loads, exports every symbol
+include/fia.h declares, and rejects invalid arguments with the documented
+status codes before any CUDA call (validation rules from the pages: GQA head
+rules, actual_seq list rules, TND cumulative lists, rope pairing, sparse_mode
+range, block_table shape, block-sparse constraints)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from attention_fia_prefill_gb300 import _binding as B
+from attention_fia_prefill_gb300 import build as fia_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+P = 1 << 20          # a fake, 16-byte aligned device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fia_build.build()
+    return B.load_library()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "fia.h")).read()
+    return re.findall(r"FIA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = header_symbols()
+    assert set(declared) == set(B.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", fia_build.LIB], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared:
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for code, name in B.STATUS_NAMES.items():
+        assert lib.fia_status_string(code).decode().startswith(name)
+
+
+def t(shape, dtype=B.DTYPE_BF16, ptr=P):
+    return B.raw_desc(ptr, dtype, shape)
+
+
+def params(lib, **kw):
+    return B.Params(**kw)
+
+
+def prefill_ws(lib, q, k, v, prm, out=None, lse=None, mask=None):
+    ws = ctypes.c_size_t(0)
+    r = lib.fia_prefill_get_workspace_size(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                           ctypes.byref(mask) if mask else None, ctypes.byref(prm.p),
+                                           ctypes.byref(out or q), ctypes.byref(lse) if lse else None,
+                                           ctypes.byref(ws))
+    return r, ws.value
+
+
+def test_prefill_valid_reports_workspace(lib):
+    q, k = t((2, 4, 300, 128)), t((2, 2, 300, 128))
+    r, ws = prefill_ws(lib, q, k, k, params(lib, num_heads=4, num_key_value_heads=2, input_layout="BNSD",
+                                            sparse_mode=3, scale_value=0.08))
+    assert r == B.FIA_OK and ws >= 256 + 2 * 3 * 4 * 16
+
+
+def test_empty_query_ok(lib):
+    q = t((0, 4, 5, 128))
+    r, ws = prefill_ws(lib, q, q, q, params(lib, num_heads=4, input_layout="BNSD"))
+    assert r == B.FIA_OK and ws == 256
+
+
+@pytest.mark.parametrize("n1,n2,code", [(6, 4, 11), (130, 2, 11), (4, 0, 0), (0, 1, 11)])
+def test_gqa_head_rules(lib, n1, n2, code):
+    """Q_N must be a multiple of KV_N with ratio <= 64; KV_N = 0 means Q_N."""
+    kvn = n2 if n2 else n1
+    q, k = t((1, max(n1, 1), 8, 128)), t((1, max(kvn, 1), 8, 128))
+    r, _ = prefill_ws(lib, q, k, k, params(lib, num_heads=n1, num_key_value_heads=n2, input_layout="BNSD"))
+    assert r == code
+
+
+@pytest.mark.parametrize("qlen,code", [([3], 0), ([3, 4, 5], 0), ([3, 4], 6), ([9], 6), ([-1], 6)])
+def test_actual_seq_list_rules(lib, qlen, code):
+    """A list of 1 is broadcast; >= B takes the first B; other counts and
+    entries outside [0, S] are errors."""
+    q = t((3, 2, 8, 64))
+    r, _ = prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="BNSD", actual_seq_qlen=qlen))
+    assert r == code
+
+
+def test_tnd_lists(lib):
+    q = t((10, 2, 64))
+    r, _ = prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="TND"))
+    assert r == B.FIA_ERR_SEQLEN if hasattr(B, "FIA_ERR_SEQLEN") else r == 6
+    r, _ = prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="TND", actual_seq_qlen=[4, 3],
+                                           actual_seq_kvlen=[4, 10]))
+    assert r == 6
+    r, _ = prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="TND", actual_seq_qlen=[4, 11],
+                                           actual_seq_kvlen=[4, 10]))
+    assert r == 6
+    r, ws = prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="TND", actual_seq_qlen=[4, 10],
+                                            actual_seq_kvlen=[4, 10], sparse_mode=3))
+    assert r == 0 and ws > 256
+
+
+@pytest.mark.parametrize("mode,code", [(9, 12), (5, 12), (-1, 12), (4, 5), (1, 12), (0, 0), (2, 0), (3, 0)])
+def test_sparse_mode_range(lib, mode, code):
+    q = t((1, 2, 8, 64))
+    r, _ = prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="BNSD", sparse_mode=mode))
+    assert r == code
+
+
+def test_causal_mask_shape(lib):
+    """Modes 2/3 accept no mask, or the (2048, 2048) form; other shapes are errors."""
+    q = t((1, 2, 8, 64))
+    m_ok, m_bad = t((2048, 2048), B.DTYPE_BOOL), t((8, 8), B.DTYPE_BOOL)
+    assert prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="BNSD", sparse_mode=2), mask=m_ok)[0] == 0
+    assert prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="BNSD", sparse_mode=2), mask=m_bad)[0] == 12
+
+
+def test_shape_dtype_layout_errors(lib):
+    q, k = t((1, 2, 8, 64)), t((1, 2, 9, 64))
+    assert prefill_ws(lib, q, k, q, params(lib, num_heads=2, input_layout="BNSD"))[0] == 3      # k != v
+    kf = t((1, 2, 8, 64), B.DTYPE_F16)
+    assert prefill_ws(lib, q, kf, kf, params(lib, num_heads=2, input_layout="BNSD"))[0] == 2    # dtype
+    assert prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="XYZ"))[0] == 4        # layout
+    q96 = t((1, 2, 8, 96))
+    assert prefill_ws(lib, q96, q96, q96, params(lib, num_heads=2, input_layout="BNSD"))[0] == 5  # head dim
+    qa = t((1, 2, 8, 64), ptr=P + 8)
+    assert prefill_ws(lib, qa, qa, qa, params(lib, num_heads=2, input_layout="BNSD"))[0] == 13   # alignment
+    lse_bad = t((1, 2, 8), B.DTYPE_F32)
+    assert prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="BNSD", softmax_lse_flag=True),
+                      lse=lse_bad)[0] == 3
+
+
+def test_workspace_too_small_rejected_before_launch(lib):
+    q = t((1, 2, 8, 64))
+    prm = params(lib, num_heads=2, input_layout="BNSD")
+    r = lib.fia_prefill(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), None, ctypes.byref(prm.p),
+                        ctypes.byref(q), None, ctypes.c_void_p(P), ctypes.c_size_t(16), None)
+    assert r == 8
+
+
+def decode_ws(lib, q, k, v, prm, qr=None, kr=None, table=None, out=None):
+    ws = ctypes.c_size_t(0)
+    ref = lambda d: ctypes.byref(d) if d is not None else None
+    r = lib.fia_decode_get_workspace_size(ref(q), ref(k), ref(v), ref(qr), ref(kr), ref(table), None,
+                                          ctypes.byref(prm.p), ref(out or q), None, ctypes.byref(ws))
+    return r, ws.value
+
+
+def test_decode_paged_rules(lib):
+    q = t((4, 8, 1, 128))
+    pool = t((40, 2, 128, 128))
+    table = t((4, 10), B.DTYPE_I32)
+    ok = params(lib, num_heads=8, num_key_value_heads=2, input_layout="BNSD", block_size=128,
+                actual_seq_kvlen=[100, 1000, 1, 1280])
+    r, ws = decode_ws(lib, q, pool, pool, ok, table=table)
+    assert r == 0 and ws > 256
+    # block_table without actual_seq_kvlen
+    r, _ = decode_ws(lib, q, pool, pool, params(lib, num_heads=8, num_key_value_heads=2, input_layout="BNSD",
+                                                block_size=128), table=table)
+    assert r == 6
+    # block_table must be 2-D with first dim B
+    assert decode_ws(lib, q, pool, pool, ok, table=t((4, 10, 1), B.DTYPE_I32))[0] == 7
+    assert decode_ws(lib, q, pool, pool, ok, table=t((3, 10), B.DTYPE_I32))[0] == 7
+    # second dim below maxBlocksPerSeq (1280 tokens need 10 blocks)
+    assert decode_ws(lib, q, pool, pool, ok, table=t((4, 9), B.DTYPE_I32))[0] in (6, 7)
+    # block_size must fit the cache and be 16-aligned
+    bad = params(lib, num_heads=8, num_key_value_heads=2, input_layout="BNSD", block_size=100,
+                 actual_seq_kvlen=[100, 1000, 1, 1280])
+    assert decode_ws(lib, q, pool, pool, bad, table=table)[0] == 7
+
+
+def test_decode_rope_pairing(lib):
+    q = t((2, 1, 128, 512))
+    lat = t((16, 128, 512))
+    prm = params(lib, num_heads=128, num_key_value_heads=1, input_layout="BSND", block_size=128,
+                 actual_seq_kvlen=[256])
+    r, _ = decode_ws(lib, q, lat, lat, prm, qr=t((2, 1, 128, 64)), kr=None, table=t((2, 2), B.DTYPE_I32))
+    assert r == 3
+
+
+def test_decode_needs_single_query_token(lib):
+    q = t((2, 4, 3, 128))
+    r, _ = decode_ws(lib, q, q, q, params(lib, num_heads=4, input_layout="BNSD"))
+    assert r == 5
+
+
+def bsa_ws(lib, q, k, v, mask, shape, prm):
+    ws = ctypes.c_size_t(0)
+    s = (ctypes.c_int64 * 2)(*shape)
+    r = lib.bsa_get_workspace_size(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(mask), s,
+                                   ctypes.byref(prm.p), ctypes.byref(q), None, ctypes.byref(ws))
+    return r, ws.value
+
+
+def test_bsa_rules(lib):
+    """aclnnBlockSparseAttentionV2 constraints: D in {64,128}; blockShapeY a
+    multiple of 128; mask shape (B, N1, ceil(S/X), ceil(S/Y)); both length
+    lists or neither; N1 % N2 == 0."""
+    q, k = t((2, 8, 1000, 128)), t((2, 2, 1000, 128))
+    good_mask = t((2, 8, 8, 8), B.DTYPE_U8)
+    prm = params(lib, num_heads=8, num_key_value_heads=2, input_layout="BNSD")
+    assert bsa_ws(lib, q, k, k, good_mask, (128, 128), prm)[0] == 0
+    assert bsa_ws(lib, q, k, k, good_mask, (128, 100), prm)[0] == 3
+    assert bsa_ws(lib, q, k, k, t((2, 8, 8, 7), B.DTYPE_U8), (128, 128), prm)[0] == 3
+    assert bsa_ws(lib, q, k, k, good_mask, (128, 128), params(lib, num_heads=8, num_key_value_heads=2,
+                                                               input_layout="BNSD", actual_seq_qlen=[5]))[0] == 6
+    k3 = t((2, 3, 1000, 128))
+    assert bsa_ws(lib, q, k3, k3, good_mask, (128, 128), params(lib, num_heads=8, num_key_value_heads=3,
+                                                                 input_layout="BNSD"))[0] == 11
+    q96 = t((2, 8, 1000, 96))
+    assert bsa_ws(lib, q96, q96, q96, good_mask, (128, 128), params(lib, num_heads=8, input_layout="BNSD"))[0] == 5
+    assert bsa_ws(lib, q, k, k, good_mask, (64, 128), prm)[0] == 5      # X not a multiple of 128 (library limit)
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(ImportError):
+        B.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,145 @@
+"""Decode parity: paged / contiguous incremental attention through the C ABI
+against the fp64 oracle.  Pools carry a NaN block that unused block_table
+entries point to, and NaN rows past each sequence's length, so any read
+outside the sequence shows up as a non-finite output."""
+import numpy as np
+import pytest
+import torch
+
+import fia_inputs
+from oracle import fia_oracle
+from tests.parity import assert_lse_close, assert_out_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_paged(fia, c, **kw):
+    dev = "cuda"
+    out, lse = fia.fia_decode(c.q.to(dev), c.k_pool.to(dev), c.v_pool.to(dev), block_table=c.block_table.to(dev),
+                              block_size=c.block_size, actual_seq_kvlen=c.kv_lens, num_heads=c.num_heads,
+                              num_key_value_heads=c.num_key_value_heads, scale_value=c.scale, input_layout="BNSD",
+                              softmax_lse_flag=True, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _oracle_paged(c):
+    return fia_oracle.fia_decode(c.q, c.k_pool, c.v_pool, num_heads=c.num_heads,
+                                 num_key_value_heads=c.num_key_value_heads, scale_value=c.scale, input_layout="BNSD",
+                                 actual_seq_kvlen=c.kv_lens, block_table=c.block_table, block_size=c.block_size)
+
+
+def _check_paged(fia, c):
+    out, lse = _run_paged(fia, c)
+    ro, rl = _oracle_paged(c)
+    assert_out_close(out, ro, c.q.dtype)
+    assert_lse_close(lse, rl)
+    return out, lse
+
+
+def test_full_paged_gqa_workload(fia):
+    """Decode GQA bf16 with paged KV: B=16, Q_N=32, KV_N=8, D=128, lengths
+    uniform on [1, 4096], block 128, random physical blocks -- every output."""
+    _check_paged(fia, fia_inputs.workload_paged_gqa_decode())
+
+
+@pytest.mark.parametrize("bs", [16, 64, 128, 256])
+def test_block_sizes(fia, bs):
+    lens = [1, 15, 16, 17, 300, 0, 513]
+    c = fia_inputs.paged_decode_case(len(lens), 8, 2, 128, lens, block_size=bs, workload=2000 + bs)
+    _check_paged(fia, c)
+
+
+@pytest.mark.parametrize("n1,n2", [(4, 4), (6, 3), (6, 2), (16, 2), (24, 1)])
+def test_group_sizes(fia, n1, n2):
+    """Head groups 1, 2, 3 (padded to 4), 8 and 24 (three blocks of 8)."""
+    c = fia_inputs.paged_decode_case(3, n1, n2, 128, [200, 1, 129], block_size=128, workload=2100 + n1)
+    _check_paged(fia, c)
+
+
+@pytest.mark.parametrize("dtype,D", [("f16", 128), ("bf16", 64), ("f16", 64)])
+def test_dtypes_and_head_dim(fia, dtype, D):
+    c = fia_inputs.paged_decode_case(4, 8, 2, D, [77, 128, 1000, 3], block_size=128, dtype=dtype, workload=2200 + D)
+    _check_paged(fia, c)
+
+
+def test_bsh_cache_layout(fia):
+    """(blocknum, block_size, KV_N * D) cache layout."""
+    c = fia_inputs.paged_decode_case(3, 8, 4, 128, [300, 20, 129], block_size=128, workload=2300, layout_kv="BSH")
+    _check_paged(fia, c)
+
+
+def test_contiguous_bnsd(fia):
+    """Non-paged decode: K/V (B, N2, S, D) with per-batch actual lengths."""
+    B, N1, N2, S, D = 3, 8, 2, 700, 128
+    q = fia_inputs.normal((B, N1, 1, D), "bf16", 2400, 1)
+    k = fia_inputs.normal((B, N2, S, D), "bf16", 2400, 2)
+    v = fia_inputs.normal((B, N2, S, D), "bf16", 2400, 3)
+    lens = [700, 1, 333]
+    out, lse = fia.fia_decode(q.cuda(), k.cuda(), v.cuda(), actual_seq_kvlen=lens, num_heads=N1,
+                              num_key_value_heads=N2, scale_value=D ** -0.5, input_layout="BNSD",
+                              softmax_lse_flag=True)
+    torch.cuda.synchronize()
+    ro, rl = fia_oracle.fia_decode(q, k, v, num_heads=N1, num_key_value_heads=N2, scale_value=D ** -0.5,
+                                   input_layout="BNSD", actual_seq_kvlen=lens)
+    assert_out_close(out, ro, torch.bfloat16)
+    assert_lse_close(lse, rl)
+
+
+def test_contiguous_bsnd(fia):
+    B, N1, N2, S, D = 2, 4, 4, 260, 64
+    q = fia_inputs.normal((B, 1, N1, D), "f16", 2500, 1)
+    k = fia_inputs.normal((B, S, N2, D), "f16", 2500, 2)
+    v = fia_inputs.normal((B, S, N2, D), "f16", 2500, 3)
+    out, lse = fia.fia_decode(q.cuda(), k.cuda(), v.cuda(), num_heads=N1, scale_value=0.1, input_layout="BSND",
+                              softmax_lse_flag=True)
+    torch.cuda.synchronize()
+    ro, rl = fia_oracle.fia_decode(q, k, v, num_heads=N1, scale_value=0.1, input_layout="BSND")
+    assert_out_close(out, ro, torch.float16)
+    assert_lse_close(lse, rl)
+
+
+def test_paged_equals_contiguous_bitwise(fia):
+    """The same cache read through a block_table or contiguously gives the
+    same bits (same kernel arithmetic, only the addressing differs)."""
+    B, N1, N2, S, D, bs = 2, 8, 2, 512, 128, 128
+    k = fia_inputs.normal((B, N2, S, D), "bf16", 2600, 2)
+    v = fia_inputs.normal((B, N2, S, D), "bf16", 2600, 3)
+    q = fia_inputs.normal((B, N1, 1, D), "bf16", 2600, 1)
+    lens = [512, 300]
+    nb = S // bs
+    perm = np.random.default_rng(1).permutation(B * nb)
+    table = torch.from_numpy(perm.reshape(B, nb).astype(np.int32))
+    kp = torch.empty((B * nb, N2, bs, D), dtype=torch.bfloat16)
+    vp = torch.empty_like(kp)
+    for b in range(B):
+        for i in range(nb):
+            kp[table[b, i]] = k[b, :, i * bs:(i + 1) * bs]
+            vp[table[b, i]] = v[b, :, i * bs:(i + 1) * bs]
+    o1, l1 = fia.fia_decode(q.cuda(), k.cuda(), v.cuda(), actual_seq_kvlen=lens, num_heads=N1, num_key_value_heads=N2,
+                            scale_value=0.088, input_layout="BNSD", softmax_lse_flag=True)
+    o2, l2 = fia.fia_decode(q.cuda(), kp.cuda(), vp.cuda(), block_table=table.cuda(), block_size=bs,
+                            actual_seq_kvlen=lens, num_heads=N1, num_key_value_heads=N2, scale_value=0.088,
+                            input_layout="BNSD", softmax_lse_flag=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_all_lengths_zero(fia):
+    c = fia_inputs.paged_decode_case(2, 4, 2, 128, [0, 0], block_size=128, workload=2700)
+    out, lse = _run_paged(fia, c)
+    assert torch.all(out == 0) and torch.all(torch.isinf(lse) & (lse > 0))
+
+
+def test_deterministic(fia):
+    c = fia_inputs.paged_decode_case(5, 16, 4, 128, [4000, 3, 1200, 128, 2049], workload=2800)
+    o1, l1 = _run_paged(fia, c)
+    o2, l2 = _run_paged(fia, c)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_device_status_ok(fia):
+    c = fia_inputs.paged_decode_case(2, 8, 2, 128, [100, 1000], workload=2900)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device="cuda")
+    _run_paged(fia, c, workspace=ws)
+    assert fia.fia_device_status(ws) == 0

@@ -1,0 +1,150 @@
+"""Prefill parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs, element by element for small cases, on sampled rows at
+the full varlen workload."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fia_inputs
+from oracle import fia_oracle
+from tests.parity import assert_lse_close, assert_out_close, assert_rows_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(fia, case, **kw):
+    dev = "cuda"
+    q, k, v = case.q.to(dev), case.k.to(dev), case.v.to(dev)
+    out, lse = fia.fia_prefill(q, k, v, num_heads=case.num_heads, num_key_value_heads=case.num_key_value_heads,
+                               scale_value=case.scale, input_layout=case.layout, sparse_mode=case.sparse_mode,
+                               actual_seq_qlen=case.actual_seq_qlen, actual_seq_kvlen=case.actual_seq_kvlen,
+                               softmax_lse_flag=True, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _oracle(case, rows=None):
+    return fia_oracle.fia_prefill(case.q, case.k, case.v, num_heads=case.num_heads,
+                                  num_key_value_heads=case.num_key_value_heads, scale_value=case.scale,
+                                  input_layout=case.layout, sparse_mode=case.sparse_mode,
+                                  actual_seq_qlen=case.actual_seq_qlen, actual_seq_kvlen=case.actual_seq_kvlen,
+                                  rows=rows)
+
+
+def _check_full(fia, case):
+    out, lse = _run(fia, case)
+    ref_o, ref_l = _oracle(case)
+    assert_out_close(out, ref_o, case.q.dtype)
+    assert_lse_close(lse, ref_l)
+    return out, lse
+
+
+def test_small_bnsd_f16_causal(fia):
+    """Prefill BNSD fp16: B=1, N=2, S=128, D=64, causal, LSE on."""
+    _check_full(fia, fia_inputs.workload_prefill_bnsd_f16_small())
+
+
+@pytest.mark.parametrize("mode", [0, 2, 3])
+@pytest.mark.parametrize("D", [64, 128])
+def test_ragged_gqa_bnsd(fia, mode, D):
+    """Several tiles with a ragged tail (S = 300), GQA 4/2, both head dims."""
+    case = fia_inputs.prefill_case(2, 4, 2, 300, 300, D, dtype="bf16", layout="BNSD", sparse_mode=mode,
+                                   workload=1000 + D + mode)
+    _check_full(fia, case)
+
+
+def test_pfa_example_shape_f16(fia):
+    """npu_prompt_flash_attention call example: q (1,8,164,128) vs k/v (1,8,1024,128), fp16."""
+    case = fia_inputs.prefill_case(1, 8, 8, 164, 1024, 128, dtype="f16", layout="BNSD", workload=7)
+    out, _ = _check_full(fia, case)
+    assert out.shape == (1, 8, 164, 128) and out.dtype == torch.float16
+
+
+@pytest.mark.parametrize("sq,skv", [(100, 300), (300, 100), (1, 257)])
+def test_right_down_causal_unequal(fia, sq, skv):
+    """sparse_mode 3 aligns the diagonal to the bottom-right corner; with
+    S_q > S_kv the leading rows have no key (0 / +inf)."""
+    case = fia_inputs.prefill_case(1, 2, 1, sq, skv, 128, dtype="bf16", layout="BNSD", sparse_mode=3,
+                                   workload=1100 + sq)
+    _check_full(fia, case)
+
+
+@pytest.mark.parametrize("layout", ["BSND", "BSH"])
+def test_layouts(fia, layout):
+    case = fia_inputs.prefill_case(2, 4, 1, 190, 190, 128, dtype="f16", layout=layout, sparse_mode=2,
+                                   workload=1200)
+    _check_full(fia, case)
+
+
+def test_actual_lengths_with_poisoned_padding(fia):
+    """actual_seq lengths shorter than S; K/V padding rows are NaN and must not
+    reach the output; query padding rows come back as 0 / +inf."""
+    case = fia_inputs.prefill_case(3, 2, 2, 260, 260, 128, dtype="bf16", layout="BNSD", sparse_mode=0,
+                                   actual_seq_qlen=[260, 5, 130], actual_seq_kvlen=[200, 1, 259],
+                                   poison_padding=True, workload=1300)
+    _check_full(fia, case)
+
+
+def test_tnd_varlen_small(fia):
+    """TND with lengths around tile boundaries, including an empty sequence."""
+    lens = [1, 127, 128, 0, 129, 300]
+    case = fia_inputs.tnd_case(lens, lens, 8, 2, 128, "bf16", sparse_mode=3, workload=1400)
+    _check_full(fia, case)
+
+
+def test_tnd_dense_unequal_lists(fia):
+    case = fia_inputs.tnd_case([50, 200], [300, 70], 4, 4, 64, "f16", sparse_mode=0, workload=1401)
+    _check_full(fia, case)
+
+
+def test_empty_kv(fia):
+    """K/V with S2 = 0: out all zeros, lse all +inf (the pages' empty rule)."""
+    q = torch.randn(1, 2, 5, 64, dtype=torch.float16, device="cuda")
+    k = torch.zeros(1, 2, 0, 64, dtype=torch.float16, device="cuda")
+    out, lse = fia.fia_prefill(q, k, k, num_heads=2, input_layout="BNSD", softmax_lse_flag=True, scale_value=0.125)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isinf(lse) & (lse > 0))
+
+
+def test_empty_query_is_noop(fia):
+    q = torch.zeros(0, 2, 5, 64, dtype=torch.float16, device="cuda")
+    out, _ = fia.fia_prefill(q, q, q, num_heads=2, input_layout="BNSD")
+    assert out.numel() == 0
+
+
+def test_deterministic(fia):
+    """Repeated calls are bitwise identical (the pages' operator is deterministic)."""
+    case = fia_inputs.tnd_case([333, 700], [333, 700], 8, 2, 128, "bf16", sparse_mode=3, workload=1500)
+    o1, l1 = _run(fia, case)
+    o2, l2 = _run(fia, case)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_gqa_equals_repeated_heads(fia):
+    case = fia_inputs.prefill_case(1, 8, 2, 257, 257, 128, dtype="bf16", layout="BNSD", sparse_mode=2,
+                                   workload=1600)
+    o1, l1 = _run(fia, case)
+    rep = fia_inputs.PrefillCase(case.q, case.k.repeat_interleave(4, dim=1), case.v.repeat_interleave(4, dim=1),
+                                 8, 8, case.scale, "BNSD", 2)
+    o2, l2 = _run(fia, rep)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_full_tnd_varlen_workload_sampled(fia):
+    """Varlen TND bf16: 8 sequences with lengths uniform on [256, 4096], GQA
+    32/8, D=128, causal, LSE on -- at full size, sampled rows vs the oracle."""
+    case = fia_inputs.workload_tnd_varlen()
+    out, lse = _run(fia, case)
+    lens = [b - a for a, b in zip([0] + case.actual_seq_qlen[:-1], case.actual_seq_qlen)]
+    starts = [0] + case.actual_seq_qlen[:-1]
+    rng = np.random.default_rng(0)
+    rows = []
+    for b in range(len(lens)):
+        for i in sorted({0, lens[b] - 1, int(rng.integers(lens[b])), 127, 128}):
+            if i < lens[b]:
+                rows.append((b, int(rng.integers(32)), i))
+    ref = _oracle(case, rows=rows)
+    assert_rows_close(out, lse, rows, ref, lambda r: (starts[r[0]] + r[2], r[1]), torch.bfloat16)
+    assert torch.isfinite(out.float()).all()
