@@ -53,13 +53,18 @@ constexpr int64_t kInt32Max = 2147483647;
 constexpr size_t kHeader = 256;   // workspace bytes [0, 256): device status word + padding
 constexpr int kMaxDecodeCtas = 1024;
 
-bool present(const fia_tensor* t) { return t != nullptr && t->data != nullptr && t->ndim > 0; }
-
 int64_t numel(const fia_tensor* t) {
   if (t == nullptr || t->ndim <= 0) return 0;
   int64_t n = 1;
   for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
   return n;
+}
+
+// An optional tensor is present when it has a rank and data.  A required tensor
+// may have no data when it holds zero elements (e.g. K/V with S2 = 0).
+bool present(const fia_tensor* t) { return t != nullptr && t->data != nullptr && t->ndim > 0; }
+bool given(const fia_tensor* t) {
+  return t != nullptr && t->ndim > 0 && (t->data != nullptr || numel(t) == 0);
 }
 
 bool is_half(int32_t dt) { return dt == FIA_DTYPE_F16 || dt == FIA_DTYPE_BF16; }
@@ -246,7 +251,7 @@ fia_status check_lse(const fia_tensor* lse, const fia_params* p, Layout L, int64
 fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_params* p,
                             const fia_tensor* out, bool bsa, Geometry& g) {
   if (p == nullptr) return fail(FIA_ERR_NULL, "params is NULL");
-  if (!present(q) || !present(k) || !present(v) || !present(out))
+  if (!given(q) || !given(k) || !given(v) || !given(out))
     return fail(FIA_ERR_NULL, "query/key/value/attention_out required");
   g.layout = parse_layout(p->input_layout);
   if (g.layout == L_BAD) return fail(FIA_ERR_LAYOUT, "input_layout '%s' not supported", p->input_layout);
@@ -626,7 +631,7 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
                            const fia_tensor* kr, const fia_tensor* table, const fia_tensor* mask, const fia_params* p,
                            const fia_tensor* out, DecodeGeometry& g) {
   if (p == nullptr) return fail(FIA_ERR_NULL, "params is NULL");
-  if (!present(q) || !present(k) || !present(v) || !present(out))
+  if (!given(q) || !given(k) || !given(v) || !given(out))
     return fail(FIA_ERR_NULL, "query/key/value/attention_out required");
   g.layout = parse_layout(p->input_layout);
   if (g.layout == L_BAD) return fail(FIA_ERR_LAYOUT, "input_layout '%s' not supported", p->input_layout);

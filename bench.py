@@ -124,9 +124,14 @@ class Timer:
         torch.cuda.synchronize()
         calls, kernels = [], []
         for _ in range(steps):
-            self.flush()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ks, ke = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if kernel_events:
+                # torch creates the CUDA event on first record: materialise the
+                # handles the library will re-record around its kernel
+                ks.record()
+                ke.record()
+            self.flush()
             s.record()
             if kernel_events:
                 fia._binding.profile_next_call(ks, ke)
@@ -412,8 +417,51 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_target(args):
+    """Plain repeated calls of one workload (warmup + steps), for ncu captures."""
+    import torch
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    from attention_fia_prefill_gb300 import build as b
+    b.build()
+    dev = torch.device("cuda", 0)
+    name = args.profile
+    if name == "decode":
+        c = fia_inputs.workload_paged_gqa_decode()
+        q, kp, vp, tb = c.q.to(dev), c.k_pool.to(dev), c.v_pool.to(dev), c.block_table.to(dev)
+
+        def call():
+            fia.fia_decode(q, kp, vp, block_table=tb, block_size=c.block_size, actual_seq_kvlen=c.kv_lens,
+                           num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                           input_layout="BNSD", softmax_lse_flag=True)
+    elif name == "prefill_tnd":
+        c = fia_inputs.workload_tnd_varlen()
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+
+        def call():
+            fia.fia_prefill(q, k, v, num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                            scale_value=c.scale, input_layout="TND", sparse_mode=3,
+                            actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
+                            softmax_lse_flag=True)
+    elif name == "bsa":
+        c = fia_inputs.workload_bsa()
+        q, k, v, m = c.q.to(dev), c.k.to(dev), c.v.to(dev), c.mask.to(dev)
+
+        def call():
+            fia.bsa_forward(q, k, v, m, c.block_shape, num_heads=c.num_heads,
+                            num_key_value_heads=c.num_key_value_heads, scale_value=c.scale, input_layout="BNSD",
+                            softmax_lse_flag=True)
+    else:
+        raise SystemExit(f"unknown profile target {name}")
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    print(f"profile target {name}: {args.warmup + args.steps} calls done")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, prefill_tnd, bsa)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -423,7 +471,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_target(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
