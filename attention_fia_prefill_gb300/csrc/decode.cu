@@ -71,8 +71,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ 
   using C = DecodeCfg<D, G>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + 3;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 6);

@@ -55,17 +55,12 @@ struct TileIter {
   }
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  return reinterpret_cast<uint8_t*>((a + 1023) & ~uintptr_t(1023));
-}
-
 template <int D, bool BF16, int MODE, bool P_TMEM>
 __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PrefillCfg<D, P_TMEM>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;

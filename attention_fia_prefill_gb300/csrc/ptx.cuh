@@ -25,6 +25,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Rounds a dynamic shared-memory pointer up to a 1024-byte boundary (the
+// 128-byte swizzle atom) with pointer arithmetic, so the compiler still knows
+// the result is a shared-memory address and emits ld/st.shared.
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* p) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 // ------------------------------------------------------------------ mbarrier

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(128, 1) selftest_kernel(const __grid_constant_
                                                           const __nv_bfloat16* p_global, float* out,
                                                           uint32_t* status) {
   extern __shared__ uint8_t raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(raw);
   uint8_t* sa = smem;            // A: up to 2 boxes of 16 KB
   uint8_t* sb = smem + 32768;    // B: up to 2 boxes
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 65536);
