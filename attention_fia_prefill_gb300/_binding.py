@@ -27,7 +27,7 @@ DTYPE_F16, DTYPE_BF16, DTYPE_F32, DTYPE_I32, DTYPE_I64, DTYPE_U8, DTYPE_BOOL, DT
 EXPORTS = [
     "fia_params_init", "fia_prefill_get_workspace_size", "fia_prefill", "fia_decode_get_workspace_size",
     "fia_decode", "bsa_get_workspace_size", "bsa_forward", "fia_device_status", "fia_status_string",
-    "fia_last_error", "fia_profile_next_call",
+    "fia_last_error", "fia_profile_next_call", "fia_decode_no_alloc",
 ]
 
 
@@ -92,6 +92,8 @@ def load_library(path: str | None = None):
     lib.fia_last_error.restype = ctypes.c_char_p
     lib.fia_profile_next_call.argtypes = [vp, vp]
     lib.fia_profile_next_call.restype = None
+    lib.fia_decode_no_alloc.argtypes = [T, T, T, T, T, T, T, P, T, T, vp]
+    lib.fia_decode_no_alloc.restype = st
     if path is None:
         _lib = lib
     return lib
@@ -250,6 +252,25 @@ def fia_decode(query, key, value, *, query_rope=None, key_rope=None, block_table
     check(lib.fia_decode(_ref(dq), _ref(dk), _ref(dv), _ref(dqr), _ref(dkr), _ref(dbt), _ref(dm), ctypes.byref(prm.p),
                          _ref(do), _ref(dl), ctypes.c_void_p(workspace.data_ptr()),
                          ctypes.c_size_t(workspace.numel()), _stream_ptr(query.device)))
+    return out, softmax_lse
+
+
+def fia_decode_no_alloc(query, key, value, *, out, softmax_lse=None, query_rope=None, key_rope=None,
+                        block_table=None, block_size=0, actual_seq_kvlen=None, atten_mask=None, num_heads=1,
+                        num_key_value_heads=0, scale_value=1.0, input_layout="BSH", inner_precise=0):
+    """fia_decode for callers that cannot allocate device memory: the caller
+    passes every output buffer and the library supplies the scratch from its
+    built-in array (see include/fia.h).  Nothing is allocated here."""
+    _require_cuda(query, key, value, query_rope, key_rope, block_table, out, softmax_lse)
+    lib = load_library()
+    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+                 input_layout=input_layout, actual_seq_kvlen=actual_seq_kvlen, block_size=block_size,
+                 softmax_lse_flag=softmax_lse is not None, inner_precise=inner_precise)
+    descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, block_table, atten_mask, out,
+                                      softmax_lse)]
+    dq, dk, dv, dqr, dkr, dbt, dm, do, dl = descs
+    check(lib.fia_decode_no_alloc(_ref(dq), _ref(dk), _ref(dv), _ref(dqr), _ref(dkr), _ref(dbt), _ref(dm),
+                                  ctypes.byref(prm.p), _ref(do), _ref(dl), _stream_ptr(query.device)))
     return out, softmax_lse
 
 

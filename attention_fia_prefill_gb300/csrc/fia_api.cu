@@ -472,6 +472,12 @@ fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, int& m
 
 }  // namespace
 
+namespace fia {
+void set_last_error(int status, const char* message) {
+  fail(static_cast<fia_status>(status), "%s", message);
+}
+}  // namespace fia
+
 // ======================================================================= ABI
 extern "C" {
 

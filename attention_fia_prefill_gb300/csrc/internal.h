@@ -100,6 +100,9 @@ struct MLAParams {
   uint32_t* status;
 };
 
+// Records the detail string fia_last_error() returns on this thread.
+void set_last_error(int status, const char* message);
+
 // Host-side launchers (defined next to their kernels).
 cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, int part, cudaStream_t s);

@@ -162,6 +162,32 @@ FIA_API fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, co
                       const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * fia_decode_no_alloc: fia_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart: it exists because some callers only
+ * hold the input and output buffers they were given (plugin hosts, inference
+ * servers that own the memory budget, code where a device allocation is not
+ * allowed) and cannot create the workspace fia_decode takes.
+ *   Arguments: as fia_decode, without the workspace.
+ *   Scratch: a 16 MiB array built into the library (one per GPU that loads it,
+ *          held until the process exits).  A call whose workspace need
+ *          (fia_decode_get_workspace_size) exceeds 16 MiB returns
+ *          FIA_ERR_WORKSPACE before touching the device.
+ *   Set-up: the first call on a device (with that device current) looks up the
+ *          array's device address; make that first call before any stream
+ *          capture.
+ *   Sharing: every call uses the same array and leaves its contents behind.
+ *          Calls that overlap on the GPU (other streams, other host threads)
+ *          race on it; serialise them.  The device status word lives in the
+ *          array and is cleared by each call; it is not exposed.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * ------------------------------------------------------------------------ */
+FIA_API fia_status fia_decode_no_alloc(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                       const fia_tensor* query_rope, const fia_tensor* key_rope,
+                                       const fia_tensor* block_table, const fia_tensor* atten_mask,
+                                       const fia_params* params, const fia_tensor* attention_out,
+                                       const fia_tensor* softmax_lse, void* stream);
+
+/* ------------------------------------------------------------------------
  * bsa_forward: block-sparse attention (aclnnBlockSparseAttentionV2).
  *   query/key/value: BNSD, BSND or TND (one layout for all three); f16/bf16;
  *          D in {64, 128}; N1 % N2 == 0.
