@@ -6,383 +6,540 @@
 // per-batch actual_seq_kvlen, and PageAttention (token j of batch b lives in
 // block block_table[b][j / block_size], row j % block_size).
 //
-// The work is memory bound (about 4 flop per KV byte), so it runs on CUDA
-// cores, laid out for HBM streaming:
-//   * each unit (batch, kv head, block of up to G query heads) is cut into
-//     128-token stages; all stages are dealt out evenly to one CTA per SM;
-//   * warp 8 streams the K and V rows of each stage into a 3-deep shared-memory
-//     ring with TMA (128-byte swizzle, so row reads are bank-conflict free);
-//   * warps 0..7 take 16 tokens each: scores with lanes split over (token,
-//     half of D), an online softmax per warp, then P V with lanes split over D;
-//     packed fp32x2 FMAs do the arithmetic;
-//   * at the end of each unit a CTA merges its 8 warps and writes one partial
-//     (O / l, lse); fia_decode_combine merges the partials of every unit in a
-//     fixed order (deterministic, no atomics).
+// Layout of the work:
+//   * a unit is (batch, kv head).  The g = Q_N / KV_N query heads of the unit
+//     are the rows of a 128-row query tile that lives in TMEM, in R = 4
+//     (g <= 32) or R = 2 (g <= 64) copies; S = Q K^T and O += P V are tcgen05
+//     MMAs with the A operand (Q, then P) read from TMEM;
+//   * every unit's keys are cut into 128-token stages; the stages of all units,
+//     in unit order, are dealt out to one CTA per SM with a fixed charge for
+//     every unit a CTA starts (a "segment"), so every CTA streams about the
+//     same number of KV bytes;
+//   * copy c of the head rows owns 128 / R of each stage's key columns: the
+//     four softmax warps share every stage, and each (segment, copy, head) is
+//     an independent partial (O / l, lse) over its keys;
+//   * two producer warps stream K (4-deep ring, freed after Q K^T) and V
+//     (3-deep ring, freed after P V) with 2-D TMA loads, one per page segment;
+//   * the CTA that completes a unit (a per-unit counter tagged with the call's
+//     epoch) merges the unit's partials in a fixed order -- deterministic, no
+//     float atomics -- and writes attention_out and softmax_lse.
+// Warps: 0..3 softmax (warp w = TMEM lanes 32w..32w+31), 4 K producer, 5 MMA
+// issuer and TMEM owner, 6 V producer.  TMEM columns: S0 [0,128),
+// S1 [128,256), O [256, 256+D), Q buffers [384, 384+D/2) and [384+D/2, 384+D).
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace fia {
 
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t ra = *reinterpret_cast<uint64_t*>(&a), rb = *reinterpret_cast<uint64_t*>(&b),
-           rc = *reinterpret_cast<uint64_t*>(&c), rd;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  return *reinterpret_cast<float2*>(&rd);
-}
-
-template <bool BF16>
-__device__ __forceinline__ float2 cvt2(uint32_t w) {
-  if constexpr (BF16) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-  } else {
-    __half2 h = *reinterpret_cast<__half2*>(&w);
-    return __half22float2(h);
-  }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float to_f32(const void* base, int64_t idx) {
-  if constexpr (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
-  else return __half2float(reinterpret_cast<const __half*>(base)[idx]);
-}
-
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-template <int D, int G>
+template <int D>
 struct DecodeCfg {
   static constexpr int kChunks = D / 64;
-  static constexpr int kStageBytes = 128 * 128 * kChunks;   // K (or V) of one stage
-  static constexpr int kStages = (D == 128 && G == 8) ? 2 : 3;
+  static constexpr int kBoxBytes = 128 * 128;
+  static constexpr int kTileBytes = kChunks * kBoxBytes;   // K (or V) of one 128-token stage
+  static constexpr int kKS = 4;
+  static constexpr int kVS = 3;
   static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kStages * kStageBytes;
-  static constexpr int kOffQ = kOffV + kStages * kStageBytes;          // f32 [G][D]
-  static constexpr int kOffP = kOffQ + G * D * 4;                      // f32 [8][16][G]
-  static constexpr int kOffMO = kOffP + 8 * 16 * G * 4;                // f32 [8][G][D]
-  static constexpr int kOffML = kOffMO + 8 * G * D * 4;                // f32 [8][G] m, [8][G] l
-  static constexpr int kOffBar = kOffML + 2 * 8 * G * 4;
-  static constexpr int kSmem = kOffBar + 64 + 1024;
-  static constexpr int kThreads = 288;
+  static constexpr int kOffV = kOffK + kKS * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVS * kTileBytes;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemUsed = kOffBar + kBarBytes + 1024;
+  static constexpr int kSmem = kSmemUsed < 122880 ? 122880 : kSmemUsed;   // one CTA (and TMEM owner) per SM
+  static constexpr int kThreads = 224;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kColQ = 384;
 };
 
-template <int D, bool BF16, int G>
-__global__ void __launch_bounds__(288, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
-  using C = DecodeCfg<D, G>;
-  constexpr int S = C::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align_smem_1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* empty = full + 3;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 6);
-  float* q_s = reinterpret_cast<float*>(smem + C::kOffQ);
-  float* p_s = reinterpret_cast<float*>(smem + C::kOffP);
-  float* mo_s = reinterpret_cast<float*>(smem + C::kOffMO);
-  float* mm_s = reinterpret_cast<float*>(smem + C::kOffML);
-  float* ml_s = mm_s + 8 * G;
+struct DecodeBars {
+  uint64_t k_full[4], k_empty[4], v_full[3], v_empty[3];
+  uint64_t s_full[2], p_full, o_done[2], o_free, q_ready[2];
+  uint64_t part_done, merge_flag_ready, drain;
+  uint32_t tmem_holder;
+  int abort_flag;
+  int merge_is_last;
+};
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg_begin = p.cta_seg[blockIdx.x], seg_end = p.cta_seg[blockIdx.x + 1];
+__device__ __forceinline__ const DecodeSeg* plan_segs(const DecodeParams& p) {
+  return p.plan_inline ? p.plan.segs : p.segs;
+}
+__device__ __forceinline__ const int32_t* plan_cta(const DecodeParams& p) {
+  return p.plan_inline ? p.plan.cta_seg : p.cta_seg;
+}
+__device__ __forceinline__ const int2* plan_units(const DecodeParams& p) {
+  return p.plan_inline ? p.plan.unit_parts : p.unit_parts;
+}
+__device__ __forceinline__ const int32_t* plan_kvlen(const DecodeParams& p) {
+  return p.plan_inline ? p.plan.kv_len : p.kv_len;
+}
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 8);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      int j = 0;
-      bool ok = true;
-      for (int si = seg_begin; si < seg_end && ok; ++si) {
-        const DecodeSeg sg = p.segs[si];
-        const int hb = sg.unit % p.head_blocks;
-        const int kvh = (sg.unit / p.head_blocks) % p.num_kv_heads;
-        const int b = sg.unit / (p.head_blocks * p.num_kv_heads);
-        (void)hb;
-        const int L = p.kv_len[b];
-        for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
-          const int s = j % S;
-          if (j >= S && !mbar_wait(&empty[s], ((j / S) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-          const int t0 = st * 128;
-          const int nvalid = min(128, L - t0);
-          const int nbox = (nvalid + p.box_rows - 1) / p.box_rows;
-          mbar_arrive_expect_tx(&full[s], 2u * C::kChunks * nbox * p.box_rows * 128u);
-          uint8_t* ks = smem + C::kOffK + s * C::kStageBytes;
-          uint8_t* vs = smem + C::kOffV + s * C::kStageBytes;
-          for (int k = 0; k < nbox; ++k) {
-            const int tok = t0 + k * p.box_rows;
-            int64_t row;
-            if (p.block_table != nullptr) {
-              const int64_t blk = p.block_table[int64_t(b) * p.table_stride + tok / p.block_size];
-              row = blk * p.row_per_blk + int64_t(kvh) * p.row_per_head + (tok % p.block_size);
-            } else {
-              row = int64_t(b) * p.row_per_blk + int64_t(kvh) * p.row_per_head + tok;
-            }
-            const int col0 = kvh * p.col_per_head;
-#pragma unroll
-            for (int c = 0; c < C::kChunks; ++c) {
-              const int off = c * 128 * 128 + k * p.box_rows * 128;
-              tma_load_2d(ks + off, &p.tm_k, &full[s], col0 + c * 64, int(row));
-              tma_load_2d(vs + off, &p.tm_v, &full[s], col0 + c * 64, int(row));
-            }
-          }
-        }
-      }
-      if (*abort_flag) {
-        for (int s = 0; s < S && s < j; ++s) {
-          const int last = j - 1 - ((j - 1 - s) % S);
-          mbar_wait(&full[s], (last / S) & 1, nullptr, p.status);
-        }
-      }
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int tid = threadIdx.x;          // 0..255
-  const int tl = lane & 15, half = lane >> 4;
-  const int r_qk = warp * 16 + tl;      // stage row this lane scores
-  constexpr int kDPL = D / 32;          // d values per lane in P V
+// Walks the CTA's stages in order and issues the TMA copies of one operand
+// (K or V) into a ring of NS stages.  The whole warp runs it: the lanes cache
+// 32 block_table entries of the current sequence so that a page lookup is a
+// register shuffle, and lane 0 issues the copies.
+template <int D, int NS>
+__device__ __forceinline__ void decode_producer(const DecodeParams& p, const CUtensorMap* tm, uint8_t* ring,
+                                                uint64_t* full, uint64_t* empty, volatile int* abort_flag,
+                                                int seg_begin, int seg_end) {
+  using C = DecodeCfg<D>;
+  const int lane = threadIdx.x & 31;
+  const DecodeSeg* segs = plan_segs(p);
+  const int32_t* kvlen = plan_kvlen(p);
+  if (lane == 0) tma_prefetch_desc(tm);
   int j = 0;
   bool ok = true;
-  for (int si = seg_begin; si < seg_end; ++si) {
-    const DecodeSeg sg = p.segs[si];
-    const int hb = sg.unit % p.head_blocks;
-    const int kvh = (sg.unit / p.head_blocks) % p.num_kv_heads;
-    const int b = sg.unit / (p.head_blocks * p.num_kv_heads);
-    const int L = p.kv_len[b];
-    const int h0 = kvh * p.group + hb * G;
-    const int nh = min(G, p.group - hb * G);
-
-    named_bar(1, 256);   // previous segment fully done with q_s and the merge area
-    for (int idx = tid; idx < G * D; idx += 256) {
-      const int h = idx / D, d = idx % D;
-      q_s[idx] = (h < nh) ? to_f32<BF16>(p.q, int64_t(b) * p.q_sb + int64_t(h0 + h) * p.q_sn + d) * p.scale_log2
-                          : 0.f;
-    }
-    named_bar(1, 256);
-
-    float m[G], l[G];
-    float2 o[G][kDPL / 2 > 0 ? kDPL / 2 : 1];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-#pragma unroll
-      for (int e = 0; e < (kDPL / 2 > 0 ? kDPL / 2 : 1); ++e) o[h][e] = make_float2(0.f, 0.f);
-    }
-
-    for (int st = sg.stage_begin; st < sg.stage_end && ok; ++st, ++j) {
-      const int s = j % S;
-      ok = mbar_wait(&full[s], (j / S) & 1, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const uint8_t* ks = smem + C::kOffK + s * C::kStageBytes;
-      const uint8_t* vs = smem + C::kOffV + s * C::kStageBytes;
-      const int nvalid = min(128, L - st * 128);
-
-      // ---- scores: lane (tl, half) covers row r_qk, half of D
-      float2 acc[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) {
-        const int c = half * (D / 16) + cc;
-        const int box = c >> 3, kc = c & 7;
-        const uint4 kw =
-            *reinterpret_cast<const uint4*>(ks + box * 16384 + r_qk * 128 + ((kc ^ (r_qk & 7)) << 4));
-        const float2 k01 = cvt2<BF16>(kw.x), k23 = cvt2<BF16>(kw.y), k45 = cvt2<BF16>(kw.z),
-                     k67 = cvt2<BF16>(kw.w);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 qa = *reinterpret_cast<const float4*>(q_s + h * D + c * 8);
-          const float4 qb = *reinterpret_cast<const float4*>(q_s + h * D + c * 8 + 4);
-          acc[h] = fma2(k01, make_float2(qa.x, qa.y), acc[h]);
-          acc[h] = fma2(k23, make_float2(qa.z, qa.w), acc[h]);
-          acc[h] = fma2(k45, make_float2(qb.x, qb.y), acc[h]);
-          acc[h] = fma2(k67, make_float2(qb.z, qb.w), acc[h]);
-        }
+  for (int si = seg_begin; si < seg_end && ok; ++si) {
+    const DecodeSeg sg = segs[si];
+    const int kvh = sg.unit % p.num_kv_heads;
+    const int b = sg.unit / p.num_kv_heads;
+    const int L = kvlen[b];
+    int cache_base = -64;     // first page index held by the lanes' cache
+    int32_t cache_blk = 0;    // lane i holds block_table[b][cache_base + i]
+    for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
+      const int s = j % NS;
+      if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((j / NS) - 1) & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
       }
-      const bool valid = r_qk < nvalid;
-      float pr[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float sc = acc[h].x + acc[h].y;
-        sc += __shfl_xor_sync(0xffffffffu, sc, 16);
-        sc = valid ? sc : -INFINITY;
-        float mx = sc;
-#pragma unroll
-        for (int o2 = 8; o2 >= 1; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-        const float m_new = fmaxf(m[h], mx);
-        const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m[h] - m_new);
-        const float pv = (sc == -INFINITY) ? 0.f : fast_exp2(sc - m_new);
-        float sum = pv;
-#pragma unroll
-        for (int o2 = 8; o2 >= 1; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
-        l[h] = l[h] * alpha + sum;
-        m[h] = m_new;
-#pragma unroll
-        for (int e = 0; e < (kDPL / 2 > 0 ? kDPL / 2 : 1); ++e) {
-          o[h][e].x *= alpha;
-          o[h][e].y *= alpha;
-        }
-        pr[h] = pv;
-      }
-      float* pw = p_s + warp * 16 * G;
-      if (half == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) pw[tl * G + h] = pr[h];
-      }
-      __syncwarp();
-
-      // ---- P V: lane covers kDPL consecutive d of every row of this warp
-      const int nrows = min(16, nvalid - warp * 16);
-      for (int t = 0; t < nrows; ++t) {
-        const int r = warp * 16 + t;
-        float ph[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) ph[h] = pw[t * G + h];
-        if constexpr (D == 128) {
-          const int box = lane >> 4, kc = (lane & 15) >> 1, hf = lane & 1;
-          const uint2 vw =
-              *reinterpret_cast<const uint2*>(vs + box * 16384 + r * 128 + ((kc ^ (r & 7)) << 4) + hf * 8);
-          const float2 v01 = cvt2<BF16>(vw.x), v23 = cvt2<BF16>(vw.y);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            o[h][0] = fma2(make_float2(ph[h], ph[h]), v01, o[h][0]);
-            o[h][1] = fma2(make_float2(ph[h], ph[h]), v23, o[h][1]);
+      const int t0 = st * 128;
+      const int nvalid = min(128, L - t0);
+      const int nbox = (nvalid + p.box_rows - 1) / p.box_rows;
+      uint8_t* dst = ring + s * C::kTileBytes;
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(C::kChunks * nbox * p.box_rows * 128));
+      for (int k = 0; k < nbox; ++k) {
+        const int tok = t0 + k * p.box_rows;
+        int64_t row;
+        if (p.block_table != nullptr) {
+          const int page = tok / p.block_size;
+          if (page < cache_base || page >= cache_base + 32) {
+            cache_base = page;
+            const int e = cache_base + lane;
+            cache_blk = e < p.table_stride ? p.block_table[int64_t(b) * p.table_stride + e] : 0;
           }
+          const int64_t blk = __shfl_sync(0xffffffffu, cache_blk, page - cache_base);
+          row = blk * p.row_per_blk + int64_t(kvh) * p.row_per_head + (tok % p.block_size);
         } else {
-          const int kc = lane >> 2, q4 = lane & 3;
-          const uint32_t vw = *reinterpret_cast<const uint32_t*>(vs + r * 128 + ((kc ^ (r & 7)) << 4) + q4 * 4);
-          const float2 v01 = cvt2<BF16>(vw);
+          row = int64_t(b) * p.row_per_blk + int64_t(kvh) * p.row_per_head + tok;
+        }
+        if (lane == 0) {
 #pragma unroll
-          for (int h = 0; h < G; ++h) o[h][0] = fma2(make_float2(ph[h], ph[h]), v01, o[h][0]);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(dst + c * C::kBoxBytes + k * p.box_rows * 128, tm, &full[s], kvh * p.col_per_head + c * 64,
+                        int(row));
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
+  }
+  if (lane == 0 && *abort_flag) {
+    // let the copies already issued land before the CTA goes away
+    for (int s = 0; s < NS && s < j; ++s) {
+      const int last = j - 1 - ((j - 1 - s) % NS);
+      mbar_wait(&full[s], (last / NS) & 1, nullptr, p.status);
+    }
+  }
+}
 
-    // ---- merge the 8 warps of this CTA and write one partial for the segment
+// Softmax threads write the query rows of one segment into a TMEM Q buffer as
+// packed pairs: row r = copy r / (32 QD) of head r % (32 QD); rows past the
+// group get zeros.  q_load issues the global loads and q_store the TMEM store,
+// so the load latency can overlap other work.
+template <int D>
+struct QRow {
+  uint4 v[D / 8];
+};
+
+template <int D>
+__device__ __forceinline__ void q_load(const DecodeParams& p, int b, int kvh, int h, QRow<D>& q) {
+  if (h < p.group) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                      (int64_t(b) * p.num_heads + kvh * p.group + h) * D);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) q.v[i] = src[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) q.v[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void q_store(uint32_t taddr, const QRow<D>& q) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t u[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      u[4 * i + 0] = q.v[c * 8 + i].x;
+      u[4 * i + 1] = q.v[c * 8 + i].y;
+      u[4 * i + 2] = q.v[c * 8 + i].z;
+      u[4 * i + 3] = q.v[c * 8 + i].w;
+    }
+    tmem_st32(taddr + c * 32, u);
+  }
+}
+
+template <int D, bool BF16, int R>
+__global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecodeCfg<D>;
+  constexpr int KS = C::kKS, VS = C::kVS;
+  constexpr int QD = 4 / R;            // TMEM lane quadrants (warps) per copy of the head rows
+  constexpr int CW = 128 / R;          // key columns of a stage each copy handles
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem_1024(smem_raw);
+  DecodeBars* bar = reinterpret_cast<DecodeBars*>(smem + C::kOffBar);
+  volatile int* abort_flag = &bar->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* cta_seg = plan_cta(p);
+  const DecodeSeg* segs = plan_segs(p);
+  const int2* unit_parts = plan_units(p);
+  const int32_t* kvlen = plan_kvlen(p);
+  const int seg_begin = p.n_cta > 0 ? cta_seg[blockIdx.x] : 0;
+  const int seg_end = p.n_cta > 0 ? cta_seg[blockIdx.x + 1] : 0;
+  const int g = p.group;
+
+  if (threadIdx.x == 0) {
+    if (blockIdx.x == 0) status_stamp(p.status);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&bar->k_full[s], 1);
+      mbar_init(&bar->k_empty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&bar->v_full[s], 1);
+      mbar_init(&bar->v_empty[s], 1);
+    }
+    mbar_init(&bar->s_full[0], 1);
+    mbar_init(&bar->s_full[1], 1);
+    mbar_init(&bar->p_full, 128);
+    mbar_init(&bar->o_done[0], 1);
+    mbar_init(&bar->o_done[1], 1);
+    mbar_init(&bar->o_free, 128);
+    mbar_init(&bar->q_ready[0], 128);
+    mbar_init(&bar->q_ready[1], 128);
+    mbar_init(&bar->part_done, 128);
+    mbar_init(&bar->merge_flag_ready, 1);
+    mbar_init(&bar->drain, 1);
+    bar->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bar->tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_holder;
+
+  if (warp == 4) {
+    decode_producer<D, KS>(p, &p.tm_k, smem + C::kOffK, bar->k_full, bar->k_empty, abort_flag, seg_begin, seg_end);
+  } else if (warp == 6) {
+    decode_producer<D, VS>(p, &p.tm_v, smem + C::kOffV, bar->v_full, bar->v_empty, abort_flag, seg_begin, seg_end);
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+      const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
+      int j = 0, segi = 0;
+      bool ok = true;
+      auto issue_pv = [&](int jj, int first, int seg_index) -> bool {
+        const int s = jj % VS;
+        if (jj == first && seg_index > 0 && !mbar_wait(&bar->o_free, (seg_index - 1) & 1, abort_flag, p.status))
+          return false;
+        if (!mbar_wait(&bar->p_full, jj & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&bar->v_full[s], (jj / VS) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t vb = v_base + s * C::kTileBytes;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        mm_s[warp * G + h] = m[h];
-        ml_s[warp * G + h] = l[h];
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts(tmem + C::kColO, tmem + (jj & 1) * 128 + kk * 8, smem_desc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
+                 idesc_pv, (jj > first || kk > 0) ? 1u : 0u);
+        mma_commit(&bar->v_empty[s]);
+        mma_commit(&bar->o_done[jj & 1]);
+        return true;
+      };
+      for (int si = seg_begin; si < seg_end && ok; ++si, ++segi) {
+        const DecodeSeg sg = segs[si];
+        if (!mbar_wait(&bar->q_ready[segi & 1], (segi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qcol = C::kColQ + (segi & 1) * (D / 2);
+        const int first = j;
+        for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
+          const int s = j % KS;
+          const int sb = j & 1;
+          if (!mbar_wait(&bar->k_full[s], (j / KS) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = k_base + s * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(tmem + sb * 128, tmem + qcol + kk * 8,
+                   smem_desc_sw128(kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(&bar->s_full[sb]);
+          mma_commit(&bar->k_empty[s]);
+          if (j > first && !issue_pv(j - 1, first, segi)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (j > first && !issue_pv(j - 1, first, segi)) { ok = false; break; }
       }
+      mma_commit(&bar->drain);
+      mbar_wait(&bar->drain, 0, nullptr, p.status);
     }
+  } else {
+    // ------------------------------------------------------------ softmax
+    // Warp w reads TMEM lanes 32w..32w+31.  Tile row r holds copy r / (32 QD)
+    // of head r % (32 QD); the copy owns key columns [cp * CW, cp * CW + CW)
+    // of every stage.
+    const int r = 32 * warp + lane;
+    const int cp = warp / QD;
+    const int h = r - cp * 32 * QD;
+    const int c0 = cp * CW;
+    const uint32_t lane_off = uint32_t(32 * warp) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    const int nseg = seg_end - seg_begin;
+
+    // Q of the first two segments (buffers 0 and 1)
+    for (int k = 0; k < 2 && k < nseg; ++k) {
+      const DecodeSeg sg = segs[seg_begin + k];
+      QRow<D> q;
+      q_load<D>(p, sg.unit / p.num_kv_heads, sg.unit % p.num_kv_heads, h, q);
+      q_store<D>(tmem + lane_off + C::kColQ + k * (D / 2), q);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar->q_ready[k]);
+    }
+
+    int j = 0;
+    for (int segi = 0; segi < nseg && ok; ++segi) {
+      const DecodeSeg sg = segs[seg_begin + segi];
+      const int kvh = sg.unit % p.num_kv_heads;
+      const int b = sg.unit / p.num_kv_heads;
+      const int L = kvlen[b];
+      const int first = j;
+      float m = -INFINITY, l = 0.f;
+      for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
+        const int sb = j & 1;
+        // Q for segment segi + 1 goes into the buffer segment segi - 1 used;
+        // its Q K^T products are complete once this segment's first S is.
+        const bool next_q = (j == first) && segi >= 1 && segi + 1 < nseg;
+        QRow<D> qn;
+        if (next_q) {
+          const DecodeSeg sn = segs[seg_begin + segi + 1];
+          q_load<D>(p, sn.unit / p.num_kv_heads, sn.unit % p.num_kv_heads, h, qn);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar->s_full[sb], (j >> 1) & 1, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (next_q) {
+          q_store<D>(tmem + lane_off + C::kColQ + ((segi + 1) & 1) * (D / 2), qn);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar->q_ready[(segi + 1) & 1]);
+        }
+        float x[CW];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+        for (int c = 0; c < CW / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_off + sb * 128 + c0 + c * 32, u);
 #pragma unroll
-      for (int e = 0; e < (kDPL / 2 > 0 ? kDPL / 2 : 1); ++e) {
-        const int d = lane * kDPL + 2 * e;
-        mo_s[(warp * G + h) * D + d] = o[h][e].x;
-        mo_s[(warp * G + h) * D + d + 1] = o[h][e].y;
+          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
+        }
+        tmem_wait_ld();
+        const int nvalid = min(128, L - st * 128);
+        if (nvalid < c0 + CW) {
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            if (c0 + c >= nvalid) x[c] = -INFINITY;
+        }
+        const float m_new = fmaxf(m, tree_max<CW>(x) * sl2);
+        const float m_use = (m == -INFINITY || m_new > m + 8.f) ? m_new : m;
+        const float alpha = (m_use == m) ? 1.f : fast_exp2(m - m_use);
+        const float mo = (m_use == -INFINITY) ? 0.f : m_use;
+        const float sum = exp2_and_sum<CW>(x, sl2, mo);
+        l = l * alpha + sum;
+        if (j > first && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&bar->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            tmem_st32(tmem + lane_off + C::kColO + c * 32, u);
+          }
+        }
+        // P row (packed pairs): this copy's CW keys at packed columns
+        // [cp * CW / 2, (cp + 1) * CW / 2), zero in the other copies' columns.
+        {
+          uint32_t u[CW / 2], z[CW / 2];
+#pragma unroll
+          for (int e = 0; e < CW / 2; ++e) {
+            u[e] = pack2(x[2 * e], x[2 * e + 1], BF16);
+            z[e] = 0u;
+          }
+#pragma unroll
+          for (int k = 0; k < R; ++k) {
+            const uint32_t col = tmem + lane_off + sb * 128 + k * (CW / 2);
+            if constexpr (CW == 32) {
+              if (k == cp) tmem_st16(col, u); else tmem_st16(col, z);
+            } else {
+              if (k == cp) tmem_st32(col, u); else tmem_st32(col, z);
+            }
+          }
+        }
+        if (nvalid < 128) {
+          // V rows past the sequence may hold anything (a pool's unused rows can
+          // be NaN); P is 0 there but 0 * NaN is not, so clear them.
+          const int s = j % VS;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar->v_full[s], (j / VS) & 1, abort_flag, p.status))) {
+            ok = false;
+            break;
+          }
+          if (r >= nvalid) {
+            uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar->p_full);
+        m = m_use;
       }
-    }
-    named_bar(1, 256);
-    for (int idx = tid; idx < G * D; idx += 256) {
-      const int h = idx / D, d = idx % D;
-      float M = -INFINITY;
+      if (!ok) break;
+      // ---- segment epilogue: one partial (O / l, lse) per (copy, head)
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&bar->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float ov[D];
 #pragma unroll
-      for (int w = 0; w < 8; ++w) M = fmaxf(M, mm_s[w * G + h]);
-      float Ls = 0.f, O = 0.f;
-      if (M != -INFINITY) {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const float f = fast_exp2(mm_s[w * G + h] - M);
-          Ls += ml_s[w * G + h] * f;
-          O += mo_s[(w * G + h) * D + d] * f;
+        for (int e = 0; e < 32; ++e) ov[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bar->o_free);     // the next segment's first P V may overwrite O now
+      const bool has = l > 0.f;
+      const float inv_l = has ? 1.f / l : 0.f;
+      const int64_t sub = int64_t(sg.part) * R + cp;
+      if (h < g) {
+        float* po = p.part_o + (sub * g + h) * D;
+#pragma unroll
+        for (int q = 0; q < D / 4; ++q)
+          *reinterpret_cast<float4*>(po + 4 * q) =
+              has ? make_float4(ov[4 * q] * inv_l, ov[4 * q + 1] * inv_l, ov[4 * q + 2] * inv_l, ov[4 * q + 3] * inv_l)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        p.part_lse[sub * g + h] = has ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+      // ---- the CTA that completes the unit merges its partials
+      __threadfence();
+      mbar_arrive(&bar->part_done);
+      if (threadIdx.x == 0) {
+        ok = mbar_wait(&bar->part_done, segi & 1, abort_flag, p.status);
+        unsigned long long* ctr = p.unit_counter + sg.unit;
+        const unsigned long long tag = (p.status.epoch & 0xffffffffull) << 32;
+        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr), nxt, prev;
+        while (true) {
+          nxt = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : (tag | 1ull);
+          prev = atomicCAS(ctr, cur, nxt);
+          if (prev == cur) break;
+          cur = prev;
+        }
+        bar->merge_is_last = (int(nxt & 0xffffffffull) == unit_parts[sg.unit].y) ? 1 : 0;
+        mbar_arrive(&bar->merge_flag_ready);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar->merge_flag_ready, segi & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
+      if (bar->merge_is_last) {
+        __threadfence();
+        const int2 up = unit_parts[sg.unit];
+        const int64_t s0 = int64_t(up.x) * R, ns = int64_t(up.y) * R;
+        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+        for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
+          const int hh = idx / (D / 4), d4 = idx % (D / 4);
+          float M = -INFINITY;
+          for (int64_t k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(p.part_lse + (s0 + k) * g + hh));
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          float Ls = 0.f;
+          if (M != -INFINITY) {
+            for (int64_t k = 0; k < ns; ++k) {
+              const float w = __expf(__ldcg(p.part_lse + (s0 + k) * g + hh) - M);
+              const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + k) * g + hh) * D) + d4);
+              Ls += w;
+              acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+            }
+          }
+          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+          const int head = kvh * g + hh;
+          T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * d4;
+          uint2 w2;
+          w2.x = pack2(acc.x * inv, acc.y * inv, BF16);
+          w2.y = pack2(acc.z * inv, acc.w * inv, BF16);
+          *reinterpret_cast<uint2*>(orow) = w2;
+          if (d4 == 0 && p.lse != nullptr)
+            p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = Ls > 0.f ? M + __logf(Ls) : INFINITY;
         }
       }
-      const bool has = Ls > 0.f;
-      p.part_o[(int64_t(sg.part) * G + h) * D + d] = has ? O / Ls : 0.f;
-      if (d == 0) p.part_lse[int64_t(sg.part) * G + h] = has ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
     }
+    // Units without any key (kv length 0): attention_out = 0, lse = +inf.
+    if (ok && blockIdx.x == 0) {
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      for (int u = 0; u < p.n_units; ++u) {
+        if (unit_parts[u].y != 0) continue;
+        const int kvh = u % p.num_kv_heads, b = u / p.num_kv_heads;
+        for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
+          const int hh = idx / (D / 4), d4 = idx % (D / 4);
+          const int head = kvh * g + hh;
+          T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * d4;
+          *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+          if (d4 == 0 && p.lse != nullptr) p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = INFINITY;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-// Merge the partials of every (batch, query head): one warp each, fixed order.
-template <int D, bool BF16, int G>
-__global__ void decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gw >= p.batch * p.num_heads) return;
-  const int b = gw / p.num_heads, h = gw % p.num_heads;
-  const int kvh = h / p.group, hg = h % p.group, hb = hg / G, hl = hg % G;
-  const int unit = (b * p.num_kv_heads + kvh) * p.head_blocks + hb;
-  const int2 up = p.unit_parts[unit];
-  float M = -INFINITY;
-  for (int k = 0; k < up.y; ++k) M = fmaxf(M, p.part_lse[int64_t(up.x + k) * G + hl]);
-  constexpr int kDPL = D / 32;
-  float acc[kDPL];
-#pragma unroll
-  for (int e = 0; e < kDPL; ++e) acc[e] = 0.f;
-  float Ls = 0.f;
-  if (M != -INFINITY) {
-    for (int k = 0; k < up.y; ++k) {
-      const float lk = p.part_lse[int64_t(up.x + k) * G + hl];
-      const float w = __expf(lk - M);
-      Ls += w;
-      const float* po = p.part_o + (int64_t(up.x + k) * G + hl) * D + lane * kDPL;
-#pragma unroll
-      for (int e = 0; e < kDPL; ++e) acc[e] += w * po[e];
-    }
-  }
-  const bool has = Ls > 0.f;
-  const float inv = has ? 1.f / Ls : 0.f;
-  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(h) * p.out_sn + lane * kDPL;
-#pragma unroll
-  for (int e = 0; e < kDPL; e += 2) {
-    const uint32_t w = pack2(acc[e] * inv, acc[e + 1] * inv, BF16);
-    *reinterpret_cast<uint32_t*>(orow + e) = w;
-  }
-  if (lane == 0 && p.lse != nullptr)
-    p.lse[int64_t(b) * p.lse_sb + int64_t(h) * p.lse_sn] = has ? M + __logf(Ls) : INFINITY;
-}
-
-template <int D, bool BF16, int G>
-static cudaError_t launch_decode_t(const DecodeParams& p, int part, cudaStream_t s) {
-  using C = DecodeCfg<D, G>;
-  if (part == 0) {
-    if (p.n_cta == 0) return cudaSuccess;
-    auto k = decode_kernel<D, BF16, G>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    k<<<p.n_cta, C::kThreads, C::kSmem, s>>>(p);
-    return cudaGetLastError();
-  }
-  const int warps = p.batch * p.num_heads;
-  if (warps > 0) decode_combine_kernel<D, BF16, G><<<(warps + 3) / 4, 128, 0, s>>>(p);
+template <int D, bool BF16>
+static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
+  using C = DecodeCfg<D>;
+  auto k = p.copies == 2 ? decode_kernel<D, BF16, 2> : decode_kernel<D, BF16, 4>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  k<<<p.n_cta > 0 ? p.n_cta : 1, C::kThreads, C::kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
-// part 0: the split-KV kernel; part 1: the combine kernel.
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, int part, cudaStream_t s) {
-#define FIA_DEC_G(DD, BB)                                         \
-  switch (p.heads_per_unit) {                                     \
-    case 1: return launch_decode_t<DD, BB, 1>(p, part, s);        \
-    case 2: return launch_decode_t<DD, BB, 2>(p, part, s);        \
-    case 4: return launch_decode_t<DD, BB, 4>(p, part, s);        \
-    case 8: return launch_decode_t<DD, BB, 8>(p, part, s);        \
-    default: return cudaErrorInvalidValue;                        \
-  }
-  if (head_dim == 128) {
-    if (bf16) { FIA_DEC_G(128, true) } else { FIA_DEC_G(128, false) }
-  } else if (head_dim == 64) {
-    if (bf16) { FIA_DEC_G(64, true) } else { FIA_DEC_G(64, false) }
-  }
-#undef FIA_DEC_G
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, cudaStream_t s) {
+  static_assert(sizeof(DecodeBars) <= DecodeCfg<128>::kBarBytes, "barrier area too small");
+  if (head_dim == 128) return bf16 ? launch_decode_t<128, true>(p, s) : launch_decode_t<128, false>(p, s);
+  if (head_dim == 64) return bf16 ? launch_decode_t<64, true>(p, s) : launch_decode_t<64, false>(p, s);
   return cudaErrorInvalidValue;
 }
 

@@ -5,6 +5,7 @@
 #include "../../include/fia.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -51,7 +52,16 @@ fia_status fail(fia_status s, const char* fmt, ...) {
 
 constexpr int64_t kInt32Max = 2147483647;
 constexpr size_t kHeader = 256;   // workspace bytes [0, 256): device status word + padding
-constexpr int kMaxDecodeCtas = 1024;
+
+// Every call gets a fresh epoch; kernels tag the workspace's status word (and
+// the decode kernel its per-unit counters) with it, so nothing in a reused
+// workspace has to be cleared between calls.
+std::atomic<unsigned long long> g_epoch{0};
+unsigned long long next_epoch() { return g_epoch.fetch_add(1, std::memory_order_relaxed) + 1; }
+
+// Status word for calls that launch no stamping kernel: cleared on the stream.
+fia_status clear_status(void* ws, cudaStream_t stream);
+constexpr int kMaxDecodeCtas = 256;   // decode CTAs per call (one per SM)
 
 int64_t numel(const fia_tensor* t) {
   if (t == nullptr || t->ndim <= 0) return 0;
@@ -375,9 +385,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   if (st != FIA_OK) return st;
   float* lse = (prm->softmax_lse_flag && present(lse_t)) ? static_cast<float*>(lse_t->data) : nullptr;
   uint8_t* base = static_cast<uint8_t*>(ws);
-  st = cuda_check(cudaMemsetAsync(base, 0, kHeader, stream), "status reset");
-  if (st != FIA_OK) return st;
-  if (g.B == 0) return FIA_OK;
+  if (g.B == 0) return clear_status(base, stream);
 
   int64_t os[3], ls[3] = {0, 0, 0};
   bns_strides(g.layout, g.N1, g.S1, g.D, os);
@@ -404,8 +412,10 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
       if (st != FIA_OK) return st;
     }
   }
-  if (items.empty()) return FIA_OK;
+  if (items.empty()) return clear_status(base, stream);
   if (g.S2 == 0) {
+    st = clear_status(base, stream);
+    if (st != FIA_OK) return st;
     // K/V with S2 = 0: every query row is empty (out = 0, lse = +inf).
     const int64_t dims[4] = {g.layout == L_TND ? 1 : g.B, g.N1, g.layout == L_TND ? g.T1 : g.S1, g.D};
     int64_t os2[3] = {os[0], os[1], os[2]}, ls2[3] = {ls[0], ls[1], ls[2]};
@@ -436,7 +446,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.scale_log2 = float(prm->scale_value * 1.4426950408889634);
   pp.bsa_mask = bsa_mask;
   pp.bsa_nqb = nqb; pp.bsa_nkb = nkb; pp.bsa_x = bx; pp.bsa_y = by;
-  pp.status = reinterpret_cast<uint32_t*>(base);
+  pp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
   return cuda_check(profiled(stream, [&] { return launch_prefill(pp, int(g.D), g.bf16, mode, stream); }),
                     "prefill launch");
 }
@@ -468,6 +478,10 @@ fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, int& m
   mode = kCausal;
   causal_mode = int(sm);
   return FIA_OK;
+}
+
+fia_status clear_status(void* ws, cudaStream_t stream) {
+  return cuda_check(cudaMemsetAsync(ws, 0, 8, stream), "status reset");
 }
 
 }  // namespace
@@ -525,10 +539,10 @@ fia_status fia_device_status(const void* workspace, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   fia_status st = cuda_check(cudaStreamSynchronize(s), "stream sync");
   if (st != FIA_OK) return st;
-  uint32_t word = 0;
+  unsigned long long word = 0;   // (epoch << 8) | code
   st = cuda_check(cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost), "status read");
   if (st != FIA_OK) return st;
-  return static_cast<fia_status>(word);
+  return static_cast<fia_status>(word & 0xffu);
 }
 
 // ---------------------------------------------------------------- prefill
@@ -714,78 +728,111 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
   return FIA_OK;
 }
 
-int heads_per_unit(int64_t group) {
-  if (group >= 8) return 8;
-  if (group >= 4) return group == 4 ? 4 : 8;
-  if (group == 3) return 4;
-  return int(group);
-}
+// Copies of the group's head rows in the decode kernel's 128-row query tile.
+int decode_copies(int64_t group) { return group <= 32 ? 4 : 2; }
 
 struct DecodePlan {
   std::vector<DecodeSeg> segs;
   std::vector<int32_t> cta_seg;
   std::vector<int2> unit_parts;
-  int n_cta = 0, n_units = 0, G = 1, HB = 1;
+  int n_cta = 0, n_units = 0;
 };
 
+// Charge, in 128-token stages, for every unit a CTA starts: loading the unit's
+// query rows and writing and merging its partials.
+constexpr double kSegmentCost = 0.5;
+
+// Deals the stages of all units (unit order = batch-major, then kv head) to at
+// most n_sm CTAs so that every CTA carries about the same cost: one per stage
+// plus kSegmentCost per segment.  Greedy fill against a capacity that grows
+// until the stages fit the CTAs.
 void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl) {
-  pl.G = heads_per_unit(g.N1 / g.N2);
-  pl.HB = int((g.N1 / g.N2 + pl.G - 1) / pl.G);
-  pl.n_units = int(g.B * g.N2 * pl.HB);
+  pl.n_units = int(g.B * g.N2);
   std::vector<int32_t> nst(size_t(pl.n_units));
-  int64_t T = 0;
+  int64_t T = 0, nonempty = 0;
   for (int u = 0; u < pl.n_units; ++u) {
-    const int b = u / int(g.N2 * pl.HB);
-    nst[size_t(u)] = (g.kv_len[size_t(b)] + 127) / 128;
+    nst[size_t(u)] = (g.kv_len[size_t(u / g.N2)] + 127) / 128;
     T += nst[size_t(u)];
+    nonempty += nst[size_t(u)] > 0;
   }
-  pl.n_cta = int(std::min<int64_t>(std::min<int64_t>(n_sm, kMaxDecodeCtas), T));
-  pl.segs.clear();
-  pl.cta_seg.assign(size_t(pl.n_cta) + 1, 0);
   pl.unit_parts.assign(size_t(pl.n_units), int2{0, 0});
-  // unit u occupies global stages [ustart[u], ustart[u] + nst[u])
-  std::vector<int64_t> ustart(size_t(pl.n_units) + 1, 0);
-  for (int u = 0; u < pl.n_units; ++u) ustart[size_t(u) + 1] = ustart[size_t(u)] + nst[size_t(u)];
-  int u = 0;
-  for (int c = 0; c < pl.n_cta; ++c) {
-    pl.cta_seg[size_t(c)] = int32_t(pl.segs.size());
-    int64_t lo = T * c / pl.n_cta, hi = T * (c + 1) / pl.n_cta;
-    while (lo < hi) {
-      while (ustart[size_t(u) + 1] <= lo) ++u;
-      const int64_t e = std::min<int64_t>(hi, ustart[size_t(u) + 1]);
-      DecodeSeg s{u, int32_t(lo - ustart[size_t(u)]), int32_t(e - ustart[size_t(u)]), int32_t(pl.segs.size())};
-      if (pl.unit_parts[size_t(u)].y == 0) pl.unit_parts[size_t(u)].x = s.part;
-      pl.unit_parts[size_t(u)].y += 1;
-      pl.segs.push_back(s);
-      lo = e;
+  pl.segs.clear();
+  const int max_cta = int(std::min<int64_t>(std::min<int64_t>(n_sm, kMaxDecodeCtas), T));
+  if (max_cta == 0) {
+    pl.n_cta = 0;
+    pl.cta_seg.assign(1, 0);
+    return;
+  }
+  double cap = (double(T) + kSegmentCost * double(nonempty + max_cta - 1)) / max_cta;
+  for (int attempt = 0; attempt < 200; ++attempt, cap *= 1.02) {
+    pl.segs.clear();
+    pl.cta_seg.assign(1, 0);
+    int c = 0;
+    double acc = 0.0;
+    bool fits = true;
+    for (int u = 0; u < pl.n_units && fits; ++u) {
+      int begin = 0, left = nst[size_t(u)];
+      pl.unit_parts[size_t(u)] = int2{int(pl.segs.size()), 0};
+      while (left > 0) {
+        if (acc > 0.0 && acc + kSegmentCost + 1.0 > cap) {
+          pl.cta_seg.push_back(int32_t(pl.segs.size()));
+          if (++c >= max_cta) { fits = false; break; }
+          acc = 0.0;
+        }
+        acc += kSegmentCost;
+        const int room = std::max(1, int(cap - acc));
+        const int k = std::min(left, room);
+        pl.segs.push_back(DecodeSeg{u, begin, begin + k, int32_t(pl.segs.size())});
+        pl.unit_parts[size_t(u)].y += 1;
+        acc += k;
+        begin += k;
+        left -= k;
+      }
+    }
+    if (fits) {
+      pl.cta_seg.push_back(int32_t(pl.segs.size()));
+      pl.n_cta = int(pl.cta_seg.size()) - 1;
+      return;
     }
   }
-  pl.cta_seg[size_t(pl.n_cta)] = int32_t(pl.segs.size());
+  // unreachable in practice: one CTA per stage always fits
+  pl.n_cta = 0;
+  pl.cta_seg.assign(1, 0);
 }
 
 struct DecodeWsLayout {
-  size_t off_segs, off_cta, off_units, off_len, off_po, off_pl, total;
+  size_t off_ctr, off_segs, off_cta, off_units, off_len, off_po, off_pl, total;
 };
 
-DecodeWsLayout decode_ws_layout(size_t n_segs, size_t n_cta, size_t n_units, size_t B, size_t G, size_t D) {
+// Workspace: status word | per-unit counters | (plan, when it does not fit in
+// the kernel parameters) | partial O | partial lse.
+DecodeWsLayout decode_ws_layout(size_t n_segs, size_t n_cta, size_t n_units, size_t B, size_t rows, size_t D,
+                                bool plan_in_ws) {
   DecodeWsLayout w;
   size_t o = kHeader;
-  w.off_segs = o; o += align_up(n_segs * sizeof(DecodeSeg), 256);
-  w.off_cta = o; o += align_up((n_cta + 1) * sizeof(int32_t), 256);
-  w.off_units = o; o += align_up(n_units * sizeof(int2), 256);
-  w.off_len = o; o += align_up(B * sizeof(int32_t), 256);
-  w.off_po = o; o += align_up(n_segs * G * D * sizeof(float), 256);
-  w.off_pl = o; o += align_up(n_segs * G * sizeof(float), 256);
+  w.off_ctr = o; o += align_up(n_units * sizeof(unsigned long long), 256);
+  w.off_segs = o; o += plan_in_ws ? align_up(n_segs * sizeof(DecodeSeg), 256) : 0;
+  w.off_cta = o; o += plan_in_ws ? align_up((n_cta + 1) * sizeof(int32_t), 256) : 0;
+  w.off_units = o; o += plan_in_ws ? align_up(n_units * sizeof(int2), 256) : 0;
+  w.off_len = o; o += plan_in_ws ? align_up(B * sizeof(int32_t), 256) : 0;
+  w.off_po = o; o += align_up(n_segs * rows * D * sizeof(float), 256);
+  w.off_pl = o; o += align_up(n_segs * rows * sizeof(float), 256);
   w.total = o;
   return w;
 }
 
+bool plan_fits_inline(size_t n_segs, size_t n_cta, size_t n_units, size_t B) {
+  return n_segs <= size_t(kInlineSegs) && n_cta <= size_t(kInlineCtas) && n_units <= size_t(kInlineUnits) &&
+         B <= size_t(kInlineBatch);
+}
+
+// Upper bound over every plan the call can make (at most kMaxDecodeCtas CTAs,
+// so at most n_units + kMaxDecodeCtas segments).
 size_t decode_ws_bound(const DecodeGeometry& g) {
-  const int G = heads_per_unit(g.N1 / g.N2);
-  const int HB = int((g.N1 / g.N2 + G - 1) / G);
-  const size_t n_units = size_t(g.B * g.N2 * HB);
+  const size_t n_units = size_t(g.B * g.N2);
   const size_t n_segs = n_units + kMaxDecodeCtas;
-  return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), size_t(G), size_t(g.D)).total;
+  const size_t rows = size_t(g.N1 / g.N2) * size_t(decode_copies(g.N1 / g.N2));
+  return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), rows, size_t(g.D), true).total;
 }
 
 fia_status check_decode_lse(const fia_tensor* lse, const fia_params* p, int64_t B, int64_t N1) {
@@ -831,23 +878,39 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   cudaStream_t stream_t = static_cast<cudaStream_t>(stream);
   DecodePlan pl;
   plan_decode(g, sm_count(), pl);
-  const DecodeWsLayout w = decode_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B),
-                                            size_t(pl.G), size_t(g.D));
+  const int copies = decode_copies(g.N1 / g.N2);
+  const size_t rows = size_t(g.N1 / g.N2) * size_t(copies);
+  const bool inl = plan_fits_inline(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B));
+  const DecodeWsLayout w = decode_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B), rows,
+                                            size_t(g.D), !inl);
   st = check_ws(workspace, workspace_bytes, w.total);
   if (st != FIA_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  st = cuda_check(cudaMemsetAsync(base, 0, kHeader, stream_t), "status reset");
-  if (st != FIA_OK) return st;
-  std::vector<uint8_t> plan(w.off_po - kHeader, 0);
-  memcpy(plan.data() + (w.off_segs - kHeader), pl.segs.data(), pl.segs.size() * sizeof(DecodeSeg));
-  memcpy(plan.data() + (w.off_cta - kHeader), pl.cta_seg.data(), pl.cta_seg.size() * sizeof(int32_t));
-  memcpy(plan.data() + (w.off_units - kHeader), pl.unit_parts.data(), pl.unit_parts.size() * sizeof(int2));
-  memcpy(plan.data() + (w.off_len - kHeader), g.kv_len.data(), g.kv_len.size() * sizeof(int32_t));
-  st = cuda_check(cudaMemcpyAsync(base + kHeader, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream_t), "plan upload");
-  if (st != FIA_OK) return st;
 
+  static_assert(sizeof(DecodeParams) <= 32000, "decode kernel parameters exceed the launch limit");
   DecodeParams dp;
   memset(&dp, 0, sizeof(dp));
+  if (inl) {
+    dp.plan_inline = 1;
+    std::copy(pl.segs.begin(), pl.segs.end(), dp.plan.segs);
+    std::copy(pl.cta_seg.begin(), pl.cta_seg.end(), dp.plan.cta_seg);
+    std::copy(pl.unit_parts.begin(), pl.unit_parts.end(), dp.plan.unit_parts);
+    std::copy(g.kv_len.begin(), g.kv_len.end(), dp.plan.kv_len);
+  } else {
+    std::vector<uint8_t> plan(w.off_po - w.off_segs, 0);
+    memcpy(plan.data() + (w.off_segs - w.off_segs), pl.segs.data(), pl.segs.size() * sizeof(DecodeSeg));
+    memcpy(plan.data() + (w.off_cta - w.off_segs), pl.cta_seg.data(), pl.cta_seg.size() * sizeof(int32_t));
+    memcpy(plan.data() + (w.off_units - w.off_segs), pl.unit_parts.data(), pl.unit_parts.size() * sizeof(int2));
+    memcpy(plan.data() + (w.off_len - w.off_segs), g.kv_len.data(), g.kv_len.size() * sizeof(int32_t));
+    st = cuda_check(cudaMemcpyAsync(base + w.off_segs, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream_t),
+                    "plan upload");
+    if (st != FIA_OK) return st;
+    dp.plan_inline = 0;
+    dp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
+    dp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
+    dp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
+    dp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
+  }
   if (pl.n_cta > 0) {
     uint64_t dims[2], strides[1];
     if (g.paged) {
@@ -881,31 +944,24 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
     if (st != FIA_OK) return st;
   }
   dp.q = query->data;
-  dp.q_sb = g.q_sb; dp.q_sn = g.q_sn;
-  dp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
   dp.out = attention_out->data;
   dp.out_sb = g.o_sb; dp.out_sn = g.o_sn;
   dp.lse = (params->softmax_lse_flag && present(softmax_lse)) ? static_cast<float*>(softmax_lse->data) : nullptr;
   dp.lse_sb = g.N1; dp.lse_sn = 1;
   dp.part_o = reinterpret_cast<float*>(base + w.off_po);
   dp.part_lse = reinterpret_cast<float*>(base + w.off_pl);
-  dp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
-  dp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
-  dp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
+  dp.unit_counter = reinterpret_cast<unsigned long long*>(base + w.off_ctr);
   dp.n_cta = pl.n_cta;
   dp.n_units = pl.n_units;
   dp.batch = int(g.B);
   dp.num_heads = int(g.N1);
   dp.num_kv_heads = int(g.N2);
   dp.group = int(g.N1 / g.N2);
-  dp.heads_per_unit = pl.G;
-  dp.head_blocks = pl.HB;
+  dp.copies = copies;
   dp.scale_log2 = float(params->scale_value * 1.4426950408889634);
-  dp.status = reinterpret_cast<uint32_t*>(base);
-  st = cuda_check(profiled(stream_t, [&] { return launch_decode(dp, int(g.D), g.bf16, 0, stream_t); }),
-                  "decode launch");
-  if (st != FIA_OK) return st;
-  return cuda_check(launch_decode(dp, int(g.D), g.bf16, 1, stream_t), "decode combine launch");
+  dp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
+  return cuda_check(profiled(stream_t, [&] { return launch_decode(dp, int(g.D), g.bf16, stream_t); }),
+                    "decode launch");
 }
 
 }  // extern "C"

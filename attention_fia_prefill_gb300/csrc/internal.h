@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace fia {
 
 constexpr int kTileM = 128;   // query rows per prefill CTA
@@ -37,16 +39,29 @@ struct PrefillParams {
   float scale_log2;               // scale * log2(e)
   const uint8_t* bsa_mask;        // [B, N1, nqb, nkb]
   int bsa_nqb, bsa_nkb, bsa_x, bsa_y;
-  uint32_t* status;
+  DevStatus status;
 };
 
-// Paged / contiguous decode (Q_S = 1).  The KV sequence of every unit
-// (batch, kv head, head block) is cut into 128-token stages; the stages of all
-// units, in unit order, are dealt out evenly to the CTAs (one per SM), so a CTA
-// may finish one unit and start the next ("segments").  Each segment leaves one
-// partial (O / l, lse) that the combine kernel merges.
+// Paged / contiguous decode (Q_S = 1).  A unit is (batch, kv head).  Every
+// unit's keys are cut into 128-token stages; the stages of all units, in unit
+// order, are dealt out to the CTAs (one per SM), so a CTA may end one unit and
+// start the next: each such piece is a "segment".
 struct DecodeSeg {
-  int32_t unit, stage_begin, stage_end, part;
+  int32_t unit, stage_begin, stage_end, part;   // part = global segment index
+};
+
+// The plan travels inside the kernel parameters when it fits these bounds
+// (no upload, no extra copy); bigger plans live in the workspace.
+constexpr int kInlineSegs = 512;
+constexpr int kInlineCtas = 256;
+constexpr int kInlineUnits = 1024;
+constexpr int kInlineBatch = 1024;
+
+struct DecodeInlinePlan {
+  DecodeSeg segs[kInlineSegs];
+  int32_t cta_seg[kInlineCtas + 1];
+  int2 unit_parts[kInlineUnits];    // {first segment, number of segments} of every unit
+  int32_t kv_len[kInlineBatch];
 };
 
 struct DecodeParams {
@@ -58,46 +73,25 @@ struct DecodeParams {
   int32_t col_per_head;           // map column offset between kv heads
   const int32_t* block_table;     // nullable (contiguous)
   int64_t table_stride;
-  const void* q;                  // element (b, h, d) at q[b*q_sb + h*q_sn + d]
-  int64_t q_sb, q_sn;
-  const int32_t* kv_len;          // [B] on device
+  const void* q;                  // query row (b * Q_N + h) of D elements
   void* out;
   int64_t out_sb, out_sn;
   float* lse;                     // nullable
   int64_t lse_sb, lse_sn;
-  float* part_o;                  // [n_parts, G, D]
-  float* part_lse;                // [n_parts, G] natural log, -inf = empty
-  const DecodeSeg* segs;
-  const int32_t* cta_seg;         // [n_cta + 1]
-  const int2* unit_parts;         // [n_units] {first part, n parts}
+  float* part_o;                  // [n_segments * copies, group, D]
+  float* part_lse;                // [n_segments * copies, group] natural log, -inf = empty
+  unsigned long long* unit_counter;   // [n_units] (epoch << 32) | segments finished
   int n_cta, n_units;
-  int batch, num_heads, num_kv_heads, group, heads_per_unit, head_blocks;
+  int batch, num_heads, num_kv_heads, group;
+  int copies;                     // copies of the head rows in the query tile (4 or 2)
   float scale_log2;
-  uint32_t* status;
-};
-
-struct MLAParams {
-  const void* q;                  // (b, h, 512) via strides
-  const void* q_rope;             // (b, h, 64)
-  int64_t q_sb, q_sn, qr_sb, qr_sn;
-  const void* latent;             // (nblk, bs, 512)
-  const void* rope;               // (nblk, bs, 64)
-  const int32_t* block_table;
-  int64_t table_stride;
-  int block_size;
-  const int32_t* kv_len;          // [B]
-  void* out;                      // (b, h, 512)
-  int64_t out_sb, out_sn;
-  float* lse;
-  int64_t lse_sb, lse_sn;
-  float* part_o;                  // [n_parts, 128, 512]
-  float* part_lse;                // [n_parts, 128]
-  const int4* chunks;             // {b, first page, n pages, part index}
-  const int2* unit_parts;         // per b: {first part, n parts}
-  int n_chunks;
-  int num_heads;
-  float scale_log2;
-  uint32_t* status;
+  DevStatus status;
+  int plan_inline;                // 1: the plan below; 0: the pointers
+  const DecodeSeg* segs;
+  const int32_t* cta_seg;
+  const int2* unit_parts;
+  const int32_t* kv_len;
+  DecodeInlinePlan plan;
 };
 
 // Records the detail string fia_last_error() returns on this thread.
@@ -105,8 +99,7 @@ void set_last_error(int status, const char* message);
 
 // Host-side launchers (defined next to their kernels).
 cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, int part, cudaStream_t s);
-cudaError_t launch_mla_decode(const MLAParams& p, int n_batches, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, cudaStream_t s);
 cudaError_t launch_fill_rows(void* out, bool half_type, float* lse, const int64_t* dims, const int64_t* out_strides,
                              const int64_t* lse_strides, const BatchInfo* batches, int mode, cudaStream_t s);
 

@@ -68,10 +68,12 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
   uint64_t* kv_empty = bars + 7;
   uint64_t* s_full = bars + 10;
   uint64_t* p_full = bars + 12;
+  // o_done[t & 1] completes when P_t V_t has been accumulated.  Two barriers
+  // alternate so the softmax may skip waits: each lags at most one phase.
   uint64_t* o_done = bars + 13;
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 15);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[blockIdx.x];
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
   }
 
   if (threadIdx.x == 0) {
+    if (blockIdx.x == 0) status_stamp(p.status);
     mbar_init(q_full, 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(&k_full[s], 1);
@@ -106,7 +109,8 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
     mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
           }
         }
         mma_commit(&kv_empty[s]);
-        mma_commit(o_done);
+        mma_commit(&o_done[jj & 1]);
         return true;
       };
       if (ok) {
@@ -246,28 +250,24 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
         for (int c = 0; c < 128; ++c)
           if (kv0 + c > lim) x[c] = -INFINITY;
       }
-      float mx = x[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
-      const float m_tile = mx * sl2;
+      const float m_tile = tree_max<128>(x) * sl2;
       const float m_new = fmaxf(m, m_tile);
       // Keep a stale max unless it grows by more than 8 (log2 units): p <= 2^8
       // stays exact in fp32 and representable in bf16/f16.
       const float m_use = (m == -INFINITY || m_new > m + 8.f) ? m_new : m;
       const float alpha = (m_use == m) ? 1.f : fast_exp2(m - m_use);
       const float mo = (m_use == -INFINITY) ? 0.f : m_use;
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float pv = fast_exp2(fmaf(x[c], sl2, -mo));
-        x[c] = pv;
-        sum += pv;
-      }
+      const float sum = exp2_and_sum<128>(x, sl2, mo);
       l = l * alpha + sum;
-      if (j > 0) {
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      // O only has to hold P_{j-1} V_{j-1} when this warp rescales it; the next
+      // P V accumulates after it on the tensor pipe anyway.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t u[32];
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
     }
     // ------------------------------------------------------------ epilogue
     if (ok && j > 0) {
-      ok = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status);
+      ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status);
       tc_fence_after();
     }
     if (ok) {

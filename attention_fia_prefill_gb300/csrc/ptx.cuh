@@ -65,19 +65,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Device status word of one call: (epoch << 8) | code, where the epoch is a
+// per-call number from the host.  The first CTA stamps (epoch << 8) when it
+// starts; an error raises the word with atomicMax, so the newest call's worst
+// code wins whatever order the writes land in, and no per-call reset is needed.
+struct DevStatus {
+  unsigned long long* word;
+  unsigned long long epoch;
+};
+
+__device__ __forceinline__ void status_stamp(const DevStatus& st) {
+  if (st.word != nullptr) atomicExch(st.word, st.epoch << 8);
+}
+
+__device__ __forceinline__ void status_raise(const DevStatus& st, unsigned code) {
+  if (st.word != nullptr) atomicMax(st.word, (st.epoch << 8) | code);
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (after recording the timeout) if the limit passes or another role of the CTA
-// has already given up (*abort != 0).
+// (after recording FIA_ERR_TIMEOUT) if the limit passes or another role of the
+// CTA has already given up (*abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+                                          const DevStatus& status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
+    if (abort != nullptr && *abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      if (status) atomicCAS(status, 0u, 10u /* FIA_ERR_TIMEOUT */);
+      if (abort != nullptr) *abort = 1;
+      status_raise(status, 10u /* FIA_ERR_TIMEOUT */);
       return false;
     }
   }
@@ -244,6 +261,38 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Maximum of x[0..N) with 8 independent accumulators (short dependency chains).
+template <int N>
+__device__ __forceinline__ float tree_max(const float* x) {
+  static_assert(N % 8 == 0, "N must be a multiple of 8");
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = x[k];
+#pragma unroll
+  for (int c = 8; c < N; c += 8)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = fmaxf(a[k], x[c + k]);
+  return fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+}
+
+// x[c] <- 2^(x[c] * sl2 - mo) in place; returns the sum (8 independent accumulators).
+template <int N>
+__device__ __forceinline__ float exp2_and_sum(float* x, float sl2, float mo) {
+  static_assert(N % 8 == 0, "N must be a multiple of 8");
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = 0.f;
+#pragma unroll
+  for (int c = 0; c < N; c += 8)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float y = fast_exp2(fmaf(x[c + k], sl2, -mo));
+      x[c + k] = y;
+      a[k] += y;
+    }
+  return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {

@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Benchmark of the fused inference attention library on one GB300 (or N replicas).
 
-Headline step: one fia_decode call (length resolution + split planning, the
-split-KV paged decode kernel and the LSE-combine kernel) on the paged GQA decode
+Headline step: one fia_decode call (length resolution + split planning on the
+host, then one split-KV paged decode kernel that also merges the partials of
+the splits with their LSE) on the paged GQA decode
 workload -- B=16, Q_N=32, KV_N=8, D=128, bf16, actual_seq_kvlen uniform on
 [1, 4096], block_size 128, random physical blocks.  value = KV bytes read per
 second (the K and V rows of every sequence, sum(L_b) * KV_N * D * 2 bytes * 2).
@@ -202,7 +203,7 @@ def measure_decode(torch, dev, timer, steps, warmup, pk, traffic):
 
     call_ms, kern_ms = timer.run(call, steps, warmup, kernel_events=True)
     res = {"call_ms": statistics.mean(call_ms), "kernel_ms": statistics.mean(kern_ms), "kv_bytes": kv_bytes,
-           "launches_per_step": 2}
+           "launches_per_step": 1}
     # end to end: pinned host inputs -> device, the call, result -> pinned host
     hq, hk, hv, ht = (t.pin_memory() for t in (c.q, c.k_pool, c.v_pool, c.block_table))
     ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()

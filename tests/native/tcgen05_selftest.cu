@@ -24,7 +24,7 @@ struct Maps {
 
 __global__ void __launch_bounds__(128, 1) selftest_kernel(const __grid_constant__ Maps m, int test,
                                                           const __nv_bfloat16* p_global, float* out,
-                                                          uint32_t* status) {
+                                                          unsigned long long* status) {
   extern __shared__ uint8_t raw[];
   uint8_t* smem = align_smem_1024(raw);
   uint8_t* sa = smem;            // A: up to 2 boxes of 16 KB
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(128, 1) selftest_kernel(const __grid_constant_
   __syncthreads();
   if (threadIdx.x == 0) {
     tc_fence_after();
-    bool ok = mbar_wait(&bars[0], 0, abort_flag, status);
+    bool ok = mbar_wait(&bars[0], 0, abort_flag, DevStatus{status, 1});
     if (ok) {
       tc_fence_after();
       const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(128, 1) selftest_kernel(const __grid_constant_
         }
       }
       mma_commit(&bars[1]);
-      mbar_wait(&bars[1], 0, abort_flag, status);
+      mbar_wait(&bars[1], 0, abort_flag, DevStatus{status, 1});
     }
   }
   __syncthreads();
@@ -159,22 +159,22 @@ extern "C" double fia_selftest_run(int test) {
   cudaMalloc(&da, ha.size() * 2);
   cudaMalloc(&db, 128 * b_cols * 2);
   cudaMalloc(&dout, 128 * 128 * 4);
-  cudaMalloc(&dstatus, 4);
+  cudaMalloc(&dstatus, 8);
   cudaMemcpy(da, ha.data(), ha.size() * 2, cudaMemcpyHostToDevice);
   cudaMemcpy(db, hb.data(), 128 * b_cols * 2, cudaMemcpyHostToDevice);
   cudaMemset(dout, 0, 128 * 128 * 4);
-  cudaMemset(dstatus, 0, 4);
+  cudaMemset(dstatus, 0, 8);
   Maps m;
   if (encode(fn, &m.a, da, K_a, 128) != CUDA_SUCCESS || encode(fn, &m.b, db, b_cols, 128) != CUDA_SUCCESS) return -2;
   const int smem = 65536 + 1024 + 1024;
   cudaFuncSetAttribute(selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   selftest_kernel<<<1, 128, smem>>>(m, test, static_cast<const __nv_bfloat16*>(da), static_cast<float*>(dout),
-                                    static_cast<uint32_t*>(dstatus));
+                                    static_cast<unsigned long long*>(dstatus));
   if (cudaDeviceSynchronize() != cudaSuccess) return -3;
   std::vector<float> out(128 * 128);
-  uint32_t st = 0;
+  unsigned long long st = 0;
   cudaMemcpy(out.data(), dout, out.size() * 4, cudaMemcpyDeviceToHost);
-  cudaMemcpy(&st, dstatus, 4, cudaMemcpyDeviceToHost);
+  cudaMemcpy(&st, dstatus, 8, cudaMemcpyDeviceToHost);
   cudaFree(da); cudaFree(db); cudaFree(dout); cudaFree(dstatus);
   if (st != 0) return -1e9;
   double maxerr = 0;

@@ -50,9 +50,10 @@ def test_block_sizes(fia, bs):
     _check_paged(fia, c)
 
 
-@pytest.mark.parametrize("n1,n2", [(4, 4), (6, 3), (6, 2), (16, 2), (24, 1)])
+@pytest.mark.parametrize("n1,n2", [(4, 4), (6, 3), (6, 2), (16, 2), (24, 1), (40, 1), (64, 1), (128, 2)])
 def test_group_sizes(fia, n1, n2):
-    """Head groups 1, 2, 3 (padded to 4), 8 and 24 (three blocks of 8)."""
+    """Head groups 1..64: a group's heads are the rows of one query tile (four
+    copies up to 32 heads, two copies above)."""
     c = fia_inputs.paged_decode_case(3, n1, n2, 128, [200, 1, 129], block_size=128, workload=2100 + n1)
     _check_paged(fia, c)
 
@@ -143,3 +144,11 @@ def test_device_status_ok(fia):
     ws = torch.empty(16 << 20, dtype=torch.uint8, device="cuda")
     _run_paged(fia, c, workspace=ws)
     assert fia.fia_device_status(ws) == 0
+
+
+def test_many_short_sequences(fia):
+    """Many units with one or two stages each: CTAs cross many unit boundaries
+    and merge partials of units they finish."""
+    lens = [1, 130, 2, 257, 0, 5, 129, 128, 64, 1000, 3, 300] * 3
+    c = fia_inputs.paged_decode_case(len(lens), 8, 2, 128, lens, block_size=128, workload=3000)
+    _check_paged(fia, c)
