@@ -22,10 +22,12 @@
 //     (3-deep ring, freed after P V) with 2-D TMA loads, one per page segment;
 //   * the CTA that completes a unit (a per-unit counter tagged with the call's
 //     epoch) merges the unit's partials in a fixed order -- deterministic, no
-//     float atomics -- and writes attention_out and softmax_lse.
+//     float atomics -- on its merge warp, off the softmax warps' path, and
+//     writes attention_out and softmax_lse.
 // Warps: 0..3 softmax (warp w = TMEM lanes 32w..32w+31), 4 K producer, 5 MMA
-// issuer and TMEM owner, 6 V producer.  TMEM columns: S0 [0,128),
-// S1 [128,256), O [256, 256+D), Q buffers [384, 384+D/2) and [384+D/2, 384+D).
+// issuer and TMEM owner, 6 V producer, 7 merge (unit counters and merges).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), Q buffers
+// [384, 384+D/2) and [384+D/2, 384+D).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -44,19 +46,29 @@ struct DecodeCfg {
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemUsed = kOffBar + kBarBytes + 1024;
   static constexpr int kSmem = kSmemUsed < 122880 ? 122880 : kSmemUsed;   // one CTA (and TMEM owner) per SM
-  static constexpr int kThreads = 224;
+  static constexpr int kThreads = 256;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kColQ = 384;
 };
 
+// Each group of MMAs (one Q K^T, one P V) ends with ONE tcgen05.commit -- a
+// second commit straight after the first does not wait for the MMAs -- so its
+// barrier serves every party that waits on it:
+//   qk_done[j % 4]: S_j is in TMEM (softmax) and K stage slot j % 4 is free
+//                   (K producer);
+//   pv_done[j % 3]: P_j V_j is accumulated in O (softmax rescale / epilogue)
+//                   and V stage slot j % 3 is free (V producer).
+// p_full[j & 1] takes the 128 softmax threads' arrivals for stage j.  A warp
+// may run one stage ahead of the others (S_{j+1} can be ready before every
+// warp has arrived for stage j), so consecutive stages use different
+// barriers; two stages ahead is impossible (S_{j+2} needs P_j V_j issued).
 struct DecodeBars {
-  uint64_t k_full[4], k_empty[4], v_full[3], v_empty[3];
-  uint64_t s_full[2], p_full, o_done[2], o_free, q_ready[2];
-  uint64_t part_done, merge_flag_ready, drain;
+  uint64_t k_full[4], qk_done[4], v_full[3], pv_done[3];
+  uint64_t p_full[2], o_free, q_ready[2];
+  uint64_t part_done[4], part_free[4];   // softmax -> merge warp hand-off ring
   uint32_t tmem_holder;
   int abort_flag;
-  int merge_is_last;
 };
 
 __device__ __forceinline__ const DecodeSeg* plan_segs(const DecodeParams& p) {
@@ -176,8 +188,90 @@ __device__ __forceinline__ void q_store(uint32_t taddr, const QRow<D>& q) {
   }
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One warp merges the partials of a finished unit, in sub-part order:
+// lse = log sum_k exp(lse_k), out = sum_k exp(lse_k - lse) O_k.  Four heads at
+// a time, lanes over D / 4 float4 columns; the loads of up to 32 sub-parts
+// are issued together so the merge costs a few L2 round trips.
 template <int D, bool BF16, int R>
-__global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+__device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2 up, int lane) {
+  const int g = p.group;
+  const int kvh = unit % p.num_kv_heads, b = unit / p.num_kv_heads;
+  const int64_t s0 = int64_t(up.x) * R;
+  const int ns = up.y * R;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  for (int h0 = 0; h0 < g; h0 += 4) {
+    float M[4], Ls[4];
+    float4 acc[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      M[t] = -INFINITY;
+      Ls[t] = 0.f;
+      acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int k0 = 0; k0 < ns; k0 += 32) {
+      const int kn = ns - k0 < 32 ? ns - k0 : 32;
+      float lk[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        lk[t] = (h0 + t < g && lane < kn) ? __ldcg(p.part_lse + (s0 + k0 + lane) * g + h0 + t) : -INFINITY;
+      // running max over the chunks; rescale what is accumulated so far
+      float wl[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float m_new = fmaxf(M[t], warp_max(lk[t]));
+        const float a = (m_new == -INFINITY) ? 1.f : __expf(M[t] - m_new);
+        acc[t].x *= a; acc[t].y *= a; acc[t].z *= a; acc[t].w *= a;
+        M[t] = m_new;
+        wl[t] = (lk[t] == -INFINITY) ? 0.f : __expf(lk[t] - m_new);
+        Ls[t] = Ls[t] * a + warp_sum(wl[t]);
+      }
+#pragma unroll 4
+      for (int k = 0; k < kn; ++k) {
+        float4 o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          o[t] = (h0 + t < g && lane < D / 4)
+                     ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + k0 + k) * g + h0 + t) * D) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float w = __shfl_sync(0xffffffffu, wl[t], k);
+          acc[t].x += w * o[t].x; acc[t].y += w * o[t].y; acc[t].z += w * o[t].z; acc[t].w += w * o[t].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int hh = h0 + t;
+      if (hh >= g) break;
+      const int head = kvh * g + hh;
+      if (lane < D / 4) {
+        const float inv = Ls[t] > 0.f ? 1.f / Ls[t] : 0.f;
+        T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * lane;
+        uint2 w2;
+        w2.x = pack2(acc[t].x * inv, acc[t].y * inv, BF16);
+        w2.y = pack2(acc[t].z * inv, acc[t].w * inv, BF16);
+        *reinterpret_cast<uint2*>(orow) = w2;
+      }
+      if (lane == 0 && p.lse != nullptr)
+        p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = Ls[t] > 0.f ? M[t] + __logf(Ls[t]) : INFINITY;
+    }
+  }
+}
+
+template <int D, bool BF16, int R>
+__global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D>;
   constexpr int KS = C::kKS, VS = C::kVS;
   constexpr int QD = 4 / R;            // TMEM lane quadrants (warps) per copy of the head rows
@@ -200,23 +294,21 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
     if (blockIdx.x == 0) status_stamp(p.status);
     for (int s = 0; s < KS; ++s) {
       mbar_init(&bar->k_full[s], 1);
-      mbar_init(&bar->k_empty[s], 1);
+      mbar_init(&bar->qk_done[s], 1);
     }
     for (int s = 0; s < VS; ++s) {
       mbar_init(&bar->v_full[s], 1);
-      mbar_init(&bar->v_empty[s], 1);
+      mbar_init(&bar->pv_done[s], 1);
     }
-    mbar_init(&bar->s_full[0], 1);
-    mbar_init(&bar->s_full[1], 1);
-    mbar_init(&bar->p_full, 128);
-    mbar_init(&bar->o_done[0], 1);
-    mbar_init(&bar->o_done[1], 1);
+    mbar_init(&bar->p_full[0], 128);
+    mbar_init(&bar->p_full[1], 128);
     mbar_init(&bar->o_free, 128);
     mbar_init(&bar->q_ready[0], 128);
     mbar_init(&bar->q_ready[1], 128);
-    mbar_init(&bar->part_done, 128);
-    mbar_init(&bar->merge_flag_ready, 1);
-    mbar_init(&bar->drain, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bar->part_done[s], 128);
+      mbar_init(&bar->part_free[s], 1);
+    }
     bar->abort_flag = 0;
     fence_mbar_init();
   }
@@ -230,9 +322,9 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
   const uint32_t tmem = bar->tmem_holder;
 
   if (warp == 4) {
-    decode_producer<D, KS>(p, &p.tm_k, smem + C::kOffK, bar->k_full, bar->k_empty, abort_flag, seg_begin, seg_end);
+    decode_producer<D, KS>(p, &p.tm_k, smem + C::kOffK, bar->k_full, bar->qk_done, abort_flag, seg_begin, seg_end);
   } else if (warp == 6) {
-    decode_producer<D, VS>(p, &p.tm_v, smem + C::kOffV, bar->v_full, bar->v_empty, abort_flag, seg_begin, seg_end);
+    decode_producer<D, VS>(p, &p.tm_v, smem + C::kOffV, bar->v_full, bar->pv_done, abort_flag, seg_begin, seg_end);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -241,11 +333,13 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
       int j = 0, segi = 0;
       bool ok = true;
+      uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
+      uint32_t last_parity = 0;
       auto issue_pv = [&](int jj, int first, int seg_index) -> bool {
         const int s = jj % VS;
         if (jj == first && seg_index > 0 && !mbar_wait(&bar->o_free, (seg_index - 1) & 1, abort_flag, p.status))
           return false;
-        if (!mbar_wait(&bar->p_full, jj & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&bar->p_full[jj & 1], (jj >> 1) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&bar->v_full[s], (jj / VS) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t vb = v_base + s * C::kTileBytes;
@@ -253,8 +347,9 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
         for (int kk = 0; kk < kTileN / 16; ++kk)
           mma_ts(tmem + C::kColO, tmem + (jj & 1) * 128 + kk * 8, smem_desc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
                  idesc_pv, (jj > first || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->v_empty[s]);
-        mma_commit(&bar->o_done[jj & 1]);
+        mma_commit(&bar->pv_done[s]);
+        last_bar = &bar->pv_done[s];
+        last_parity = (jj / VS) & 1;
         return true;
       };
       for (int si = seg_begin; si < seg_end && ok; ++si, ++segi) {
@@ -265,7 +360,7 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
         const int first = j;
         for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
           const int s = j % KS;
-          const int sb = j & 1;
+          const int sb = j & 1;   // S buffer
           if (!mbar_wait(&bar->k_full[s], (j / KS) & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kb = k_base + s * C::kTileBytes;
@@ -274,15 +369,67 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
             mma_ts(tmem + sb * 128, tmem + qcol + kk * 8,
                    smem_desc_sw128(kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024), idesc_qk,
                    kk > 0 ? 1u : 0u);
-          mma_commit(&bar->s_full[sb]);
-          mma_commit(&bar->k_empty[s]);
+          mma_commit(&bar->qk_done[s]);
+          last_bar = &bar->qk_done[s];
+          last_parity = (j / KS) & 1;
           if (j > first && !issue_pv(j - 1, first, segi)) { ok = false; break; }
         }
         if (!ok) break;
         if (j > first && !issue_pv(j - 1, first, segi)) { ok = false; break; }
       }
-      mma_commit(&bar->drain);
-      mbar_wait(&bar->drain, 0, nullptr, p.status);
+      // Every MMA issued has finished before TMEM goes: the latest commit
+      // tracks them all (the one before it on the same barrier has completed,
+      // so the barrier is at most one phase behind).
+      if (last_bar != nullptr) mbar_wait(last_bar, last_parity, nullptr, p.status);
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ merge warp
+    // After each segment's partials are out, bump the unit's counter; the CTA
+    // that finishes a unit merges it here, off the softmax warps' path.
+    bool ok = true;
+    const int nseg = seg_end - seg_begin;
+    for (int segi = 0; segi < nseg && ok; ++segi) {
+      const DecodeSeg sg = segs[seg_begin + segi];
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar->part_done[segi & 3], (segi >> 2) & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) mbar_arrive(&bar->part_free[segi & 3]);   // the slot may take segment segi + 4
+      __threadfence();
+      const int2 up = unit_parts[sg.unit];
+      int last = 0;
+      if (lane == 0) {
+        unsigned long long* ctr = p.unit_counter + sg.unit;
+        const unsigned long long tag = (p.status.epoch & 0xffffffffull) << 32;
+        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr), nxt, prev;
+        while (true) {
+          nxt = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : (tag | 1ull);
+          prev = atomicCAS(ctr, cur, nxt);
+          if (prev == cur) break;
+          cur = prev;
+        }
+        last = int(nxt & 0xffffffffull) == up.y;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence();
+        merge_unit<D, BF16, R>(p, sg.unit, up, lane);
+      }
+    }
+    // Units without any key (kv length 0): attention_out = 0, lse = +inf.
+    if (ok && blockIdx.x == 0) {
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      for (int u = 0; u < p.n_units; ++u) {
+        if (unit_parts[u].y != 0) continue;
+        const int kvh = u % p.num_kv_heads, b = u / p.num_kv_heads;
+        for (int hh = 0; hh < g; ++hh) {
+          const int head = kvh * g + hh;
+          if (lane < D / 4) {
+            T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * lane;
+            *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+          }
+          if (lane == 0 && p.lse != nullptr) p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = INFINITY;
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -327,7 +474,7 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
           const DecodeSeg sn = segs[seg_begin + segi + 1];
           q_load<D>(p, sn.unit / p.num_kv_heads, sn.unit % p.num_kv_heads, h, qn);
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar->s_full[sb], (j >> 1) & 1, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar->qk_done[j % KS], (j / KS) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }
@@ -338,15 +485,17 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
           tc_fence_before();
           mbar_arrive(&bar->q_ready[(segi + 1) & 1]);
         }
+        uint32_t su[CW / 32][32];
+#pragma unroll
+        for (int c = 0; c < CW / 32; ++c) tmem_ld32(tmem + lane_off + sb * 128 + c0 + c * 32, su[c]);
+        tmem_wait_ld(su[0]);
+#pragma unroll
+        for (int c = 1; c < CW / 32; ++c) tmem_regs_after_wait(su[c]);
         float x[CW];
 #pragma unroll
-        for (int c = 0; c < CW / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_off + sb * 128 + c0 + c * 32, u);
+        for (int c = 0; c < CW / 32; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
-        }
-        tmem_wait_ld();
+          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(su[c][e]);
         const int nvalid = min(128, L - st * 128);
         if (nvalid < c0 + CW) {
 #pragma unroll
@@ -361,7 +510,7 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
         l = l * alpha + sum;
         if (j > first && __any_sync(0xffffffffu, alpha != 1.f)) {
           if (!__all_sync(0xffffffffu,
-                          mbar_wait(&bar->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status))) {
+                          mbar_wait(&bar->pv_done[(j - 1) % VS], ((j - 1) / VS) & 1, abort_flag, p.status))) {
             ok = false;
             break;
           }
@@ -370,7 +519,7 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
           for (int c = 0; c < D / 32; ++c) {
             uint32_t u[32];
             tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
-            tmem_wait_ld();
+            tmem_wait_ld(u);
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
             tmem_st32(tmem + lane_off + C::kColO + c * 32, u);
@@ -415,106 +564,53 @@ __global__ void __launch_bounds__(224, 1) decode_kernel(const __grid_constant__ 
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bar->p_full);
+        mbar_arrive(&bar->p_full[j & 1]);
         m = m_use;
       }
       if (!ok) break;
       // ---- segment epilogue: one partial (O / l, lse) per (copy, head)
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(&bar->o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status))) {
+                      mbar_wait(&bar->pv_done[(j - 1) % VS], ((j - 1) / VS) & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float ov[D];
+      const bool has = l > 0.f;
+      const float inv_l = has ? 1.f / l : 0.f;
+      const int64_t sub = int64_t(sg.part) * R + cp;
+      float* po = p.part_o + (sub * g + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
         tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) ov[c * 32 + e] = __uint_as_float(u[e]);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bar->o_free);     // the next segment's first P V may overwrite O now
-      const bool has = l > 0.f;
-      const float inv_l = has ? 1.f / l : 0.f;
-      const int64_t sub = int64_t(sg.part) * R + cp;
-      if (h < g) {
-        float* po = p.part_o + (sub * g + h) * D;
-#pragma unroll
-        for (int q = 0; q < D / 4; ++q)
-          *reinterpret_cast<float4*>(po + 4 * q) =
-              has ? make_float4(ov[4 * q] * inv_l, ov[4 * q + 1] * inv_l, ov[4 * q + 2] * inv_l, ov[4 * q + 3] * inv_l)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-        p.part_lse[sub * g + h] = has ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-      }
-      // ---- the CTA that completes the unit merges its partials
-      __threadfence();
-      mbar_arrive(&bar->part_done);
-      if (threadIdx.x == 0) {
-        ok = mbar_wait(&bar->part_done, segi & 1, abort_flag, p.status);
-        unsigned long long* ctr = p.unit_counter + sg.unit;
-        const unsigned long long tag = (p.status.epoch & 0xffffffffull) << 32;
-        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr), nxt, prev;
-        while (true) {
-          nxt = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : (tag | 1ull);
-          prev = atomicCAS(ctr, cur, nxt);
-          if (prev == cur) break;
-          cur = prev;
+        tmem_wait_ld(u);
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bar->o_free);     // the next segment's first P V may overwrite O now
         }
-        bar->merge_is_last = (int(nxt & 0xffffffffull) == unit_parts[sg.unit].y) ? 1 : 0;
-        mbar_arrive(&bar->merge_flag_ready);
+        if (h < g) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(po + c * 32 + 4 * q) =
+                has ? make_float4(__uint_as_float(u[4 * q]) * inv_l, __uint_as_float(u[4 * q + 1]) * inv_l,
+                                  __uint_as_float(u[4 * q + 2]) * inv_l, __uint_as_float(u[4 * q + 3]) * inv_l)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar->merge_flag_ready, segi & 1, abort_flag, p.status))) {
+      if (h < g) p.part_lse[sub * g + h] = has ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      // The partials must be visible to whichever CTA merges the unit: a
+      // device-scope fence by the writing thread before it signals.
+      __threadfence();
+      // hand the segment to the merge warp through a 4-slot ring; a slot is
+      // reused only after the merge warp has taken its previous segment
+      if (segi >= 4 &&
+          !__all_sync(0xffffffffu, mbar_wait(&bar->part_free[segi & 3], ((segi >> 2) - 1) & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
-      if (bar->merge_is_last) {
-        __threadfence();
-        const int2 up = unit_parts[sg.unit];
-        const int64_t s0 = int64_t(up.x) * R, ns = int64_t(up.y) * R;
-        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-        for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
-          const int hh = idx / (D / 4), d4 = idx % (D / 4);
-          float M = -INFINITY;
-          for (int64_t k = 0; k < ns; ++k) M = fmaxf(M, __ldcg(p.part_lse + (s0 + k) * g + hh));
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          float Ls = 0.f;
-          if (M != -INFINITY) {
-            for (int64_t k = 0; k < ns; ++k) {
-              const float w = __expf(__ldcg(p.part_lse + (s0 + k) * g + hh) - M);
-              const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + k) * g + hh) * D) + d4);
-              Ls += w;
-              acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-            }
-          }
-          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-          const int head = kvh * g + hh;
-          T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * d4;
-          uint2 w2;
-          w2.x = pack2(acc.x * inv, acc.y * inv, BF16);
-          w2.y = pack2(acc.z * inv, acc.w * inv, BF16);
-          *reinterpret_cast<uint2*>(orow) = w2;
-          if (d4 == 0 && p.lse != nullptr)
-            p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = Ls > 0.f ? M + __logf(Ls) : INFINITY;
-        }
-      }
-    }
-    // Units without any key (kv length 0): attention_out = 0, lse = +inf.
-    if (ok && blockIdx.x == 0) {
-      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      for (int u = 0; u < p.n_units; ++u) {
-        if (unit_parts[u].y != 0) continue;
-        const int kvh = u % p.num_kv_heads, b = u / p.num_kv_heads;
-        for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
-          const int hh = idx / (D / 4), d4 = idx % (D / 4);
-          const int head = kvh * g + hh;
-          T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * d4;
-          *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
-          if (d4 == 0 && p.lse != nullptr) p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = INFINITY;
-        }
-      }
+      mbar_arrive(&bar->part_done[segi & 3]);      // release: the merge warp takes over
+      (void)kvh;
+      (void)b;
     }
   }
 

@@ -764,7 +764,7 @@ void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl) {
     return;
   }
   double cap = (double(T) + kSegmentCost * double(nonempty + max_cta - 1)) / max_cta;
-  for (int attempt = 0; attempt < 200; ++attempt, cap *= 1.02) {
+  for (int attempt = 0; attempt < 1000; ++attempt, cap *= 1.005) {
     pl.segs.clear();
     pl.cta_seg.assign(1, 0);
     int c = 0;

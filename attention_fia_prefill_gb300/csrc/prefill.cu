@@ -9,12 +9,13 @@
 //   warp 0      TMA producer: Q once, then K/V tiles through a ring of stages
 //   warp 1      MMA issuer (one thread) and TMEM owner:
 //                 S_j = Q K_j^T   (tcgen05, SS, fp32 accumulator in TMEM)
-//                 O  += P_j V_j   (tcgen05, P read from TMEM or shared memory)
+//                 O  += P_j V_j   (tcgen05, P read from TMEM)
 //   warps 2..5  softmax: one thread per query row (= TMEM lane); reads S_j from
 //               TMEM, masks, keeps the running max/sum in registers, writes P_j
 //               (bf16/f16), rescales O in TMEM when the max grows by more than
 //               2^8, and runs the epilogue (O / l, LSE).
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256 + D).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256 + D); P_j overwrites
+// the first 64 columns of S_j as packed 16-bit pairs.
 // Shared memory tiles are 128 rows x 128 bytes boxes with the 128-byte swizzle
 // that both TMA and the tcgen05 shared-memory descriptors understand.
 #include "internal.h"
@@ -22,18 +23,16 @@
 
 namespace fia {
 
-template <int D, bool P_TMEM>
+template <int D>
 struct PrefillCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kBoxBytes = 128 * 128;
   static constexpr int kTileBytes = kChunks * kBoxBytes;
-  static constexpr int kStages = (D == 128 && !P_TMEM) ? 2 : 3;
-  static constexpr int kPBytes = P_TMEM ? 0 : 2 * kBoxBytes;
+  static constexpr int kStages = 3;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemUsed = kOffBar + kBarBytes + 1024;
   // at least ~120 KB so that a second CTA never shares the SM (and its TMEM)
@@ -55,9 +54,9 @@ struct TileIter {
   }
 };
 
-template <int D, bool BF16, int MODE, bool P_TMEM>
+template <int D, bool BF16, int MODE>
 __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using C = PrefillCfg<D, P_TMEM>;
+  using C = PrefillCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -65,13 +64,16 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = bars + 4;
-  uint64_t* kv_empty = bars + 7;
+  // pv_done[s] completes each time P_t V_t of a tile t in stage s has been
+  // accumulated: it frees the stage for the producer and tells the softmax
+  // that O is up to date.  One tcgen05.commit per group of MMAs -- a second
+  // commit straight after the first does not wait for them.
+  uint64_t* pv_done = bars + 7;
   uint64_t* s_full = bars + 10;
+  // p_full[t & 1] takes the 128 softmax threads' arrivals for tile t: a warp
+  // may run one tile ahead of the others (S_{t+1} can be ready before every
+  // warp has arrived for tile t), never two (S_{t+2} needs P_t V_t issued).
   uint64_t* p_full = bars + 12;
-  // o_done[t & 1] completes when P_t V_t has been accumulated.  Two barriers
-  // alternate so the softmax may skip waits: each lags at most one phase.
-  uint64_t* o_done = bars + 13;
-  uint64_t* drain = bars + 15;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
 
@@ -104,14 +106,12 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
     for (int s = 0; s < 3; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&pv_done[s], 1);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 128);
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
-    mbar_init(drain, 1);
+    mbar_init(&p_full[0], 128);
+    mbar_init(&p_full[1], 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
       int j = 0;
       for (int t = iter.next(-1); t >= 0; t = iter.next(t), ++j) {
         const int s = j % S;
-        if (j >= S && !mbar_wait(&kv_empty[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
+        if (j >= S && !mbar_wait(&pv_done[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
         uint8_t* ks = smem + C::kOffK + s * C::kTileBytes;
         uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
@@ -171,9 +171,11 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
       int j = 0;
+      uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
+      uint32_t last_parity = 0;
       auto issue_pv = [&](int jj) -> bool {
         const int s = jj % S;
-        if (!mbar_wait(p_full, jj & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&p_full[jj & 1], (jj >> 1) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&v_full[s], (jj / S) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t v_base = smem_u32(smem + C::kOffV + s * C::kTileBytes);
@@ -183,16 +185,11 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
           // of 16 keys is 16 rows = 2048 bytes; the next 64 columns of D sit
           // one 16 KB box further (leading byte offset).
           const uint64_t bdesc = smem_desc_sw128(v_base + kk * 2048, C::kBoxBytes, 1024);
-          if constexpr (P_TMEM) {
-            mma_ts(tmem + C::kColO, tmem + (jj & 1) * 128 + kk * 8, bdesc, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-          } else {
-            const uint32_t p_base = smem_u32(smem + C::kOffP);
-            const uint64_t adesc = smem_desc_sw128(p_base + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024);
-            mma_ss(tmem + C::kColO, adesc, bdesc, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
+          mma_ts(tmem + C::kColO, tmem + (jj & 1) * 128 + kk * 8, bdesc, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&kv_empty[s]);
-        mma_commit(&o_done[jj & 1]);
+        mma_commit(&pv_done[s]);
+        last_bar = &pv_done[s];
+        last_parity = (jj / S) & 1;
         return true;
       };
       if (ok) {
@@ -210,13 +207,16 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
             mma_ss(tmem + sb * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&s_full[sb]);
+          last_bar = &s_full[sb];
+          last_parity = (j >> 1) & 1;
           if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
         }
         if (ok && j >= 1) issue_pv(j - 1);
       }
-      // Wait until every MMA this thread issued has finished before TMEM goes.
-      mma_commit(drain);
-      mbar_wait(drain, 0, nullptr, p.status);
+      // Every MMA this thread issued has finished before TMEM goes: the latest
+      // commit tracks them all (the one before it has completed, so its barrier
+      // is at most one phase behind).
+      if (last_bar != nullptr) mbar_wait(last_bar, last_parity, nullptr, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -232,15 +232,17 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
       const int sb = j & 1;
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
+      uint32_t su[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + sb * 128 + c * 32, su[c]);
+      tmem_wait_ld(su[0]);
+#pragma unroll
+      for (int c = 1; c < 4; ++c) tmem_regs_after_wait(su[c]);
       float x[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_off + sb * 128 + c * 32, u);
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
-      }
-      tmem_wait_ld();
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(su[c][e]);
       const int kv0 = t * kTileN;
       const bool ragged = kv0 + kTileN > bi.kv_len;
       const bool need_mask = ragged || (MODE == kCausal && kv0 + kTileN - 1 > q0 + diag_off);
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
       // O only has to hold P_{j-1} V_{j-1} when this warp rescales it; the next
       // P V accumulates after it on the tensor pipe anyway.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) % S], ((j - 1) / S) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }
@@ -272,33 +274,19 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
           for (int c = 0; c < D / 32; ++c) {
             uint32_t u[32];
             tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
-            tmem_wait_ld();
+            tmem_wait_ld(u);
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
             tmem_st32(tmem + lane_off + C::kColO + c * 32, u);
           }
         }
       }
-      if constexpr (P_TMEM) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t u[32];
+      for (int c = 0; c < 2; ++c) {
+        uint32_t u[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) u[e] = pack2(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1], BF16);
-          tmem_st32(tmem + lane_off + sb * 128 + c * 32, u);
-        }
-      } else {
-        uint8_t* pb = smem + C::kOffP;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint4 w;
-          w.x = pack2(x[8 * q + 0], x[8 * q + 1], BF16);
-          w.y = pack2(x[8 * q + 2], x[8 * q + 3], BF16);
-          w.z = pack2(x[8 * q + 4], x[8 * q + 5], BF16);
-          w.w = pack2(x[8 * q + 6], x[8 * q + 7], BF16);
-          const int box = q >> 3, qq = q & 7;
-          *reinterpret_cast<uint4*>(pb + box * C::kBoxBytes + r * 128 + ((qq ^ (r & 7)) << 4)) = w;
-        }
+        for (int e = 0; e < 32; ++e) u[e] = pack2(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1], BF16);
+        tmem_st32(tmem + lane_off + sb * 128 + c * 32, u);
       }
       if (ragged) {
         // Rows of V past the batch's keys may hold anything (even NaN); P is 0
@@ -314,15 +302,15 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
               *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      if constexpr (P_TMEM) tmem_wait_st();
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[j & 1]);
       m = m_use;
     }
     // ------------------------------------------------------------ epilogue
     if (ok && j > 0) {
-      ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status);
+      ok = mbar_wait(&pv_done[(j - 1) % S], ((j - 1) / S) & 1, abort_flag, p.status);
       tc_fence_after();
     }
     if (ok) {
@@ -338,7 +326,7 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
         uint32_t u[32];
         if (j > 0) {
           tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
-          tmem_wait_ld();
+          tmem_wait_ld(u);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) u[e] = 0u;
@@ -374,29 +362,23 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
   }
 }
 
-template <int D, bool BF16, int MODE, bool P_TMEM>
+template <int D, bool BF16, int MODE>
 static cudaError_t launch_one(const PrefillParams& p, cudaStream_t s) {
-  using C = PrefillCfg<D, P_TMEM>;
-  auto k = prefill_kernel<D, BF16, MODE, P_TMEM>;
+  using C = PrefillCfg<D>;
+  auto k = prefill_kernel<D, BF16, MODE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   k<<<p.n_items, C::kThreads, C::kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
-#ifndef FIA_P_IN_SMEM
-constexpr bool kPInTmem = true;
-#else
-constexpr bool kPInTmem = false;
-#endif
-
 cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
 #define FIA_DISPATCH_MODE(DD, BB)                                                            \
   switch (mode) {                                                                          \
-    case kDense: return launch_one<DD, BB, kDense, kPInTmem>(p, s);                        \
-    case kCausal: return launch_one<DD, BB, kCausal, kPInTmem>(p, s);                      \
-    case kBlockSparse: return launch_one<DD, BB, kBlockSparse, kPInTmem>(p, s);            \
+    case kDense: return launch_one<DD, BB, kDense>(p, s);                        \
+    case kCausal: return launch_one<DD, BB, kCausal>(p, s);                      \
+    case kBlockSparse: return launch_one<DD, BB, kBlockSparse>(p, s);            \
     default: return cudaErrorInvalidValue;                                                 \
   }
   if (head_dim == 128) {

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(128, 1) selftest_kernel(const __grid_constant_
     for (int c = 0; c < 4; ++c) {
       uint32_t u[32];
       tmem_ld32(tmem + (uint32_t(32 * warp) << 16) + c * 32, u);
-      tmem_wait_ld();
+      tmem_wait_ld(u);
       const int r = 32 * warp + lane;
       for (int e = 0; e < 32; ++e) out[r * 128 + c * 32 + e] = __uint_as_float(u[e]);
     }
