@@ -201,10 +201,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // One warp merges the partials of a finished unit, in sub-part order:
 // lse = log sum_k exp(lse_k), out = sum_k exp(lse_k - lse) O_k.  Four heads at
-// a time, lanes over D / 4 float4 columns; the loads of up to 32 sub-parts
-// are issued together so the merge costs a few L2 round trips.
+// a time, lanes over D / 4 float4 columns; the lse values and the O rows of
+// eight sub-parts are loaded together, so a merge costs few L2 round trips.
 template <int D, bool BF16, int R>
 __device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2 up, int lane) {
+  constexpr int KB = 8;   // sub-parts per batch of loads
   const int g = p.group;
   const int kvh = unit % p.num_kv_heads, b = unit / p.num_kv_heads;
   const int64_t s0 = int64_t(up.x) * R;
@@ -219,13 +220,21 @@ __device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2
       Ls[t] = 0.f;
       acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int k0 = 0; k0 < ns; k0 += 32) {
-      const int kn = ns - k0 < 32 ? ns - k0 : 32;
+    for (int k0 = 0; k0 < ns; k0 += KB) {
+      const int kn = ns - k0 < KB ? ns - k0 : KB;
       float lk[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t)
         lk[t] = (h0 + t < g && lane < kn) ? __ldcg(p.part_lse + (s0 + k0 + lane) * g + h0 + t) : -INFINITY;
-      // running max over the chunks; rescale what is accumulated so far
+      float4 o[KB][4];
+#pragma unroll
+      for (int k = 0; k < KB; ++k)
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          o[k][t] = (k < kn && h0 + t < g && lane < D / 4)
+                        ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + k0 + k) * g + h0 + t) * D) + lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      // running max over the batches; rescale what is accumulated so far
       float wl[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -236,20 +245,13 @@ __device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2
         wl[t] = (lk[t] == -INFINITY) ? 0.f : __expf(lk[t] - m_new);
         Ls[t] = Ls[t] * a + warp_sum(wl[t]);
       }
-#pragma unroll 4
-      for (int k = 0; k < kn; ++k) {
-        float4 o[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          o[t] = (h0 + t < g && lane < D / 4)
-                     ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + k0 + k) * g + h0 + t) * D) + lane)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < KB; ++k)
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float w = __shfl_sync(0xffffffffu, wl[t], k);
-          acc[t].x += w * o[t].x; acc[t].y += w * o[t].y; acc[t].z += w * o[t].z; acc[t].w += w * o[t].w;
+          acc[t].x += w * o[k][t].x; acc[t].y += w * o[k][t].y; acc[t].z += w * o[k][t].z; acc[t].w += w * o[k][t].w;
         }
-      }
     }
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -416,9 +418,11 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       }
     }
     // Units without any key (kv length 0): attention_out = 0, lse = +inf.
-    if (ok && blockIdx.x == 0) {
+    // Spread over the CTAs: a serial walk over every unit's plan entry in
+    // one CTA would hold the whole launch back.
+    if (ok) {
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      for (int u = 0; u < p.n_units; ++u) {
+      for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
         if (unit_parts[u].y != 0) continue;
         const int kvh = u % p.num_kv_heads, b = u / p.num_kv_heads;
         for (int hh = 0; hh < g; ++hh) {
@@ -456,12 +460,73 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       mbar_arrive(&bar->q_ready[k]);
     }
 
+    // A segment's epilogue (read O, write the partial) runs after the next
+    // segment's first stage: by then the segment's last P V has completed
+    // (it was issued before that stage's Q K^T), so nothing waits for it.
+    // That stage never touches O, and the next P V waits for o_free.  The
+    // partial is handed to the merge warp one stage later again, so the
+    // device-scope fence that makes it visible to other CTAs overlaps work.
+    struct Pending {
+      int segi, part, jlast;
+      float m, l;
+    };
+    Pending epi{-1, 0, 0, 0.f, 0.f};
+    int rel = -1;
+    auto release = [&](int sidx) -> bool {
+      __threadfence();
+      // 4-slot ring: a slot is reused only after the merge warp took its
+      // previous segment
+      if (sidx >= 4 &&
+          !__all_sync(0xffffffffu, mbar_wait(&bar->part_free[sidx & 3], ((sidx >> 2) - 1) & 1, abort_flag, p.status)))
+        return false;
+      mbar_arrive(&bar->part_done[sidx & 3]);
+      return true;
+    };
+    // one partial (O / l, lse) per (copy, head) of segment epi.segi
+    auto epilogue = [&]() -> bool {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&bar->pv_done[epi.jlast % VS], (epi.jlast / VS) & 1, abort_flag, p.status)))
+        return false;
+      tc_fence_after();
+      const bool has = epi.l > 0.f;
+      const float inv_l = has ? 1.f / epi.l : 0.f;
+      const int64_t sub = int64_t(epi.part) * R + cp;
+      float* po = p.part_o + (sub * g + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
+        tmem_wait_ld(u);
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bar->o_free);     // the next segment's first P V may overwrite O now
+        }
+        if (h < g) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(po + c * 32 + 4 * q) =
+                has ? make_float4(__uint_as_float(u[4 * q]) * inv_l, __uint_as_float(u[4 * q + 1]) * inv_l,
+                                  __uint_as_float(u[4 * q + 2]) * inv_l, __uint_as_float(u[4 * q + 3]) * inv_l)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (h < g) p.part_lse[sub * g + h] = has ? (epi.m + __log2f(epi.l)) * 0.69314718055994531f : -INFINITY;
+      rel = epi.segi;
+      epi.segi = -1;
+      return true;
+    };
+    // work deferred from earlier segments, done after a stage's P is handed over
+    auto catch_up = [&]() -> bool {
+      if (rel >= 0) {
+        if (!release(rel)) return false;
+        rel = -1;
+      }
+      return epi.segi < 0 || epilogue();
+    };
     int j = 0;
     for (int segi = 0; segi < nseg && ok; ++segi) {
       const DecodeSeg sg = segs[seg_begin + segi];
-      const int kvh = sg.unit % p.num_kv_heads;
-      const int b = sg.unit / p.num_kv_heads;
-      const int L = kvlen[b];
+      const int L = kvlen[sg.unit / p.num_kv_heads];
       const int first = j;
       float m = -INFINITY, l = 0.f;
       for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
@@ -562,56 +627,20 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           }
         }
         tmem_wait_st();
-        fence_proxy_async_smem();
+        if (nvalid < 128) fence_proxy_async_smem();   // the cleared V rows, for the tensor core
         tc_fence_before();
         mbar_arrive(&bar->p_full[j & 1]);
         m = m_use;
+        if (!catch_up()) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) break;
-      // ---- segment epilogue: one partial (O / l, lse) per (copy, head)
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(&bar->pv_done[(j - 1) % VS], ((j - 1) / VS) & 1, abort_flag, p.status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const bool has = l > 0.f;
-      const float inv_l = has ? 1.f / l : 0.f;
-      const int64_t sub = int64_t(sg.part) * R + cp;
-      float* po = p.part_o + (sub * g + h) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_off + C::kColO + c * 32, u);
-        tmem_wait_ld(u);
-        if (c == D / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(&bar->o_free);     // the next segment's first P V may overwrite O now
-        }
-        if (h < g) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(po + c * 32 + 4 * q) =
-                has ? make_float4(__uint_as_float(u[4 * q]) * inv_l, __uint_as_float(u[4 * q + 1]) * inv_l,
-                                  __uint_as_float(u[4 * q + 2]) * inv_l, __uint_as_float(u[4 * q + 3]) * inv_l)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-      if (h < g) p.part_lse[sub * g + h] = has ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-      // The partials must be visible to whichever CTA merges the unit: a
-      // device-scope fence by the writing thread before it signals.
-      __threadfence();
-      // hand the segment to the merge warp through a 4-slot ring; a slot is
-      // reused only after the merge warp has taken its previous segment
-      if (segi >= 4 &&
-          !__all_sync(0xffffffffu, mbar_wait(&bar->part_free[segi & 3], ((segi >> 2) - 1) & 1, abort_flag, p.status))) {
-        ok = false;
-        break;
-      }
-      mbar_arrive(&bar->part_done[segi & 3]);      // release: the merge warp takes over
-      (void)kvh;
-      (void)b;
+      epi = Pending{segi, sg.part, j - 1, m, l};
     }
+    if (ok) ok = catch_up();
+    if (ok && rel >= 0) release(rel);
   }
 
   tc_fence_before();

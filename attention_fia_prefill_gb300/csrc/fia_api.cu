@@ -739,13 +739,15 @@ struct DecodePlan {
 };
 
 // Charge, in 128-token stages, for every unit a CTA starts: loading the unit's
-// query rows and writing and merging its partials.
-constexpr double kSegmentCost = 0.5;
+// query rows, draining the pipeline and writing its partials.
+constexpr double kSegmentCost = 1.0;
 
 // Deals the stages of all units (unit order = batch-major, then kv head) to at
 // most n_sm CTAs so that every CTA carries about the same cost: one per stage
 // plus kSegmentCost per segment.  Greedy fill against a capacity that grows
-// until the stages fit the CTAs.
+// until the stages fit the CTAs.  Within a CTA, the pieces of units that other
+// CTAs share go first: the CTA that completes a unit merges it, and a split
+// unit finished early is merged while the CTA still streams, not at its end.
 void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl) {
   pl.n_units = int(g.B * g.N2);
   std::vector<int32_t> nst(size_t(pl.n_units));
@@ -792,6 +794,9 @@ void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl) {
     if (fits) {
       pl.cta_seg.push_back(int32_t(pl.segs.size()));
       pl.n_cta = int(pl.cta_seg.size()) - 1;
+      for (int c = 0; c < pl.n_cta; ++c)
+        std::stable_partition(pl.segs.begin() + pl.cta_seg[size_t(c)], pl.segs.begin() + pl.cta_seg[size_t(c) + 1],
+                              [&](const DecodeSeg& sg) { return pl.unit_parts[size_t(sg.unit)].y > 1; });
       return;
     }
   }
