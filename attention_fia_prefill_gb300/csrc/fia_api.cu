@@ -729,7 +729,6 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
 }
 
 // Copies of the group's head rows in the decode kernel's 128-row query tile.
-int decode_copies(int64_t group) { return group <= 32 ? 4 : 2; }
 
 struct DecodePlan {
   std::vector<DecodeSeg> segs;
@@ -836,7 +835,7 @@ bool plan_fits_inline(size_t n_segs, size_t n_cta, size_t n_units, size_t B) {
 size_t decode_ws_bound(const DecodeGeometry& g) {
   const size_t n_units = size_t(g.B * g.N2);
   const size_t n_segs = n_units + kMaxDecodeCtas;
-  const size_t rows = size_t(g.N1 / g.N2) * size_t(decode_copies(g.N1 / g.N2));
+  const size_t rows = size_t(g.N1 / g.N2);
   return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), rows, size_t(g.D), true).total;
 }
 
@@ -883,8 +882,7 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   cudaStream_t stream_t = static_cast<cudaStream_t>(stream);
   DecodePlan pl;
   plan_decode(g, sm_count(), pl);
-  const int copies = decode_copies(g.N1 / g.N2);
-  const size_t rows = size_t(g.N1 / g.N2) * size_t(copies);
+  const size_t rows = size_t(g.N1 / g.N2);
   const bool inl = plan_fits_inline(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B));
   const DecodeWsLayout w = decode_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B), rows,
                                             size_t(g.D), !inl);
@@ -962,7 +960,6 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   dp.num_heads = int(g.N1);
   dp.num_kv_heads = int(g.N2);
   dp.group = int(g.N1 / g.N2);
-  dp.copies = copies;
   dp.scale_log2 = float(params->scale_value * 1.4426950408889634);
   dp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
   return cuda_check(profiled(stream_t, [&] { return launch_decode(dp, int(g.D), g.bf16, stream_t); }),

@@ -45,7 +45,8 @@ struct PrefillParams {
 // Paged / contiguous decode (Q_S = 1).  A unit is (batch, kv head).  Every
 // unit's keys are cut into 128-token stages; the stages of all units, in unit
 // order, are dealt out to the CTAs (one per SM), so a CTA may end one unit and
-// start the next: each such piece is a "segment".
+// start the next: each such piece is a "segment", and each segment leaves one
+// partial (O / l, lse) per query head of the unit.
 struct DecodeSeg {
   int32_t unit, stage_begin, stage_end, part;   // part = global segment index
 };
@@ -78,12 +79,11 @@ struct DecodeParams {
   int64_t out_sb, out_sn;
   float* lse;                     // nullable
   int64_t lse_sb, lse_sn;
-  float* part_o;                  // [n_segments * copies, group, D]
-  float* part_lse;                // [n_segments * copies, group] natural log, -inf = empty
+  float* part_o;                  // [n_segments, group, D]
+  float* part_lse;                // [n_segments, group] natural log, -inf = empty
   unsigned long long* unit_counter;   // [n_units] (epoch << 32) | segments finished
   int n_cta, n_units;
   int batch, num_heads, num_kv_heads, group;
-  int copies;                     // copies of the head rows in the query tile (4 or 2)
   float scale_log2;
   DevStatus status;
   int plan_inline;                // 1: the plan below; 0: the pointers
