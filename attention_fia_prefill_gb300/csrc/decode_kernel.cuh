@@ -81,7 +81,7 @@ struct DecodeCfg {
 // barrier serves every party that waits on it:
 //   qk_done[j % KS]: S^T_j is in TMEM (softmax) and K slot j % KS is free;
 //   pv_done[j % VS]: O^T_j is in TMEM (softmax) and V slot j % VS is free.
-// p_full[j & 1]: the softmax threads' P^T_j is in shared memory.
+// p_full[j & 1]: the softmax warps' P^T_j is in shared memory.
 // sync[j & 1]: the four softmax warps' maxima and votes of stage j are in.
 // esync[s & 1]: the warps' sums of segment s are in (epilogue).
 struct DecodeBars {
@@ -120,13 +120,22 @@ __device__ __forceinline__ void decode_producer(const DecodeParams& p, const CUt
   if (lane == 0) tma_prefetch_desc(tm);
   int j = 0;
   bool ok = true;
+  int pf_base = -64;          // page ids of the next segment, loaded one segment early
+  int32_t pf_blk = 0;
   for (int si = seg_begin; si < seg_end && ok; ++si) {
     const DecodeSeg sg = segs[si];
     const int kvh = sg.unit % p.num_kv_heads;
     const int b = sg.unit / p.num_kv_heads;
     const int L = kvlen[b];
-    int cache_base = -64;     // first page index held by the lanes' cache
-    int32_t cache_blk = 0;    // lane i holds block_table[b][cache_base + i]
+    int cache_base = pf_base;   // first page index held by the lanes' cache
+    int32_t cache_blk = pf_blk; // lane i holds block_table[b][cache_base + i]
+    pf_base = -64;
+    if (p.block_table != nullptr && si + 1 < seg_end) {
+      const DecodeSeg sn = segs[si + 1];
+      pf_base = (sn.stage_begin * 128) / p.block_size;
+      const int e = pf_base + lane;
+      pf_blk = e < p.table_stride ? p.block_table[int64_t(sn.unit / p.num_kv_heads) * p.table_stride + e] : 0;
+    }
     for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
       const int s = j % NS;
       if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((j / NS) - 1) & 1, abort_flag, p.status))) {
@@ -169,6 +178,14 @@ __device__ __forceinline__ void decode_producer(const DecodeParams& p, const CUt
       mbar_wait(&full[s], (last / NS) & 1, nullptr, p.status);
     }
   }
+}
+
+// One arrival per softmax warp: the warp barrier orders every lane's earlier
+// writes before lane 0's (releasing) arrive, and four arrivals instead of 128
+// keep the barrier traffic off the per-stage path.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -364,14 +381,14 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       mbar_init(&bar->qk_done[s], 1);
       mbar_init(&bar->v_full[s], 1);
       mbar_init(&bar->pv_done[s], 1);
-      mbar_init(&bar->part_done[s], 128);
+      mbar_init(&bar->part_done[s], 4);
       mbar_init(&bar->part_free[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar->p_full[s], 128);
-      mbar_init(&bar->q_ready[s], 128);
-      mbar_init(&bar->sync[s], 128);
-      mbar_init(&bar->esync[s], 128);
+      mbar_init(&bar->p_full[s], 4);
+      mbar_init(&bar->q_ready[s], 4);
+      mbar_init(&bar->sync[s], 4);
+      mbar_init(&bar->esync[s], 4);
       bar->vote[s] = -1;
     }
     bar->abort_flag = 0;
@@ -402,23 +419,35 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
                                                                  bar->pv_done, abort_flag, seg_begin, seg_end);
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(128, G, BF16 ? 1 : 0, 0, 0);   // K (M) and Q (N) K-major
-      constexpr uint32_t idesc_pv = idesc_f16(128, G, BF16 ? 1 : 0, 1, 0);   // V^T MN-major, P^T K-major
-      // V^T as the A operand: M = d runs along a V row, the second 64-wide
-      // half of M is one box further (for D = 64: the next slot or the spare
-      // tile; rows 64..127 of O^T are then not read).
-      constexpr uint32_t v_lbo = C::kBoxBytes;
-      const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
-      const uint32_t q_base = smem_u32(smem + C::kOffQ), p_base = smem_u32(smem + C::kOffP);
-      int j = 0, segi = 0;
-      bool ok = true;
-      uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
-      uint32_t last_parity = 0;
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj % VS;
-        if (!mbar_wait(&bar->p_full[jj & 1], (jj >> 1) & 1, abort_flag, p.status)) return false;
-        if (!mbar_wait(&bar->v_full[s], (jj / VS) & 1, abort_flag, p.status)) return false;
+    // Lane 0 issues the tcgen05 work; the whole warp runs the loop so that,
+    // before a ragged stage's P V, it can clear the V rows past the sequence
+    // (a pool's unused rows may hold NaN, and P = 0 times NaN is not 0).
+    constexpr uint32_t idesc_qk = idesc_f16(128, G, BF16 ? 1 : 0, 0, 0);   // K (M) and Q (N) K-major
+    constexpr uint32_t idesc_pv = idesc_f16(128, G, BF16 ? 1 : 0, 1, 0);   // V^T MN-major, P^T K-major
+    // V^T as the A operand: M = d runs along a V row, the second 64-wide half
+    // of M is one box further (for D = 64: the next slot or the spare tile;
+    // rows 64..127 of O^T are then not read).
+    constexpr uint32_t v_lbo = C::kBoxBytes;
+    const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
+    const uint32_t q_base = smem_u32(smem + C::kOffQ), p_base = smem_u32(smem + C::kOffP);
+    int j = 0, segi = 0;
+    bool ok = true;
+    uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
+    uint32_t last_parity = 0;
+    // P V of stage jj (whose inputs are in); nvalid = its keys (< 128: clear the rest of V first)
+    auto do_pv = [&](int jj, int nvalid) {
+      const int s = jj % VS;
+      if (nvalid < 128) {
+        mbar_wait(&bar->v_full[s], (jj / VS) & 1, abort_flag, p.status);   // complete: an acquire per lane
+        uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
+        for (int c = 0; c < C::kChunks; ++c)
+          for (int u = lane; u < (128 - nvalid) * 8; u += 32)
+            *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + (nvalid + (u >> 3)) * 128 + (u & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
         tc_fence_after();
         const uint32_t vb = v_base + s * C::kTileBytes;
         const uint32_t pb = p_base + (jj & 1) * C::kPBytes;
@@ -428,37 +457,84 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
                  smem_desc_sw128(pb + (kk >> 2) * (G * 128) + (kk & 3) * 32, 16, 1024), idesc_pv,
                  kk > 0 ? 1u : 0u);
         mma_commit(&bar->pv_done[s]);
-        last_bar = &bar->pv_done[s];
-        last_parity = (jj / VS) & 1;
-        return true;
-      };
-      for (int si = seg_begin; si < seg_end && ok; ++si, ++segi) {
-        const DecodeSeg sg = segs[si];
-        if (!mbar_wait(&bar->q_ready[segi & 1], (segi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t qb = q_base + (segi & 1) * C::kQBytes;
-        for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
-          const int s = j % KS;
-          if (!mbar_wait(&bar->k_full[s], (j / KS) & 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kb = k_base + s * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + (j & 1) * G, smem_desc_sw128(kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024),
-                   smem_desc_sw128(qb + (kk >> 2) * (G * 128) + (kk & 3) * 32, 16, 1024), idesc_qk,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(&bar->qk_done[s]);
-          last_bar = &bar->qk_done[s];
-          last_parity = (j / KS) & 1;
-          if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
-        }
       }
-      if (ok && j > 0) issue_pv(j - 1);
-      // Every MMA issued has finished before TMEM goes: the latest commit
-      // tracks them all (the one before it on the same barrier has completed,
-      // so the barrier is at most one phase behind).
-      if (last_bar != nullptr) mbar_wait(last_bar, last_parity, nullptr, p.status);
+      last_bar = &bar->pv_done[s];
+      last_parity = (jj / VS) & 1;
+    };
+    // Each step issues Q K^T_j and P V_{j-1} in whichever order their inputs
+    // arrive (the two are independent), so neither waits behind the other:
+    // a segment's last P V does not wait for the next unit's first K tile,
+    // nor Q K^T_j for a slow P_{j-1}.
+    int prev_nvalid = 128;
+    for (int si = seg_begin; si < seg_end && ok; ++si, ++segi) {
+      const DecodeSeg sg = segs[si];
+      const uint32_t qb = q_base + (segi & 1) * C::kQBytes;
+      const int L = kvlen[sg.unit / p.num_kv_heads];
+      bool q_ok = false;   // lane 0's view
+      for (int st = sg.stage_begin; st < sg.stage_end && ok; ++st, ++j) {
+        const int s = j % KS;
+        bool qk = false, pv = (j == 0);
+        const uint64_t t0 = globaltimer();
+        while (!(qk && pv)) {
+          int ev = 0;
+          if (lane == 0) {
+            if (!qk) {
+              if (!q_ok) q_ok = mbar_test_wait(&bar->q_ready[segi & 1], (segi >> 1) & 1);
+              if (q_ok && mbar_test_wait(&bar->k_full[s], (j / KS) & 1)) ev |= 1;
+            }
+            if (!pv && mbar_test_wait(&bar->p_full[(j - 1) & 1], ((j - 1) >> 1) & 1) &&
+                mbar_test_wait(&bar->v_full[(j - 1) % VS], ((j - 1) / VS) & 1))
+              ev |= 2;
+            if (ev == 0) {
+              if (*abort_flag) {
+                ev = 4;
+              } else if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                status_raise(p.status, 10u /* FIA_ERR_TIMEOUT */);
+                ev = 4;
+              }
+            }
+          }
+          ev = __shfl_sync(0xffffffffu, ev, 0);
+          if (ev & 4) {
+            ok = false;
+            break;
+          }
+          if (ev & 1) {
+            if (lane == 0) {
+              tc_fence_after();
+              const uint32_t kb = k_base + s * C::kTileBytes;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tmem + (j & 1) * G, smem_desc_sw128(kb + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(qb + (kk >> 2) * (G * 128) + (kk & 3) * 32, 16, 1024), idesc_qk,
+                       kk > 0 ? 1u : 0u);
+              mma_commit(&bar->qk_done[s]);
+            }
+            last_bar = &bar->qk_done[s];
+            last_parity = (j / KS) & 1;
+            qk = true;
+          }
+          if (ev & 2) {
+            do_pv(j - 1, prev_nvalid);
+            pv = true;
+          }
+          if (ev == 0) __nanosleep(32);   // yield the issue slots: softmax warp 1 shares this scheduler
+        }
+        prev_nvalid = min(128, L - st * 128);
+      }
     }
+    if (ok && j > 0) {
+      const int jj = j - 1;
+      if (__all_sync(0xffffffffu, mbar_wait(&bar->p_full[jj & 1], (jj >> 1) & 1, abort_flag, p.status) &&
+                                      mbar_wait(&bar->v_full[jj % VS], (jj / VS) & 1, abort_flag, p.status)))
+        do_pv(jj, prev_nvalid);
+    }
+    // Every MMA issued has finished before TMEM goes: the latest commit
+    // tracks them all (the one before it on the same barrier has completed,
+    // so the barrier is at most one phase behind).
+    if (last_bar != nullptr && lane == 0) mbar_wait(last_bar, last_parity, nullptr, p.status);
+    __syncwarp();
   } else if (warp == 7) {
     // ------------------------------------------------------------ merge warp
     // After each segment's partials are out, bump the unit's counter; the CTA
@@ -472,8 +548,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         break;
       }
       if (lane == 0) mbar_arrive(&bar->part_free[segi & 3]);   // the slot may take segment segi + 4
-      __threadfence();
       const int2 up = unit_parts[sg.unit];
+      if (up.y == 1) continue;   // written directly by the softmax warps
+      __threadfence();
       int last = 0;
       if (lane == 0) {
         unsigned long long* ctr = p.unit_counter + sg.unit;
@@ -522,13 +599,21 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
     bool ok = true;
     const int nseg = seg_end - seg_begin;
 
-    // Q of the first two segments (buffers 0 and 1)
-    for (int k = 0; k < 2 && k < nseg; ++k) {
-      QPieces<D, GL> q;
-      q_load<D, GL>(p, segs[seg_begin + k].unit, r, q);
-      q_store<D, GL>(q_tiles + k * C::kQBytes, g, r, q);
-      fence_proxy_async_smem();
-      mbar_arrive(&bar->q_ready[k]);
+    // Q of the first two segments (buffers 0 and 1), both loads in flight
+    {
+      QPieces<D, GL> q0, q1;
+      if (nseg > 0) q_load<D, GL>(p, segs[seg_begin].unit, r, q0);
+      if (nseg > 1) q_load<D, GL>(p, segs[seg_begin + 1].unit, r, q1);
+      if (nseg > 0) {
+        q_store<D, GL>(q_tiles, g, r, q0);
+        fence_proxy_async_smem();
+        warp_arrive(&bar->q_ready[0]);
+      }
+      if (nseg > 1) {
+        q_store<D, GL>(q_tiles + C::kQBytes, g, r, q1);
+        fence_proxy_async_smem();
+        warp_arrive(&bar->q_ready[1]);
+      }
     }
 
     // A segment's partials are handed to the merge warp one stage later, so
@@ -542,7 +627,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       if (sidx >= 4 &&
           !__all_sync(0xffffffffu, mbar_wait(&bar->part_free[sidx & 3], ((sidx >> 2) - 1) & 1, abort_flag, p.status)))
         return false;
-      mbar_arrive(&bar->part_done[sidx & 3]);
+      warp_arrive(&bar->part_done[sidx & 3]);
       return true;
     };
 
@@ -572,7 +657,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         if (next_q) {
           q_store<D, GL>(q_tiles + ((segi + 1) & 1) * C::kQBytes, g, r, qn);
           fence_proxy_async_smem();
-          mbar_arrive(&bar->q_ready[(segi + 1) & 1]);
+          warp_arrive(&bar->q_ready[(segi + 1) & 1]);
         }
         uint32_t su[GL];
         tmem_load_cols<GL>(tmem + lane_off + (j & 1) * G, su);
@@ -597,7 +682,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         }
         const bool any_w = __any_sync(0xffffffffu, raise);
         if (lane == 0) atomicMax(&bar->vote[bsel], (j << 1) | (any_w ? 1 : 0));
-        mbar_arrive(&bar->sync[bsel]);
+        warp_arrive(&bar->sync[bsel]);
         if (!__all_sync(0xffffffffu, mbar_wait(&bar->sync[bsel], (j >> 1) & 1, abort_flag, p.status))) {
           ok = false;
           break;
@@ -626,26 +711,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
             *reinterpret_cast<uint16_t*>(pt + sw128_offset(h, r, G)) = uint16_t(bits & 0xffffu);
           }
         }
-        if (nvalid < 128) {
-          // V rows past the sequence may hold anything (a pool's unused rows can
-          // be NaN); P is 0 there but 0 * NaN is not, so clear them.
-          const int sv = j % VS;
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar->v_full[sv], (j / VS) & 1, abort_flag, p.status))) {
-            ok = false;
-            break;
-          }
-          if (r >= nvalid) {
-            uint8_t* vs = smem + C::kOffV + sv * C::kTileBytes;
-#pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();   // P^T (and cleared V rows) for the tensor core
+        fence_proxy_async_smem();   // P^T for the tensor core
         tc_fence_before();
-        mbar_arrive(&bar->p_full[bsel]);
+        warp_arrive(&bar->p_full[bsel]);
         // fold O^T_{j-1} (relative to the previous max) into the registers,
         // then move everything to this stage's max
         if (j > first) {
@@ -692,20 +760,36 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           if (lane == (h & 31)) wsum[h * 4 + warp] = wsv;
         }
       }
-      mbar_arrive(&bar->esync[segi & 1]);
+      warp_arrive(&bar->esync[segi & 1]);
       if (!__all_sync(0xffffffffu, mbar_wait(&bar->esync[segi & 1], (segi >> 1) & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
       const int64_t part = sg.part;
+      // a unit that lies in this one segment is final here: attention_out and
+      // softmax_lse directly, no partial and no merge
+      const bool whole = unit_parts[sg.unit].y == 1;
+      const int kvh = sg.unit % p.num_kv_heads, b = sg.unit / p.num_kv_heads;
 #pragma unroll
       for (int h = 0; h < GL; ++h) {
         if (h < g) {
           const float4 w4 = *reinterpret_cast<const float4*>(wsum + h * 4);
           const float l = (w4.x + w4.y) + (w4.z + w4.w);
           const bool has = l > 0.f;
-          if (r < D) p.part_o[(part * g + h) * D + r] = has ? acc[h] / l : 0.f;
-          if (r == h) p.part_lse[part * g + h] = has ? (m[h] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          if (whole) {
+            const int head = kvh * g + h;
+            if (r < D) {
+              const uint32_t bits = pack2(has ? acc[h] / l : 0.f, 0.f, BF16);
+              reinterpret_cast<uint16_t*>(p.out)[int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + r] =
+                  uint16_t(bits & 0xffffu);
+            }
+            if (r == h && p.lse != nullptr)
+              p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] =
+                  has ? (m[h] + __log2f(l)) * 0.69314718055994531f : INFINITY;
+          } else {
+            if (r < D) p.part_o[(part * g + h) * D + r] = has ? acc[h] / l : 0.f;
+            if (r == h) p.part_lse[part * g + h] = has ? (m[h] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          }
         }
       }
       if (rel >= 0 && !release(rel)) {

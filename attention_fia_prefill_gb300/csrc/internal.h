@@ -53,10 +53,11 @@ struct DecodeSeg {
 
 // The plan travels inside the kernel parameters when it fits these bounds
 // (no upload, no extra copy); bigger plans live in the workspace.
-constexpr int kInlineSegs = 512;
-constexpr int kInlineCtas = 256;
-constexpr int kInlineUnits = 1024;
-constexpr int kInlineBatch = 1024;
+// (Every byte of the parameter block is sent with each launch: ~9 KB here.)
+constexpr int kInlineSegs = 320;
+constexpr int kInlineCtas = 160;
+constexpr int kInlineUnits = 256;
+constexpr int kInlineBatch = 256;
 
 struct DecodeInlinePlan {
   DecodeSeg segs[kInlineSegs];

@@ -152,3 +152,13 @@ def test_many_short_sequences(fia):
     lens = [1, 130, 2, 257, 0, 5, 129, 128, 64, 1000, 3, 300] * 3
     c = fia_inputs.paged_decode_case(len(lens), 8, 2, 128, lens, block_size=128, workload=3000)
     _check_paged(fia, c)
+
+
+@pytest.mark.gpu
+def test_plan_in_workspace(fia):
+    """More units than the launch parameters carry (here 320 > 256): the plan
+    is uploaded into the workspace instead."""
+    rng = np.random.default_rng(77)
+    lens = [int(x) for x in rng.integers(0, 300, size=160)]
+    c = fia_inputs.paged_decode_case(len(lens), 8, 2, 128, lens, block_size=128, workload=3100)
+    _check_paged(fia, c)
