@@ -180,14 +180,6 @@ __device__ __forceinline__ void decode_producer(const DecodeParams& p, const CUt
   }
 }
 
-// One arrival per softmax warp: the warp barrier orders every lane's earlier
-// writes before lane 0's (releasing) arrive, and four arrivals instead of 128
-// keep the barrier traffic off the per-stage path.
-__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -722,7 +722,21 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
     if (st != FIA_OK) return st;
     g.bs = 0;
   }
-  if (g.mla) return fail(FIA_ERR_UNSUPPORTED, "MLA decode is not implemented yet");
+  if (g.mla) {
+    // MLA: key = value = the 512-d latent cache, plus a 64-d rope part of q and k
+    if (D != 512) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes a 512-d latent query (got %lld)", (long long)D);
+    if (g.N2 != 1) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes num_key_value_heads = 1");
+    if (g.N1 > 128) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes at most 128 query heads");
+    if (qr->dtype != q->dtype || kr->dtype != q->dtype) return fail(FIA_ERR_DTYPE, "query_rope/key_rope must match query");
+    if (qr->ndim != q->ndim || numel(qr) != numel(q) / 8 || qr->shape[qr->ndim - 1] != 64)
+      return fail(FIA_ERR_SHAPE, "query_rope must be the query's shape with last dim 64");
+    if (kr->ndim != k->ndim || numel(kr) != numel(k) / 8 || kr->shape[kr->ndim - 1] != 64)
+      return fail(FIA_ERR_SHAPE, "key_rope must be the key's shape with last dim 64");
+    if (!aligned16(qr->data) || !aligned16(kr->data)) return fail(FIA_ERR_ALIGNMENT, "rope tensors not 16-byte aligned");
+    if (k->data != v->data) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes value = key (the latent cache)");
+    g.Dv = 512;
+    return FIA_OK;
+  }
   if (D != 64 && D != 128) return fail(FIA_ERR_UNSUPPORTED, "decode head dim %lld (kernels take 64 or 128)", (long long)D);
   g.Dv = D;
   return FIA_OK;
@@ -747,12 +761,12 @@ constexpr double kSegmentCost = 1.0;
 // until the stages fit the CTAs.  Within a CTA, the pieces of units that other
 // CTAs share go first: the CTA that completes a unit merges it, and a split
 // unit finished early is merged while the CTA still streams, not at its end.
-void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl) {
+void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl, int stage_keys = 128) {
   pl.n_units = int(g.B * g.N2);
   std::vector<int32_t> nst(size_t(pl.n_units));
   int64_t T = 0, nonempty = 0;
   for (int u = 0; u < pl.n_units; ++u) {
-    nst[size_t(u)] = (g.kv_len[size_t(u / g.N2)] + 127) / 128;
+    nst[size_t(u)] = int32_t((g.kv_len[size_t(u / g.N2)] + stage_keys - 1) / stage_keys);
     T += nst[size_t(u)];
     nonempty += nst[size_t(u)] > 0;
   }
@@ -839,6 +853,33 @@ size_t decode_ws_bound(const DecodeGeometry& g) {
   return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), rows, size_t(g.D), true).total;
 }
 
+// MLA: stages of 32 keys, one plan slot per CTA pair, partials per output half.
+constexpr int kMlaStageKeys = 32;
+constexpr int kMlaMaxPairs = 128;
+
+struct MlaWsLayout {
+  size_t off_ctr, off_segs, off_cta, off_units, off_len, off_po, off_pl, total;
+};
+
+MlaWsLayout mla_ws_layout(size_t n_segs, size_t n_pairs, size_t B, size_t N1, bool plan_in_ws) {
+  MlaWsLayout w;
+  size_t o = kHeader;
+  w.off_ctr = o; o += align_up(2 * B * sizeof(unsigned long long), 256);
+  w.off_segs = o; o += plan_in_ws ? align_up(n_segs * sizeof(DecodeSeg), 256) : 0;
+  w.off_cta = o; o += plan_in_ws ? align_up((n_pairs + 1) * sizeof(int32_t), 256) : 0;
+  w.off_units = o; o += plan_in_ws ? align_up(B * sizeof(int2), 256) : 0;
+  w.off_len = o; o += plan_in_ws ? align_up(B * sizeof(int32_t), 256) : 0;
+  w.off_po = o; o += align_up(2 * n_segs * N1 * 256 * sizeof(float), 256);
+  w.off_pl = o; o += align_up(2 * n_segs * N1 * sizeof(float), 256);
+  w.total = o;
+  return w;
+}
+
+size_t mla_ws_bound(const DecodeGeometry& g) {
+  const size_t n_segs = size_t(g.B) + kMlaMaxPairs;
+  return mla_ws_layout(n_segs, kMlaMaxPairs, size_t(g.B), size_t(g.N1), true).total;
+}
+
 fia_status check_decode_lse(const fia_tensor* lse, const fia_params* p, int64_t B, int64_t N1) {
   if (p->softmax_lse_flag == 0) return FIA_OK;
   if (!present(lse)) return fail(FIA_ERR_NULL, "softmax_lse_flag set but softmax_lse absent");
@@ -846,6 +887,85 @@ fia_status check_decode_lse(const fia_tensor* lse, const fia_params* p, int64_t 
   if (!(lse->ndim == 4 && lse->shape[0] == B && lse->shape[1] == N1 && lse->shape[2] == 1 && lse->shape[3] == 1))
     return fail(FIA_ERR_SHAPE, "softmax_lse must be (B, N1, 1, 1)");
   return FIA_OK;
+}
+
+// MLA decode (key = value = the latent cache, plus rope): plan the batches'
+// 32-key stages over CTA pairs and launch the pair kernel.
+fia_status run_mla(const DecodeGeometry& g, const fia_tensor* query, const fia_tensor* key, const fia_tensor* qr,
+                   const fia_tensor* kr, const fia_tensor* block_table, const fia_params* params,
+                   const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  DecodePlan pl;
+  const int pairs = std::max(1, std::min(kMlaMaxPairs, sm_count() / 2));
+  plan_decode(g, pairs, pl, kMlaStageKeys);
+  const bool inl = plan_fits_inline(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B));
+  const MlaWsLayout w = mla_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(g.B), size_t(g.N1), !inl);
+  fia_status st = check_ws(workspace, workspace_bytes, w.total);
+  if (st != FIA_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  static_assert(sizeof(MlaParams) <= 32000, "MLA kernel parameters exceed the launch limit");
+  MlaParams mp;
+  memset(&mp, 0, sizeof(mp));
+  if (inl) {
+    mp.plan_inline = 1;
+    std::copy(pl.segs.begin(), pl.segs.end(), mp.plan.segs);
+    std::copy(pl.cta_seg.begin(), pl.cta_seg.end(), mp.plan.cta_seg);
+    std::copy(pl.unit_parts.begin(), pl.unit_parts.end(), mp.plan.unit_parts);
+    std::copy(g.kv_len.begin(), g.kv_len.end(), mp.plan.kv_len);
+  } else {
+    std::vector<uint8_t> plan(w.off_po - w.off_segs, 0);
+    memcpy(plan.data() + (w.off_segs - w.off_segs), pl.segs.data(), pl.segs.size() * sizeof(DecodeSeg));
+    memcpy(plan.data() + (w.off_cta - w.off_segs), pl.cta_seg.data(), pl.cta_seg.size() * sizeof(int32_t));
+    memcpy(plan.data() + (w.off_units - w.off_segs), pl.unit_parts.data(), pl.unit_parts.size() * sizeof(int2));
+    memcpy(plan.data() + (w.off_len - w.off_segs), g.kv_len.data(), g.kv_len.size() * sizeof(int32_t));
+    st = cuda_check(cudaMemcpyAsync(base + w.off_segs, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream),
+                    "plan upload");
+    if (st != FIA_OK) return st;
+    mp.plan_inline = 0;
+    mp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
+    mp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
+    mp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
+    mp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
+  }
+  const uint64_t qrows = uint64_t(g.B * g.N1);
+  uint64_t dims[2], strides[1];
+  dims[0] = 512; dims[1] = qrows; strides[0] = 1024;
+  st = make_map(&mp.tm_q, query->data, 2, dims, strides, 128);
+  if (st != FIA_OK) return st;
+  dims[0] = 64; strides[0] = 128;
+  st = make_map(&mp.tm_qr, qr->data, 2, dims, strides, 128);
+  if (st != FIA_OK) return st;
+  if (pl.n_cta > 0) {
+    const uint64_t rows = uint64_t(g.paged ? g.nblk * g.bs : g.B * g.S2);
+    mp.box_rows = g.paged ? int(std::min<int64_t>(g.bs, 32)) : 32;
+    mp.block_size = g.paged ? int(g.bs) : (1 << 30);
+    mp.row_per_blk = g.paged ? g.bs : g.S2;
+    mp.block_table = g.paged ? static_cast<const int32_t*>(block_table->data) : nullptr;
+    mp.table_stride = g.paged ? block_table->shape[1] : 0;
+    dims[0] = 512; dims[1] = rows; strides[0] = 1024;
+    st = make_map(&mp.tm_lat, key->data, 2, dims, strides, uint32_t(mp.box_rows));
+    if (st != FIA_OK) return st;
+    dims[0] = 64; strides[0] = 128;
+    st = make_map(&mp.tm_rope, kr->data, 2, dims, strides, uint32_t(mp.box_rows));
+    if (st != FIA_OK) return st;
+  }
+  mp.out = attention_out->data;
+  mp.out_sb = g.o_sb;
+  mp.out_sn = g.o_sn;
+  mp.lse = (params->softmax_lse_flag && present(softmax_lse)) ? static_cast<float*>(softmax_lse->data) : nullptr;
+  mp.lse_sb = g.N1;
+  mp.lse_sn = 1;
+  mp.part_o = reinterpret_cast<float*>(base + w.off_po);
+  mp.part_lse = reinterpret_cast<float*>(base + w.off_pl);
+  mp.part_stride_o = int64_t(pl.segs.size()) * g.N1 * 256;
+  mp.part_stride_lse = int64_t(pl.segs.size()) * g.N1;
+  mp.unit_counter = reinterpret_cast<unsigned long long*>(base + w.off_ctr);
+  mp.n_pairs = pl.n_cta;
+  mp.n_units = pl.n_units;
+  mp.num_heads = int(g.N1);
+  mp.scale_log2 = float(params->scale_value * 1.4426950408889634);
+  mp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
+  return cuda_check(profiled(stream, [&] { return launch_mla(mp, g.bf16, stream); }), "MLA decode launch");
 }
 
 }  // namespace
@@ -865,7 +985,7 @@ fia_status fia_decode_get_workspace_size(const fia_tensor* query, const fia_tens
   if (st != FIA_OK) return st;
   st = check_decode_lse(softmax_lse, params, g.B, g.N1);
   if (st != FIA_OK) return st;
-  *workspace_bytes = decode_ws_bound(g);
+  *workspace_bytes = g.mla ? mla_ws_bound(g) : decode_ws_bound(g);
   return FIA_OK;
 }
 
@@ -880,6 +1000,9 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   st = check_decode_lse(softmax_lse, params, g.B, g.N1);
   if (st != FIA_OK) return st;
   cudaStream_t stream_t = static_cast<cudaStream_t>(stream);
+  if (g.mla)
+    return run_mla(g, query, key, query_rope, key_rope, block_table, params, attention_out, softmax_lse, workspace,
+                   workspace_bytes, stream_t);
   DecodePlan pl;
   plan_decode(g, sm_count(), pl);
   const size_t rows = size_t(g.N1 / g.N2);

@@ -95,12 +95,45 @@ struct DecodeParams {
   DecodeInlinePlan plan;
 };
 
+// MLA decode (latent D = 512 shared by key and value, plus a 64-d rope part of
+// the key).  A unit is a batch; the plan's segments are run by CTA pairs:
+// CTA 2c + h computes the scores of pair c's segments over all query heads and
+// accumulates half h of the 512-wide output.
+struct MlaParams {
+  CUtensorMap tm_lat, tm_rope;    // 2-D maps over the cache: (512 | 64 columns, rows), box (64, box_rows)
+  CUtensorMap tm_q, tm_qr;        // 2-D maps over q (512 columns) and q_rope (64), rows = b * Q_N + h, box (64, 128)
+  int box_rows;                   // min(block_size, 32)
+  int block_size;
+  int64_t row_per_blk;            // cache row of token 0 of block 1 (paged) / of batch 1 (contiguous)
+  const int32_t* block_table;     // nullable (contiguous)
+  int64_t table_stride;
+  void* out;                      // attention_out (B, 1, Q_N, 512)
+  int64_t out_sb, out_sn;
+  float* lse;                     // nullable, (B, Q_N, 1, 1)
+  int64_t lse_sb, lse_sn;
+  float* part_o;                  // [2 halves][n_segments][Q_N][256]
+  float* part_lse;                // [2 halves][n_segments][Q_N]
+  int64_t part_stride_o, part_stride_lse;   // elements per half
+  unsigned long long* unit_counter;   // [B][2] (epoch << 32) | segments finished
+  int n_pairs, n_units;
+  int num_heads;
+  float scale_log2;
+  DevStatus status;
+  int plan_inline;
+  const DecodeSeg* segs;
+  const int32_t* cta_seg;         // per pair
+  const int2* unit_parts;
+  const int32_t* kv_len;
+  DecodeInlinePlan plan;
+};
+
 // Records the detail string fia_last_error() returns on this thread.
 void set_last_error(int status, const char* message);
 
 // Host-side launchers (defined next to their kernels).
 cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, cudaStream_t s);
+cudaError_t launch_mla(const MlaParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_fill_rows(void* out, bool half_type, float* lse, const int64_t* dims, const int64_t* out_strides,
                              const int64_t* lse_strides, const BatchInfo* batches, int mode, cudaStream_t s);
 

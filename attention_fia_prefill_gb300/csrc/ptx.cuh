@@ -65,6 +65,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One arrival per warp: the warp barrier orders every lane's earlier writes
+// before lane 0's (releasing) arrive; a barrier counting warps instead of
+// threads keeps the arrival traffic small.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Non-blocking check: has the phase with the given parity completed?
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

@@ -10,7 +10,7 @@ second (the K and V rows of every sequence, sum(L_b) * KV_N * D * 2 bytes * 2).
 
 The other hot-path workloads are measured in the same run under "sections":
 varlen TND causal prefill (TFLOP/s), block-sparse prefill (TFLOP/s), MLA decode
-(when present) and the small fp16 prefill.  Inputs are seeded synthetic tensors
+(cache GB/s) and the small fp16 prefill.  Inputs are seeded synthetic tensors
 of the workloads' shapes (fia_inputs.py).  The L2 is flushed (a 512 MB write)
 before every timed call; times are CUDA events on the launching stream.
 
@@ -280,6 +280,31 @@ def measure_bsa(torch, dev, timer, steps, warmup, pk, traffic):
                                  traffic.get("bsa_kernel"))}
 
 
+def measure_mla(torch, dev, timer, steps, warmup, pk, traffic):
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    c = fia_inputs.workload_mla_decode()
+    cache_bytes = sum(c.kv_lens) * (512 + 64) * 2
+    q, qr, lat, rope, tb = (t.to(dev) for t in (c.q, c.q_rope, c.latent, c.rope, c.block_table))
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], c.num_heads, 1, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        fia.fia_decode(q, lat, lat, query_rope=qr, key_rope=rope, block_table=tb, block_size=c.block_size,
+                       actual_seq_kvlen=c.kv_lens, num_heads=c.num_heads, num_key_value_heads=1, scale_value=c.scale,
+                       input_layout="BSND", softmax_lse_flag=True, out=out, softmax_lse=lse, workspace=ws)
+
+    call_ms, kern_ms = timer.run(call, steps, warmup, kernel_events=True)
+    km = statistics.mean(kern_ms)
+    return {"workload": "MLA decode bf16 B=32, 128 heads, latent 512 + rope 64, kv length 8192, block 128",
+            "metric": "latent+rope cache GB/s", "unit": "GB/s",
+            "value": round(cache_bytes / (statistics.mean(call_ms) * 1e-3) / 1e9, 2),
+            "ms_per_call": statistics.mean(call_ms), "kernel_ms": km, "cache_bytes": cache_bytes,
+            "roofline": roofline("hbm", cache_bytes / (km * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s",
+                                 traffic.get("mla_kernel"))}
+
+
 def measure_small_prefill(torch, dev, timer, steps, warmup, pk):
     import attention_fia_prefill_gb300 as fia
     import fia_inputs
@@ -341,7 +366,7 @@ def run_ours(args):
     dec, case = measure_decode(torch, dev, timer, args.steps, args.warmup, pk, traffic)
     sections = {}
     if not args.headline_only:
-        for name, fn in (("prefill_tnd", measure_prefill_tnd), ("bsa", measure_bsa)):
+        for name, fn in (("prefill_tnd", measure_prefill_tnd), ("bsa", measure_bsa), ("mla_decode", measure_mla)):
             try:
                 sections[name] = fn(torch, dev, timer, args.steps, args.warmup, pk, traffic)
             except Exception as e:  # a section failure is reported, not hidden
@@ -452,6 +477,14 @@ def run_profile_target(args):
             fia.bsa_forward(q, k, v, m, c.block_shape, num_heads=c.num_heads,
                             num_key_value_heads=c.num_key_value_heads, scale_value=c.scale, input_layout="BNSD",
                             softmax_lse_flag=True)
+    elif name == "mla":
+        c = fia_inputs.workload_mla_decode()
+        q, qr, lat, rope, tb = (t.to(dev) for t in (c.q, c.q_rope, c.latent, c.rope, c.block_table))
+
+        def call():
+            fia.fia_decode(q, lat, lat, query_rope=qr, key_rope=rope, block_table=tb, block_size=c.block_size,
+                           actual_seq_kvlen=c.kv_lens, num_heads=c.num_heads, num_key_value_heads=1,
+                           scale_value=c.scale, input_layout="BSND", softmax_lse_flag=True)
     else:
         raise SystemExit(f"unknown profile target {name}")
     for _ in range(args.warmup + args.steps):

@@ -193,11 +193,17 @@ class MLACase:
     scale: float
 
 
-def mla_decode_case(B, N1, kv_lens, block_size=128, Dl=512, Dr=64, workload=400, extra_blocks=0) -> MLACase:
+def mla_decode_case(B, N1, kv_lens, block_size=128, Dl=512, Dr=64, workload=400, extra_blocks=0,
+                    poison=False) -> MLACase:
+    """Paged latent + rope caches.  With poison=True one extra block is NaN and
+    unused block_table entries point at it, and the rows past each sequence's
+    length in its last block are NaN, so a read outside a sequence is seen."""
     nb = [(L + block_size - 1) // block_size for L in kv_lens]
     total = sum(nb) + extra_blocks
     perm = rng(workload, 10).permutation(total)
-    max_blocks = max(nb)
+    max_blocks = max(max(nb), 1)
+    nblk = total + (1 if poison else 0)
+    unused = total if poison else (perm[-1] if total else 0)
     table = np.zeros((B, max_blocks), dtype=np.int32)
     pos = 0
     for b in range(B):
@@ -205,9 +211,16 @@ def mla_decode_case(B, N1, kv_lens, block_size=128, Dl=512, Dr=64, workload=400,
             if i < nb[b]:
                 table[b, i] = perm[pos]; pos += 1
             else:
-                table[b, i] = perm[-1]
-    latent = normal((total, block_size, Dl), "bf16", workload, 2)
-    rope = normal((total, block_size, Dr), "bf16", workload, 3)
+                table[b, i] = unused
+    latent = normal((nblk, block_size, Dl), "bf16", workload, 2)
+    rope = normal((nblk, block_size, Dr), "bf16", workload, 3)
+    if poison:
+        latent[total] = float("nan"); rope[total] = float("nan")
+        for b in range(B):
+            tail = kv_lens[b] % block_size
+            if nb[b] and tail:
+                last = int(table[b, nb[b] - 1])
+                latent[last, tail:] = float("nan"); rope[last, tail:] = float("nan")
     q = normal((B, 1, N1, Dl), "bf16", workload, 1)
     qr = normal((B, 1, N1, Dr), "bf16", workload, 4)
     return MLACase(q, qr, latent, rope, torch.from_numpy(table), list(kv_lens), block_size, N1,
