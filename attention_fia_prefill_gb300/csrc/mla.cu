@@ -41,6 +41,7 @@ constexpr int kMlaSmem = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 64;
 constexpr int kHalf = 256;                   // output columns per CTA
+constexpr int kPrefetch = 6;                 // stages ahead warmed in L2
 
 struct MlaBars {
   uint64_t k_full[2], qk_done[2], pv_done[2], p_full[2];
@@ -238,6 +239,27 @@ __global__ void __launch_bounds__(256, 1) mla_kernel(const __grid_constant__ Mla
             for (int c = 0; c < kLatChunks; ++c)
               tma_load_2d(dst + c * kKBox + k * p.box_rows * 128, &p.tm_lat, &bar->k_full[s], c * 64, int(row));
             tma_load_2d(dst + kLatChunks * kKBox + k * p.box_rows * 128, &p.tm_rope, &bar->k_full[s], 0, int(row));
+          }
+        }
+        // The ring holds two stages only (Q' takes most of shared memory), so
+        // the tiles kPrefetch stages ahead are pulled into L2 now: their loads
+        // then wait for L2, not for HBM.
+        const int pst = st + kPrefetch;
+        if (pst < sg.stage_end) {
+          const int ptok = pst * kMlaKeys;
+          int64_t prow = -1;
+          if (p.block_table != nullptr) {
+            const int page = ptok / p.block_size;
+            const bool cached = page >= cache_base && page < cache_base + 32;
+            const int64_t blk = __shfl_sync(0xffffffffu, cache_blk, cached ? page - cache_base : 0);
+            if (cached) prow = blk * p.row_per_blk + (ptok % p.block_size);
+          } else {
+            prow = int64_t(b) * p.row_per_blk + ptok;
+          }
+          if (lane == 0 && prow >= 0) {
+#pragma unroll
+            for (int c = 0; c < kLatChunks; ++c) tma_prefetch_l2_2d(&p.tm_lat, c * 64, int(prow));
+            tma_prefetch_l2_2d(&p.tm_rope, 0, int(prow));
           }
         }
       }

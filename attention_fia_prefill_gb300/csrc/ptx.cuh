@@ -134,6 +134,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_
       : "memory");
 }
 
+// Warms L2 with a tile a later tma_load_2d of the same coordinates will read
+// (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(desc)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"

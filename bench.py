@@ -495,7 +495,7 @@ def run_profile_target(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, prefill_tnd, bsa)")
+    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, prefill_tnd, bsa, mla)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
