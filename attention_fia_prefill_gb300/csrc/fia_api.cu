@@ -315,22 +315,34 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
   return FIA_OK;
 }
 
-int causal_tiles(const BatchInfo& bi, int q_tile, int mode) {
-  const int q0 = q_tile * kTileM;
+// KV tiles that the 128 query rows from q0 visit under a causal mask.
+int causal_tiles(const BatchInfo& bi, int q0, int mode) {
   const int off = mode == 3 ? bi.kv_len - bi.q_len : 0;
   const int last_row = std::min(q0 + kTileM - 1, bi.q_len - 1);
   const int maxkey = std::min(bi.kv_len - 1, last_row + off);
   return maxkey >= 0 ? maxkey / kTileN + 1 : 0;
 }
 
+// Work items: 256-row pairs of query tiles for the dense/causal kernel, single
+// 128-row tiles for the block-sparse one.  cost = tile products (Q K^T + P V
+// per 128 x 128 tile) the CTA runs.
 void build_items(const Geometry& g, int prefill_mode, int causal_mode, std::vector<WorkItem>& items) {
   items.clear();
+  const int rows = prefill_mode == kBlockSparse ? kTileM : 2 * kTileM;
   for (int64_t b = 0; b < g.B; ++b) {
     const BatchInfo& bi = g.batches[size_t(b)];
-    const int nqt = (bi.q_len + kTileM - 1) / kTileM;
+    const int nqt = (bi.q_len + rows - 1) / rows;
+    const int full = (bi.kv_len + kTileN - 1) / kTileN;
     for (int64_t h = 0; h < g.N1; ++h)
       for (int qt = 0; qt < nqt; ++qt) {
-        const int cost = prefill_mode == kCausal ? causal_tiles(bi, qt, causal_mode) : (bi.kv_len + kTileN - 1) / kTileN;
+        int cost = full;
+        if (prefill_mode != kBlockSparse) {
+          const int q0 = qt * rows;
+          const int na = prefill_mode == kCausal ? causal_tiles(bi, q0, causal_mode) : full;
+          const int nb = q0 + kTileM >= bi.q_len ? 0
+                         : std::max(na, prefill_mode == kCausal ? causal_tiles(bi, q0 + kTileM, causal_mode) : full);
+          cost = na + nb;
+        }
         items.push_back(WorkItem{int32_t(b), int32_t(h), qt, cost});
       }
   }
@@ -447,7 +459,11 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.bsa_mask = bsa_mask;
   pp.bsa_nqb = nqb; pp.bsa_nkb = nkb; pp.bsa_x = bx; pp.bsa_y = by;
   pp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
-  return cuda_check(profiled(stream, [&] { return launch_prefill(pp, int(g.D), g.bf16, mode, stream); }),
+  return cuda_check(profiled(stream,
+                             [&] {
+                               return mode == kBlockSparse ? launch_prefill(pp, int(g.D), g.bf16, mode, stream)
+                                                           : launch_prefill_pair(pp, int(g.D), g.bf16, mode, stream);
+                             }),
                     "prefill launch");
 }
 

@@ -17,7 +17,9 @@ struct BatchInfo {
   int32_t q_start, q_len, kv_start, kv_len;
 };
 
-// One prefill CTA: query rows [q_tile*128, q_tile*128+128) of (batch b, query head h).
+// One prefill CTA of (batch b, query head h): query rows [q_tile*128,
+// q_tile*128+128) for the block-sparse kernel, [q_tile*256, q_tile*256+256)
+// (two 128-row tiles) for the dense/causal kernel.
 struct WorkItem {
   int32_t b, h, q_tile, cost;
 };
@@ -132,6 +134,7 @@ void set_last_error(int status, const char* message);
 
 // Host-side launchers (defined next to their kernels).
 cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
+cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, cudaStream_t s);
 cudaError_t launch_mla(const MlaParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_fill_rows(void* out, bool half_type, float* lse, const int64_t* dims, const int64_t* out_strides,

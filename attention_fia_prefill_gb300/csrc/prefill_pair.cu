@@ -1,0 +1,397 @@
+// Prefill attention (dense and causal modes) with two query tiles per CTA.
+//
+// Operation: as prefill.cu -- torch_npu.npu_prompt_flash_attention ("功能说明",
+// formula) and npu_fused_infer_attention_score_v2 (Q_S > 1, softmax_lse):
+// out = softmax(scale * Q K^T + mask) V with sparse_mode 0 (no mask) or the
+// causal modes 2 / 3 computed from indices.
+//
+// One CTA owns 256 query rows of one (batch, query head): tile A (rows
+// q0..q0+127) and tile B (q0+128..q0+255).  Both read every K/V tile the CTA
+// loads, and the tensor core alternates between them: while warpgroup A
+// exponentiates S_A(j), the MMA warp runs P_B(j-1) V and Q_B K(j)^T, and the
+// other way round, so the softmax of one tile hides behind the products of the
+// other (one tile alone leaves the tensor core idle while its softmax runs).
+//   warp 0      TMA producer: Q_A and Q_B once, K/V tiles through a ring
+//   warp 1      MMA issuer (one thread) and TMEM owner, in the order
+//                 P_A(j) V, Q_A K(j+1)^T, P_B(j) V, Q_B K(j+1)^T
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one thread
+//               per query row (= TMEM lane), running max / sum in registers,
+//               P written over S in TMEM, O rescaled in TMEM when the max grows
+//               by more than 2^8, epilogue O / l and LSE.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D,
+// 256+2D).  Causal: tile B needs the K/V tiles of tile A plus at most one; the
+// CTA walks tile B's range and tile A stops early.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fia {
+namespace {
+
+template <int D>
+struct PairCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kBoxBytes = 128 * 128;
+  static constexpr int kTileBytes = kChunks * kBoxBytes;
+  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr int kOffQ = 0;                                   // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = kOffBar + kBarBytes + 1024;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256;                            // O_A; O_B at kColO + D
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+// Key tiles needed by the query rows [qa, qa + 128) of a batch.
+__device__ __forceinline__ int tiles_for_rows(const BatchInfo& bi, int qa, int mode, int diag_off) {
+  if (mode != kCausal) return (bi.kv_len + kTileN - 1) / kTileN;
+  const int last_row = min(qa + kTileM - 1, bi.q_len - 1);
+  const int maxkey = min(bi.kv_len - 1, last_row + diag_off);
+  return maxkey >= 0 ? maxkey / kTileN + 1 : 0;
+}
+
+template <int D, bool BF16, int MODE>
+__global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_constant__ PrefillParams p) {
+  using C = PairCfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem_1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;     // [S]
+  uint64_t* v_full = bars + 4;     // [S]
+  // kv_free[s]: P_B V of the tile in stage s is done (one commit per MMA
+  // group): the stage is free, and O_B holds it.
+  uint64_t* kv_free = bars + 7;    // [S]
+  uint64_t* s_full = bars + 10;    // [2]: S_A, S_B of the next tile are in TMEM
+  uint64_t* pa_full = bars + 12;   // [2] by tile parity: warpgroup A's P is in (4 warp arrivals)
+  uint64_t* pb_full = bars + 14;   // [2]
+  uint64_t* pva_done = bars + 18;  // [2] by tile parity: P_A V done (O_A up to date)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[blockIdx.x];
+  const BatchInfo bi = p.batches[it.b];
+  const int q0 = it.q_tile * 2 * kTileM;
+  const int kvh = it.h / p.group;
+  const int diag_off = (MODE == kCausal && p.causal_offset_mode == 3) ? (bi.kv_len - bi.q_len) : 0;
+  const int na = tiles_for_rows(bi, q0, MODE, diag_off);
+  // Tile B walks at least tile A's range (its rows past the batch are computed
+  // but not written); a pair whose tile B starts past the batch runs tile A
+  // alone.  nl = tiles the CTA loads; the last tile product of each K/V tile
+  // (tile B's when it has rows, else tile A's) releases the stage.
+  const bool has_b = q0 + kTileM < bi.q_len;
+  const int nb = has_b ? max(na, tiles_for_rows(bi, q0 + kTileM, MODE, diag_off)) : 0;
+  const int nl = max(na, nb);
+
+  if (threadIdx.x == 0) {
+    if (blockIdx.x == 0) status_stamp(p.status);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_free[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&pa_full[t], 4);
+      mbar_init(&pb_full[t], 4);
+      mbar_init(&pva_done[t], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const bool is_tnd = p.is_tnd != 0;
+  const int q_row0 = is_tnd ? bi.q_start + q0 : q0;
+  const int kv_row0 = is_tnd ? bi.kv_start : 0;
+  const int b_coord = is_tnd ? 0 : it.b;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(smem + C::kOffQ + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c * 64,
+                      q_row0 + t * kTileM, it.h, b_coord);
+      int j = 0;
+      for (; j < nl; ++j) {
+        const int s = j % S;
+        if (j >= S && !mbar_wait(&kv_free[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
+        uint8_t* ks = smem + C::kOffK + s * C::kTileBytes;
+        uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
+        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(ks + c * C::kBoxBytes, &p.tm_k, &k_full[s], c * 64, kv_row0 + j * kTileN, kvh, b_coord);
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[s], c * 64, kv_row0 + j * kTileN, kvh, b_coord);
+      }
+      if (*abort_flag) {
+        mbar_wait(q_full, 0, nullptr, p.status);
+        for (int s = 0; s < S && s < j; ++s) {
+          const int last = j - 1 - ((j - 1 - s) % S);
+          mbar_wait(&k_full[s], (last / S) & 1, nullptr, p.status);
+          mbar_wait(&v_full[s], (last / S) & 1, nullptr, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
+      uint32_t last_parity = 0;
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      // S_t = Q_t K(j)^T
+      auto qk = [&](int t, int j) -> bool {
+        const int s = j % S;
+        if (!mbar_wait(&k_full[s], (j / S) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(smem + C::kOffK + s * C::kTileBytes);
+        const uint32_t qt = q_base + t * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + t * 128, smem_desc_sw128(qt + off, 16, 1024), smem_desc_sw128(k_base + off, 16, 1024), idesc_qk,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[t]);
+        last_bar = &s_full[t];
+        last_parity = j & 1;
+        return true;
+      };
+      // O_t += P_t(j) V(j): P read from tile t's S columns in TMEM; V is
+      // [keys x D], an MN-major operand (16 keys = 2048 bytes per K-step, the
+      // next 64 columns of D one box further)
+      auto pv = [&](int t, int j) -> bool {
+        const int s = j % S;
+        if (!mbar_wait(t == 0 ? &pa_full[j & 1] : &pb_full[j & 1], (j >> 1) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(smem + C::kOffV + s * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts(tmem + C::kColO + t * D, tmem + t * 128 + kk * 8, smem_desc_sw128(v_base + kk * 2048, C::kBoxBytes, 1024),
+                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        if (t == 0 && nb > 0) {
+          mma_commit(&pva_done[j & 1]);
+          last_bar = &pva_done[j & 1];
+          last_parity = (j >> 1) & 1;
+        } else {
+          mma_commit(&kv_free[s]);
+          last_bar = &kv_free[s];
+          last_parity = (j / S) & 1;
+        }
+        return true;
+      };
+      if (ok && na > 0) ok = qk(0, 0);
+      if (ok && nb > 0) ok = qk(1, 0);
+      for (int j = 0; j < nl && ok; ++j) {
+        if (j < na) {
+          ok = pv(0, j);
+          if (ok && j + 1 < na) ok = qk(0, j + 1);
+        }
+        if (ok && j < nb) {
+          ok = pv(1, j);
+          if (ok && j + 1 < nb) ok = qk(1, j + 1);
+        }
+      }
+      // Every MMA issued has finished before TMEM goes: the latest commit
+      // tracks them all (the one before it on the same barrier has completed).
+      if (last_bar != nullptr) mbar_wait(last_bar, last_parity, nullptr, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) >> 2;              // 0: tile A, 1: tile B
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+    const uint32_t col_s = t * 128;
+    const uint32_t col_o = C::kColO + t * D;
+    const int n = t == 0 ? na : nb;
+    const int tile_q0 = q0 + t * kTileM;
+    const int i = tile_q0 + r;
+    const int diag = i + diag_off;
+    const float sl2 = p.scale_log2;
+    uint64_t* my_pfull = t == 0 ? pa_full : pb_full;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, p.status))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t su[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + col_s + c * 32, su[c]);
+      tmem_wait_ld(su[0]);
+#pragma unroll
+      for (int c = 1; c < 4; ++c) tmem_regs_after_wait(su[c]);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(su[c][e]);
+      const int kv0 = j * kTileN;
+      const bool ragged = kv0 + kTileN > bi.kv_len;
+      const bool need_mask = ragged || (MODE == kCausal && kv0 + kTileN - 1 > tile_q0 + diag_off);
+      if (need_mask) {
+        const int lim = (MODE == kCausal) ? min(bi.kv_len - 1, diag) : bi.kv_len - 1;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kv0 + c > lim) x[c] = -INFINITY;
+      }
+      const float m_new = fmaxf(m, tree_max<128>(x) * sl2);
+      // Keep a stale max unless it grows by more than 8 (log2 units): p <= 2^8
+      // stays exact in fp32 and representable in bf16/f16.
+      const float m_use = (m == -INFINITY || m_new > m + 8.f) ? m_new : m;
+      const float alpha = (m_use == m) ? 1.f : fast_exp2(m - m_use);
+      const float mo = (m_use == -INFINITY) ? 0.f : m_use;
+      const float sum = exp2_and_sum<128>(x, sl2, mo);
+      l = l * alpha + sum;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) u[e] = pack2(x[c * 32 + 2 * e], x[c * 32 + 2 * e + 1], BF16);
+        tmem_st16(tmem + lane_off + col_s + c * 16, u);
+      }
+      // O_t holds P_t(j-1) V already: Q_t K(j)^T, whose S this thread just
+      // read, was issued after that P V on the same tensor pipe.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_off + col_o + c * 32, u);
+          tmem_wait_ld(u);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+          tmem_st32(tmem + lane_off + col_o + c * 32, u);
+        }
+      }
+      // Rows of V past the batch's keys may hold anything (even NaN); P is 0
+      // there but 0 * NaN is not, so they are cleared before the first P V that
+      // reads this tile: tile A's if it uses the tile, else tile B's.
+      if (ragged && (t == 0 || j >= na)) {
+        const int s = j % S;
+        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status))) { ok = false; break; }
+        if (r >= bi.kv_len - kv0) {
+          uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(&my_pfull[j & 1]);
+      m = m_use;
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && n > 0) {
+      const int jl = n - 1;
+      ok = __all_sync(0xffffffffu, (t == 0 && nb > 0)
+                                       ? mbar_wait(&pva_done[jl & 1], (jl >> 1) & 1, abort_flag, p.status)
+                                       : mbar_wait(&kv_free[jl % S], (jl / S) & 1, abort_flag, p.status));
+      tc_fence_after();
+    }
+    if (ok) {
+      const bool row_valid = i < bi.q_len;
+      const bool has = l > 0.f;
+      const float inv_l = has ? 1.f / l : 0.f;
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      T* orow = reinterpret_cast<T*>(p.out) + (is_tnd ? int64_t(bi.q_start + i) * p.out_ss
+                                                       : int64_t(it.b) * p.out_sb + int64_t(i) * p.out_ss) +
+                int64_t(it.h) * p.out_sn;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_off + col_o + c * 32, u);
+          tmem_wait_ld(u);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = 0u;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(u[8 * q + 0]) * inv_l, __uint_as_float(u[8 * q + 1]) * inv_l, BF16);
+            w.y = pack2(__uint_as_float(u[8 * q + 2]) * inv_l, __uint_as_float(u[8 * q + 3]) * inv_l, BF16);
+            w.z = pack2(__uint_as_float(u[8 * q + 4]) * inv_l, __uint_as_float(u[8 * q + 5]) * inv_l, BF16);
+            w.w = pack2(__uint_as_float(u[8 * q + 6]) * inv_l, __uint_as_float(u[8 * q + 7]) * inv_l, BF16);
+            if (!has) w = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+          }
+        }
+      }
+      if (row_valid && p.lse != nullptr) {
+        const float lse = has ? (m + __log2f(l)) * 0.69314718055994531f : INFINITY;
+        float* lp = p.lse + (is_tnd ? int64_t(bi.q_start + i) * p.lse_ss
+                                    : int64_t(it.b) * p.lse_sb + int64_t(i) * p.lse_ss) +
+                    int64_t(it.h) * p.lse_sn;
+        *lp = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool BF16, int MODE>
+cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
+  using C = PairCfg<D>;
+  auto k = prefill_pair_kernel<D, BF16, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  k<<<p.n_items, C::kThreads, C::kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s) {
+  if (p.n_items == 0) return cudaSuccess;
+  if (mode != kDense && mode != kCausal) return cudaErrorInvalidValue;
+  const bool causal = mode == kCausal;
+  if (head_dim == 128) {
+    if (bf16) return causal ? launch_pair_one<128, true, kCausal>(p, s) : launch_pair_one<128, true, kDense>(p, s);
+    return causal ? launch_pair_one<128, false, kCausal>(p, s) : launch_pair_one<128, false, kDense>(p, s);
+  }
+  if (head_dim == 64) {
+    if (bf16) return causal ? launch_pair_one<64, true, kCausal>(p, s) : launch_pair_one<64, true, kDense>(p, s);
+    return causal ? launch_pair_one<64, false, kCausal>(p, s) : launch_pair_one<64, false, kDense>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fia

@@ -252,7 +252,7 @@ def measure_prefill_tnd(torch, dev, timer, steps, warmup, pk, traffic):
             "value": round(flops / (statistics.mean(call_ms) * 1e-3) / 1e12, 2), "ms_per_call": statistics.mean(call_ms),
             "kernel_ms": km, "flops": flops, "seq_lens": c.actual_seq_qlen,
             "roofline": roofline("tensor", flops / (km * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s",
-                                 traffic.get("prefill_kernel"))}
+                                 traffic.get("prefill_pair_kernel"))}
 
 
 def measure_bsa(torch, dev, timer, steps, warmup, pk, traffic):

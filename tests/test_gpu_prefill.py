@@ -55,6 +55,15 @@ def test_ragged_gqa_bnsd(fia, mode, D):
     _check_full(fia, case)
 
 
+@pytest.mark.parametrize("mode,D,dtype", [(0, 64, "f16"), (2, 128, "bf16"), (3, 128, "f16")])
+def test_long_rows_ring_reuse(fia, mode, D, dtype):
+    """1000 query rows x 1100 keys: query-tile pairs with a ragged last pair,
+    nine K/V tiles cycling through the shared-memory ring several times."""
+    case = fia_inputs.prefill_case(1, 2, 1, 1000, 1100, D, dtype=dtype, layout="BNSD", sparse_mode=mode,
+                                   workload=1700 + D + mode)
+    _check_full(fia, case)
+
+
 def test_pfa_example_shape_f16(fia):
     """npu_prompt_flash_attention call example: q (1,8,164,128) vs k/v (1,8,1024,128), fp16."""
     case = fia_inputs.prefill_case(1, 8, 8, 164, 1024, 128, dtype="f16", layout="BNSD", workload=7)
