@@ -161,7 +161,15 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
-      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      // Descriptors of every operand buffer, built once; an MMA's K-slice
+      // only moves the start address (bits 0..13, in 16-byte units), which
+      // stays below 2^14 here, so a constant added to the whole descriptor
+      // selects it.
+      const uint64_t qd0 = smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+      const uint64_t qd1 = smem_desc_sw128(smem_u32(smem + C::kOffQ + C::kTileBytes), 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(smem_u32(smem + C::kOffV), C::kBoxBytes, 1024);
+      constexpr uint64_t kStageStep = C::kTileBytes >> 4;
       uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
       uint32_t last_parity = 0;
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
@@ -170,13 +178,13 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         const int s = j % S;
         if (!mbar_wait(&k_full[s], (j / S) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t k_base = smem_u32(smem + C::kOffK + s * C::kTileBytes);
-        const uint32_t qt = q_base + t * C::kTileBytes;
+        const uint64_t qd = t == 0 ? qd0 : qd1;
+        const uint64_t kd = kd0 + uint64_t(s) * kStageStep;
+        const uint32_t dst = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, smem_desc_sw128(qt + off, 16, 1024), smem_desc_sw128(k_base + off, 16, 1024), idesc_qk,
-                 kk > 0 ? 1u : 0u);
+          const uint64_t off = uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
+          mma_ss(dst, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t]);
         last_bar = &s_full[t];
@@ -191,11 +199,12 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         if (!mbar_wait(t == 0 ? &pa_full[j & 1] : &pb_full[j & 1], (j >> 1) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t v_base = smem_u32(smem + C::kOffV + s * C::kTileBytes);
+        const uint64_t vd = vd0 + uint64_t(s) * kStageStep;
+        const uint32_t dst = tmem + C::kColO + t * D;
+        const uint32_t pt = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts(tmem + C::kColO + t * D, tmem + t * 128 + kk * 8, smem_desc_sw128(v_base + kk * 2048, C::kBoxBytes, 1024),
-                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(dst, pt + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         if (t == 0 && nb > 0) {
           mma_commit(&pva_done[j & 1]);
           last_bar = &pva_done[j & 1];
@@ -241,52 +250,93 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     for (int j = 0; j < n; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, p.status))) { ok = false; break; }
       tc_fence_after();
+      // S in two halves: the second half's load is in flight while the
+      // first half is masked and reduced.
       uint32_t su[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + col_s + c * 32, su[c]);
+      tmem_ld32(tmem + lane_off + col_s, su[0]);
+      tmem_ld32(tmem + lane_off + col_s + 32, su[1]);
       tmem_wait_ld(su[0]);
-#pragma unroll
-      for (int c = 1; c < 4; ++c) tmem_regs_after_wait(su[c]);
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(su[c][e]);
+      tmem_regs_after_wait(su[1]);
+      tmem_ld32(tmem + lane_off + col_s + 64, su[2]);
+      tmem_ld32(tmem + lane_off + col_s + 96, su[3]);
+      float* x = reinterpret_cast<float*>(&su[0][0]);
       const int kv0 = j * kTileN;
       const bool ragged = kv0 + kTileN > bi.kv_len;
       const bool need_mask = ragged || (MODE == kCausal && kv0 + kTileN - 1 > tile_q0 + diag_off);
+      const int lim = (MODE == kCausal) ? min(bi.kv_len - 1, diag) : bi.kv_len - 1;
+      float a[8];
       if (need_mask) {
-        const int lim = (MODE == kCausal) ? min(bi.kv_len - 1, diag) : bi.kv_len - 1;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (kv0 + c > lim) x[c] = -INFINITY;
+        for (int c = 0; c < 64; ++c)
+          if (kv0 + c > lim) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      const float m_new = fmaxf(m, tree_max<128>(x) * sl2);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        a[k] = fmax3(__uint_as_float(su[0][k]), __uint_as_float(su[0][8 + k]), __uint_as_float(su[0][16 + k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] = fmax3(a[k], __uint_as_float(su[0][24 + k]), __uint_as_float(su[1][k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        a[k] = fmax3(a[k], __uint_as_float(su[1][8 + k]), __uint_as_float(su[1][16 + k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] = fmaxf(a[k], __uint_as_float(su[1][24 + k]));
+      tmem_wait_ld(su[2]);
+      tmem_regs_after_wait(su[3]);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 64; c < 128; ++c)
+          if (kv0 + c > lim) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        a[k] = fmax3(a[k], __uint_as_float(su[2][k]), __uint_as_float(su[2][8 + k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        a[k] = fmax3(a[k], __uint_as_float(su[2][16 + k]), __uint_as_float(su[2][24 + k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] = fmax3(a[k], __uint_as_float(su[3][k]), __uint_as_float(su[3][8 + k]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        a[k] = fmax3(a[k], __uint_as_float(su[3][16 + k]), __uint_as_float(su[3][24 + k]));
+      const float m_tile = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+      const float m_new = fmaxf(m, m_tile * sl2);
       // Keep a stale max unless it grows by more than 8 (log2 units): p <= 2^8
       // stays exact in fp32 and representable in bf16/f16.
       const float m_use = (m == -INFINITY || m_new > m + 8.f) ? m_new : m;
       const float alpha = (m_use == m) ? 1.f : fast_exp2(m - m_use);
       const float mo = (m_use == -INFINITY) ? 0.f : m_use;
-      const float sum = exp2_and_sum<128>(x, sl2, mo);
-      l = l * alpha + sum;
+      // p = 2^(s * scale * log2(e) - m) in packed pairs, written back as P
+      // (16-bit pairs over the first 64 columns of S) 32 keys at a time.
+      const uint64_t sc2 = f2_pack(sl2, sl2), nmo2 = f2_pack(-mo, -mo);
+      uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t u[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) u[e] = pack2(x[c * 32 + 2 * e], x[c * 32 + 2 * e + 1], BF16);
+        for (int e = 0; e < 16; ++e) {
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nmo2), y0, y1);
+          y0 = fast_exp2(y0);
+          y1 = fast_exp2(y1);
+          acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(y0, y1));
+          u[e] = pack2(y0, y1, BF16);
+        }
         tmem_st16(tmem + lane_off + col_s + c * 16, u);
       }
+      float s0, s1;
+      f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+      l = l * alpha + (s0 + s1);
       // O_t holds P_t(j-1) V already: Q_t K(j)^T, whose S this thread just
       // read, was issued after that P V on the same tensor pipe.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_off + col_o + c * 32, u);
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t u[16];
+          tmem_ld16(tmem + lane_off + col_o + c * 16, u);
           tmem_wait_ld(u);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-          tmem_st32(tmem + lane_off + col_o + c * 32, u);
+          for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+          tmem_st16(tmem + lane_off + col_o + c * 16, u);
         }
       }
       // Rows of V past the batch's keys may hold anything (even NaN); P is 0
