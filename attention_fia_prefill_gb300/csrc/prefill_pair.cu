@@ -69,7 +69,10 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
   uint64_t* s_full = bars + 10;    // [2]: S_A, S_B of the next tile are in TMEM
   uint64_t* pa_full = bars + 12;   // [2] by tile parity: warpgroup A's P is in (4 warp arrivals)
   uint64_t* pb_full = bars + 14;   // [2]
-  uint64_t* pva_done = bars + 18;  // [2] by tile parity: P_A V done (O_A up to date)
+  // pva_done: tile A's last P V is done (its epilogue may read O_A).  Earlier
+  // P_A V products need no commit of their own: each is followed on the
+  // tensor pipe by a Q K^T whose commit covers it.
+  uint64_t* pva_done = bars + 18;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
 
@@ -100,8 +103,8 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       mbar_init(&s_full[t], 1);
       mbar_init(&pa_full[t], 4);
       mbar_init(&pb_full[t], 4);
-      mbar_init(&pva_done[t], 1);
     }
+    mbar_init(pva_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -173,10 +176,12 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
       uint32_t last_parity = 0;
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      // A K/V stage is waited for once, by the first product that reads it
+      // (tile A's, unless the tile is past tile A's range).
       // S_t = Q_t K(j)^T
       auto qk = [&](int t, int j) -> bool {
         const int s = j % S;
-        if (!mbar_wait(&k_full[s], (j / S) & 1, abort_flag, p.status)) return false;
+        if ((t == 0 || j >= na) && !mbar_wait(&k_full[s], (j / S) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint64_t qd = t == 0 ? qd0 : qd1;
         const uint64_t kd = kd0 + uint64_t(s) * kStageStep;
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       auto pv = [&](int t, int j) -> bool {
         const int s = j % S;
         if (!mbar_wait(t == 0 ? &pa_full[j & 1] : &pb_full[j & 1], (j >> 1) & 1, abort_flag, p.status)) return false;
-        if (!mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status)) return false;
+        if ((t == 0 || j >= na) && !mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint64_t vd = vd0 + uint64_t(s) * kStageStep;
         const uint32_t dst = tmem + C::kColO + t * D;
@@ -206,9 +211,11 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         for (int kk = 0; kk < kTileN / 16; ++kk)
           mma_ts(dst, pt + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         if (t == 0 && nb > 0) {
-          mma_commit(&pva_done[j & 1]);
-          last_bar = &pva_done[j & 1];
-          last_parity = (j >> 1) & 1;
+          if (j == na - 1) {
+            mma_commit(pva_done);
+            last_bar = pva_done;
+            last_parity = 0;
+          }
         } else {
           mma_commit(&kv_free[s]);
           last_bar = &kv_free[s];
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     if (ok && n > 0) {
       const int jl = n - 1;
       ok = __all_sync(0xffffffffu, (t == 0 && nb > 0)
-                                       ? mbar_wait(&pva_done[jl & 1], (jl >> 1) & 1, abort_flag, p.status)
+                                       ? mbar_wait(pva_done, 0, abort_flag, p.status)
                                        : mbar_wait(&kv_free[jl % S], (jl / S) & 1, abort_flag, p.status));
       tc_fence_after();
     }
