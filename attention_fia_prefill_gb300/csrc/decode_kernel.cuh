@@ -93,18 +93,10 @@ struct DecodeBars {
   int vote[2];
 };
 
-__device__ __forceinline__ const DecodeSeg* plan_segs(const DecodeParams& p) {
-  return p.plan_inline ? p.plan.segs : p.segs;
-}
-__device__ __forceinline__ const int32_t* plan_cta(const DecodeParams& p) {
-  return p.plan_inline ? p.plan.cta_seg : p.cta_seg;
-}
-__device__ __forceinline__ const int2* plan_units(const DecodeParams& p) {
-  return p.plan_inline ? p.plan.unit_parts : p.unit_parts;
-}
-__device__ __forceinline__ const int32_t* plan_kvlen(const DecodeParams& p) {
-  return p.plan_inline ? p.plan.kv_len : p.kv_len;
-}
+__device__ __forceinline__ const DecodeSeg* plan_segs(const DecodeParams& p) { return p.segs; }
+__device__ __forceinline__ const int32_t* plan_cta(const DecodeParams& p) { return p.cta_seg; }
+__device__ __forceinline__ const int2* plan_units(const DecodeParams& p) { return p.unit_parts; }
+__device__ __forceinline__ const int32_t* plan_kvlen(const DecodeParams& p) { return p.kv_len; }
 
 // Walks the CTA's stages in order and issues the TMA copies of one operand
 // (K or V) into a ring of NS stages.  The whole warp runs it: the lanes cache
@@ -805,7 +797,7 @@ template <int D, bool BF16, int GL>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
   using C = DecodeCfg<D, GL>;
   auto k = decode_kernel<D, BF16, GL>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = set_smem_once<decode_kernel<D, BF16, GL>>(C::kSmem);
   if (e != cudaSuccess) return e;
   k<<<p.n_cta > 0 ? p.n_cta : 1, C::kThreads, C::kSmem, s>>>(p);
   return cudaGetLastError();

@@ -855,10 +855,6 @@ DecodeWsLayout decode_ws_layout(size_t n_segs, size_t n_cta, size_t n_units, siz
   return w;
 }
 
-bool plan_fits_inline(size_t n_segs, size_t n_cta, size_t n_units, size_t B) {
-  return n_segs <= size_t(kInlineSegs) && n_cta <= size_t(kInlineCtas) && n_units <= size_t(kInlineUnits) &&
-         B <= size_t(kInlineBatch);
-}
 
 // Upper bound over every plan the call can make (at most kMaxDecodeCtas CTAs,
 // so at most n_units + kMaxDecodeCtas segments).
@@ -905,6 +901,19 @@ fia_status check_decode_lse(const fia_tensor* lse, const fia_params* p, int64_t 
   return FIA_OK;
 }
 
+// Copies a decode plan into the workspace (one host-to-device copy on the
+// call's stream; the staging buffer may go once the call returns).
+fia_status upload_plan(const DecodePlan& pl, const std::vector<int32_t>& kv_len, uint8_t* base, size_t off_segs,
+                       size_t off_cta, size_t off_units, size_t off_len, size_t off_end, cudaStream_t stream) {
+  std::vector<uint8_t> plan(off_end - off_segs, 0);
+  memcpy(plan.data(), pl.segs.data(), pl.segs.size() * sizeof(DecodeSeg));
+  memcpy(plan.data() + (off_cta - off_segs), pl.cta_seg.data(), pl.cta_seg.size() * sizeof(int32_t));
+  memcpy(plan.data() + (off_units - off_segs), pl.unit_parts.data(), pl.unit_parts.size() * sizeof(int2));
+  memcpy(plan.data() + (off_len - off_segs), kv_len.data(), kv_len.size() * sizeof(int32_t));
+  return cuda_check(cudaMemcpyAsync(base + off_segs, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream),
+                    "plan upload");
+}
+
 // MLA decode (key = value = the latent cache, plus rope): plan the batches'
 // 32-key stages over CTA pairs and launch the pair kernel.
 fia_status run_mla(const DecodeGeometry& g, const fia_tensor* query, const fia_tensor* key, const fia_tensor* qr,
@@ -914,35 +923,18 @@ fia_status run_mla(const DecodeGeometry& g, const fia_tensor* query, const fia_t
   DecodePlan pl;
   const int pairs = std::max(1, std::min(kMlaMaxPairs, sm_count() / 2));
   plan_decode(g, pairs, pl, kMlaStageKeys);
-  const bool inl = plan_fits_inline(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B));
-  const MlaWsLayout w = mla_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(g.B), size_t(g.N1), !inl);
+  const MlaWsLayout w = mla_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(g.B), size_t(g.N1), true);
   fia_status st = check_ws(workspace, workspace_bytes, w.total);
   if (st != FIA_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  static_assert(sizeof(MlaParams) <= 32000, "MLA kernel parameters exceed the launch limit");
   MlaParams mp;
   memset(&mp, 0, sizeof(mp));
-  if (inl) {
-    mp.plan_inline = 1;
-    std::copy(pl.segs.begin(), pl.segs.end(), mp.plan.segs);
-    std::copy(pl.cta_seg.begin(), pl.cta_seg.end(), mp.plan.cta_seg);
-    std::copy(pl.unit_parts.begin(), pl.unit_parts.end(), mp.plan.unit_parts);
-    std::copy(g.kv_len.begin(), g.kv_len.end(), mp.plan.kv_len);
-  } else {
-    std::vector<uint8_t> plan(w.off_po - w.off_segs, 0);
-    memcpy(plan.data() + (w.off_segs - w.off_segs), pl.segs.data(), pl.segs.size() * sizeof(DecodeSeg));
-    memcpy(plan.data() + (w.off_cta - w.off_segs), pl.cta_seg.data(), pl.cta_seg.size() * sizeof(int32_t));
-    memcpy(plan.data() + (w.off_units - w.off_segs), pl.unit_parts.data(), pl.unit_parts.size() * sizeof(int2));
-    memcpy(plan.data() + (w.off_len - w.off_segs), g.kv_len.data(), g.kv_len.size() * sizeof(int32_t));
-    st = cuda_check(cudaMemcpyAsync(base + w.off_segs, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream),
-                    "plan upload");
-    if (st != FIA_OK) return st;
-    mp.plan_inline = 0;
-    mp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
-    mp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
-    mp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
-    mp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
-  }
+  st = upload_plan(pl, g.kv_len, base, w.off_segs, w.off_cta, w.off_units, w.off_len, w.off_po, stream);
+  if (st != FIA_OK) return st;
+  mp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
+  mp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
+  mp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
+  mp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
   const uint64_t qrows = uint64_t(g.B * g.N1);
   uint64_t dims[2], strides[1];
   dims[0] = 512; dims[1] = qrows; strides[0] = 1024;
@@ -1022,37 +1014,20 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   DecodePlan pl;
   plan_decode(g, sm_count(), pl);
   const size_t rows = size_t(g.N1 / g.N2);
-  const bool inl = plan_fits_inline(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B));
   const DecodeWsLayout w = decode_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B), rows,
-                                            size_t(g.D), !inl);
+                                            size_t(g.D), true);
   st = check_ws(workspace, workspace_bytes, w.total);
   if (st != FIA_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(workspace);
 
-  static_assert(sizeof(DecodeParams) <= 32000, "decode kernel parameters exceed the launch limit");
   DecodeParams dp;
   memset(&dp, 0, sizeof(dp));
-  if (inl) {
-    dp.plan_inline = 1;
-    std::copy(pl.segs.begin(), pl.segs.end(), dp.plan.segs);
-    std::copy(pl.cta_seg.begin(), pl.cta_seg.end(), dp.plan.cta_seg);
-    std::copy(pl.unit_parts.begin(), pl.unit_parts.end(), dp.plan.unit_parts);
-    std::copy(g.kv_len.begin(), g.kv_len.end(), dp.plan.kv_len);
-  } else {
-    std::vector<uint8_t> plan(w.off_po - w.off_segs, 0);
-    memcpy(plan.data() + (w.off_segs - w.off_segs), pl.segs.data(), pl.segs.size() * sizeof(DecodeSeg));
-    memcpy(plan.data() + (w.off_cta - w.off_segs), pl.cta_seg.data(), pl.cta_seg.size() * sizeof(int32_t));
-    memcpy(plan.data() + (w.off_units - w.off_segs), pl.unit_parts.data(), pl.unit_parts.size() * sizeof(int2));
-    memcpy(plan.data() + (w.off_len - w.off_segs), g.kv_len.data(), g.kv_len.size() * sizeof(int32_t));
-    st = cuda_check(cudaMemcpyAsync(base + w.off_segs, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream_t),
-                    "plan upload");
-    if (st != FIA_OK) return st;
-    dp.plan_inline = 0;
-    dp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
-    dp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
-    dp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
-    dp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
-  }
+  st = upload_plan(pl, g.kv_len, base, w.off_segs, w.off_cta, w.off_units, w.off_len, w.off_po, stream_t);
+  if (st != FIA_OK) return st;
+  dp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
+  dp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
+  dp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
+  dp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
   if (pl.n_cta > 0) {
     uint64_t dims[2], strides[1];
     if (g.paged) {

@@ -2,11 +2,28 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 #include "ptx.cuh"
 
 namespace fia {
+
+// Raises a kernel's dynamic shared-memory limit on the first launch on each
+// device; later launches skip the driver call (it costs microseconds of host
+// time on every launch otherwise).
+template <auto Kernel>
+cudaError_t set_smem_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};   // one bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 constexpr int kTileM = 128;   // query rows per prefill CTA
 constexpr int kTileN = 128;   // keys per KV tile
@@ -53,20 +70,10 @@ struct DecodeSeg {
   int32_t unit, stage_begin, stage_end, part;   // part = global segment index
 };
 
-// The plan travels inside the kernel parameters when it fits these bounds
-// (no upload, no extra copy); bigger plans live in the workspace.
-// (Every byte of the parameter block is sent with each launch: ~9 KB here.)
-constexpr int kInlineSegs = 320;
-constexpr int kInlineCtas = 160;
-constexpr int kInlineUnits = 256;
-constexpr int kInlineBatch = 256;
-
-struct DecodeInlinePlan {
-  DecodeSeg segs[kInlineSegs];
-  int32_t cta_seg[kInlineCtas + 1];
-  int2 unit_parts[kInlineUnits];    // {first segment, number of segments} of every unit
-  int32_t kv_len[kInlineBatch];
-};
+// The plan (segments, per-CTA segment ranges, per-unit {first segment,
+// segment count}, kv lengths) lives in the workspace, uploaded with the call:
+// every byte of the kernel parameter block is sent with each launch, and a
+// plan carried there (~9 KB) cost ~1 us per launch.
 
 struct DecodeParams {
   CUtensorMap tm_k, tm_v;         // 2-D maps (row width in elements, rows), box (64, box_rows)
@@ -89,12 +96,10 @@ struct DecodeParams {
   int batch, num_heads, num_kv_heads, group;
   float scale_log2;
   DevStatus status;
-  int plan_inline;                // 1: the plan below; 0: the pointers
   const DecodeSeg* segs;
   const int32_t* cta_seg;
-  const int2* unit_parts;
+  const int2* unit_parts;         // {first segment, number of segments} of every unit
   const int32_t* kv_len;
-  DecodeInlinePlan plan;
 };
 
 // MLA decode (latent D = 512 shared by key and value, plus a 64-d rope part of
@@ -121,12 +126,10 @@ struct MlaParams {
   int num_heads;
   float scale_log2;
   DevStatus status;
-  int plan_inline;
   const DecodeSeg* segs;
   const int32_t* cta_seg;         // per pair
   const int2* unit_parts;
   const int32_t* kv_len;
-  DecodeInlinePlan plan;
 };
 
 // Records the detail string fia_last_error() returns on this thread.

@@ -53,10 +53,10 @@ struct MlaBars {
 static_assert(sizeof(MlaBars) <= 512, "barrier area");
 static_assert(kMlaSmem <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ const DecodeSeg* mla_segs(const MlaParams& p) { return p.plan_inline ? p.plan.segs : p.segs; }
-__device__ __forceinline__ const int32_t* mla_cta(const MlaParams& p) { return p.plan_inline ? p.plan.cta_seg : p.cta_seg; }
-__device__ __forceinline__ const int2* mla_units(const MlaParams& p) { return p.plan_inline ? p.plan.unit_parts : p.unit_parts; }
-__device__ __forceinline__ const int32_t* mla_kvlen(const MlaParams& p) { return p.plan_inline ? p.plan.kv_len : p.kv_len; }
+__device__ __forceinline__ const DecodeSeg* mla_segs(const MlaParams& p) { return p.segs; }
+__device__ __forceinline__ const int32_t* mla_cta(const MlaParams& p) { return p.cta_seg; }
+__device__ __forceinline__ const int2* mla_units(const MlaParams& p) { return p.unit_parts; }
+__device__ __forceinline__ const int32_t* mla_kvlen(const MlaParams& p) { return p.kv_len; }
 
 __device__ __forceinline__ float mla_warp_max(float v) {
 #pragma unroll
@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(256, 1) mla_kernel(const __grid_constant__ Mla
 template <bool BF16>
 cudaError_t launch_mla_t(const MlaParams& p, cudaStream_t s) {
   auto k = mla_kernel<BF16>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem);
+  cudaError_t e = set_smem_once<mla_kernel<BF16>>(kMlaSmem);
   if (e != cudaSuccess) return e;
   k<<<p.n_pairs > 0 ? 2 * p.n_pairs : 2, 256, kMlaSmem, s>>>(p);
   return cudaGetLastError();

@@ -259,8 +259,26 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
       const float m_use = (m == -INFINITY || m_new > m + 8.f) ? m_new : m;
       const float alpha = (m_use == m) ? 1.f : fast_exp2(m - m_use);
       const float mo = (m_use == -INFINITY) ? 0.f : m_use;
-      const float sum = exp2_and_sum<128>(x, sl2, mo);
-      l = l * alpha + sum;
+      // p = 2^(s * scale * log2(e) - m) in packed pairs; the row sum in the
+      // same order as the two-tile kernel's, so an all-ones block-sparse mask
+      // reproduces dense prefill bit for bit.
+      {
+        const uint64_t sc2 = f2_pack(sl2, sl2), nmo2 = f2_pack(-mo, -mo);
+        uint64_t acc2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nmo2), y0, y1);
+          y0 = fast_exp2(y0);
+          y1 = fast_exp2(y1);
+          acc2[e & 1] = f2_add(acc2[e & 1], f2_pack(y0, y1));
+          x[2 * e] = y0;
+          x[2 * e + 1] = y1;
+        }
+        float s0, s1;
+        f2_unpack(f2_add(acc2[0], acc2[1]), s0, s1);
+        l = l * alpha + (s0 + s1);
+      }
       // O only has to hold P_{j-1} V_{j-1} when this warp rescales it; the next
       // P V accumulates after it on the tensor pipe anyway.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -366,7 +384,7 @@ template <int D, bool BF16, int MODE>
 static cudaError_t launch_one(const PrefillParams& p, cudaStream_t s) {
   using C = PrefillCfg<D>;
   auto k = prefill_kernel<D, BF16, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = set_smem_once<prefill_kernel<D, BF16, MODE>>(C::kSmem);
   if (e != cudaSuccess) return e;
   k<<<p.n_items, C::kThreads, C::kSmem, s>>>(p);
   return cudaGetLastError();

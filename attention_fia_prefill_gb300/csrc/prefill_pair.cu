@@ -428,7 +428,7 @@ template <int D, bool BF16, int MODE>
 cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
   using C = PairCfg<D>;
   auto k = prefill_pair_kernel<D, BF16, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = set_smem_once<prefill_pair_kernel<D, BF16, MODE>>(C::kSmem);
   if (e != cudaSuccess) return e;
   k<<<p.n_items, C::kThreads, C::kSmem, s>>>(p);
   return cudaGetLastError();
