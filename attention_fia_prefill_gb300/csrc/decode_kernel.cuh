@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
       int last = 0;
       if (lane == 0) {
         unsigned long long* ctr = p.unit_counter + sg.unit;
-        const unsigned long long tag = (p.status.epoch & 0xffffffffull) << 32;
+        const unsigned long long tag = unit_tag(p.status.epoch);
         unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr), nxt, prev;
         while (true) {
           nxt = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : (tag | 1ull);

@@ -91,7 +91,7 @@ struct DecodeParams {
   int64_t lse_sb, lse_sn;
   float* part_o;                  // [n_segments, group, D]
   float* part_lse;                // [n_segments, group] natural log, -inf = empty
-  unsigned long long* unit_counter;   // [n_units] (epoch << 32) | segments finished
+  unsigned long long* unit_counter;   // [n_units] (unit_tag(epoch): high half) | segments finished
   int n_cta, n_units;
   int batch, num_heads, num_kv_heads, group;
   float scale_log2;
@@ -121,7 +121,7 @@ struct MlaParams {
   float* part_o;                  // [2 halves][n_segments][Q_N][256]
   float* part_lse;                // [2 halves][n_segments][Q_N]
   int64_t part_stride_o, part_stride_lse;   // elements per half
-  unsigned long long* unit_counter;   // [B][2] (epoch << 32) | segments finished
+  unsigned long long* unit_counter;   // [B][2] (unit_tag(epoch): high half) | segments finished
   int n_pairs, n_units;
   int num_heads;
   float scale_log2;

@@ -95,6 +95,17 @@ struct DevStatus {
   unsigned long long epoch;
 };
 
+// Tag of a call in the high half of a per-unit completion counter.  The
+// counters live in the caller's workspace, whose bytes may hold whatever an
+// earlier call left there (plan entries, partial results): a bare epoch, a
+// small integer, would match such leftovers.  The epoch is spread over 31
+// bits (multiplicative hashing with the golden-ratio constant, Knuth) and the
+// top bit set, so a stale word matches a given call with probability 2^-31.
+__device__ __forceinline__ unsigned long long unit_tag(unsigned long long epoch) {
+  const uint32_t x = (uint32_t(epoch) ^ uint32_t(epoch >> 32)) * 2654435761u;
+  return (unsigned long long)(x | 0x80000000u) << 32;
+}
+
 __device__ __forceinline__ void status_stamp(const DevStatus& st) {
   if (st.word != nullptr) atomicExch(st.word, st.epoch << 8);
 }
