@@ -281,14 +281,21 @@ def paged_rows(pool: np.ndarray, table: np.ndarray, b: int, kvh: int, L: int, bs
 
 def fia_decode(q, k, v, *, num_heads: int, num_key_value_heads: int = 0, scale_value: float = 1.0,
                input_layout: str = "BNSD", actual_seq_kvlen=None, block_table=None, block_size: int = 0,
-               query_rope=None, key_rope=None, atten_mask=None, rows=None):
-    """Incremental attention (Q_S = 1).  sparse_mode / pre_tokens / next_tokens
-    do not apply to Q_S = 1 without rope (parameter descriptions).
+               query_rope=None, key_rope=None, atten_mask=None, rows=None, sparse_mode: int = 0):
+    """Incremental attention against a (paged) KV cache.  With Q_S = 1 the
+    sparse_mode / pre_tokens / next_tokens parameters do not apply
+    (npu_fused_infer_attention_score_v2, parameter descriptions).  With Q_S > 1
+    query tokens (several new tokens per step) the mask is the formula's
+    sparse_mode pattern over the Q_S x S_kv score block: 0 none, 2 left-up
+    causal (j <= i), 3 right-down causal (j <= i + S_kv - Q_S, the last query
+    token seeing the whole cache).
 
-    q: BNSD (B,N1,1,D), BSND (B,1,N1,D) or BSH (B,1,N1*D).  With block_table,
-    k/v are paged pools; otherwise k/v follow input_layout.  With query_rope /
-    key_rope (MLA) scores add q_rope . k_rope and key_rope is paged like k.
-    Returns (out in q's layout, lse (B, N1, 1, 1)); with rows=[(b,h)] returns pairs."""
+    q: BNSD (B,N1,Q_S,D), BSND (B,Q_S,N1,D) or BSH (B,Q_S,N1*D).  With
+    block_table, k/v are paged pools; otherwise k/v follow input_layout.  With
+    query_rope / key_rope (MLA) scores add q_rope . k_rope and key_rope is
+    paged like k.  Returns (out in q's layout, lse (B, N1, Q_S, 1)); with
+    rows=[(b,h)] returns pairs (out row, lse) for Q_S = 1, else (out rows
+    (Q_S, D_v), lse (Q_S,))."""
     N1 = int(num_heads)
     N2 = int(num_key_value_heads) or N1
     g = N1 // N2
@@ -329,17 +336,19 @@ def fia_decode(q, k, v, *, num_heads: int, num_key_value_heads: int = 0, scale_v
 
         def vrows(b, h): return Vb[b, h // g, :kl[b], :]
 
+    QS = Q.shape[2]
+
     def qrow(b, h):
-        qq = Q[b, h, :1, :]
+        qq = Q[b, h, :, :]
         if QR is not None:
-            qq = np.concatenate([qq, QR[b, h, :1, :]], axis=1)
+            qq = np.concatenate([qq, QR[b, h, :, :]], axis=1)
         return qq
 
     def allowed(b):
         m = _mask_for_batch_decode(atten_mask, b)
-        ok = np.ones((1, kl[b]), dtype=bool)
+        ok = allowed_matrix(QS, kl[b], sparse_mode if QS > 1 else 0)
         if m is not None:
-            ok &= (m[:kl[b]] == 0)[None, :]
+            ok = ok & (m[:kl[b]] == 0)[None, :]
         return ok
 
     if rows is not None:
@@ -351,18 +360,18 @@ def fia_decode(q, k, v, *, num_heads: int, num_key_value_heads: int = 0, scale_v
                 cache[key] = (krows(b, h), vrows(b, h))
             kk, vv = cache[key]
             o, l = attention_rows(qrow(b, h), kk, vv, allowed(b), scale_value)
-            res.append((o[0], l[0]))
+            res.append((o[0], l[0]) if QS == 1 else (o, l))
         return res
 
-    out = np.zeros((B, N1, 1, Dv))
-    lse = np.full((B, N1, 1, 1), np.inf)
+    out = np.zeros((B, N1, QS, Dv))
+    lse = np.full((B, N1, QS, 1), np.inf)
     for b in range(B):
         for kvh in range(N2):
             kk, vv = krows(b, kvh * g), vrows(b, kvh * g)
             for h in range(kvh * g, (kvh + 1) * g):
                 o, l = attention_rows(qrow(b, h), kk, vv, allowed(b), scale_value)
-                out[b, h, 0] = o[0]
-                lse[b, h, 0, 0] = l[0]
+                out[b, h] = o
+                lse[b, h, :, 0] = l
     return _from_bnsd(out, input_layout), lse
 
 

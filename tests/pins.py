@@ -241,6 +241,38 @@ def check_decode_equals_prefill_row(orc):
     assert np.allclose(o1, o2, atol=ATOL) and np.allclose(l1, l2, atol=ATOL), "decode == one-row prefill"
 
 
+def check_multitoken_decode_vs_library(orc):
+    """Q_S new tokens against a paged cache, right-down causal (sparse_mode 3):
+    token t of a sequence of L keys sees keys 0 .. L - Q_S + t.  Reference: the
+    cache gathered here by hand and the library's attention with that mask;
+    mode 0 lets every token see the whole cache."""
+    B, N1, N2, QS, D, bs = 2, 4, 2, 3, 8, 4
+    lens = [10, 2]
+    nblk = 6
+    kp, vp = _rand((nblk, N2, bs, D), 90), _rand((nblk, N2, bs, D), 91)
+    table = np.array([[4, 1, 5], [0, 2, 3]], dtype=np.int32)
+    q = _rand((B, N1, QS, D), 92)
+    for mode in (3, 0):
+        out, lse = orc.fia_decode(q, kp, vp, num_heads=N1, num_key_value_heads=N2, scale_value=0.35,
+                                  input_layout="BNSD", actual_seq_kvlen=lens, block_table=table, block_size=bs,
+                                  sparse_mode=mode)
+        assert out.shape == (B, N1, QS, D) and lse.shape == (B, N1, QS, 1)
+        for b in range(B):
+            L = lens[b]
+            for h in range(N1):
+                kv = h // (N1 // N2)
+                kk = torch.stack([kp[table[b, j // bs], kv, j % bs] for j in range(L)])
+                vv = torch.stack([vp[table[b, j // bs], kv, j % bs] for j in range(L)])
+                allowed = np.array([[mode == 0 or j <= L - QS + t for j in range(L)] for t in range(QS)])
+                live = allowed.any(axis=1)
+                ref = _sdpa(q[b, h].numpy()[live], kk.numpy(), vv.numpy(), allowed[live], 0.35)
+                assert np.allclose(out[b, h][live], ref, atol=ATOL), "multi-token decode != library attention"
+                s = 0.35 * (q[b, h].numpy() @ kk.numpy().T)
+                ref_lse = logsumexp(np.where(allowed[live], s[live], -np.inf), axis=1)
+                assert np.allclose(lse[b, h, live, 0], ref_lse, atol=ATOL), "multi-token lse"
+                assert np.all(out[b, h][~live] == 0) and np.all(np.isinf(lse[b, h, ~live, 0])), "tokens with no key"
+
+
 def check_mla_equals_concatenated_attention(orc):
     B, N1, Dl, Dr, bs = 2, 4, 16, 4, 4
     lens = [7, 8]
@@ -306,6 +338,7 @@ ALL_CHECKS = [
     check_rows_vs_library, check_prefill_causal_vs_library, check_gqa_vs_library, check_closed_forms,
     check_mask_modes_by_counting, check_softmax_rows_sum_to_one, check_layouts_agree,
     check_tnd_equals_per_sequence, check_actual_lengths_equal_truncation, check_paged_equals_contiguous,
-    check_decode_equals_prefill_row, check_mla_equals_concatenated_attention, check_bsa, check_lse_merge,
+    check_decode_equals_prefill_row, check_multitoken_decode_vs_library, check_mla_equals_concatenated_attention,
+    check_bsa, check_lse_merge,
     check_empty_rules,
 ]

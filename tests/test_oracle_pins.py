@@ -40,6 +40,9 @@ MUTATIONS = [
      "kl = resolve_lengths(None, B, Kb.shape[2])\n        Dv = Vb.shape[3]", "decode ignores kv lengths"),
     ("kk = np.concatenate([kk, paged_rows(KR, table, b, h // g, kl[b], block_size, Dr)], axis=1)",
      "kk = kk", "MLA rope term dropped"),
+    ("ok = allowed_matrix(QS, kl[b], sparse_mode if QS > 1 else 0)", "ok = allowed_matrix(QS, kl[b], 0)",
+     "multi-token decode ignores its mask"),
+    ("qq = Q[b, h, :, :]", "qq = Q[b, h, :1, :]", "multi-token decode uses the first token only"),
 ]
 
 
