@@ -228,19 +228,21 @@ def fia_prefill(query, key, value, *, atten_mask=None, actual_seq_qlen=None, act
 
 def fia_decode(query, key, value, *, query_rope=None, key_rope=None, block_table=None, block_size=0,
                actual_seq_kvlen=None, atten_mask=None, num_heads=1, num_key_value_heads=0, scale_value=1.0,
-               input_layout="BSH", softmax_lse_flag=False, inner_precise=0, out=None, softmax_lse=None,
-               workspace=None):
-    """Incremental attention (Q_S = 1), paged or contiguous, optionally MLA."""
+               input_layout="BSH", sparse_mode=0, softmax_lse_flag=False, inner_precise=0, out=None,
+               softmax_lse=None, workspace=None):
+    """Incremental attention against a paged or contiguous cache, optionally
+    MLA.  Q_S = 1, or up to 16 new tokens per sequence (sparse_mode 0, 2 or 3
+    over the Q_S x S_kv block; 3 = each token sees the cache up to itself)."""
     import torch
     _require_cuda(query, key, value, query_rope, key_rope, block_table)
     lib = load_library()
     prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
-                 input_layout=input_layout, actual_seq_kvlen=actual_seq_kvlen, block_size=block_size,
-                 softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
+                 input_layout=input_layout, sparse_mode=sparse_mode, actual_seq_kvlen=actual_seq_kvlen,
+                 block_size=block_size, softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
     if out is None:
         out = torch.empty_like(query)
     if softmax_lse_flag and softmax_lse is None:
-        softmax_lse = torch.empty((query.shape[0], num_heads, 1, 1), dtype=torch.float32, device=query.device)
+        softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
     descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, block_table, atten_mask, out,
                                       softmax_lse)]
     dq, dk, dv, dqr, dkr, dbt, dm, do, dl = descs
@@ -257,15 +259,16 @@ def fia_decode(query, key, value, *, query_rope=None, key_rope=None, block_table
 
 def fia_decode_no_alloc(query, key, value, *, out, softmax_lse=None, query_rope=None, key_rope=None,
                         block_table=None, block_size=0, actual_seq_kvlen=None, atten_mask=None, num_heads=1,
-                        num_key_value_heads=0, scale_value=1.0, input_layout="BSH", inner_precise=0):
+                        num_key_value_heads=0, scale_value=1.0, input_layout="BSH", sparse_mode=0,
+                        inner_precise=0):
     """fia_decode for callers that cannot allocate device memory: the caller
     passes every output buffer and the library supplies the scratch from its
     built-in array (see include/fia.h).  Nothing is allocated here."""
     _require_cuda(query, key, value, query_rope, key_rope, block_table, out, softmax_lse)
     lib = load_library()
     prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
-                 input_layout=input_layout, actual_seq_kvlen=actual_seq_kvlen, block_size=block_size,
-                 softmax_lse_flag=softmax_lse is not None, inner_precise=inner_precise)
+                 input_layout=input_layout, sparse_mode=sparse_mode, actual_seq_kvlen=actual_seq_kvlen,
+                 block_size=block_size, softmax_lse_flag=softmax_lse is not None, inner_precise=inner_precise)
     descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, block_table, atten_mask, out,
                                       softmax_lse)]
     dq, dk, dv, dqr, dkr, dbt, dm, do, dl = descs

@@ -207,7 +207,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
 template <int D, bool BF16>
 __device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2 up, int lane) {
   constexpr int KB = 8;   // parts per batch of loads
-  const int g = p.group;
+  const int g = p.rows;   // rows of the unit: heads x query tokens
   const int kvh = unit % p.num_kv_heads, b = unit / p.num_kv_heads;
   const int64_t s0 = up.x;
   const int ns = up.y;
@@ -258,17 +258,19 @@ __device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2
     for (int t = 0; t < 4; ++t) {
       const int hh = h0 + t;
       if (hh >= g) break;
-      const int head = kvh * g + hh;
+      const int head = kvh * p.group + hh / p.q_tokens, tok = hh % p.q_tokens;
       if (lane < D / 4) {
         const float inv = Ls[t] > 0.f ? 1.f / Ls[t] : 0.f;
-        T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * lane;
+        T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
+                  int64_t(tok) * p.out_ss + 4 * lane;
         uint2 w2;
         w2.x = pack2(acc[t].x * inv, acc[t].y * inv, BF16);
         w2.y = pack2(acc[t].z * inv, acc[t].w * inv, BF16);
         *reinterpret_cast<uint2*>(orow) = w2;
       }
       if (lane == 0 && p.lse != nullptr)
-        p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = Ls[t] > 0.f ? M[t] + __logf(Ls[t]) : INFINITY;
+        p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] =
+            Ls[t] > 0.f ? M[t] + __logf(Ls[t]) : INFINITY;
     }
   }
 }
@@ -313,14 +315,17 @@ struct QPieces {
 
 template <int D, int GL>
 __device__ __forceinline__ void q_load(const DecodeParams& p, int unit, int t, QPieces<D, GL>& q) {
-  const int g = p.group;
   const int kvh = unit % p.num_kv_heads, b = unit / p.num_kv_heads;
-  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                    (int64_t(b) * p.num_heads + int64_t(kvh) * g) * D);
+  const uint16_t* qb = static_cast<const uint16_t*>(p.q) + int64_t(b) * p.q_sb;
 #pragma unroll
   for (int i = 0; i < QPieces<D, GL>::kPer; ++i) {
     const int piece = t + 128 * i;
-    if (piece < g * (D / 8)) q.v[i] = src[piece];
+    const int row = piece / (D / 8);   // head kvh * group + row / Q_S, token row % Q_S
+    if (row < p.rows) {
+      const int head = kvh * p.group + row / p.q_tokens, tok = row % p.q_tokens;
+      q.v[i] = *reinterpret_cast<const uint4*>(qb + int64_t(head) * p.q_sn + int64_t(tok) * p.q_ss +
+                                               (piece % (D / 8)) * 8);
+    }
   }
 }
 
@@ -356,7 +361,7 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
   const int32_t* kvlen = plan_kvlen(p);
   const int seg_begin = p.n_cta > 0 ? cta_seg[blockIdx.x] : 0;
   const int seg_end = p.n_cta > 0 ? cta_seg[blockIdx.x + 1] : 0;
-  const int g = p.group;
+  const int g = p.rows;   // rows of a unit (of S^T's N): heads x query tokens
 
   if (threadIdx.x == 0) {
     if (blockIdx.x == 0) status_stamp(p.status);
@@ -562,12 +567,14 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         if (unit_parts[u].y != 0) continue;
         const int kvh = u % p.num_kv_heads, b = u / p.num_kv_heads;
         for (int hh = 0; hh < g; ++hh) {
-          const int head = kvh * g + hh;
+          const int head = kvh * p.group + hh / p.q_tokens, tok = hh % p.q_tokens;
           if (lane < D / 4) {
-            T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + 4 * lane;
+            T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
+                      int64_t(tok) * p.out_ss + 4 * lane;
             *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
           }
-          if (lane == 0 && p.lse != nullptr) p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] = INFINITY;
+          if (lane == 0 && p.lse != nullptr)
+            p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] = INFINITY;
         }
       }
     }
@@ -647,11 +654,17 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         tmem_load_cols<GL>(tmem + lane_off + (j & 1) * G, su);
         const int nvalid = min(128, L - st * 128);
         const bool valid = r < nvalid;
+        // several query tokens: row h is token h % Q_S, which sees keys up to
+        // klim + h % Q_S (sparse_mode 3: klim = S_kv - Q_S; 2: klim = 0)
+        const bool causal = p.q_causal != 0;
+        const int kfrom = st * 128 + r - (p.q_causal == 3 ? L - p.q_tokens : 0);
         float s[GL];
         bool raise = false;
 #pragma unroll
         for (int h = 0; h < GL; ++h) {
-          s[h] = (valid && h < g) ? __uint_as_float(su[h]) * sl2 : -INFINITY;
+          bool live = valid && h < g;
+          if (causal) live = live && kfrom <= h % p.q_tokens;
+          s[h] = live ? __uint_as_float(su[h]) * sl2 : -INFINITY;
           raise |= s[h] > m[h] + 8.f;
         }
         // publish the warp maxima and the vote; meet the other three warps
@@ -761,14 +774,14 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
           const float l = (w4.x + w4.y) + (w4.z + w4.w);
           const bool has = l > 0.f;
           if (whole) {
-            const int head = kvh * g + h;
+            const int head = kvh * p.group + h / p.q_tokens, tok = h % p.q_tokens;
             if (r < D) {
               const uint32_t bits = pack2(has ? acc[h] / l : 0.f, 0.f, BF16);
-              reinterpret_cast<uint16_t*>(p.out)[int64_t(b) * p.out_sb + int64_t(head) * p.out_sn + r] =
-                  uint16_t(bits & 0xffffu);
+              reinterpret_cast<uint16_t*>(p.out)[int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
+                                                 int64_t(tok) * p.out_ss + r] = uint16_t(bits & 0xffffu);
             }
             if (r == h && p.lse != nullptr)
-              p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn] =
+              p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] =
                   has ? (m[h] + __log2f(l)) * 0.69314718055994531f : INFINITY;
           } else {
             if (r < D) p.part_o[(part * g + h) * D + r] = has ? acc[h] / l : 0.f;
@@ -806,11 +819,11 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t s) {
 template <int D, bool BF16>
 cudaError_t launch_decode_group(const DecodeParams& p, cudaStream_t s) {
   static_assert(sizeof(DecodeBars) <= 512, "barrier area too small");
-  if (p.group <= 4) return launch_decode_t<D, BF16, 4>(p, s);
-  if (p.group <= 8) return launch_decode_t<D, BF16, 8>(p, s);
-  if (p.group <= 16) return launch_decode_t<D, BF16, 16>(p, s);
-  if (p.group <= 32) return launch_decode_t<D, BF16, 32>(p, s);
-  if (p.group <= 64) return launch_decode_t<D, BF16, 64>(p, s);
+  if (p.rows <= 4) return launch_decode_t<D, BF16, 4>(p, s);
+  if (p.rows <= 8) return launch_decode_t<D, BF16, 8>(p, s);
+  if (p.rows <= 16) return launch_decode_t<D, BF16, 16>(p, s);
+  if (p.rows <= 32) return launch_decode_t<D, BF16, 32>(p, s);
+  if (p.rows <= 64) return launch_decode_t<D, BF16, 64>(p, s);
   return cudaErrorInvalidValue;
 }
 

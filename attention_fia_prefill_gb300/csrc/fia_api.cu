@@ -660,7 +660,10 @@ struct DecodeGeometry {
   bool bf16, paged, mla, kv_bnbd;
   int64_t bs, nblk, S2;
   std::vector<int32_t> kv_len;
-  int64_t q_sb, q_sn, o_sb, o_sn;
+  int64_t q_sb, q_sn, q_ss, o_sb, o_sn, o_ss;
+  int64_t QS = 1;         // query tokens per sequence
+  int q_causal = 0;       // with QS > 1: sparse_mode 0, 2 or 3
+  int64_t rows() const { return (N1 / N2) * QS; }
 };
 
 fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_tensor* qr,
@@ -683,7 +686,17 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
   int64_t Bq, Sq, D;
   st = dense_dims(q, g.layout, g.N1, Bq, Sq, D, "query");
   if (st != FIA_OK) return st;
-  if (Sq != 1) return fail(FIA_ERR_UNSUPPORTED, "fia_decode takes Q_S = 1 (got %lld)", (long long)Sq);
+  // Several new tokens per sequence: the unit's rows are its heads x tokens,
+  // at most 64 (the widest kernel tile), and the mask over the Q_S x S_kv block
+  // is none (0) or causal (2 top-left, 3 bottom-right).
+  if (Sq < 1 || Sq > 16) return fail(FIA_ERR_UNSUPPORTED, "fia_decode takes Q_S in 1..16 (got %lld)", (long long)Sq);
+  g.QS = Sq;
+  if (Sq > 1) {
+    const int64_t sm = p->sparse_mode;
+    if (sm != 0 && sm != 2 && sm != 3)
+      return fail(FIA_ERR_UNSUPPORTED, "decode with Q_S > 1 takes sparse_mode 0, 2 or 3 (got %lld)", (long long)sm);
+    g.q_causal = int(sm);
+  }
   g.B = Bq;
   g.D = D;
   g.bf16 = q->dtype == FIA_DTYPE_BF16;
@@ -692,9 +705,9 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
   if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data))
     return fail(FIA_ERR_ALIGNMENT, "query/key/value/attention_out must be 16-byte aligned");
   int64_t qs[3];
-  bns_strides(g.layout, g.N1, 1, D, qs);
-  g.q_sb = qs[0]; g.q_sn = qs[1];
-  g.o_sb = qs[0]; g.o_sn = qs[1];
+  bns_strides(g.layout, g.N1, Sq, D, qs);
+  g.q_sb = qs[0]; g.q_sn = qs[1]; g.q_ss = qs[2];
+  g.o_sb = qs[0]; g.o_sn = qs[1]; g.o_ss = qs[2];
   g.paged = present(table);
   if (g.paged) {
     if (table->dtype != FIA_DTYPE_I32 || table->ndim != 2 || table->shape[0] != g.B)
@@ -741,6 +754,7 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
   if (g.mla) {
     // MLA: key = value = the 512-d latent cache, plus a 64-d rope part of q and k
     if (D != 512) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes a 512-d latent query (got %lld)", (long long)D);
+    if (g.QS != 1) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes Q_S = 1");
     if (g.N2 != 1) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes num_key_value_heads = 1");
     if (g.N1 > 128) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes at most 128 query heads");
     if (qr->dtype != q->dtype || kr->dtype != q->dtype) return fail(FIA_ERR_DTYPE, "query_rope/key_rope must match query");
@@ -754,6 +768,8 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
     return FIA_OK;
   }
   if (D != 64 && D != 128) return fail(FIA_ERR_UNSUPPORTED, "decode head dim %lld (kernels take 64 or 128)", (long long)D);
+  if (g.rows() > 64)
+    return fail(FIA_ERR_UNSUPPORTED, "decode rows per KV head (Q_N / KV_N x Q_S = %lld) above 64", (long long)g.rows());
   g.Dv = D;
   return FIA_OK;
 }
@@ -866,7 +882,7 @@ DecodeWsLayout decode_ws_layout(size_t n_segs, size_t n_cta, size_t n_units, siz
 size_t decode_ws_bound(const DecodeGeometry& g) {
   const size_t n_units = size_t(g.B * g.N2);
   const size_t n_segs = n_units + kMaxDecodeCtas;
-  const size_t rows = size_t(g.N1 / g.N2);
+  const size_t rows = size_t(g.rows());
   return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), rows, size_t(g.D), true).total;
 }
 
@@ -897,12 +913,12 @@ size_t mla_ws_bound(const DecodeGeometry& g) {
   return mla_ws_layout(n_segs, kMlaMaxPairs, size_t(g.B), size_t(g.N1), true).total;
 }
 
-fia_status check_decode_lse(const fia_tensor* lse, const fia_params* p, int64_t B, int64_t N1) {
+fia_status check_decode_lse(const fia_tensor* lse, const fia_params* p, int64_t B, int64_t N1, int64_t QS) {
   if (p->softmax_lse_flag == 0) return FIA_OK;
   if (!present(lse)) return fail(FIA_ERR_NULL, "softmax_lse_flag set but softmax_lse absent");
   if (lse->dtype != FIA_DTYPE_F32) return fail(FIA_ERR_DTYPE, "softmax_lse must be fp32");
-  if (!(lse->ndim == 4 && lse->shape[0] == B && lse->shape[1] == N1 && lse->shape[2] == 1 && lse->shape[3] == 1))
-    return fail(FIA_ERR_SHAPE, "softmax_lse must be (B, N1, 1, 1)");
+  if (!(lse->ndim == 4 && lse->shape[0] == B && lse->shape[1] == N1 && lse->shape[2] == QS && lse->shape[3] == 1))
+    return fail(FIA_ERR_SHAPE, "softmax_lse must be (B, N1, Q_S, 1)");
   return FIA_OK;
 }
 
@@ -996,7 +1012,7 @@ fia_status fia_decode_get_workspace_size(const fia_tensor* query, const fia_tens
   DecodeGeometry g;
   fia_status st = decode_geometry(query, key, value, query_rope, key_rope, block_table, atten_mask, params, attention_out, g);
   if (st != FIA_OK) return st;
-  st = check_decode_lse(softmax_lse, params, g.B, g.N1);
+  st = check_decode_lse(softmax_lse, params, g.B, g.N1, g.QS);
   if (st != FIA_OK) return st;
   *workspace_bytes = g.mla ? mla_ws_bound(g) : decode_ws_bound(g);
   return FIA_OK;
@@ -1010,7 +1026,7 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   DecodeGeometry g;
   fia_status st = decode_geometry(query, key, value, query_rope, key_rope, block_table, atten_mask, params, attention_out, g);
   if (st != FIA_OK) return st;
-  st = check_decode_lse(softmax_lse, params, g.B, g.N1);
+  st = check_decode_lse(softmax_lse, params, g.B, g.N1, g.QS);
   if (st != FIA_OK) return st;
   cudaStream_t stream_t = static_cast<cudaStream_t>(stream);
   if (g.mla)
@@ -1018,7 +1034,7 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
                    workspace_bytes, stream_t);
   DecodePlan pl;
   plan_decode(g, sm_count(), pl, 128, kDecodeSegmentCost);
-  const size_t rows = size_t(g.N1 / g.N2);
+  const size_t rows = size_t(g.rows());
   const DecodeWsLayout w = decode_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B), rows,
                                             size_t(g.D), true);
   st = check_ws(workspace, workspace_bytes, w.total);
@@ -1066,10 +1082,14 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
     if (st != FIA_OK) return st;
   }
   dp.q = query->data;
+  dp.q_sb = g.q_sb; dp.q_sn = g.q_sn; dp.q_ss = g.q_ss;
   dp.out = attention_out->data;
-  dp.out_sb = g.o_sb; dp.out_sn = g.o_sn;
+  dp.out_sb = g.o_sb; dp.out_sn = g.o_sn; dp.out_ss = g.o_ss;
   dp.lse = (params->softmax_lse_flag && present(softmax_lse)) ? static_cast<float*>(softmax_lse->data) : nullptr;
-  dp.lse_sb = g.N1; dp.lse_sn = 1;
+  dp.lse_sb = g.N1 * g.QS; dp.lse_sn = g.QS; dp.lse_ss = 1;   // (B, N1, Q_S, 1)
+  dp.q_tokens = int(g.QS);
+  dp.q_causal = g.q_causal;
+  dp.rows = int(g.rows());
   dp.part_o = reinterpret_cast<float*>(base + w.off_po);
   dp.part_lse = reinterpret_cast<float*>(base + w.off_pl);
   dp.unit_counter = reinterpret_cast<unsigned long long*>(base + w.off_ctr);

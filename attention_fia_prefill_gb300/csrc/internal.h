@@ -84,13 +84,19 @@ struct DecodeParams {
   int32_t col_per_head;           // map column offset between kv heads
   const int32_t* block_table;     // nullable (contiguous)
   int64_t table_stride;
-  const void* q;                  // query row (b * Q_N + h) of D elements
+  // Row r of a unit (rows = group * q_tokens): head kvh * group + r / q_tokens,
+  // query token r % q_tokens.  Element strides of q / out / lse for (b, n, s).
+  const void* q;
+  int64_t q_sb, q_sn, q_ss;
   void* out;
-  int64_t out_sb, out_sn;
+  int64_t out_sb, out_sn, out_ss;
   float* lse;                     // nullable
-  int64_t lse_sb, lse_sn;
-  float* part_o;                  // [n_segments, group, D]
-  float* part_lse;                // [n_segments, group] natural log, -inf = empty
+  int64_t lse_sb, lse_sn, lse_ss;
+  int q_tokens;                   // Q_S (1..16)
+  int q_causal;                   // with Q_S > 1: 0 none, 2 key <= token, 3 key <= S_kv - Q_S + token
+  int rows;                       // group * q_tokens (<= 64)
+  float* part_o;                  // [n_segments, rows, D]
+  float* part_lse;                // [n_segments, rows] natural log, -inf = empty
   unsigned long long* unit_counter;   // [n_units] (unit_tag(epoch): high half) | segments finished
   int n_cta, n_units;
   int batch, num_heads, num_kv_heads, group;

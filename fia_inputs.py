@@ -132,7 +132,7 @@ class DecodeCase:
 
 
 def paged_decode_case(B, N1, N2, D, kv_lens, block_size=128, dtype="bf16", workload=200,
-                      extra_table_cols=1, poison=True, layout_kv="BNBD") -> DecodeCase:
+                      extra_table_cols=1, poison=True, layout_kv="BNBD", q_tokens=1) -> DecodeCase:
     """Paged KV cache: each sequence's logical blocks map to a random permutation of
     a shared physical pool.  One extra pool block is filled with NaN; unused
     block_table entries point at it, as do the unused tail rows of each sequence's
@@ -166,7 +166,7 @@ def paged_decode_case(B, N1, N2, D, kv_lens, block_size=128, dtype="bf16", workl
                     k[last, :, tail:] = float("nan"); v[last, :, tail:] = float("nan")
                 else:
                     k[last, tail:] = float("nan"); v[last, tail:] = float("nan")
-    q = normal((B, N1, 1, D), dtype, workload, 1)
+    q = normal((B, N1, q_tokens, D), dtype, workload, 1)
     return DecodeCase(q, k, v, torch.from_numpy(table), list(kv_lens), block_size, N1, N2,
                       1.0 / math.sqrt(D), {"poison_block": poison_id, "layout_kv": layout_kv})
 

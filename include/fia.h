@@ -10,8 +10,9 @@
  *
  * Three entry points cover the pages' cases:
  *   fia_prefill  -- full attention, Q_S >= 1 (PromptFlashAttention)
- *   fia_decode   -- incremental attention, Q_S = 1, paged or contiguous KV cache,
- *                   optionally MLA (query_rope / key_rope) (IncreFlashAttention)
+ *   fia_decode   -- incremental attention, Q_S = 1 (or up to 16 new tokens),
+ *                   paged or contiguous KV cache, optionally MLA (query_rope /
+ *                   key_rope) (IncreFlashAttention)
  *   bsa_forward  -- block-sparse attention selected by blockSparseMask
  *                   (aclnnBlockSparseAttentionV2)
  * Each has a first phase that validates the arguments and reports the scratch
@@ -136,8 +137,14 @@ FIA_API fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, c
                        const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
- * fia_decode: incremental attention, one query token per batch (Q_S = 1).
- *   query  (B,N1,1,D) BNSD | (B,1,N1,D) BSND | (B,1,H) BSH; f16 or bf16.
+ * fia_decode: incremental attention, Q_S new query tokens per batch.
+ *   query  (B,N1,Q_S,D) BNSD | (B,Q_S,N1,D) BSND | (B,Q_S,H) BSH; f16 or bf16.
+ *          Q_S = 1, or 2..16 with (N1 / N2) * Q_S <= 64 (not with MLA); then
+ *          sparse_mode masks the Q_S x S_kv block as in the formula
+ *          (npu_fused_infer_attention_score_v2, sparse_mode): 0 none, 2 key j
+ *          <= token i, 3 key j <= i + S_kv - Q_S (the last token sees the whole
+ *          cache); other modes return FIA_ERR_UNSUPPORTED.  With Q_S = 1
+ *          sparse_mode is ignored, as on the pages.
  *   key/value, contiguous (block_table absent): the query's layout with N2 heads.
  *   key/value, paged (block_table present, PageAttention):
  *          (blocknum, N2, block_size, D)  or  (blocknum, block_size, N2*D);
@@ -149,7 +156,7 @@ FIA_API fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, c
  *          (blocknum, block_size, 512), key_rope (blocknum, block_size, 64).
  *          scores = scale * (q . k + q_rope . k_rope).
  *   atten_mask: must be absent (masked decode is not implemented).
- *   attention_out: the query's shape; softmax_lse fp32 (B,N1,1,1) if flagged.
+ *   attention_out: the query's shape; softmax_lse fp32 (B,N1,Q_S,1) if flagged.
  * ------------------------------------------------------------------------ */
 FIA_API fia_status fia_decode_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
                                          const fia_tensor* query_rope, const fia_tensor* key_rope,

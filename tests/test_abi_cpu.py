@@ -184,9 +184,27 @@ def test_decode_rope_pairing(lib):
     assert r == 3
 
 
-def test_decode_needs_single_query_token(lib):
+def test_decode_query_token_limits(lib):
+    """Q_S new tokens: 1..16, heads-per-KV-head x Q_S rows at most 64, and
+    sparse_mode 0, 2 or 3 when Q_S > 1 (no MLA)."""
     q = t((2, 4, 3, 128))
-    r, _ = decode_ws(lib, q, q, q, params(lib, num_heads=4, input_layout="BNSD"))
+    r, _ = decode_ws(lib, q, q, q, params(lib, num_heads=4, input_layout="BNSD", sparse_mode=3))
+    assert r == 0
+    q17 = t((2, 4, 17, 128))
+    r, _ = decode_ws(lib, q17, q17, q17, params(lib, num_heads=4, input_layout="BNSD"))
+    assert r == 5
+    wide = t((2, 32, 3, 128))   # 32 heads on one KV head x 3 tokens = 96 rows
+    kv = t((2, 1, 3, 128))
+    r, _ = decode_ws(lib, wide, kv, kv, params(lib, num_heads=32, num_key_value_heads=1, input_layout="BNSD"))
+    assert r == 5
+    r, _ = decode_ws(lib, q, q, q, params(lib, num_heads=4, input_layout="BNSD", sparse_mode=4))
+    assert r == 5
+    qm = t((2, 2, 128, 512))
+    lat = t((16, 128, 512))
+    prm = params(lib, num_heads=128, num_key_value_heads=1, input_layout="BSND", block_size=128,
+                 actual_seq_kvlen=[256])
+    r, _ = decode_ws(lib, qm, lat, lat, prm, qr=t((2, 2, 128, 64)), kr=t((16, 128, 64)),
+                     table=t((2, 2), B.DTYPE_I32))
     assert r == 5
 
 

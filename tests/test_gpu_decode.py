@@ -156,9 +156,56 @@ def test_many_short_sequences(fia):
 
 @pytest.mark.gpu
 def test_plan_in_workspace(fia):
-    """More units than the launch parameters carry (here 320 > 256): the plan
-    is uploaded into the workspace instead."""
+    """A 160-batch plan (320 units, ~330 segments) read from the workspace."""
     rng = np.random.default_rng(77)
     lens = [int(x) for x in rng.integers(0, 300, size=160)]
     c = fia_inputs.paged_decode_case(len(lens), 8, 2, 128, lens, block_size=128, workload=3100)
     _check_paged(fia, c)
+
+
+# ------------------------------------------------------- several query tokens
+def _check_tokens(fia, c, mode):
+    out, lse = _run_paged(fia, c, sparse_mode=mode)
+    ro, rl = fia_oracle.fia_decode(c.q, c.k_pool, c.v_pool, num_heads=c.num_heads,
+                                   num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                                   input_layout="BNSD", actual_seq_kvlen=c.kv_lens, block_table=c.block_table,
+                                   block_size=c.block_size, sparse_mode=mode)
+    assert out.shape == c.q.shape and lse.shape == (c.q.shape[0], c.num_heads, c.q.shape[2], 1)
+    assert_out_close(out, ro, c.q.dtype)
+    assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("qs", [2, 4, 8])
+def test_query_tokens_causal(fia, qs):
+    """Q_S new tokens per sequence, right-down causal (sparse_mode 3): token t
+    sees the cache up to key S_kv - Q_S + t.  Lengths shorter than Q_S leave
+    the first tokens without keys (0 / +inf)."""
+    c = fia_inputs.paged_decode_case(4, 8, 2, 128, [300, 5, 1000, 129], block_size=64, workload=3200 + qs,
+                                     q_tokens=qs)
+    _check_tokens(fia, c, 3)
+
+
+@pytest.mark.parametrize("mode,qs,D,n1,n2", [(0, 4, 128, 8, 2), (2, 3, 128, 4, 4), (3, 16, 64, 4, 1),
+                                             (3, 2, 128, 32, 1)])
+def test_query_tokens_modes(fia, mode, qs, D, n1, n2):
+    """No mask, top-left causal, and the widest row count (64 = 4 heads x 16
+    tokens, 32 heads x 2 tokens)."""
+    c = fia_inputs.paged_decode_case(3, n1, n2, D, [700, 17, 2050], block_size=128, workload=3300 + mode + qs,
+                                     q_tokens=qs)
+    _check_tokens(fia, c, mode)
+
+
+def test_query_tokens_full_workload_sampled(fia):
+    """The headline paged workload (B=16, 32/8 heads, D=128, U[1,4096]) with
+    4 new tokens per sequence, causal: sampled (batch, head) rows."""
+    base = fia_inputs.workload_paged_gqa_decode()
+    c = fia_inputs.paged_decode_case(16, 32, 8, 128, base.kv_lens, block_size=128, workload=3400, q_tokens=4)
+    out, lse = _run_paged(fia, c, sparse_mode=3)
+    rng = np.random.default_rng(9)
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(16, size=12), rng.integers(32, size=12))] + [(15, 31)]
+    ref = fia_oracle.fia_decode(c.q, c.k_pool, c.v_pool, num_heads=32, num_key_value_heads=8, scale_value=c.scale,
+                                input_layout="BNSD", actual_seq_kvlen=c.kv_lens, block_table=c.block_table,
+                                block_size=128, sparse_mode=3, rows=rows)
+    for (b, h), (ro, rl) in zip(rows, ref):
+        assert_out_close(out[b, h], torch.from_numpy(ro), c.q.dtype)
+        assert_lse_close(lse[b, h, :, 0], torch.from_numpy(rl))
