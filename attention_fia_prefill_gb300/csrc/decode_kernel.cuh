@@ -656,8 +656,9 @@ __global__ void __launch_bounds__(256, 1) decode_kernel(const __grid_constant__ 
         const bool valid = r < nvalid;
         // several query tokens: row h is token h % Q_S, which sees keys up to
         // klim + h % Q_S (sparse_mode 3: klim = S_kv - Q_S; 2: klim = 0)
-        const bool causal = p.q_causal != 0;
-        const int kfrom = st * 128 + r - (p.q_causal == 3 ? L - p.q_tokens : 0);
+        const int klim = p.q_causal == 3 ? L - p.q_tokens : 0;
+        const bool causal = p.q_causal != 0 && st * 128 + 127 > klim;   // a key of this stage is past a limit
+        const int kfrom = st * 128 + r - klim;
         float s[GL];
         bool raise = false;
 #pragma unroll

@@ -10,7 +10,8 @@ second (the K and V rows of every sequence, sum(L_b) * KV_N * D * 2 bytes * 2).
 
 The other hot-path workloads are measured in the same run under "sections":
 varlen TND causal prefill (TFLOP/s), block-sparse prefill (TFLOP/s), MLA decode
-(cache GB/s) and the small fp16 prefill.  Inputs are seeded synthetic tensors
+(cache GB/s), the headline decode with 4 new tokens per sequence (KV GB/s) and
+the small fp16 prefill.  Inputs are seeded synthetic tensors
 of the workloads' shapes (fia_inputs.py).  The L2 is flushed (a 512 MB write)
 before every timed call; times are CUDA events on the launching stream.
 
@@ -305,6 +306,36 @@ def measure_mla(torch, dev, timer, steps, warmup, pk, traffic):
                                  traffic.get("mla_kernel"))}
 
 
+def measure_decode_tokens(torch, dev, timer, steps, warmup, pk, traffic):
+    """The headline paged workload with 4 new tokens per sequence (speculative
+    decoding), right-down causal: the same cache bytes, 4x the query rows."""
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    base = fia_inputs.workload_paged_gqa_decode()
+    c = fia_inputs.paged_decode_case(16, 32, 8, 128, base.kv_lens, block_size=128, workload=3400, q_tokens=4)
+    kv_bytes = sum(c.kv_lens) * c.num_key_value_heads * 128 * 2 * 2
+    q, kp, vp, tb = c.q.to(dev), c.k_pool.to(dev), c.v_pool.to(dev), c.block_table.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], c.num_heads, q.shape[2], 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        fia.fia_decode(q, kp, vp, block_table=tb, block_size=c.block_size, actual_seq_kvlen=c.kv_lens,
+                       num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                       input_layout="BNSD", sparse_mode=3, softmax_lse_flag=True, out=out, softmax_lse=lse,
+                       workspace=ws)
+
+    call_ms, kern_ms = timer.run(call, steps, warmup, kernel_events=True)
+    km = statistics.mean(kern_ms)
+    return {"workload": "paged GQA decode bf16, 4 query tokens (causal): B=16, Q_N=32, KV_N=8, D=128, "
+                        "U[1,4096], block 128",
+            "metric": "paged decode KV GB/s", "unit": "GB/s",
+            "value": round(kv_bytes / (statistics.mean(call_ms) * 1e-3) / 1e9, 2),
+            "ms_per_call": statistics.mean(call_ms), "kernel_ms": km, "kv_bytes": kv_bytes,
+            "roofline": roofline("hbm", kv_bytes / (km * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s",
+                                 traffic.get("decode_kernel_q4"))}
+
+
 def measure_small_prefill(torch, dev, timer, steps, warmup, pk):
     import attention_fia_prefill_gb300 as fia
     import fia_inputs
@@ -366,7 +397,8 @@ def run_ours(args):
     dec, case = measure_decode(torch, dev, timer, args.steps, args.warmup, pk, traffic)
     sections = {}
     if not args.headline_only:
-        for name, fn in (("prefill_tnd", measure_prefill_tnd), ("bsa", measure_bsa), ("mla_decode", measure_mla)):
+        for name, fn in (("prefill_tnd", measure_prefill_tnd), ("bsa", measure_bsa), ("mla_decode", measure_mla),
+                         ("decode_q4", measure_decode_tokens)):
             try:
                 sections[name] = fn(torch, dev, timer, args.steps, args.warmup, pk, traffic)
             except Exception as e:  # a section failure is reported, not hidden
