@@ -202,6 +202,7 @@ struct Geometry {
   int64_t B, N1, N2, S1, S2, D, T1, T2;
   bool bf16;
   std::vector<BatchInfo> batches;
+  int band_pre = 0, band_next = 0;   // sparse_mode 4, clamped to +-2^30
 };
 
 // Shapes of q/k/v in a dense layout -> (B, N, S, D).  BSH splits H by heads.
@@ -260,6 +261,11 @@ fia_status check_lse(const fia_tensor* lse, const fia_params* p, Layout L, int64
 // Common validation of q/k/v/out for the dense prefill and block-sparse calls.
 fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_params* p,
                             const fia_tensor* out, bool bsa, Geometry& g) {
+  if (p != nullptr) {
+    const int64_t lim = int64_t(1) << 30;
+    g.band_pre = int(std::max(-lim, std::min(lim, p->pre_tokens)));
+    g.band_next = int(std::max(-lim, std::min(lim, p->next_tokens)));
+  }
   if (p == nullptr) return fail(FIA_ERR_NULL, "params is NULL");
   if (!given(q) || !given(k) || !given(v) || !given(out))
     return fail(FIA_ERR_NULL, "query/key/value/attention_out required");
@@ -323,6 +329,16 @@ int causal_tiles(const BatchInfo& bi, int q0, int mode) {
   return maxkey >= 0 ? maxkey / kTileN + 1 : 0;
 }
 
+// sparse_mode 4: K/V tiles that the rows [q0, q0 + 256) of a pair (both tiles
+// walk the union of their bands) may see.
+int band_tiles(const BatchInfo& bi, int q0, int pre, int next) {
+  const int64_t d = int64_t(bi.kv_len) - bi.q_len;
+  const int64_t last = std::min<int64_t>(q0 + 2 * kTileM - 1, bi.q_len - 1);
+  const int64_t lo = std::max<int64_t>(0, q0 + d - pre);
+  const int64_t hi = std::min<int64_t>(bi.kv_len - 1, last + d + next);
+  return hi < lo ? 0 : int(hi / kTileN - lo / kTileN + 1);
+}
+
 // Work items: 256-row pairs of query tiles for the dense/causal kernel, single
 // 128-row tiles for the block-sparse one.  cost = tile products (Q K^T + P V
 // per 128 x 128 tile) the CTA runs.
@@ -336,7 +352,11 @@ void build_items(const Geometry& g, int prefill_mode, int causal_mode, std::vect
     for (int64_t h = 0; h < g.N1; ++h)
       for (int qt = 0; qt < nqt; ++qt) {
         int cost = full;
-        if (prefill_mode != kBlockSparse) {
+        if (prefill_mode == kBand) {
+          const int q0 = qt * rows;
+          const int n = band_tiles(bi, q0, g.band_pre, g.band_next);
+          cost = q0 + kTileM >= bi.q_len ? n : 2 * n;
+        } else if (prefill_mode != kBlockSparse) {
           const int q0 = qt * rows;
           const int na = prefill_mode == kCausal ? causal_tiles(bi, q0, causal_mode) : full;
           const int nb = q0 + kTileM >= bi.q_len ? 0
@@ -455,6 +475,8 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.group = int(g.N1 / g.N2);
   pp.is_tnd = g.layout == L_TND;
   pp.causal_offset_mode = causal_mode;
+  pp.band_pre = g.band_pre;
+  pp.band_next = g.band_next;
   pp.scale_log2 = float(prm->scale_value * 1.4426950408889634);
   pp.bsa_mask = bsa_mask;
   pp.bsa_nqb = nqb; pp.bsa_nkb = nkb; pp.bsa_x = bx; pp.bsa_y = by;
@@ -482,7 +504,6 @@ fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, int& m
     if (!present(mask)) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode 1 needs atten_mask");
     return fail(FIA_ERR_UNSUPPORTED, "sparse_mode 1 (allMask) is not implemented");
   }
-  if (sm == 4) return fail(FIA_ERR_UNSUPPORTED, "sparse_mode 4 (band) is not implemented");
   if (present(mask)) {
     // The 2048 x 2048 lower-triangular mask the pages ask for in modes 2/3 is
     // only a compressed form of the pattern; the kernels derive it from indices.
@@ -491,7 +512,7 @@ fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, int& m
                      (n < 3 || mask->shape[0] == 1) && (n < 4 || mask->shape[1] == 1));
     if (!ok) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode %lld mask must be (2048,2048)", (long long)sm);
   }
-  mode = kCausal;
+  mode = sm == 4 ? kBand : kCausal;
   causal_mode = int(sm);
   return FIA_OK;
 }

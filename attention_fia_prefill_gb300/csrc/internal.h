@@ -41,7 +41,9 @@ struct WorkItem {
   int32_t b, h, q_tile, cost;
 };
 
-enum PrefillMode : int { kDense = 0, kCausal = 1, kBlockSparse = 2 };
+// kBand: sparse_mode 4, key j of query row i allowed when
+// i + d - pre <= j <= i + d + next, d = kv_len - q_len of the batch.
+enum PrefillMode : int { kDense = 0, kCausal = 1, kBlockSparse = 2, kBand = 3 };
 
 struct PrefillParams {
   CUtensorMap tm_q, tm_k, tm_v;   // 4-D maps (D, S, N, B); TND uses (D, T, N, 1)
@@ -55,6 +57,7 @@ struct PrefillParams {
   int num_heads, num_kv_heads, group;
   int is_tnd;
   int causal_offset_mode;         // 2: diagonal j <= i; 3: j <= i + kv_len - q_len
+  int band_pre, band_next;        // kBand: pre_tokens / next_tokens, clamped to +-2^30
   float scale_log2;               // scale * log2(e)
   const uint8_t* bsa_mask;        // [B, N1, nqb, nkb]
   int bsa_nqb, bsa_nkb, bsa_x, bsa_y;

@@ -82,13 +82,26 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
   const int q0 = it.q_tile * 2 * kTileM;
   const int kvh = it.h / p.group;
   const int diag_off = (MODE == kCausal && p.causal_offset_mode == 3) ? (bi.kv_len - bi.q_len) : 0;
-  const int na = tiles_for_rows(bi, q0, MODE, diag_off);
+  int na = tiles_for_rows(bi, q0, MODE, diag_off);
   // Tile B walks at least tile A's range (its rows past the batch are computed
   // but not written); a pair whose tile B starts past the batch runs tile A
   // alone.  nl = tiles the CTA loads; the last tile product of each K/V tile
   // (tile B's when it has rows, else tile A's) releases the stage.
   const bool has_b = q0 + kTileM < bi.q_len;
-  const int nb = has_b ? max(na, tiles_for_rows(bi, q0 + kTileM, MODE, diag_off)) : 0;
+  int nb = has_b ? max(na, tiles_for_rows(bi, q0 + kTileM, MODE, diag_off)) : 0;
+  // sparse_mode 4 (band): both tiles walk the K/V tiles of the union of their
+  // rows' bands, from tile jt0 on; the softmax masks each row's edges.
+  int jt0 = 0;
+  const int64_t band_d = int64_t(bi.kv_len) - bi.q_len;
+  if (MODE == kBand) {
+    const int64_t last = min(q0 + 2 * kTileM - 1, bi.q_len - 1);
+    const int64_t lo = max(int64_t(0), q0 + band_d - p.band_pre);
+    const int64_t hi = min(int64_t(bi.kv_len) - 1, last + band_d + p.band_next);
+    const int n = hi < lo ? 0 : int(hi / kTileN - lo / kTileN + 1);
+    jt0 = hi < lo ? 0 : int(lo / kTileN);
+    na = n;
+    nb = has_b ? n : 0;
+  }
   const int nl = max(na, nb);
 
   if (threadIdx.x == 0) {
@@ -144,11 +157,11 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(ks + c * C::kBoxBytes, &p.tm_k, &k_full[s], c * 64, kv_row0 + j * kTileN, kvh, b_coord);
+          tma_load_4d(ks + c * C::kBoxBytes, &p.tm_k, &k_full[s], c * 64, kv_row0 + (jt0 + j) * kTileN, kvh, b_coord);
         mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[s], c * 64, kv_row0 + j * kTileN, kvh, b_coord);
+          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[s], c * 64, kv_row0 + (jt0 + j) * kTileN, kvh, b_coord);
       }
       if (*abort_flag) {
         mbar_wait(q_full, 0, nullptr, p.status);
@@ -267,15 +280,22 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       tmem_ld32(tmem + lane_off + col_s + 64, su[2]);
       tmem_ld32(tmem + lane_off + col_s + 96, su[3]);
       float* x = reinterpret_cast<float*>(&su[0][0]);
-      const int kv0 = j * kTileN;
+      const int kv0 = (jt0 + j) * kTileN;
       const bool ragged = kv0 + kTileN > bi.kv_len;
-      const bool need_mask = ragged || (MODE == kCausal && kv0 + kTileN - 1 > tile_q0 + diag_off);
-      const int lim = (MODE == kCausal) ? min(bi.kv_len - 1, diag) : bi.kv_len - 1;
+      // keys allowed for this row: [lim_lo, lim]
+      int lim = (MODE == kCausal) ? min(bi.kv_len - 1, diag) : bi.kv_len - 1;
+      int lim_lo = 0;
+      if (MODE == kBand) {
+        lim = int(min(int64_t(bi.kv_len) - 1, int64_t(i) + band_d + p.band_next));
+        lim_lo = int(max(int64_t(0), int64_t(i) + band_d - p.band_pre));
+      }
+      const bool need_mask = ragged || (MODE == kCausal && kv0 + kTileN - 1 > tile_q0 + diag_off) ||
+                             (MODE == kBand && (kv0 + kTileN - 1 > lim || kv0 < lim_lo));
       float a[8];
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (kv0 + c > lim) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          if (kv0 + c > lim || (MODE == kBand && kv0 + c < lim_lo)) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -292,7 +312,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       if (need_mask) {
 #pragma unroll
         for (int c = 64; c < 128; ++c)
-          if (kv0 + c > lim) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          if (kv0 + c > lim || (MODE == kBand && kv0 + c < lim_lo)) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -438,16 +458,20 @@ cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
 
 cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
-  if (mode != kDense && mode != kCausal) return cudaErrorInvalidValue;
-  const bool causal = mode == kCausal;
+#define FIA_PAIR_MODES(DD, BB)                                          \
+  switch (mode) {                                                       \
+    case kDense: return launch_pair_one<DD, BB, kDense>(p, s);          \
+    case kCausal: return launch_pair_one<DD, BB, kCausal>(p, s);        \
+    case kBand: return launch_pair_one<DD, BB, kBand>(p, s);            \
+    default: return cudaErrorInvalidValue;                              \
+  }
   if (head_dim == 128) {
-    if (bf16) return causal ? launch_pair_one<128, true, kCausal>(p, s) : launch_pair_one<128, true, kDense>(p, s);
-    return causal ? launch_pair_one<128, false, kCausal>(p, s) : launch_pair_one<128, false, kDense>(p, s);
+    if (bf16) { FIA_PAIR_MODES(128, true) } else { FIA_PAIR_MODES(128, false) }
   }
   if (head_dim == 64) {
-    if (bf16) return causal ? launch_pair_one<64, true, kCausal>(p, s) : launch_pair_one<64, true, kDense>(p, s);
-    return causal ? launch_pair_one<64, false, kCausal>(p, s) : launch_pair_one<64, false, kDense>(p, s);
+    if (bf16) { FIA_PAIR_MODES(64, true) } else { FIA_PAIR_MODES(64, false) }
   }
+#undef FIA_PAIR_MODES
   return cudaErrorInvalidValue;
 }
 

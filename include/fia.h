@@ -100,9 +100,9 @@ typedef struct fia_params {
                                      Q_N / KV_N <= 64                                          */
   double scale_value;             /* softmax_scale / scale_value; default 1.0; must be > 0     */
   const char* input_layout;       /* "BSH", "BSND", "BNSD" or "TND"; default "BSH"             */
-  int64_t sparse_mode;            /* 0..4; 2 = leftUpCausal, 3 = rightDownCausal              */
-  int64_t pre_tokens;             /* default 2147483647                                        */
-  int64_t next_tokens;            /* default 2147483647                                        */
+  int64_t sparse_mode;            /* 0..4; 2 = leftUpCausal, 3 = rightDownCausal, 4 = band     */
+  int64_t pre_tokens;             /* band (mode 4) width before the diagonal; default 2^31-1   */
+  int64_t next_tokens;            /* band (mode 4) width after the diagonal; default 2^31-1    */
   const int64_t* actual_seq_qlen;   /* host array or NULL; TND: cumulative, no leading 0       */
   int64_t n_actual_seq_qlen;
   const int64_t* actual_seq_kvlen;  /* host array or NULL; TND: cumulative, no leading 0       */
@@ -120,10 +120,13 @@ FIA_API void fia_params_init(fia_params* p);
  *   query  (B,S1,H) BSH | (B,S1,N1,D) BSND | (B,N1,S1,D) BNSD | (T1,N1,D) TND;
  *          f16 or bf16.  D is 64 or 128.
  *   key, value: same layout and element type, N2 heads, identical shapes.
- *   atten_mask: optional.  sparse_mode 2/3 compute the causal pattern from
+ *   atten_mask: optional.  sparse_mode 2/3/4 compute their pattern from
  *          indices; a mask given there must be (2048,2048) / (1,2048,2048) /
- *          (1,1,2048,2048) and is not read.  Modes 0 (with a mask), 1 and 4
- *          return FIA_ERR_UNSUPPORTED.
+ *          (1,1,2048,2048) and is not read.  Mode 4 (band): query row i sees
+ *          keys i + d - pre_tokens .. i + d + next_tokens, d = S2 - S1 of the
+ *          batch (npu_fused_infer_attention_score_v2, sparse_mode; pre/next
+ *          clamped to +-2^30).  Modes 0 (with a mask) and 1 return
+ *          FIA_ERR_UNSUPPORTED.
  *   attention_out: the query's shape and element type.
  *   softmax_lse: fp32 (B,N1,S1,1), or (T1,N1,1) for TND; used when
  *          params->softmax_lse_flag != 0 (may be absent otherwise).

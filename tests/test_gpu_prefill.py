@@ -157,3 +157,32 @@ def test_full_tnd_varlen_workload_sampled(fia):
     ref = _oracle(case, rows=rows)
     assert_rows_close(out, lse, rows, ref, lambda r: (starts[r[0]] + r[2], r[1]), torch.bfloat16)
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------- band (mode 4)
+def _check_band(fia, case, pre, nxt):
+    out, lse = _run(fia, case, pre_tokens=pre, next_tokens=nxt)
+    ref_o, ref_l = fia_oracle.fia_prefill(case.q, case.k, case.v, num_heads=case.num_heads,
+                                          num_key_value_heads=case.num_key_value_heads, scale_value=case.scale,
+                                          input_layout=case.layout, sparse_mode=4,
+                                          actual_seq_qlen=case.actual_seq_qlen,
+                                          actual_seq_kvlen=case.actual_seq_kvlen, pre_tokens=pre, next_tokens=nxt)
+    assert_out_close(out, ref_o, case.q.dtype)
+    assert_lse_close(lse, ref_l)
+
+
+@pytest.mark.parametrize("sq,skv,pre,nxt,D", [(300, 300, 100, 50, 128), (200, 500, 64, 0, 128), (700, 600, 130, 260, 64),
+                                              (520, 520, 0, 0, 128), (300, 300, 2000, 2000, 64)])
+def test_band(fia, sq, skv, pre, nxt, D):
+    """sparse_mode 4: row i sees keys i + S_kv - S_q - pre .. i + S_kv - S_q + next
+    (both edges inside a tile, a band narrower than a tile, a band wider than
+    the sequence)."""
+    case = fia_inputs.prefill_case(2, 4, 2, sq, skv, D, dtype="bf16", layout="BNSD", sparse_mode=4,
+                                   workload=1800 + sq + pre)
+    _check_band(fia, case, pre, nxt)
+
+
+def test_band_tnd_varlen(fia):
+    lens = [1, 127, 300, 0, 1000, 129]
+    case = fia_inputs.tnd_case(lens, lens, 8, 2, 128, "bf16", sparse_mode=4, workload=1900)
+    _check_band(fia, case, 256, 32)
