@@ -202,7 +202,11 @@ struct Geometry {
   int64_t B, N1, N2, S1, S2, D, T1, T2;
   bool bf16;
   std::vector<BatchInfo> batches;
-  int band_pre = 0, band_next = 0;   // sparse_mode 4, clamped to +-2^30
+  int band_pre = 0, band_next = 0;   // sparse_mode 4 / explicit mask, clamped to +-2^30
+  // explicit atten_mask (sparse_mode 0 with a mask, 1)
+  const uint8_t* mask = nullptr;
+  int64_t mask_sb = 0, mask_ss = 0;
+  int mask_cs = 1;
 };
 
 // Shapes of q/k/v in a dense layout -> (B, N, S, D).  BSH splits H by heads.
@@ -329,10 +333,11 @@ int causal_tiles(const BatchInfo& bi, int q0, int mode) {
   return maxkey >= 0 ? maxkey / kTileN + 1 : 0;
 }
 
-// sparse_mode 4: K/V tiles that the rows [q0, q0 + 256) of a pair (both tiles
-// walk the union of their bands) may see.
-int band_tiles(const BatchInfo& bi, int q0, int pre, int next) {
-  const int64_t d = int64_t(bi.kv_len) - bi.q_len;
+// sparse_mode 4 (shift: d = kv_len - q_len) and the explicit mask's band (d =
+// 0): K/V tiles that the rows [q0, q0 + 256) of a pair (both tiles walk the
+// union of their bands) may see.
+int band_tiles(const BatchInfo& bi, int q0, int pre, int next, bool shift) {
+  const int64_t d = shift ? int64_t(bi.kv_len) - bi.q_len : 0;
   const int64_t last = std::min<int64_t>(q0 + 2 * kTileM - 1, bi.q_len - 1);
   const int64_t lo = std::max<int64_t>(0, q0 + d - pre);
   const int64_t hi = std::min<int64_t>(bi.kv_len - 1, last + d + next);
@@ -352,9 +357,9 @@ void build_items(const Geometry& g, int prefill_mode, int causal_mode, std::vect
     for (int64_t h = 0; h < g.N1; ++h)
       for (int qt = 0; qt < nqt; ++qt) {
         int cost = full;
-        if (prefill_mode == kBand) {
+        if (prefill_mode == kBand || prefill_mode == kMask) {
           const int q0 = qt * rows;
-          const int n = band_tiles(bi, q0, g.band_pre, g.band_next);
+          const int n = band_tiles(bi, q0, g.band_pre, g.band_next, prefill_mode == kBand);
           cost = q0 + kTileM >= bi.q_len ? n : 2 * n;
         } else if (prefill_mode != kBlockSparse) {
           const int q0 = qt * rows;
@@ -477,6 +482,10 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.causal_offset_mode = causal_mode;
   pp.band_pre = g.band_pre;
   pp.band_next = g.band_next;
+  pp.attn_mask = g.mask;
+  pp.mask_sb = g.mask_sb;
+  pp.mask_ss = g.mask_ss;
+  pp.mask_cs = g.mask_cs;
   pp.scale_log2 = float(prm->scale_value * 1.4426950408889634);
   pp.bsa_mask = bsa_mask;
   pp.bsa_nqb = nqb; pp.bsa_nkb = nkb; pp.bsa_x = bx; pp.bsa_y = by;
@@ -489,20 +498,56 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
                     "prefill launch");
 }
 
+// An explicit atten_mask for the prefill kernels: bool / int8 / uint8, nonzero
+// = masked, shapes (S1,S2), (B,S1,S2), (1,S1,S2), (B,1,S1,S2), (1,1,S1,S2)
+// (npu_fused_infer_attention_score_v2 and npu_prompt_flash_attention,
+// atten_mask).  Indices are batch-local (row i, key j of the batch); the last
+// two dims must cover every batch's query and key lengths.
+fia_status explicit_mask(const fia_tensor* mask, Geometry& g) {
+  if (mask->dtype != FIA_DTYPE_BOOL && mask->dtype != FIA_DTYPE_U8 && mask->dtype != FIA_DTYPE_I8)
+    return fail(FIA_ERR_DTYPE, "atten_mask must be bool, int8 or uint8");
+  const int n = mask->ndim;
+  if (n < 2 || n > 4) return fail(FIA_ERR_SHAPE, "atten_mask must be 2-D, 3-D or 4-D");
+  const int64_t ms1 = mask->shape[n - 2], ms2 = mask->shape[n - 1];
+  const int64_t mb = n >= 3 ? mask->shape[0] : 1;
+  if (n == 4 && mask->shape[1] != 1) return fail(FIA_ERR_SHAPE, "4-D atten_mask must be (B or 1, 1, S1, S2)");
+  if (mb != 1 && mb != g.B)
+    return fail(FIA_ERR_SHAPE, "atten_mask batch dim %lld is neither 1 nor B=%lld", (long long)mb, (long long)g.B);
+  int64_t maxq = 0, maxk = 0;
+  for (const auto& bi : g.batches) { maxq = std::max<int64_t>(maxq, bi.q_len); maxk = std::max<int64_t>(maxk, bi.kv_len); }
+  if (ms1 < maxq || ms2 < maxk)
+    return fail(FIA_ERR_SHAPE, "atten_mask (%lld, %lld) smaller than the query / key lengths (%lld, %lld)",
+                (long long)ms1, (long long)ms2, (long long)maxq, (long long)maxk);
+  if (ms1 * ms2 > 0 && mask->data == nullptr) return fail(FIA_ERR_NULL, "atten_mask data is NULL");
+  g.mask = static_cast<const uint8_t*>(mask->data);
+  g.mask_ss = ms2;
+  g.mask_sb = mb > 1 ? ms1 * ms2 : 0;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(mask->data);
+  g.mask_cs = 1;
+  for (int cs : {16, 8, 4})
+    if (a % cs == 0 && ms2 % cs == 0) { g.mask_cs = cs; break; }
+  return FIA_OK;
+}
+
 // Mask semantics accepted by the prefill kernels.
-fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, int& mode, int& causal_mode) {
+fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, Geometry& g, int& mode, int& causal_mode) {
   const int64_t sm = p->sparse_mode;
   if (sm < 0 || sm > 8) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode %lld not in 0..4", (long long)sm);
   if (sm >= 5) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode %lld (prefix/global/dilated/block_local) is not supported", (long long)sm);
-  if (sm == 0) {
-    if (present(mask)) return fail(FIA_ERR_UNSUPPORTED, "explicit atten_mask (sparse_mode 0) is not implemented");
-    mode = kDense;
+  if (sm == 0 || sm == 1) {
     causal_mode = 0;
+    if (!present(mask)) {
+      if (sm == 1) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode 1 needs atten_mask");
+      mode = kDense;   // no mask: pre_tokens / next_tokens are ignored
+      return FIA_OK;
+    }
+    fia_status st = explicit_mask(mask, g);
+    if (st != FIA_OK) return st;
+    // mode 0 keeps the band pre_tokens .. next_tokens around the diagonal;
+    // mode 1 (allMask) is the mask alone
+    if (sm == 1) g.band_pre = g.band_next = 1 << 30;
+    mode = kMask;
     return FIA_OK;
-  }
-  if (sm == 1) {
-    if (!present(mask)) return fail(FIA_ERR_SPARSE_MODE, "sparse_mode 1 needs atten_mask");
-    return fail(FIA_ERR_UNSUPPORTED, "sparse_mode 1 (allMask) is not implemented");
   }
   if (present(mask)) {
     // The 2048 x 2048 lower-triangular mask the pages ask for in modes 2/3 is
@@ -594,7 +639,7 @@ fia_status fia_prefill_get_workspace_size(const fia_tensor* query, const fia_ten
   fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g);
   if (st != FIA_OK) return st;
   int mode, cm;
-  st = prefill_mask_mode(params, atten_mask, mode, cm);
+  st = prefill_mask_mode(params, atten_mask, g, mode, cm);
   if (st != FIA_OK) return st;
   st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
   if (st != FIA_OK) return st;
@@ -610,7 +655,7 @@ fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, const fia
   fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g);
   if (st != FIA_OK) return st;
   int mode, cm;
-  st = prefill_mask_mode(params, atten_mask, mode, cm);
+  st = prefill_mask_mode(params, atten_mask, g, mode, cm);
   if (st != FIA_OK) return st;
   st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
   if (st != FIA_OK) return st;

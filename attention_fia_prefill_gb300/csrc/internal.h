@@ -43,7 +43,9 @@ struct WorkItem {
 
 // kBand: sparse_mode 4, key j of query row i allowed when
 // i + d - pre <= j <= i + d + next, d = kv_len - q_len of the batch.
-enum PrefillMode : int { kDense = 0, kCausal = 1, kBlockSparse = 2, kBand = 3 };
+// kMask: an explicit atten_mask (sparse_mode 0 with a mask, 1), key j of row i
+// allowed when mask[i][j] == 0 and i - pre <= j <= i + next (mode 1: no band).
+enum PrefillMode : int { kDense = 0, kCausal = 1, kBlockSparse = 2, kBand = 3, kMask = 4 };
 
 struct PrefillParams {
   CUtensorMap tm_q, tm_k, tm_v;   // 4-D maps (D, S, N, B); TND uses (D, T, N, 1)
@@ -57,7 +59,10 @@ struct PrefillParams {
   int num_heads, num_kv_heads, group;
   int is_tnd;
   int causal_offset_mode;         // 2: diagonal j <= i; 3: j <= i + kv_len - q_len
-  int band_pre, band_next;        // kBand: pre_tokens / next_tokens, clamped to +-2^30
+  int band_pre, band_next;        // kBand / kMask: pre_tokens / next_tokens, clamped to +-2^30
+  const uint8_t* attn_mask;       // kMask: byte (i, j) of batch b at b * mask_sb + i * mask_ss + j
+  int64_t mask_sb, mask_ss;       // mask_sb = 0 for a mask shared by all batches
+  int mask_cs;                    // copy granule in bytes (16, 8, 4: alignment of base and rows; 1: plain loads)
   float scale_log2;               // scale * log2(e)
   const uint8_t* bsa_mask;        // [B, N1, nqb, nkb]
   int bsa_nqb, bsa_nkb, bsa_x, bsa_y;

@@ -2,8 +2,9 @@
 //
 // Operation: as prefill.cu -- torch_npu.npu_prompt_flash_attention ("功能说明",
 // formula) and npu_fused_infer_attention_score_v2 (Q_S > 1, softmax_lse):
-// out = softmax(scale * Q K^T + mask) V with sparse_mode 0 (no mask) or the
-// causal modes 2 / 3 computed from indices.
+// out = softmax(scale * Q K^T + mask) V with sparse_mode 0 (no mask), the
+// causal modes 2 / 3 and the band mode 4 computed from indices, or an explicit
+// atten_mask (sparse_mode 0 with a mask, 1) read from memory.
 //
 // One CTA owns 256 query rows of one (batch, query head): tile A (rows
 // q0..q0+127) and tile B (q0+128..q0+255).  Both read every K/V tile the CTA
@@ -21,6 +22,9 @@
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D,
 // 256+2D).  Causal: tile B needs the K/V tiles of tile A plus at most one; the
 // CTA walks tile B's range and tile A stops early.
+// Explicit mask: each softmax thread copies its row's 128 mask bytes for the
+// next K/V tile into its own 128-byte shared slot (cp.async, in flight while
+// the current tile is processed) and turns them into a 128-bit mask.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -39,10 +43,14 @@ struct PairCfg {
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kOffBar + kBarBytes + 1024;
+  // explicit atten_mask: one 128-byte slot per softmax thread (256 rows),
+  // 16-byte chunk q of row r at (q ^ (r & 7)) * 16 (no bank conflicts)
+  static constexpr int kOffMask = kOffBar + kBarBytes;
+  static constexpr int kSmemMask = kOffMask + 256 * 128 + 1024;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;                            // O_A; O_B at kColO + D
-  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kSmemMask <= 227 * 1024, "shared memory budget");
 };
 
 // Key tiles needed by the query rows [qa, qa + 128) of a batch.
@@ -89,11 +97,12 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
   // (tile B's when it has rows, else tile A's) releases the stage.
   const bool has_b = q0 + kTileM < bi.q_len;
   int nb = has_b ? max(na, tiles_for_rows(bi, q0 + kTileM, MODE, diag_off)) : 0;
-  // sparse_mode 4 (band): both tiles walk the K/V tiles of the union of their
-  // rows' bands, from tile jt0 on; the softmax masks each row's edges.
+  // sparse_mode 4 (band) and the explicit mask (band i - pre .. i + next): both
+  // tiles walk the K/V tiles of the union of their rows' bands, from tile jt0
+  // on; the softmax masks each row's edges.
   int jt0 = 0;
-  const int64_t band_d = int64_t(bi.kv_len) - bi.q_len;
-  if (MODE == kBand) {
+  const int64_t band_d = MODE == kBand ? int64_t(bi.kv_len) - bi.q_len : 0;
+  if (MODE == kBand || MODE == kMask) {
     const int64_t last = min(q0 + 2 * kTileM - 1, bi.q_len - 1);
     const int64_t lo = max(int64_t(0), q0 + band_d - p.band_pre);
     const int64_t hi = min(int64_t(bi.kv_len) - 1, last + band_d + p.band_next);
@@ -265,9 +274,56 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     const int diag = i + diag_off;
     const float sl2 = p.scale_log2;
     uint64_t* my_pfull = t == 0 ? pa_full : pb_full;
+    // explicit mask: this row's bytes of K/V tile jj into the thread's slot
+    const bool mrow = MODE == kMask && i < bi.q_len;
+    const uint8_t* mask_row = MODE == kMask ? p.attn_mask + int64_t(it.b) * p.mask_sb + int64_t(i) * p.mask_ss : nullptr;
+    uint8_t* mslot = smem + C::kOffMask + (t * 128 + r) * 128;
+    const int r7 = r & 7;
+    auto mask_fetch = [&](int jj) {
+      const int kvj = (jt0 + jj) * kTileN;
+      const int valid = min(bi.kv_len - kvj, kTileN);   // bytes of the row inside the batch
+      const uint8_t* src = mask_row + kvj;
+      const uint32_t dst = smem_u32(mslot);
+      if (p.mask_cs == 16) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (16 * q < valid) cp_async_zfill<16>(dst + ((q ^ r7) << 4), src + 16 * q, min(16, valid - 16 * q));
+      } else if (p.mask_cs == 8) {
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+          if (8 * h < valid)
+            cp_async_zfill<8>(dst + (((h >> 1) ^ r7) << 4) + (h & 1) * 8, src + 8 * h, min(8, valid - 8 * h));
+      } else if (p.mask_cs == 4) {
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          if (4 * h < valid)
+            cp_async_zfill<4>(dst + (((h >> 2) ^ r7) << 4) + (h & 3) * 4, src + 4 * h, min(4, valid - 4 * h));
+      } else {
+#pragma unroll 4
+        for (int c = 0; c < kTileN; ++c)
+          if (c < valid) mslot[(((c >> 4) ^ r7) << 4) + (c & 15)] = __ldg(src + c);
+      }
+      cp_async_commit();
+    };
+    if (mrow && n > 0) mask_fetch(0);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
+      // mb: bit c of mb[c >> 5] set when atten_mask masks key kv0 + c
+      uint32_t mb[4] = {0u, 0u, 0u, 0u};
+      if (mrow) {
+        cp_async_wait_all();
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint4 a0 = *reinterpret_cast<const uint4*>(mslot + (((2 * w) ^ r7) << 4));
+          const uint4 a1 = *reinterpret_cast<const uint4*>(mslot + (((2 * w + 1) ^ r7) << 4));
+          mb[w] = nonzero_bytes4(a0.x) | (nonzero_bytes4(a0.y) << 4) | (nonzero_bytes4(a0.z) << 8) |
+                  (nonzero_bytes4(a0.w) << 12) | (nonzero_bytes4(a1.x) << 16) | (nonzero_bytes4(a1.y) << 20) |
+                  (nonzero_bytes4(a1.z) << 24) | (nonzero_bytes4(a1.w) << 28);
+        }
+        // the slot is read (mb depends on every byte): refill it with the next tile
+        if (j + 1 < n) mask_fetch(j + 1);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, p.status))) { ok = false; break; }
       tc_fence_after();
       // S in two halves: the second half's load is in flight while the
@@ -285,17 +341,20 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       // keys allowed for this row: [lim_lo, lim]
       int lim = (MODE == kCausal) ? min(bi.kv_len - 1, diag) : bi.kv_len - 1;
       int lim_lo = 0;
-      if (MODE == kBand) {
+      constexpr bool kBanded = MODE == kBand || MODE == kMask;
+      if (kBanded) {
         lim = int(min(int64_t(bi.kv_len) - 1, int64_t(i) + band_d + p.band_next));
         lim_lo = int(max(int64_t(0), int64_t(i) + band_d - p.band_pre));
       }
       const bool need_mask = ragged || (MODE == kCausal && kv0 + kTileN - 1 > tile_q0 + diag_off) ||
-                             (MODE == kBand && (kv0 + kTileN - 1 > lim || kv0 < lim_lo));
+                             (kBanded && (kv0 + kTileN - 1 > lim || kv0 < lim_lo)) ||
+                             (MODE == kMask && (mb[0] | mb[1] | mb[2] | mb[3]) != 0u);
       float a[8];
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (kv0 + c > lim || (MODE == kBand && kv0 + c < lim_lo)) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          if (kv0 + c > lim || (kBanded && kv0 + c < lim_lo) || (MODE == kMask && ((mb[c >> 5] >> (c & 31)) & 1u)))
+            su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -312,7 +371,8 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       if (need_mask) {
 #pragma unroll
         for (int c = 64; c < 128; ++c)
-          if (kv0 + c > lim || (MODE == kBand && kv0 + c < lim_lo)) su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          if (kv0 + c > lim || (kBanded && kv0 + c < lim_lo) || (MODE == kMask && ((mb[c >> 5] >> (c & 31)) & 1u)))
+            su[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -387,6 +447,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       warp_arrive(&my_pfull[j & 1]);
       m = m_use;
     }
+    if (MODE == kMask) cp_async_wait_all();   // no copy into the slot outlives the loop
     // ------------------------------------------------------------ epilogue
     if (ok && n > 0) {
       const int jl = n - 1;
@@ -448,9 +509,10 @@ template <int D, bool BF16, int MODE>
 cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
   using C = PairCfg<D>;
   auto k = prefill_pair_kernel<D, BF16, MODE>;
-  cudaError_t e = set_smem_once<prefill_pair_kernel<D, BF16, MODE>>(C::kSmem);
+  constexpr int smem = MODE == kMask ? C::kSmemMask : C::kSmem;
+  cudaError_t e = set_smem_once<prefill_pair_kernel<D, BF16, MODE>>(smem);
   if (e != cudaSuccess) return e;
-  k<<<p.n_items, C::kThreads, C::kSmem, s>>>(p);
+  k<<<p.n_items, C::kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -463,6 +525,7 @@ cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim, bool bf16,
     case kDense: return launch_pair_one<DD, BB, kDense>(p, s);          \
     case kCausal: return launch_pair_one<DD, BB, kCausal>(p, s);        \
     case kBand: return launch_pair_one<DD, BB, kBand>(p, s);            \
+    case kMask: return launch_pair_one<DD, BB, kMask>(p, s);            \
     default: return cudaErrorInvalidValue;                              \
   }
   if (head_dim == 128) {

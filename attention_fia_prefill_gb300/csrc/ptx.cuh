@@ -183,6 +183,31 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Per-thread asynchronous copy of N (4, 8 or 16) bytes global -> shared.  Only
+// src_bytes (<= N) are read; the rest of the destination is zero-filled.  Both
+// addresses are N-byte aligned.  Completion: cp_async_commit + cp_async_wait_all
+// by the issuing thread, which then sees the data.
+template <int N>
+__device__ __forceinline__ void cp_async_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  static_assert(N == 4 || N == 8 || N == 16, "cp.async size");
+  if constexpr (N == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(N), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Bit k (k = 0..3) set when byte k of w is nonzero: the high bit of
+// ((b & 0x7f) + 0x7f) | b is set iff b != 0 (no carry leaves a byte), and the
+// multiply gathers bits 7, 15, 23, 31 into bits 28..31 (the partial products
+// land on distinct positions, so nothing carries into them).
+__device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t w) {
+  const uint32_t hi = (((w & 0x7f7f7f7fu) + 0x7f7f7f7fu) | w) & 0x80808080u;
+  return (hi * 0x00204081u) >> 28;
+}
+
 // ------------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

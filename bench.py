@@ -9,7 +9,8 @@ workload -- B=16, Q_N=32, KV_N=8, D=128, bf16, actual_seq_kvlen uniform on
 second (the K and V rows of every sequence, sum(L_b) * KV_N * D * 2 bytes * 2).
 
 The other hot-path workloads are measured in the same run under "sections":
-varlen TND causal prefill (TFLOP/s), block-sparse prefill (TFLOP/s), MLA decode
+varlen TND causal prefill (TFLOP/s), the same with a 1024-key sliding window
+(sparse_mode 4), block-sparse prefill (TFLOP/s), MLA decode
 (cache GB/s), the headline decode with 4 new tokens per sequence (KV GB/s) and
 the small fp16 prefill.  Inputs are seeded synthetic tensors
 of the workloads' shapes (fia_inputs.py).  The L2 is flushed (a 512 MB write)
@@ -256,6 +257,38 @@ def measure_prefill_tnd(torch, dev, timer, steps, warmup, pk, traffic):
                                  traffic.get("prefill_pair_kernel"))}
 
 
+def measure_prefill_band(torch, dev, timer, steps, warmup, pk, traffic):
+    """The varlen TND workload with a sliding window (sparse_mode 4,
+    pre_tokens 1024, next_tokens 0): each row sees its 1025 latest keys."""
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    c = fia_inputs.workload_tnd_varlen()
+    pre = 1024
+    lens = [b - a for a, b in zip([0] + c.actual_seq_qlen[:-1], c.actual_seq_qlen)]
+    pairs = sum(sum(min(i + 1, pre + 1) for i in range(L)) for L in lens)
+    flops = pairs * c.num_heads * 4 * c.q.shape[-1]
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], c.num_heads, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        fia.fia_prefill(q, k, v, num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                        scale_value=c.scale, input_layout="TND", sparse_mode=4, pre_tokens=pre, next_tokens=0,
+                        actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
+                        softmax_lse_flag=True, out=out, softmax_lse=lse, workspace=ws)
+
+    call_ms, kern_ms = timer.run(call, steps, warmup, kernel_events=True)
+    km = statistics.mean(kern_ms)
+    return {"workload": "varlen TND band prefill bf16 (window 1024 keys back), 8 seqs U[256,4096], "
+                        "Q_N=32, KV_N=8, D=128, LSE",
+            "metric": "prefill attention TFLOP/s", "unit": "TFLOP/s",
+            "value": round(flops / (statistics.mean(call_ms) * 1e-3) / 1e12, 2), "ms_per_call": statistics.mean(call_ms),
+            "kernel_ms": km, "flops": flops,
+            "roofline": roofline("tensor", flops / (km * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s",
+                                 traffic.get("prefill_pair_kernel_band"))}
+
+
 def measure_bsa(torch, dev, timer, steps, warmup, pk, traffic):
     import attention_fia_prefill_gb300 as fia
     import fia_inputs
@@ -397,8 +430,8 @@ def run_ours(args):
     dec, case = measure_decode(torch, dev, timer, args.steps, args.warmup, pk, traffic)
     sections = {}
     if not args.headline_only:
-        for name, fn in (("prefill_tnd", measure_prefill_tnd), ("bsa", measure_bsa), ("mla_decode", measure_mla),
-                         ("decode_q4", measure_decode_tokens)):
+        for name, fn in (("prefill_tnd", measure_prefill_tnd), ("prefill_band", measure_prefill_band),
+                         ("bsa", measure_bsa), ("mla_decode", measure_mla), ("decode_q4", measure_decode_tokens)):
             try:
                 sections[name] = fn(torch, dev, timer, args.steps, args.warmup, pk, traffic)
             except Exception as e:  # a section failure is reported, not hidden

@@ -102,6 +102,40 @@ def tnd_case(lengths_q, lengths_kv, N1, N2, D, dtype="bf16", sparse_mode=3, work
                        cumsum_no_leading_zero(lengths_q), cumsum_no_leading_zero(lengths_kv))
 
 
+def atten_mask(shape, kind="random", density=0.3, dtype="u8", workload=600) -> torch.Tensor:
+    """Seeded atten_mask of the given shape (..., S1m, S2m); nonzero = masked.
+
+    kind "random": i.i.d. entries, `density` of them nonzero.  "blocks": each
+    128 x 128 tile is all visible, all masked or random (a third each), and a
+    few rows are masked in full.  "causal": key j of row i masked when j > i.
+    Nonzero entries take assorted values (1..255 for uint8, nonzero int8)."""
+    g = rng(workload, 50)
+    S1, S2 = shape[-2], shape[-1]
+    if kind == "causal":
+        m = np.broadcast_to(np.arange(S2)[None, :] > np.arange(S1)[:, None], shape)
+    elif kind == "random":
+        m = g.random(size=shape) < density
+    elif kind == "blocks":
+        m = g.random(size=shape) < density
+        t1, t2 = -(-S1 // 128), -(-S2 // 128)
+        pick = g.integers(0, 3, size=tuple(shape[:-2]) + (t1, t2))
+        full = np.repeat(np.repeat(pick, 128, axis=-2), 128, axis=-1)[..., :S1, :S2]
+        m = np.where(full == 0, False, np.where(full == 1, True, m))
+        rows = g.integers(0, S1, size=max(1, S1 // 64))
+        m[..., rows, :] = True
+    else:
+        raise ValueError(kind)
+    m = np.ascontiguousarray(m)
+    if dtype == "bool":
+        return torch.from_numpy(m.copy())
+    if dtype == "u8":
+        vals = g.integers(1, 256, size=m.shape)
+    else:
+        vals = g.choice(np.r_[np.arange(-128, 0), np.arange(1, 128)], size=m.shape)
+    out = np.where(m, vals, 0).astype(np.uint8 if dtype == "u8" else np.int8)
+    return torch.from_numpy(out)
+
+
 # The five workloads the pages' operator is exercised on (sizes fixed here).
 def workload_prefill_bnsd_f16_small() -> PrefillCase:
     """Prefill BNSD fp16: B=1, Q_N=KV_N=2, S=128, D=64, causal, LSE on."""

@@ -125,8 +125,15 @@ FIA_API void fia_params_init(fia_params* p);
  *          (1,1,2048,2048) and is not read.  Mode 4 (band): query row i sees
  *          keys i + d - pre_tokens .. i + d + next_tokens, d = S2 - S1 of the
  *          batch (npu_fused_infer_attention_score_v2, sparse_mode; pre/next
- *          clamped to +-2^30).  Modes 0 (with a mask) and 1 return
- *          FIA_ERR_UNSUPPORTED.
+ *          clamped to +-2^30).  Mode 0 with a mask, and mode 1 (allMask,
+ *          mask required): bool/int8/uint8, device memory, contiguous, shape
+ *          (S1m,S2m), (B|1,S1m,S2m) or (B|1,1,S1m,S2m) with S1m / S2m at least
+ *          every batch's query / key length; byte [b][i][j] != 0 masks key j of
+ *          the batch's query row i (batch-local indices, also for TND).  Mode 0
+ *          also keeps only i - pre_tokens <= j <= i + next_tokens.  A mask
+ *          whose address and S2m are multiples of 16 bytes is read fastest
+ *          (8 and 4 next; otherwise byte by byte).  A row with every key
+ *          masked gives out 0 and lse +inf.
  *   attention_out: the query's shape and element type.
  *   softmax_lse: fp32 (B,N1,S1,1), or (T1,N1,1) for TND; used when
  *          params->softmax_lse_flag != 0 (may be absent otherwise).

@@ -121,6 +121,26 @@ def test_causal_mask_shape(lib):
     assert prefill_ws(lib, q, q, q, params(lib, num_heads=2, input_layout="BNSD", sparse_mode=2), mask=m_bad)[0] == 12
 
 
+def test_explicit_mask_rules(lib):
+    """Modes 0 / 1 with an explicit atten_mask: bool / int8 / uint8 in the shapes
+    (S1,S2), (B|1,S1,S2), (B|1,1,S1,S2) covering the query / key lengths."""
+    q, k = t((2, 2, 8, 64)), t((2, 2, 10, 64))
+
+    def ws(mode, mask):
+        return prefill_ws(lib, q, k, k, params(lib, num_heads=2, input_layout="BNSD", sparse_mode=mode), mask=mask)[0]
+
+    for dt in (B.DTYPE_BOOL, B.DTYPE_U8, B.DTYPE_I8):
+        for shape in ((8, 10), (2, 8, 10), (1, 8, 10), (2, 1, 8, 10), (1, 1, 8, 16), (9, 11)):
+            assert ws(1, t(shape, dt)) == 0 and ws(0, t(shape, dt)) == 0, (dt, shape)
+    assert ws(1, t((8, 10), B.DTYPE_F16)) == 2        # element type
+    assert ws(1, t((7, 10), B.DTYPE_U8)) == 3         # fewer rows than S1
+    assert ws(1, t((8, 9), B.DTYPE_U8)) == 3          # fewer columns than S2
+    assert ws(1, t((3, 8, 10), B.DTYPE_U8)) == 3      # batch dim neither 1 nor B
+    assert ws(1, t((2, 2, 8, 10), B.DTYPE_U8)) == 3   # head dim must be 1
+    assert ws(1, t((10,), B.DTYPE_U8)) == 3           # rank
+    assert ws(1, None) == 12                          # mode 1 needs the mask
+
+
 def test_shape_dtype_layout_errors(lib):
     q, k = t((1, 2, 8, 64)), t((1, 2, 9, 64))
     assert prefill_ws(lib, q, k, q, params(lib, num_heads=2, input_layout="BNSD"))[0] == 3      # k != v

@@ -186,3 +186,72 @@ def test_band_tnd_varlen(fia):
     lens = [1, 127, 300, 0, 1000, 129]
     case = fia_inputs.tnd_case(lens, lens, 8, 2, 128, "bf16", sparse_mode=4, workload=1900)
     _check_band(fia, case, 256, 32)
+
+
+# ------------------------------------------------------------ explicit atten_mask
+def _check_mask(fia, case, mask, pre=2147483647, nxt=2147483647):
+    out, lse = _run(fia, case, atten_mask=mask.to("cuda"), pre_tokens=pre, next_tokens=nxt)
+    ref_o, ref_l = fia_oracle.fia_prefill(case.q, case.k, case.v, num_heads=case.num_heads,
+                                          num_key_value_heads=case.num_key_value_heads, scale_value=case.scale,
+                                          input_layout=case.layout, sparse_mode=case.sparse_mode, atten_mask=mask,
+                                          actual_seq_qlen=case.actual_seq_qlen,
+                                          actual_seq_kvlen=case.actual_seq_kvlen, pre_tokens=pre, next_tokens=nxt)
+    assert_out_close(out, ref_o, case.q.dtype)
+    assert_lse_close(lse, ref_l)
+    return out, lse
+
+
+# (mode, D, dtype, mask shape (B=2, S1=300, S2=260 + pad), mask dtype, kind, pre, next).  The
+# padding of the key axis picks the copy granule: 260 -> 4 bytes, 264 -> 8, 272 -> 16, 261 -> 1.
+MASK_CASES = [
+    (1, 128, "bf16", (300, 272), "u8", "random", None, None),
+    (1, 64, "f16", (2, 300, 264), "bool", "blocks", None, None),
+    (1, 128, "bf16", (1, 300, 260), "i8", "blocks", None, None),
+    (0, 128, "bf16", (2, 1, 300, 261), "u8", "random", 100, 20),
+    (0, 64, "bf16", (1, 1, 304, 272), "bool", "blocks", None, None),
+    (0, 128, "f16", (300, 264), "i8", "random", 0, 300),
+]
+
+
+@pytest.mark.parametrize("mode,D,dtype,mshape,mdtype,kind,pre,nxt", MASK_CASES)
+def test_explicit_mask(fia, mode, D, dtype, mshape, mdtype, kind, pre, nxt):
+    """sparse_mode 1 (mask alone) and 0 (mask and the pre/next window): every
+    mask shape the pages list, bool / int8 / uint8 with assorted nonzero bytes,
+    each copy granule, ragged query and key tails, fully masked rows."""
+    case = fia_inputs.prefill_case(2, 4, 2, 300, 260, D, dtype=dtype, layout="BNSD", sparse_mode=mode,
+                                   workload=2000 + D + mode + mshape[-1])
+    mask = fia_inputs.atten_mask(mshape, kind, dtype=mdtype, workload=2100 + mshape[-1])
+    kw = {} if pre is None else {"pre": pre, "nxt": nxt}
+    _check_mask(fia, case, mask, **kw)
+
+
+def test_mask_causal_equals_mode2(fia):
+    """A lower-triangular mask in sparse_mode 1 gives the same bits as sparse_mode 2
+    (tiles past the diagonal only add exact zeros), and an all-zero mask in
+    sparse_mode 0 the same bits as no mask."""
+    case = fia_inputs.prefill_case(1, 4, 2, 700, 700, 128, dtype="bf16", layout="BNSD", sparse_mode=1, workload=2200)
+    causal = fia_inputs.atten_mask((700, 704), "causal")
+    out_m, lse_m = _run(fia, case, atten_mask=causal.cuda())
+    case.sparse_mode = 2
+    out_c, lse_c = _run(fia, case)
+    assert torch.equal(out_m, out_c) and torch.equal(lse_m, lse_c)
+    case.sparse_mode = 0
+    out_z, lse_z = _run(fia, case, atten_mask=torch.zeros((700, 700), dtype=torch.bool, device="cuda"))
+    out_d, lse_d = _run(fia, case)
+    assert torch.equal(out_z, out_d) and torch.equal(lse_z, lse_d)
+
+
+def test_mask_tnd_varlen(fia):
+    """TND: the mask is indexed with each sequence's own row / key numbers."""
+    lens_q, lens_kv = [1, 127, 300, 0, 700, 129], [5, 127, 260, 3, 700, 200]
+    case = fia_inputs.tnd_case(lens_q, lens_kv, 8, 2, 128, "bf16", sparse_mode=1, workload=2300)
+    mask = fia_inputs.atten_mask((6, 700, 704), "blocks", workload=2301)
+    _check_mask(fia, case, mask)
+
+
+def test_mask_2k_full(fia):
+    """2048 x 2048 with a tile-structured mask (visible, masked and random
+    tiles): sixteen K/V tiles through the ring, element by element."""
+    case = fia_inputs.prefill_case(1, 8, 2, 2048, 2048, 128, dtype="bf16", layout="BNSD", sparse_mode=1, workload=2400)
+    mask = fia_inputs.atten_mask((2048, 2048), "blocks", workload=2401)
+    _check_mask(fia, case, mask)
