@@ -375,6 +375,43 @@ def fia_decode(q, k, v, *, num_heads: int, num_key_value_heads: int = 0, scale_v
     return _from_bnsd(out, input_layout), lse
 
 
+def fia_prefill_paged(q, k, v, *, block_table, block_size: int, actual_seq_kvlen, num_heads: int,
+                      num_key_value_heads: int = 0, input_layout: str = "BNSD", **prefill_kw):
+    """Prefill (any Q_S) against a paged KV cache: chunked prefill, where a new
+    chunk of query tokens attends to the sequence's cached keys
+    (npu_fused_infer_attention_score_v2, page attention).  Key j of batch b is
+    row j % block_size of block block_table[b][j // block_size] (paged_rows);
+    with each batch's keys gathered that way the computation is fia_prefill's,
+    under the same sparse_mode / atten_mask / pre_tokens / next_tokens.
+    actual_seq_kvlen holds every batch's own key count (the cache is not TND,
+    also when the query is); k / v are (blocknum, KV_N, block_size, D) or
+    (blocknum, block_size, KV_N * D)."""
+    N1 = int(num_heads)
+    N2 = int(num_key_value_heads) or N1
+    table = np.asarray(block_table.cpu().numpy() if hasattr(block_table, "cpu") else block_table)
+    B = table.shape[0]
+    kl = resolve_lengths(actual_seq_kvlen, B, table.shape[1] * block_size)
+    Kp, Vp = f64(k), f64(v)
+    Dk = Kp.shape[-1] if Kp.ndim == 4 else Kp.shape[-1] // N2
+    Dv = Vp.shape[-1] if Vp.ndim == 4 else Vp.shape[-1] // N2
+
+    def gathered(pool, D):
+        per_batch = [np.stack([paged_rows(pool, table, b, h, kl[b], block_size, D) for h in range(N2)])
+                     for b in range(B)]                      # (N2, L_b, D) each
+        if input_layout == "TND":
+            return np.concatenate([x.transpose(1, 0, 2) for x in per_batch], axis=0) if B else np.zeros((0, N2, D))
+        S = max(kl) if B else 0
+        out = np.zeros((B, N2, S, D))
+        for b in range(B):
+            out[b, :, :kl[b], :] = per_batch[b]
+        return _from_bnsd(out, input_layout)
+
+    K, V = gathered(Kp, Dk), gathered(Vp, Dv)
+    kv_list = list(np.cumsum(kl)) if input_layout == "TND" else kl
+    return fia_prefill(q, K, V, num_heads=N1, num_key_value_heads=N2, input_layout=input_layout,
+                       actual_seq_kvlen=kv_list, **prefill_kw)
+
+
 def _mask_for_batch_decode(mask, b: int):
     """Decode atten_mask shapes (B, KV_S), (B, 1, KV_S), (B, 1, 1, KV_S)."""
     if mask is None:

@@ -273,6 +273,57 @@ def check_multitoken_decode_vs_library(orc):
                 assert np.all(out[b, h][~live] == 0) and np.all(np.isinf(lse[b, h, ~live, 0])), "tokens with no key"
 
 
+def check_paged_prefill_equals_contiguous(orc):
+    """Chunked prefill against a paged cache equals prefill over the contiguous
+    keys the pages scatter: the pool here is filled by hand (logical block i of
+    batch b goes to physical block perm[...], row r of it = key i * bs + r), in
+    both cache layouts, for a padded and a TND query, causal and band masks."""
+    B, N1, N2, D, bs = 2, 4, 2, 8, 4
+    lens_q, lens_kv = [3, 5], [9, 6]
+    S = max(lens_kv)
+    k, v = _rand((B, N2, S, D), 130), _rand((B, N2, S, D), 131)
+    perm = [5, 1, 3, 0, 4]          # physical block of each (batch, logical block), in order
+    nblk = 7
+    table = np.full((B, 3), 6, dtype=np.int32)
+    pools = {"BNBD": (torch.full((nblk, N2, bs, D), float("nan"), dtype=torch.float64),
+                      torch.full((nblk, N2, bs, D), float("nan"), dtype=torch.float64)),
+             "BBH": (torch.full((nblk, bs, N2 * D), float("nan"), dtype=torch.float64),
+                     torch.full((nblk, bs, N2 * D), float("nan"), dtype=torch.float64))}
+    pos = 0
+    for b in range(B):
+        for i in range(-(-lens_kv[b] // bs)):
+            blk = perm[pos]; pos += 1
+            table[b, i] = blk
+            for r in range(bs):
+                j = i * bs + r
+                if j >= lens_kv[b]:
+                    continue
+                pools["BNBD"][0][blk, :, r] = k[b, :, j]; pools["BNBD"][1][blk, :, r] = v[b, :, j]
+                pools["BBH"][0][blk, r] = k[b, :, j].reshape(-1); pools["BBH"][1][blk, r] = v[b, :, j].reshape(-1)
+    q = _rand((B, N1, max(lens_q), D), 132)
+    for layout_kv, (kp, vp) in pools.items():
+        for mode, extra in ((3, {}), (4, {"pre_tokens": 2, "next_tokens": 0}), (2, {})):
+            want_o, want_l = orc.fia_prefill(q, k, v, num_heads=N1, num_key_value_heads=N2, scale_value=0.4,
+                                             input_layout="BNSD", sparse_mode=mode, actual_seq_qlen=lens_q,
+                                             actual_seq_kvlen=lens_kv, **extra)
+            got_o, got_l = orc.fia_prefill_paged(q, kp, vp, block_table=table, block_size=bs,
+                                                 actual_seq_kvlen=lens_kv, num_heads=N1, num_key_value_heads=N2,
+                                                 scale_value=0.4, input_layout="BNSD", sparse_mode=mode,
+                                                 actual_seq_qlen=lens_q, **extra)
+            assert np.array_equal(got_o, want_o) and np.array_equal(got_l, want_l), "paged prefill != contiguous"
+        # TND query: rows of both sequences packed, kv lengths per batch
+        qt = torch.cat([q[b, :, :lens_q[b]].transpose(0, 1) for b in range(B)])
+        got_o, got_l = orc.fia_prefill_paged(qt, kp, vp, block_table=table, block_size=bs, actual_seq_kvlen=lens_kv,
+                                             num_heads=N1, num_key_value_heads=N2, scale_value=0.4,
+                                             input_layout="TND", sparse_mode=3, actual_seq_qlen=[3, 8])
+        want_o, want_l = orc.fia_prefill(q, k, v, num_heads=N1, num_key_value_heads=N2, scale_value=0.4,
+                                         input_layout="BNSD", sparse_mode=3, actual_seq_qlen=lens_q,
+                                         actual_seq_kvlen=lens_kv)
+        for b, (s0, L) in enumerate(((0, 3), (3, 5))):
+            assert np.array_equal(got_o[s0:s0 + L], want_o[b, :, :L].transpose(1, 0, 2)), "TND paged prefill"
+            assert np.array_equal(got_l[s0:s0 + L, :, 0], want_l[b, :, :L, 0].T), "TND paged lse"
+
+
 def check_mla_equals_concatenated_attention(orc):
     B, N1, Dl, Dr, bs = 2, 4, 16, 4, 4
     lens = [7, 8]
@@ -338,7 +389,8 @@ ALL_CHECKS = [
     check_rows_vs_library, check_prefill_causal_vs_library, check_gqa_vs_library, check_closed_forms,
     check_mask_modes_by_counting, check_softmax_rows_sum_to_one, check_layouts_agree,
     check_tnd_equals_per_sequence, check_actual_lengths_equal_truncation, check_paged_equals_contiguous,
-    check_decode_equals_prefill_row, check_multitoken_decode_vs_library, check_mla_equals_concatenated_attention,
+    check_decode_equals_prefill_row, check_multitoken_decode_vs_library, check_paged_prefill_equals_contiguous,
+    check_mla_equals_concatenated_attention,
     check_bsa, check_lse_merge,
     check_empty_rules,
 ]

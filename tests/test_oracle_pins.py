@@ -43,6 +43,11 @@ MUTATIONS = [
     ("ok = allowed_matrix(QS, kl[b], sparse_mode if QS > 1 else 0)", "ok = allowed_matrix(QS, kl[b], 0)",
      "multi-token decode ignores its mask"),
     ("qq = Q[b, h, :, :]", "qq = Q[b, h, :1, :]", "multi-token decode uses the first token only"),
+    ("per_batch = [np.stack([paged_rows(pool, table, b, h, kl[b], block_size, D) for h in range(N2)])",
+     "per_batch = [np.stack([paged_rows(pool, table, b, 0, kl[b], block_size, D) for h in range(N2)])",
+     "paged prefill reads kv head 0 only"),
+    ("kv_list = list(np.cumsum(kl)) if input_layout == \"TND\" else kl", "kv_list = kl",
+     "paged prefill TND kv list not cumulative"),
 ]
 
 
