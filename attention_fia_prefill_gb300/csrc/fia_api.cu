@@ -207,6 +207,10 @@ struct Geometry {
   const uint8_t* mask = nullptr;
   int64_t mask_sb = 0, mask_ss = 0;
   int mask_cs = 1;
+  // paged K/V (chunked prefill): pools (blocknum, KV_N, bs, D) or (blocknum, bs, KV_N*D)
+  bool paged = false, kv_bnbd = false;
+  int64_t bs = 0, nblk = 0, table_stride = 0;
+  const int32_t* table = nullptr;
 };
 
 // Shapes of q/k/v in a dense layout -> (B, N, S, D).  BSH splits H by heads.
@@ -262,9 +266,45 @@ fia_status check_lse(const fia_tensor* lse, const fia_params* p, Layout L, int64
   return FIA_OK;
 }
 
-// Common validation of q/k/v/out for the dense prefill and block-sparse calls.
+// Paged key/value pools for prefill (npu_fused_infer_attention_score_v2, page
+// attention): block_table int32 (B, >= maxBlockNumPerSeq), block_size a
+// multiple of 128 in 128..512, key/value (blocknum, KV_N, bs, D) or
+// (blocknum, bs, KV_N*D) with the same shape.  Sets the pool fields and
+// S2 = table columns x block_size; D of the key comes back in Dk.
+fia_status paged_pools(const fia_tensor* k, const fia_tensor* v, const fia_tensor* table, const fia_params* p,
+                       Geometry& g, int64_t& Dk) {
+  if (table->dtype != FIA_DTYPE_I32 || table->ndim != 2)
+    return fail(FIA_ERR_BLOCK_TABLE, "block_table must be int32 (B, maxBlocksPerSeq)");
+  if (!aligned16(table->data)) return fail(FIA_ERR_ALIGNMENT, "block_table not 16-byte aligned");
+  if (p->actual_seq_kvlen == nullptr) return fail(FIA_ERR_SEQLEN, "page attention needs actual_seq_kvlen");
+  g.bs = p->block_size;
+  if (g.bs < 128 || g.bs > 512 || g.bs % 128 != 0)
+    return fail(FIA_ERR_BLOCK_TABLE, "block_size %lld: 128..512, a multiple of 128", (long long)g.bs);
+  if (k->ndim == 4) {
+    g.kv_bnbd = true;
+    if (k->shape[1] != g.N2 || k->shape[2] != g.bs)
+      return fail(FIA_ERR_SHAPE, "paged key must be (blocknum, KV_N, block_size, D)");
+    Dk = k->shape[3];
+  } else if (k->ndim == 3) {
+    g.kv_bnbd = false;
+    if (k->shape[1] != g.bs || k->shape[2] % g.N2 != 0)
+      return fail(FIA_ERR_SHAPE, "paged key must be (blocknum, block_size, KV_N*D)");
+    Dk = k->shape[2] / g.N2;
+  } else {
+    return fail(FIA_ERR_SHAPE, "paged key must be 3-D or 4-D");
+  }
+  g.paged = true;
+  g.nblk = k->shape[0];
+  g.table = static_cast<const int32_t*>(table->data);
+  g.table_stride = table->shape[1];
+  g.S2 = table->shape[1] * g.bs;
+  return FIA_OK;
+}
+
+// Common validation of q/k/v/out for the dense prefill and block-sparse calls
+// (and the paged prefill, with a block_table).
 fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_params* p,
-                            const fia_tensor* out, bool bsa, Geometry& g) {
+                            const fia_tensor* out, bool bsa, Geometry& g, const fia_tensor* table = nullptr) {
   if (p != nullptr) {
     const int64_t lim = int64_t(1) << 30;
     g.band_pre = int(std::max(-lim, std::min(lim, p->pre_tokens)));
@@ -286,7 +326,12 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
   int64_t Bq, Bk, Dk;
   st = dense_dims(q, g.layout, g.N1, Bq, g.S1, g.D, "query");
   if (st != FIA_OK) return st;
-  st = dense_dims(k, g.layout, g.N2, Bk, g.S2, Dk, "key");
+  if (present(table)) {
+    st = paged_pools(k, v, table, p, g, Dk);
+    Bk = table->shape[0];
+  } else {
+    st = dense_dims(k, g.layout, g.N2, Bk, g.S2, Dk, "key");
+  }
   if (st != FIA_OK) return st;
   if (Dk != g.D) return fail(FIA_ERR_SHAPE, "query D=%lld, key D=%lld", (long long)g.D, (long long)Dk);
   if (g.D != 64 && g.D != 128) return fail(FIA_ERR_UNSUPPORTED, "head dim %lld (kernels take 64 or 128)", (long long)g.D);
@@ -302,7 +347,15 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
     std::vector<int32_t> qs, ql, ks, kl;
     st = resolve_tnd(p->actual_seq_qlen, p->n_actual_seq_qlen, g.T1, qs, ql, "actual_seq_qlen");
     if (st != FIA_OK) return st;
-    st = resolve_tnd(p->actual_seq_kvlen, p->n_actual_seq_kvlen, g.T2, ks, kl, "actual_seq_kvlen");
+    if (g.paged) {
+      // the cache is paged, not TND: one key count per sequence
+      if (Bk != int64_t(ql.size())) return fail(FIA_ERR_BLOCK_TABLE, "block_table must have one row per sequence");
+      g.T2 = 0;
+      st = resolve_lengths(p->actual_seq_kvlen, p->n_actual_seq_kvlen, Bk, g.S2, kl, "actual_seq_kvlen");
+      ks.assign(kl.size(), 0);
+    } else {
+      st = resolve_tnd(p->actual_seq_kvlen, p->n_actual_seq_kvlen, g.T2, ks, kl, "actual_seq_kvlen");
+    }
     if (st != FIA_OK) return st;
     if (ql.size() != kl.size()) return fail(FIA_ERR_SEQLEN, "TND lists must have the same number of entries");
     g.B = int64_t(ql.size());
@@ -321,6 +374,18 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
     if (st != FIA_OK) return st;
     g.batches.resize(size_t(g.B));
     for (int64_t b = 0; b < g.B; ++b) g.batches[size_t(b)] = BatchInfo{0, ql[size_t(b)], 0, kl[size_t(b)]};
+  }
+  if (g.paged) {
+    int64_t need_blocks = 0, max_blocks = 0;
+    for (const auto& bi : g.batches) {
+      need_blocks += (bi.kv_len + g.bs - 1) / g.bs;
+      max_blocks = std::max<int64_t>(max_blocks, (bi.kv_len + g.bs - 1) / g.bs);
+    }
+    if (g.table_stride < max_blocks)
+      return fail(FIA_ERR_BLOCK_TABLE, "block_table has fewer columns than maxBlocksPerSeq");
+    if (g.nblk < need_blocks)
+      return fail(FIA_ERR_BLOCK_TABLE, "blocknum %lld below the %lld blocks the lengths need", (long long)g.nblk,
+                  (long long)need_blocks);
   }
   return FIA_OK;
 }
@@ -450,10 +515,11 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
     }
   }
   if (items.empty()) return clear_status(base, stream);
-  if (g.S2 == 0) {
+  if (g.S2 == 0 || (g.paged && g.nblk == 0)) {
     st = clear_status(base, stream);
     if (st != FIA_OK) return st;
-    // K/V with S2 = 0: every query row is empty (out = 0, lse = +inf).
+    // K/V with S2 = 0 (or an empty pool, so every length is 0): every query
+    // row is empty (out = 0, lse = +inf).
     const int64_t dims[4] = {g.layout == L_TND ? 1 : g.B, g.N1, g.layout == L_TND ? g.T1 : g.S1, g.D};
     int64_t os2[3] = {os[0], os[1], os[2]}, ls2[3] = {ls[0], ls[1], ls[2]};
     return cuda_check(launch_fill_rows(out->data, true, lse, dims, os2, ls2, d_batches, 1, stream), "fill rows");
@@ -464,10 +530,23 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   const int64_t Bmap = g.layout == L_TND ? 1 : g.B;
   st = dense_map(&pp.tm_q, q, g.layout, Bmap, g.N1, g.S1, g.D);
   if (st != FIA_OK) return st;
-  st = dense_map(&pp.tm_k, k, g.layout, Bmap, g.N2, g.S2, g.D);
-  if (st != FIA_OK) return st;
-  st = dense_map(&pp.tm_v, v, g.layout, Bmap, g.N2, g.S2, g.D);
-  if (st != FIA_OK) return st;
+  if (g.paged) {
+    // the pool as a (D, block_size, KV_N, blocknum) tensor: BNSD-like for
+    // (blocknum, KV_N, bs, D), BSND-like for (blocknum, bs, KV_N*D)
+    const Layout pl = g.kv_bnbd ? L_BNSD : L_BSND;
+    st = dense_map(&pp.tm_k, k, pl, g.nblk, g.N2, g.bs, g.D);
+    if (st != FIA_OK) return st;
+    st = dense_map(&pp.tm_v, v, pl, g.nblk, g.N2, g.bs, g.D);
+    if (st != FIA_OK) return st;
+    pp.block_table = g.table;
+    pp.table_stride = g.table_stride;
+    pp.block_size = int(g.bs);
+  } else {
+    st = dense_map(&pp.tm_k, k, g.layout, Bmap, g.N2, g.S2, g.D);
+    if (st != FIA_OK) return st;
+    st = dense_map(&pp.tm_v, v, g.layout, Bmap, g.N2, g.S2, g.D);
+    if (st != FIA_OK) return st;
+  }
   pp.out = out->data;
   pp.lse = lse;
   pp.out_sb = os[0]; pp.out_sn = os[1]; pp.out_ss = os[2];
@@ -632,11 +711,28 @@ fia_status fia_prefill_get_workspace_size(const fia_tensor* query, const fia_ten
                                           const fia_tensor* atten_mask, const fia_params* params,
                                           const fia_tensor* attention_out, const fia_tensor* softmax_lse,
                                           size_t* workspace_bytes) {
+  return fia_prefill_paged_get_workspace_size(query, key, value, nullptr, atten_mask, params, attention_out,
+                                              softmax_lse, workspace_bytes);
+}
+
+fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                       const fia_tensor* atten_mask, const fia_params* params, const fia_tensor* attention_out,
+                       const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return fia_prefill_paged(query, key, value, nullptr, atten_mask, params, attention_out, softmax_lse, workspace,
+                           workspace_bytes, stream);
+}
+
+// block_table NULL: contiguous key/value (fia_prefill).
+fia_status fia_prefill_paged_get_workspace_size(const fia_tensor* query, const fia_tensor* key_cache,
+                                                const fia_tensor* value_cache, const fia_tensor* block_table,
+                                                const fia_tensor* atten_mask, const fia_params* params,
+                                                const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                                                size_t* workspace_bytes) {
   if (workspace_bytes == nullptr) return fail(FIA_ERR_NULL, "workspace_bytes is NULL");
   *workspace_bytes = kHeader;
   if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;   // empty query
   Geometry g;
-  fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g);
+  fia_status st = prefill_geometry(query, key_cache, value_cache, params, attention_out, false, g, block_table);
   if (st != FIA_OK) return st;
   int mode, cm;
   st = prefill_mask_mode(params, atten_mask, g, mode, cm);
@@ -647,20 +743,21 @@ fia_status fia_prefill_get_workspace_size(const fia_tensor* query, const fia_ten
   return FIA_OK;
 }
 
-fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
-                       const fia_tensor* atten_mask, const fia_params* params, const fia_tensor* attention_out,
-                       const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream) {
+fia_status fia_prefill_paged(const fia_tensor* query, const fia_tensor* key_cache, const fia_tensor* value_cache,
+                             const fia_tensor* block_table, const fia_tensor* atten_mask, const fia_params* params,
+                             const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
+                             size_t workspace_bytes, void* stream) {
   if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
   Geometry g;
-  fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g);
+  fia_status st = prefill_geometry(query, key_cache, value_cache, params, attention_out, false, g, block_table);
   if (st != FIA_OK) return st;
   int mode, cm;
   st = prefill_mask_mode(params, atten_mask, g, mode, cm);
   if (st != FIA_OK) return st;
   st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
   if (st != FIA_OK) return st;
-  return run_prefill(g, mode, cm, query, key, value, attention_out, softmax_lse, params, nullptr, 0, 0, 0, 0, workspace,
-                     workspace_bytes, static_cast<cudaStream_t>(stream));
+  return run_prefill(g, mode, cm, query, key_cache, value_cache, attention_out, softmax_lse, params, nullptr, 0, 0, 0,
+                     0, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------ block-sparse

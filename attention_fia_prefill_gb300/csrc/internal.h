@@ -48,7 +48,9 @@ struct WorkItem {
 enum PrefillMode : int { kDense = 0, kCausal = 1, kBlockSparse = 2, kBand = 3, kMask = 4 };
 
 struct PrefillParams {
-  CUtensorMap tm_q, tm_k, tm_v;   // 4-D maps (D, S, N, B); TND uses (D, T, N, 1)
+  // 4-D maps (D, S, N, B); TND uses (D, T, N, 1).  With a paged cache the K/V
+  // maps cover the pool as (D, block_size, KV_N, blocknum).
+  CUtensorMap tm_q, tm_k, tm_v;
   void* out;                      // attention_out, query layout, element type of q
   float* lse;                     // nullable
   int64_t out_sb, out_sn, out_ss; // element strides of out for (b, n, s)
@@ -63,6 +65,9 @@ struct PrefillParams {
   const uint8_t* attn_mask;       // kMask: byte (i, j) of batch b at b * mask_sb + i * mask_ss + j
   int64_t mask_sb, mask_ss;       // mask_sb = 0 for a mask shared by all batches
   int mask_cs;                    // copy granule in bytes (16, 8, 4: alignment of base and rows; 1: plain loads)
+  const int32_t* block_table;     // paged K/V: [B, table_stride] block ids; nullptr = contiguous K/V
+  int64_t table_stride;
+  int block_size;                 // a multiple of 128: a 128-key tile lies in one block
   float scale_log2;               // scale * log2(e)
   const uint8_t* bsa_mask;        // [B, N1, nqb, nkb]
   int bsa_nqb, bsa_nkb, bsa_x, bsa_y;

@@ -22,6 +22,8 @@
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D,
 // 256+2D).  Causal: tile B needs the K/V tiles of tile A plus at most one; the
 // CTA walks tile B's range and tile A stops early.
+// Paged K/V (chunked prefill against a block table): the producer takes each
+// 128-key tile from its block (block_size is a multiple of 128).
 // Explicit mask: each softmax thread copies its row's 128 mask bytes for the
 // next K/V tile into its own 128-byte shared slot (cp.async, in flight while
 // the current tile is processed) and turns them into a 128-bit mask.
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
 
   const bool is_tnd = p.is_tnd != 0;
   const int q_row0 = is_tnd ? bi.q_start + q0 : q0;
-  const int kv_row0 = is_tnd ? bi.kv_start : 0;
+  const int kv_row0 = is_tnd && p.block_table == nullptr ? bi.kv_start : 0;
   const int b_coord = is_tnd ? 0 : it.b;
 
   if (warp == 0) {
@@ -160,17 +162,25 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       int j = 0;
       for (; j < nl; ++j) {
         const int s = j % S;
+        // K/V tile coordinates: (row, batch) of a contiguous tensor, or (row in
+        // block, block id) of a paged pool (the table read overlaps the wait)
+        const int key = (jt0 + j) * kTileN;
+        int kv_r = kv_row0 + key, kv_b = b_coord;
+        if (p.block_table != nullptr) {
+          kv_b = __ldg(p.block_table + int64_t(it.b) * p.table_stride + key / p.block_size);
+          kv_r = key % p.block_size;
+        }
         if (j >= S && !mbar_wait(&kv_free[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
         uint8_t* ks = smem + C::kOffK + s * C::kTileBytes;
         uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(ks + c * C::kBoxBytes, &p.tm_k, &k_full[s], c * 64, kv_row0 + (jt0 + j) * kTileN, kvh, b_coord);
+          tma_load_4d(ks + c * C::kBoxBytes, &p.tm_k, &k_full[s], c * 64, kv_r, kvh, kv_b);
         mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[s], c * 64, kv_row0 + (jt0 + j) * kTileN, kvh, b_coord);
+          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[s], c * 64, kv_r, kvh, kv_b);
       }
       if (*abort_flag) {
         mbar_wait(q_full, 0, nullptr, p.status);

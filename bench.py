@@ -10,7 +10,8 @@ second (the K and V rows of every sequence, sum(L_b) * KV_N * D * 2 bytes * 2).
 
 The other hot-path workloads are measured in the same run under "sections":
 varlen TND causal prefill (TFLOP/s), the same with a 1024-key sliding window
-(sparse_mode 4), block-sparse prefill (TFLOP/s), MLA decode
+(sparse_mode 4), chunked prefill against a paged cache (TFLOP/s), block-sparse
+prefill (TFLOP/s), MLA decode
 (cache GB/s), the headline decode with 4 new tokens per sequence (KV GB/s) and
 the small fp16 prefill.  Inputs are seeded synthetic tensors
 of the workloads' shapes (fia_inputs.py).  The L2 is flushed (a 512 MB write)
@@ -289,6 +290,37 @@ def measure_prefill_band(torch, dev, timer, steps, warmup, pk, traffic):
                                  traffic.get("prefill_pair_kernel_band"))}
 
 
+def measure_chunked_prefill(torch, dev, timer, steps, warmup, pk, traffic):
+    """Chunked prefill against a paged cache: 8 sequences, a 2048-token chunk
+    after a cached context U[0, 14336], 256-token blocks, right-down causal."""
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    c = fia_inputs.workload_chunked_prefill()
+    D = c.q.shape[-1]
+    pairs = sum(sum(L - ql + i + 1 for i in range(ql)) for ql, L in zip(c.q_lens, c.kv_lens))
+    flops = pairs * c.num_heads * 4 * D
+    q, kp, vp, tab = c.q.to(dev), c.k_pool.to(dev), c.v_pool.to(dev), c.block_table.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], c.num_heads, q.shape[2], 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        fia.fia_prefill_paged(q, kp, vp, tab, block_size=c.block_size, actual_seq_kvlen=c.kv_lens,
+                              actual_seq_qlen=c.actual_seq_qlen, num_heads=c.num_heads,
+                              num_key_value_heads=c.num_key_value_heads, scale_value=c.scale, input_layout="BNSD",
+                              sparse_mode=3, softmax_lse_flag=True, out=out, softmax_lse=lse, workspace=ws)
+
+    call_ms, kern_ms = timer.run(call, steps, warmup, kernel_events=True)
+    km = statistics.mean(kern_ms)
+    return {"workload": "chunked prefill bf16 against a paged cache: 8 x 2048-token chunks after cached contexts "
+                        "U[0,14336], Q_N=32, KV_N=8, D=128, block 256, sparse_mode 3, LSE",
+            "metric": "prefill attention TFLOP/s", "unit": "TFLOP/s",
+            "value": round(flops / (statistics.mean(call_ms) * 1e-3) / 1e12, 2), "ms_per_call": statistics.mean(call_ms),
+            "kernel_ms": km, "flops": flops, "kv_lens": c.kv_lens,
+            "roofline": roofline("tensor", flops / (km * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s",
+                                 traffic.get("prefill_pair_kernel_chunked"))}
+
+
 def measure_bsa(torch, dev, timer, steps, warmup, pk, traffic):
     import attention_fia_prefill_gb300 as fia
     import fia_inputs
@@ -431,6 +463,7 @@ def run_ours(args):
     sections = {}
     if not args.headline_only:
         for name, fn in (("prefill_tnd", measure_prefill_tnd), ("prefill_band", measure_prefill_band),
+                         ("chunked_prefill", measure_chunked_prefill),
                          ("bsa", measure_bsa), ("mla_decode", measure_mla), ("decode_q4", measure_decode_tokens)):
             try:
                 sections[name] = fn(torch, dev, timer, args.steps, args.warmup, pk, traffic)

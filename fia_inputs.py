@@ -212,6 +212,55 @@ def workload_paged_gqa_decode(B=16, N1=32, N2=8, D=128, max_len=4096, workload=2
 
 
 # --------------------------------------------------------------------------------------
+# Prefill against a paged cache (chunked prefill)
+# --------------------------------------------------------------------------------------
+@dataclass
+class PagedPrefillCase:
+    q: torch.Tensor               # BNSD (B, N1, max q_len, D) / BSND / BSH, or TND (T, N1, D)
+    k_pool: torch.Tensor          # (nblk, N2, bs, D) or (nblk, bs, N2*D)
+    v_pool: torch.Tensor
+    block_table: torch.Tensor     # int32 (B, max_blocks)
+    q_lens: list
+    kv_lens: list
+    actual_seq_qlen: list         # per batch, or cumulative for TND
+    block_size: int
+    num_heads: int
+    num_key_value_heads: int
+    scale: float
+    layout: str
+    meta: dict = field(default_factory=dict)
+
+
+def paged_prefill_case(q_lens, kv_lens, N1, N2, D, block_size=256, dtype="bf16", layout="BNSD", layout_kv="BNBD",
+                       workload=700) -> PagedPrefillCase:
+    """A chunk of q_lens[b] new query rows per sequence against kv_lens[b]
+    cached keys (the chunk's own keys included) in a paged pool built like
+    paged_decode_case's: shuffled blocks, a NaN block behind unused table
+    entries, NaN rows past each sequence's length in its last block."""
+    B = len(kv_lens)
+    dc = paged_decode_case(B, N1, N2, D, kv_lens, block_size, dtype, workload, layout_kv=layout_kv)
+    if layout == "TND":
+        q = normal((sum(q_lens), N1, D), dtype, workload, 20)
+        aq = cumsum_no_leading_zero(q_lens)
+    else:
+        S = max(q_lens) if q_lens else 0
+        shape = {"BNSD": (B, N1, S, D), "BSND": (B, S, N1, D), "BSH": (B, S, N1 * D)}[layout]
+        q = normal(shape, dtype, workload, 20)
+        aq = list(q_lens)
+    return PagedPrefillCase(q, dc.k_pool, dc.v_pool, dc.block_table, list(q_lens), list(kv_lens), aq, block_size,
+                            N1, N2, 1.0 / math.sqrt(D), layout, {"layout_kv": layout_kv, **dc.meta})
+
+
+def workload_chunked_prefill(B=8, chunk=2048, max_ctx=14336, N1=32, N2=8, D=128, block_size=256,
+                             workload=6) -> PagedPrefillCase:
+    """Chunked prefill bf16: a 2048-token chunk per sequence after a cached
+    context uniform on [0, max_ctx], paged in 256-token blocks, GQA 32/8."""
+    ctx = uniform_ints(0, max_ctx, B, workload, 0)
+    return paged_prefill_case([chunk] * B, [c + chunk for c in ctx], N1, N2, D, block_size, "bf16", "BNSD", "BNBD",
+                              workload)
+
+
+# --------------------------------------------------------------------------------------
 # MLA decode
 # --------------------------------------------------------------------------------------
 @dataclass

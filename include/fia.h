@@ -147,6 +147,34 @@ FIA_API fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, c
                        const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * fia_prefill_paged: fia_prefill with key/value in a paged cache (chunked
+ * prefill: a chunk of new query tokens against a sequence's cached keys).
+ *   npu_fused_infer_attention_score_v2, page attention: key j of batch b is
+ *   row j % block_size of block block_table[b][j / block_size].
+ *   query, atten_mask, sparse_mode (0..4), pre/next tokens, attention_out and
+ *          softmax_lse as in fia_prefill (BSH/BSND/BNSD/TND query).
+ *   key_cache, value_cache: device, same shape, the query's element type,
+ *          (blocknum, KV_N, block_size, D) or (blocknum, block_size, KV_N*D).
+ *   block_table: device int32 (B, >= maxBlockNumPerSeq); B = the query's batch
+ *          (the number of sequences for TND).  Entries are not range-checked
+ *          (the pages leave them to the caller); an id outside the pool reads
+ *          as zeros.  NULL block_table = fia_prefill.
+ *   params->block_size: 128..512, a multiple of 128; params->actual_seq_kvlen
+ *          is required and holds each batch's key count (not cumulative,
+ *          also for a TND query: the cache is not TND).
+ *   blocknum must cover the blocks the lengths need (FIA_ERR_BLOCK_TABLE).
+ * ------------------------------------------------------------------------ */
+FIA_API fia_status fia_prefill_paged_get_workspace_size(const fia_tensor* query, const fia_tensor* key_cache,
+                                                const fia_tensor* value_cache, const fia_tensor* block_table,
+                                                const fia_tensor* atten_mask, const fia_params* params,
+                                                const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                                                size_t* workspace_bytes);
+FIA_API fia_status fia_prefill_paged(const fia_tensor* query, const fia_tensor* key_cache, const fia_tensor* value_cache,
+                             const fia_tensor* block_table, const fia_tensor* atten_mask, const fia_params* params,
+                             const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * fia_decode: incremental attention, Q_S new query tokens per batch.
  *   query  (B,N1,Q_S,D) BNSD | (B,Q_S,N1,D) BSND | (B,Q_S,H) BSH; f16 or bf16.
  *          Q_S = 1, or 2..16 with (N1 / N2) * Q_S <= 64 (not with MLA); then

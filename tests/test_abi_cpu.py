@@ -141,6 +141,37 @@ def test_explicit_mask_rules(lib):
     assert ws(1, None) == 12                          # mode 1 needs the mask
 
 
+def test_paged_prefill_rules(lib):
+    """Prefill against a paged cache: block_size 128..512 in steps of 128,
+    actual_seq_kvlen required, block_table (B, >= max blocks) int32, blocknum
+    covering the lengths, one table row per TND sequence."""
+    q = t((2, 4, 300, 128))
+    kp = t((9, 2, 256, 128))
+
+    def ws(q, kp, table, bs=256, kv=(500, 300), layout="BNSD", ql=None):
+        prm = params(lib, num_heads=4, num_key_value_heads=2, input_layout=layout, sparse_mode=3, block_size=bs,
+                     actual_seq_kvlen=list(kv) if kv is not None else None, actual_seq_qlen=ql)
+        w = ctypes.c_size_t(0)
+        return lib.fia_prefill_paged_get_workspace_size(ctypes.byref(q), ctypes.byref(kp), ctypes.byref(kp),
+                                                        ctypes.byref(table), None, ctypes.byref(prm.p),
+                                                        ctypes.byref(q), None, ctypes.byref(w))
+
+    tab = t((2, 3), B.DTYPE_I32)
+    assert ws(q, kp, tab) == 0
+    assert ws(q, t((9, 256, 256)), tab) == 0                      # (blocknum, bs, KV_N*D)
+    assert ws(q, t((9, 2, 128, 128)), tab, bs=128) == 6             # 500 keys > 3 table columns x 128
+    assert ws(q, t((9, 2, 64, 128)), tab, bs=64) == 7               # block_size below 128
+    assert ws(q, t((9, 2, 640, 128)), tab, bs=640) == 7             # above 512
+    assert ws(q, t((3, 2, 256, 128)), tab) == 7                     # 3 blocks < 2 + 2 needed
+    assert ws(q, kp, t((2, 3), B.DTYPE_I64)) == 7                   # table dtype
+    assert ws(q, kp, t((3, 3), B.DTYPE_I32)) == 3                   # table rows != B
+    assert ws(q, kp, tab, kv=None) == 6                             # actual_seq_kvlen required
+    assert ws(q, t((9, 2, 256, 128)), tab, bs=128) == 3             # pool block dim != block_size
+    qt = t((800, 4, 128))
+    assert ws(qt, kp, tab, layout="TND", ql=[300, 800]) == 0
+    assert ws(qt, kp, t((3, 3), B.DTYPE_I32), layout="TND", ql=[300, 800]) == 7
+
+
 def test_shape_dtype_layout_errors(lib):
     q, k = t((1, 2, 8, 64)), t((1, 2, 9, 64))
     assert prefill_ws(lib, q, k, q, params(lib, num_heads=2, input_layout="BNSD"))[0] == 3      # k != v
