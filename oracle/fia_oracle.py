@@ -195,19 +195,37 @@ def fia_prefill(q, k, v, *, num_heads: int, num_key_value_heads: int = 0, scale_
                 input_layout: str = "BSH", sparse_mode: int = 0, atten_mask=None,
                 actual_seq_qlen=None, actual_seq_kvlen=None,
                 pre_tokens: int = INT32_MAX, next_tokens: int = INT32_MAX,
-                rows=None):
+                rows=None, query_rope=None, key_rope=None):
     """Full attention (Q_S >= 1) over contiguous key/value.
 
     Returns (attention_out, softmax_lse) as float64 arrays: out has the query's
     shape with value's head dim; lse is (B, Q_N, Q_S, 1) or (T, Q_N, 1).
     With rows=[(b, h, i), ...] only those query rows are computed and a list of
-    (out_row, lse) pairs is returned instead (used at full sizes)."""
+    (out_row, lse) pairs is returned instead (used at full sizes).
+    MLA prefill (npu_fused_infer_attention_score_v2, query D 128 with
+    query_rope / key_rope of D 64, or query / key D 192 with value D 128): the
+    score of a pair is scale * (q . k + q_rope . k_rope), i.e. the product over
+    the concatenation [q, q_rope] . [k, k_rope]; value keeps its own D."""
     N1 = int(num_heads)
     N2 = int(num_key_value_heads) or N1
     if N1 % N2:
         raise ValueError("num_heads must be a multiple of num_key_value_heads")
     g = N1 // N2
+    if (query_rope is None) != (key_rope is None):
+        raise ValueError("query_rope and key_rope must be given together")
     Q, K, V = f64(q), f64(k), f64(v)
+    if query_rope is not None:
+        if input_layout == "BSH":
+            # (B, S, N*D) and (B, S, N*64): concatenate per head
+            B_, S1_, _ = Q.shape
+            Q = np.concatenate([Q.reshape(B_, S1_, N1, -1), f64(query_rope).reshape(B_, S1_, N1, -1)],
+                               axis=3).reshape(B_, S1_, -1)
+            B_, S2_, _ = K.shape
+            K = np.concatenate([K.reshape(B_, S2_, N2, -1), f64(key_rope).reshape(B_, S2_, N2, -1)],
+                               axis=3).reshape(B_, S2_, -1)
+        else:
+            Q = np.concatenate([Q, f64(query_rope)], axis=-1)
+            K = np.concatenate([K, f64(key_rope)], axis=-1)
     if input_layout == "TND":
         qs, ql = tnd_lengths(actual_seq_qlen)
         ks, kl = tnd_lengths(actual_seq_kvlen)

@@ -324,6 +324,42 @@ def check_paged_prefill_equals_contiguous(orc):
             assert np.array_equal(got_l[s0:s0 + L, :, 0], want_l[b, :, :L, 0].T), "TND paged lse"
 
 
+def check_mla_prefill_vs_library(orc):
+    """MLA prefill: scores over [q, q_rope] . [k, k_rope], value with its own
+    D.  Reference: the library's attention on the concatenation built here, per
+    sequence and head of a TND batch (right-down causal); the BSH layout
+    (rope concatenated per head) agrees with BNSD."""
+    N1, N2, D, Dr, Dv = 4, 2, 8, 4, 6
+    lq, lk = [3, 5], [4, 5]
+    q, qr = _rand((8, N1, D), 140), _rand((8, N1, Dr), 141)
+    k, kr, v = _rand((9, N2, D), 142), _rand((9, N2, Dr), 143), _rand((9, N2, Dv), 144)
+    out, lse = orc.fia_prefill(q, k, v, query_rope=qr, key_rope=kr, num_heads=N1, num_key_value_heads=N2,
+                               scale_value=0.3, input_layout="TND", sparse_mode=3, actual_seq_qlen=[3, 8],
+                               actual_seq_kvlen=[4, 9])
+    assert out.shape == (8, N1, Dv) and lse.shape == (8, N1, 1)
+    for b, (q0, k0) in enumerate(((0, 0), (3, 4))):
+        for h in range(N1):
+            kv = h // (N1 // N2)
+            qc = torch.cat([q[q0:q0 + lq[b], h], qr[q0:q0 + lq[b], h]], dim=1).numpy()
+            kc = torch.cat([k[k0:k0 + lk[b], kv], kr[k0:k0 + lk[b], kv]], dim=1).numpy()
+            vv = v[k0:k0 + lk[b], kv].numpy()
+            allowed = np.array([[j <= i + lk[b] - lq[b] for j in range(lk[b])] for i in range(lq[b])])
+            ref = _sdpa(qc, kc, vv, allowed, 0.3)
+            assert np.allclose(out[q0:q0 + lq[b], h], ref, atol=ATOL), "MLA prefill != library attention"
+            ref_lse = logsumexp(np.where(allowed, 0.3 * qc @ kc.T, -np.inf), axis=1)
+            assert np.allclose(lse[q0:q0 + lq[b], h, 0], ref_lse, atol=ATOL), "MLA prefill lse"
+    # BSH (heads packed in H) against BNSD
+    qb, qrb = _rand((2, N1, 5, D), 145), _rand((2, N1, 5, Dr), 146)
+    kb, krb, vb = _rand((2, N2, 6, D), 147), _rand((2, N2, 6, Dr), 148), _rand((2, N2, 6, Dv), 149)
+    o1, l1 = orc.fia_prefill(qb, kb, vb, query_rope=qrb, key_rope=krb, num_heads=N1, num_key_value_heads=N2,
+                             scale_value=0.3, input_layout="BNSD", sparse_mode=2)
+    bsh = lambda x: x.transpose(1, 2).reshape(x.shape[0], x.shape[2], -1)
+    o2, l2 = orc.fia_prefill(bsh(qb), bsh(kb), bsh(vb), query_rope=bsh(qrb), key_rope=bsh(krb), num_heads=N1,
+                             num_key_value_heads=N2, scale_value=0.3, input_layout="BSH", sparse_mode=2)
+    assert np.allclose(o2, bsh(torch.from_numpy(o1)).numpy(), atol=ATOL) and np.allclose(l1, l2, atol=ATOL), \
+        "MLA prefill BSH != BNSD"
+
+
 def check_mla_equals_concatenated_attention(orc):
     B, N1, Dl, Dr, bs = 2, 4, 16, 4, 4
     lens = [7, 8]
@@ -390,7 +426,7 @@ ALL_CHECKS = [
     check_mask_modes_by_counting, check_softmax_rows_sum_to_one, check_layouts_agree,
     check_tnd_equals_per_sequence, check_actual_lengths_equal_truncation, check_paged_equals_contiguous,
     check_decode_equals_prefill_row, check_multitoken_decode_vs_library, check_paged_prefill_equals_contiguous,
-    check_mla_equals_concatenated_attention,
+    check_mla_prefill_vs_library, check_mla_equals_concatenated_attention,
     check_bsa, check_lse_merge,
     check_empty_rules,
 ]

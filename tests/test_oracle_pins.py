@@ -48,6 +48,10 @@ MUTATIONS = [
      "paged prefill reads kv head 0 only"),
     ("kv_list = list(np.cumsum(kl)) if input_layout == \"TND\" else kl", "kv_list = kl",
      "paged prefill TND kv list not cumulative"),
+    ("            K = np.concatenate([K, f64(key_rope)], axis=-1)",
+     "            K = np.concatenate([K, 0 * f64(key_rope)], axis=-1)", "MLA prefill rope term dropped"),
+    ("            Q = np.concatenate([Q, f64(query_rope)], axis=-1)",
+     "            Q = np.concatenate([f64(query_rope), Q], axis=-1)", "MLA prefill rope on the wrong side"),
 ]
 
 
