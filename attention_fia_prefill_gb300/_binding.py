@@ -25,8 +25,8 @@ DTYPE_F16, DTYPE_BF16, DTYPE_F32, DTYPE_I32, DTYPE_I64, DTYPE_U8, DTYPE_BOOL, DT
 
 # Every symbol include/fia.h declares.
 EXPORTS = [
-    "fia_params_init", "fia_prefill_get_workspace_size", "fia_prefill", "fia_prefill_paged_get_workspace_size",
-    "fia_prefill_paged", "fia_decode_get_workspace_size",
+    "fia_params_init", "fia_prefill_get_workspace_size", "fia_prefill", "fia_prefill_mla_get_workspace_size",
+    "fia_prefill_mla", "fia_prefill_paged_get_workspace_size", "fia_prefill_paged", "fia_decode_get_workspace_size",
     "fia_decode", "bsa_get_workspace_size", "bsa_forward", "fia_device_status", "fia_status_string",
     "fia_last_error", "fia_profile_next_call", "fia_decode_no_alloc",
 ]
@@ -77,6 +77,10 @@ def load_library(path: str | None = None):
     lib.fia_prefill_get_workspace_size.restype = st
     lib.fia_prefill.argtypes = [T, T, T, T, P, T, T, vp, ctypes.c_size_t, vp]
     lib.fia_prefill.restype = st
+    lib.fia_prefill_mla_get_workspace_size.argtypes = [T, T, T, T, T, T, P, T, T, sz]
+    lib.fia_prefill_mla_get_workspace_size.restype = st
+    lib.fia_prefill_mla.argtypes = [T, T, T, T, T, T, P, T, T, vp, ctypes.c_size_t, vp]
+    lib.fia_prefill_mla.restype = st
     lib.fia_prefill_paged_get_workspace_size.argtypes = [T, T, T, T, T, P, T, T, sz]
     lib.fia_prefill_paged_get_workspace_size.restype = st
     lib.fia_prefill_paged.argtypes = [T, T, T, T, T, P, T, T, vp, ctypes.c_size_t, vp]
@@ -228,6 +232,40 @@ def fia_prefill(query, key, value, *, atten_mask=None, actual_seq_qlen=None, act
     check(lib.fia_prefill(_ref(dq), _ref(dk), _ref(dv), _ref(dm), ctypes.byref(prm.p), _ref(do), _ref(dl),
                           ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
                           _stream_ptr(query.device)))
+    return out, softmax_lse
+
+
+def fia_prefill_mla(query, key, value, *, query_rope=None, key_rope=None, atten_mask=None, actual_seq_qlen=None,
+                    actual_seq_kvlen=None, num_heads=1, num_key_value_heads=0, scale_value=1.0, input_layout="TND",
+                    sparse_mode=0, pre_tokens=INT32_MAX, next_tokens=INT32_MAX, softmax_lse_flag=False,
+                    inner_precise=0, out=None, softmax_lse=None, workspace=None):
+    """MLA prefill: query/key D 192 (or D 128 with query_rope / key_rope of D 64),
+    value D 128.  Returns (attention_out with value's head dim, softmax_lse or None)."""
+    import torch
+    _require_cuda(query, key, value, query_rope, key_rope, atten_mask)
+    lib = load_library()
+    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+                 input_layout=input_layout, sparse_mode=sparse_mode, pre_tokens=pre_tokens, next_tokens=next_tokens,
+                 actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen,
+                 softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
+    if out is None:
+        nkv = num_key_value_heads or num_heads
+        dv = value.shape[-1] // nkv if input_layout == "BSH" else value.shape[-1]
+        shape = list(query.shape)
+        shape[-1] = num_heads * dv if input_layout == "BSH" else dv
+        out = torch.empty(shape, dtype=query.dtype, device=query.device)
+    if softmax_lse_flag and softmax_lse is None:
+        softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
+    descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, atten_mask, out, softmax_lse)]
+    dq, dk, dv_, dqr, dkr, dm, do, dl = (_ref(d) for d in descs)
+    ws = ctypes.c_size_t(0)
+    check(lib.fia_prefill_mla_get_workspace_size(dq, dk, dv_, dqr, dkr, dm, ctypes.byref(prm.p), do, dl,
+                                                 ctypes.byref(ws)))
+    if workspace is None or workspace.numel() < ws.value:
+        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
+    check(lib.fia_prefill_mla(dq, dk, dv_, dqr, dkr, dm, ctypes.byref(prm.p), do, dl,
+                              ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
+                              _stream_ptr(query.device)))
     return out, softmax_lse
 
 

@@ -207,6 +207,12 @@ struct Geometry {
   const uint8_t* mask = nullptr;
   int64_t mask_sb = 0, mask_ss = 0;
   int mask_cs = 1;
+  // head dims the kernels run with: scores over Dqk, value / output Dv (MLA
+  // prefill: 192 / 128, with the rope columns from qr / kr when given)
+  int64_t Dqk = 0, Dv = 0;
+  bool mla = false;
+  const fia_tensor* qr = nullptr;
+  const fia_tensor* kr = nullptr;
   // paged K/V (chunked prefill): pools (blocknum, KV_N, bs, D) or (blocknum, bs, KV_N*D)
   bool paged = false, kv_bnbd = false;
   int64_t bs = 0, nblk = 0, table_stride = 0;
@@ -303,8 +309,11 @@ fia_status paged_pools(const fia_tensor* k, const fia_tensor* v, const fia_tenso
 
 // Common validation of q/k/v/out for the dense prefill and block-sparse calls
 // (and the paged prefill, with a block_table).
+// MLA prefill (mla): value and output have D 128; query/key D 192, or D 128
+// plus query_rope / key_rope of D 64.
 fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_params* p,
-                            const fia_tensor* out, bool bsa, Geometry& g, const fia_tensor* table = nullptr) {
+                            const fia_tensor* out, bool bsa, Geometry& g, const fia_tensor* table = nullptr,
+                            bool mla = false, const fia_tensor* qr = nullptr, const fia_tensor* kr = nullptr) {
   if (p != nullptr) {
     const int64_t lim = int64_t(1) << 30;
     g.band_pre = int(std::max(-lim, std::min(lim, p->pre_tokens)));
@@ -321,8 +330,8 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
   if (out->dtype != q->dtype) return fail(FIA_ERR_DTYPE, "attention_out must have the query's dtype");
   fia_status st = resolve_heads(p, g.N1, g.N2);
   if (st != FIA_OK) return st;
-  if (!same_shape(k, v)) return fail(FIA_ERR_SHAPE, "key and value shapes differ");
-  if (!same_shape(q, out)) return fail(FIA_ERR_SHAPE, "attention_out must have the query's shape");
+  if (!mla && !same_shape(k, v)) return fail(FIA_ERR_SHAPE, "key and value shapes differ");
+  if (!mla && !same_shape(q, out)) return fail(FIA_ERR_SHAPE, "attention_out must have the query's shape");
   int64_t Bq, Bk, Dk;
   st = dense_dims(q, g.layout, g.N1, Bq, g.S1, g.D, "query");
   if (st != FIA_OK) return st;
@@ -334,7 +343,42 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
   }
   if (st != FIA_OK) return st;
   if (Dk != g.D) return fail(FIA_ERR_SHAPE, "query D=%lld, key D=%lld", (long long)g.D, (long long)Dk);
-  if (g.D != 64 && g.D != 128) return fail(FIA_ERR_UNSUPPORTED, "head dim %lld (kernels take 64 or 128)", (long long)g.D);
+  g.Dqk = g.Dv = g.D;
+  if (mla) {
+    if (present(table)) return fail(FIA_ERR_UNSUPPORTED, "MLA prefill takes contiguous key/value");
+    int64_t Bv, Sv, Dv, Bo, So, Do;
+    st = dense_dims(v, g.layout, g.N2, Bv, Sv, Dv, "value");
+    if (st != FIA_OK) return st;
+    st = dense_dims(out, g.layout, g.N1, Bo, So, Do, "attention_out");
+    if (st != FIA_OK) return st;
+    if (Bv != Bk || Sv != g.S2) return fail(FIA_ERR_SHAPE, "value must match key but for its head dim");
+    if (Dv != 128) return fail(FIA_ERR_UNSUPPORTED, "MLA prefill takes value D 128 (got %lld)", (long long)Dv);
+    if (Bo != Bq || So != g.S1 || Do != Dv)
+      return fail(FIA_ERR_SHAPE, "attention_out must be the query's shape with value's head dim");
+    if (present(qr) != present(kr)) return fail(FIA_ERR_SHAPE, "query_rope and key_rope must be given together");
+    if (present(qr)) {
+      if (g.D != 128) return fail(FIA_ERR_UNSUPPORTED, "with query_rope / key_rope, query and key take D 128");
+      if (qr->dtype != q->dtype || kr->dtype != q->dtype) return fail(FIA_ERR_DTYPE, "rope tensors must match query");
+      int64_t Br, Sr, Dr;
+      st = dense_dims(qr, g.layout, g.N1, Br, Sr, Dr, "query_rope");
+      if (st != FIA_OK) return st;
+      if (Br != Bq || Sr != g.S1 || Dr != 64) return fail(FIA_ERR_SHAPE, "query_rope must be the query's shape with D 64");
+      st = dense_dims(kr, g.layout, g.N2, Br, Sr, Dr, "key_rope");
+      if (st != FIA_OK) return st;
+      if (Br != Bk || Sr != g.S2 || Dr != 64) return fail(FIA_ERR_SHAPE, "key_rope must be the key's shape with D 64");
+      if (!aligned16(qr->data) || !aligned16(kr->data)) return fail(FIA_ERR_ALIGNMENT, "rope tensors not 16-byte aligned");
+    } else if (g.D != 192) {
+      return fail(FIA_ERR_UNSUPPORTED, "MLA prefill takes query/key D 192, or D 128 with rope tensors (got %lld)",
+                  (long long)g.D);
+    }
+    g.mla = true;
+    g.qr = qr;
+    g.kr = kr;
+    g.Dqk = 192;
+    g.Dv = 128;
+  } else if (g.D != 64 && g.D != 128) {
+    return fail(FIA_ERR_UNSUPPORTED, "head dim %lld (kernels take 64 or 128)", (long long)g.D);
+  }
   if (!(p->scale_value > 0.0) || !std::isfinite(p->scale_value))
     return fail(FIA_ERR_UNSUPPORTED, "scale_value must be finite and > 0");
   if (p->inner_precise < 0 || p->inner_precise > 4) return fail(FIA_ERR_UNSUPPORTED, "inner_precise %d", p->inner_precise);
@@ -490,7 +534,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   if (g.B == 0) return clear_status(base, stream);
 
   int64_t os[3], ls[3] = {0, 0, 0};
-  bns_strides(g.layout, g.N1, g.S1, g.D, os);
+  bns_strides(g.layout, g.N1, g.S1, g.Dv, os);
   if (g.layout == L_TND) { ls[0] = 0; ls[1] = 1; ls[2] = g.N1; }
   else { ls[0] = g.N1 * g.S1; ls[1] = g.S1; ls[2] = 1; }
 
@@ -509,7 +553,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
     bool padded = false;
     for (const auto& bi : g.batches) padded |= bi.q_len < g.S1;
     if (padded) {
-      const int64_t dims[4] = {g.B, g.N1, g.S1, g.D};
+      const int64_t dims[4] = {g.B, g.N1, g.S1, g.Dv};
       st = cuda_check(launch_fill_rows(out->data, true, lse, dims, os, ls, d_batches, 0, stream), "fill rows");
       if (st != FIA_OK) return st;
     }
@@ -520,7 +564,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
     if (st != FIA_OK) return st;
     // K/V with S2 = 0 (or an empty pool, so every length is 0): every query
     // row is empty (out = 0, lse = +inf).
-    const int64_t dims[4] = {g.layout == L_TND ? 1 : g.B, g.N1, g.layout == L_TND ? g.T1 : g.S1, g.D};
+    const int64_t dims[4] = {g.layout == L_TND ? 1 : g.B, g.N1, g.layout == L_TND ? g.T1 : g.S1, g.Dv};
     int64_t os2[3] = {os[0], os[1], os[2]}, ls2[3] = {ls[0], ls[1], ls[2]};
     return cuda_check(launch_fill_rows(out->data, true, lse, dims, os2, ls2, d_batches, 1, stream), "fill rows");
   }
@@ -544,8 +588,20 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   } else {
     st = dense_map(&pp.tm_k, k, g.layout, Bmap, g.N2, g.S2, g.D);
     if (st != FIA_OK) return st;
-    st = dense_map(&pp.tm_v, v, g.layout, Bmap, g.N2, g.S2, g.D);
+    st = dense_map(&pp.tm_v, v, g.layout, Bmap, g.N2, g.S2, g.Dv);
     if (st != FIA_OK) return st;
+  }
+  // the score columns past 128 (MLA prefill): separate rope tensors, or
+  // columns 128..191 of query / key
+  pp.tm_qr = pp.tm_q;
+  pp.tm_kr = pp.tm_k;
+  pp.rope_col = 128;
+  if (g.qr != nullptr) {
+    st = dense_map(&pp.tm_qr, g.qr, g.layout, Bmap, g.N1, g.S1, 64);
+    if (st != FIA_OK) return st;
+    st = dense_map(&pp.tm_kr, g.kr, g.layout, Bmap, g.N2, g.S2, 64);
+    if (st != FIA_OK) return st;
+    pp.rope_col = 0;
   }
   pp.out = out->data;
   pp.lse = lse;
@@ -572,7 +628,8 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   return cuda_check(profiled(stream,
                              [&] {
                                return mode == kBlockSparse ? launch_prefill(pp, int(g.D), g.bf16, mode, stream)
-                                                           : launch_prefill_pair(pp, int(g.D), g.bf16, mode, stream);
+                                                           : launch_prefill_pair(pp, int(g.Dqk), int(g.Dv), g.bf16,
+                                                                                 mode, stream);
                              }),
                     "prefill launch");
 }
@@ -620,6 +677,7 @@ fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, Geomet
       mode = kDense;   // no mask: pre_tokens / next_tokens are ignored
       return FIA_OK;
     }
+    if (g.mla) return fail(FIA_ERR_UNSUPPORTED, "an explicit atten_mask with MLA prefill is not implemented");
     fia_status st = explicit_mask(mask, g);
     if (st != FIA_OK) return st;
     // mode 0 keeps the band pre_tokens .. next_tokens around the diagonal;
@@ -758,6 +816,45 @@ fia_status fia_prefill_paged(const fia_tensor* query, const fia_tensor* key_cach
   if (st != FIA_OK) return st;
   return run_prefill(g, mode, cm, query, key_cache, value_cache, attention_out, softmax_lse, params, nullptr, 0, 0, 0,
                      0, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+fia_status fia_prefill_mla_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                              const fia_tensor* query_rope, const fia_tensor* key_rope,
+                                              const fia_tensor* atten_mask, const fia_params* params,
+                                              const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                                              size_t* workspace_bytes) {
+  if (workspace_bytes == nullptr) return fail(FIA_ERR_NULL, "workspace_bytes is NULL");
+  *workspace_bytes = kHeader;
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;   // empty query
+  Geometry g;
+  fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g, nullptr, true, query_rope,
+                                   key_rope);
+  if (st != FIA_OK) return st;
+  int mode, cm;
+  st = prefill_mask_mode(params, atten_mask, g, mode, cm);
+  if (st != FIA_OK) return st;
+  st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
+  if (st != FIA_OK) return st;
+  *workspace_bytes = prefill_ws_bytes(g.batches.size(), count_items(g));
+  return FIA_OK;
+}
+
+fia_status fia_prefill_mla(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                           const fia_tensor* query_rope, const fia_tensor* key_rope, const fia_tensor* atten_mask,
+                           const fia_params* params, const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  Geometry g;
+  fia_status st = prefill_geometry(query, key, value, params, attention_out, false, g, nullptr, true, query_rope,
+                                   key_rope);
+  if (st != FIA_OK) return st;
+  int mode, cm;
+  st = prefill_mask_mode(params, atten_mask, g, mode, cm);
+  if (st != FIA_OK) return st;
+  st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
+  if (st != FIA_OK) return st;
+  return run_prefill(g, mode, cm, query, key, value, attention_out, softmax_lse, params, nullptr, 0, 0, 0, 0, workspace,
+                     workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------ block-sparse

@@ -51,6 +51,11 @@ struct PrefillParams {
   // 4-D maps (D, S, N, B); TND uses (D, T, N, 1).  With a paged cache the K/V
   // maps cover the pool as (D, block_size, KV_N, blocknum).
   CUtensorMap tm_q, tm_k, tm_v;
+  // scores over 192 columns (MLA prefill): columns 128..191 of Q / K come from
+  // tm_qr / tm_kr at column rope_col (separate 64-wide rope tensors, rope_col
+  // 0, or the same 192-wide tensors, rope_col 128)
+  CUtensorMap tm_qr, tm_kr;
+  int rope_col;
   void* out;                      // attention_out, query layout, element type of q
   float* lse;                     // nullable
   int64_t out_sb, out_sn, out_ss; // element strides of out for (b, n, s)
@@ -156,7 +161,8 @@ void set_last_error(int status, const char* message);
 
 // Host-side launchers (defined next to their kernels).
 cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
-cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
+cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int head_dim_v, bool bf16, int mode,
+                                cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, cudaStream_t s);
 cudaError_t launch_mla(const MlaParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_fill_rows(void* out, bool half_type, float* lse, const int64_t* dims, const int64_t* out_strides,

@@ -19,8 +19,8 @@
 //               per query row (= TMEM lane), running max / sum in registers,
 //               P written over S in TMEM, O rescaled in TMEM when the max grows
 //               by more than 2^8, epilogue O / l and LSE.
-// TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D,
-// 256+2D).  Causal: tile B needs the K/V tiles of tile A plus at most one; the
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+DV), O_B [256+DV,
+// 256+2DV).  Causal: tile B needs the K/V tiles of tile A plus at most one; the
 // CTA walks tile B's range and tile A stops early.
 // Paged K/V (chunked prefill against a block table): the producer takes each
 // 128-key tile from its block (block_size is a multiple of 128).
@@ -33,26 +33,34 @@
 namespace fia {
 namespace {
 
-template <int D>
+// DQK: head dim of the scores (Q and K; 192 = MLA's 128 + 64 rope columns),
+// DV: head dim of V and O.  K and V have rings of their own: a K stage is free
+// once its last Q K^T is done, a V stage once its last P V is.
+template <int DQK, int DV>
 struct PairCfg {
-  static constexpr int kChunks = D / 64;
+  static constexpr int kChunksQK = DQK / 64;
+  static constexpr int kChunksV = DV / 64;
   static constexpr int kBoxBytes = 128 * 128;
-  static constexpr int kTileBytes = kChunks * kBoxBytes;
-  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr int kTileQK = kChunksQK * kBoxBytes;
+  static constexpr int kTileV = kChunksV * kBoxBytes;
+  static constexpr int kKStages = DQK == 64 ? 3 : 2;
+  static constexpr int kVStages = DQK == 64 ? 3 : DQK == 128 ? 2 : 1;
   static constexpr int kOffQ = 0;                                   // Q_A, Q_B
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffK = kOffQ + 2 * kTileQK;
+  static constexpr int kOffV = kOffK + kKStages * kTileQK;
+  static constexpr int kOffBar = kOffV + kVStages * kTileV;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = kOffBar + kBarBytes + 1024;
   // explicit atten_mask: one 128-byte slot per softmax thread (256 rows),
   // 16-byte chunk q of row r at (q ^ (r & 7)) * 16 (no bank conflicts)
   static constexpr int kOffMask = kOffBar + kBarBytes;
   static constexpr int kSmemMask = kOffMask + 256 * 128 + 1024;
+  static constexpr bool kMaskFits = kSmemMask <= 227 * 1024;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;                            // O_A; O_B at kColO + D
-  static_assert(kSmemMask <= 227 * 1024, "shared memory budget");
+  static constexpr uint32_t kColO = 256;                            // O_A; O_B at kColO + DV
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kKStages <= 3 && kVStages <= 3, "barrier slots");
 };
 
 // Key tiles needed by the query rows [qa, qa + 128) of a batch.
@@ -63,28 +71,30 @@ __device__ __forceinline__ int tiles_for_rows(const BatchInfo& bi, int qa, int m
   return maxkey >= 0 ? maxkey / kTileN + 1 : 0;
 }
 
-template <int D, bool BF16, int MODE>
+template <int DQK, int DV, bool BF16, int MODE>
 __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_constant__ PrefillParams p) {
-  using C = PairCfg<D>;
-  constexpr int S = C::kStages;
+  using C = PairCfg<DQK, DV>;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;     // [S]
-  uint64_t* v_full = bars + 4;     // [S]
-  // kv_free[s]: P_B V of the tile in stage s is done (one commit per MMA
+  uint64_t* k_full = bars + 1;     // [KS]
+  uint64_t* v_full = bars + 4;     // [VS]
+  // v_free[s]: P_B V of the tile in V stage s is done (one commit per MMA
   // group): the stage is free, and O_B holds it.
-  uint64_t* kv_free = bars + 7;    // [S]
-  uint64_t* s_full = bars + 10;    // [2]: S_A, S_B of the next tile are in TMEM
-  uint64_t* pa_full = bars + 12;   // [2] by tile parity: warpgroup A's P is in (4 warp arrivals)
-  uint64_t* pb_full = bars + 14;   // [2]
+  uint64_t* v_free = bars + 7;     // [VS]
+  // s_full[3 t + s]: S_t of the tile in K stage s is in TMEM.  The last one of
+  // a tile (S_B, or S_A when the pair has no tile B) also frees the K stage.
+  uint64_t* s_full = bars + 10;    // [2][3]
+  uint64_t* pa_full = bars + 16;   // [2] by tile parity: warpgroup A's P is in (4 warp arrivals)
+  uint64_t* pb_full = bars + 18;   // [2]
   // pva_done: tile A's last P V is done (its epilogue may read O_A).  Earlier
   // P_A V products need no commit of their own: each is followed on the
   // tensor pipe by a Q K^T whose commit covers it.
-  uint64_t* pva_done = bars + 18;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+  uint64_t* pva_done = bars + 20;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[blockIdx.x];
@@ -118,13 +128,16 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
   if (threadIdx.x == 0) {
     if (blockIdx.x == 0) status_stamp(p.status);
     mbar_init(q_full, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_full[3 + s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_free[s], 1);
+      mbar_init(&v_free[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&s_full[t], 1);
       mbar_init(&pa_full[t], 4);
       mbar_init(&pb_full[t], 4);
     }
@@ -152,16 +165,28 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
+      // 64-column chunks of Q / K: the first 128 columns from tm_q / tm_k, a
+      // third (DQK = 192) from tm_qr / tm_kr at column rope_col (a separate
+      // rope tensor, or columns 128..191 of the same one)
+      auto qk_src = [&](int c, const CUtensorMap* m, const CUtensorMap* mr, int& col) -> const CUtensorMap* {
+        col = c < 2 ? c * 64 : p.rope_col;
+        return c < 2 ? m : mr;
+      };
+      mbar_arrive_expect_tx(q_full, 2 * C::kTileQK);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(smem + C::kOffQ + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c * 64,
-                      q_row0 + t * kTileM, it.h, b_coord);
-      int j = 0;
+        for (int c = 0; c < C::kChunksQK; ++c) {
+          int col;
+          const CUtensorMap* m = qk_src(c, &p.tm_q, &p.tm_qr, col);
+          tma_load_4d(smem + C::kOffQ + t * C::kTileQK + c * C::kBoxBytes, m, q_full, col, q_row0 + t * kTileM, it.h,
+                      b_coord);
+        }
+      // the Q K^T that frees a K stage: tile B's, or tile A's without a tile B
+      uint64_t* k_rel = s_full + (nb > 0 ? 3 : 0);
+      int j = 0, nk = 0, nv = 0;   // tiles loaded; K and V loads issued
       for (; j < nl; ++j) {
-        const int s = j % S;
+        const int sk = j % KS, sv = j % VS;
         // K/V tile coordinates: (row, batch) of a contiguous tensor, or (row in
         // block, block id) of a paged pool (the table read overlaps the wait)
         const int key = (jt0 + j) * kTileN;
@@ -170,24 +195,34 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
           kv_b = __ldg(p.block_table + int64_t(it.b) * p.table_stride + key / p.block_size);
           kv_r = key % p.block_size;
         }
-        if (j >= S && !mbar_wait(&kv_free[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
-        uint8_t* ks = smem + C::kOffK + s * C::kTileBytes;
-        uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
-        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+        if (j >= KS && !mbar_wait(&k_rel[sk], ((j / KS) - 1) & 1, abort_flag, p.status)) break;
+        uint8_t* ks = smem + C::kOffK + sk * C::kTileQK;
+        mbar_arrive_expect_tx(&k_full[sk], C::kTileQK);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(ks + c * C::kBoxBytes, &p.tm_k, &k_full[s], c * 64, kv_r, kvh, kv_b);
-        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunksQK; ++c) {
+          int col;
+          const CUtensorMap* m = qk_src(c, &p.tm_k, &p.tm_kr, col);
+          tma_load_4d(ks + c * C::kBoxBytes, m, &k_full[sk], col, kv_r, kvh, kv_b);
+        }
+        nk = j + 1;
+        if (j >= VS && !mbar_wait(&v_free[sv], ((j / VS) - 1) & 1, abort_flag, p.status)) break;
+        uint8_t* vs = smem + C::kOffV + sv * C::kTileV;
+        mbar_arrive_expect_tx(&v_full[sv], C::kTileV);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[s], c * 64, kv_r, kvh, kv_b);
+        for (int c = 0; c < C::kChunksV; ++c)
+          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[sv], c * 64, kv_r, kvh, kv_b);
+        nv = j + 1;
       }
       if (*abort_flag) {
+        // let every copy in flight land before the CTA exits
         mbar_wait(q_full, 0, nullptr, p.status);
-        for (int s = 0; s < S && s < j; ++s) {
-          const int last = j - 1 - ((j - 1 - s) % S);
-          mbar_wait(&k_full[s], (last / S) & 1, nullptr, p.status);
-          mbar_wait(&v_full[s], (last / S) & 1, nullptr, p.status);
+        for (int s = 0; s < KS && s < nk; ++s) {
+          const int last = nk - 1 - ((nk - 1 - s) % KS);
+          mbar_wait(&k_full[s], (last / KS) & 1, nullptr, p.status);
+        }
+        for (int s = 0; s < VS && s < nv; ++s) {
+          const int last = nv - 1 - ((nv - 1 - s) % VS);
+          mbar_wait(&v_full[s], (last / VS) & 1, nullptr, p.status);
         }
       }
     }
@@ -195,16 +230,16 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+      constexpr uint32_t idesc_pv = idesc_f16(128, DV, BF16 ? 1 : 0, 0, 1);
       // Descriptors of every operand buffer, built once; an MMA's K-slice
       // only moves the start address (bits 0..13, in 16-byte units), which
       // stays below 2^14 here, so a constant added to the whole descriptor
       // selects it.
       const uint64_t qd0 = smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
-      const uint64_t qd1 = smem_desc_sw128(smem_u32(smem + C::kOffQ + C::kTileBytes), 16, 1024);
+      const uint64_t qd1 = smem_desc_sw128(smem_u32(smem + C::kOffQ + C::kTileQK), 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
       const uint64_t vd0 = smem_desc_sw128(smem_u32(smem + C::kOffV), C::kBoxBytes, 1024);
-      constexpr uint64_t kStageStep = C::kTileBytes >> 4;
+      constexpr uint64_t kStepK = C::kTileQK >> 4, kStepV = C::kTileV >> 4;
       uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
       uint32_t last_parity = 0;
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
@@ -212,32 +247,32 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       // (tile A's, unless the tile is past tile A's range).
       // S_t = Q_t K(j)^T
       auto qk = [&](int t, int j) -> bool {
-        const int s = j % S;
-        if ((t == 0 || j >= na) && !mbar_wait(&k_full[s], (j / S) & 1, abort_flag, p.status)) return false;
+        const int s = j % KS;
+        if ((t == 0 || j >= na) && !mbar_wait(&k_full[s], (j / KS) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint64_t qd = t == 0 ? qd0 : qd1;
-        const uint64_t kd = kd0 + uint64_t(s) * kStageStep;
+        const uint64_t kd = kd0 + uint64_t(s) * kStepK;
         const uint32_t dst = tmem + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint64_t off = uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
           mma_ss(dst, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[t]);
-        last_bar = &s_full[t];
-        last_parity = j & 1;
+        mma_commit(&s_full[3 * t + s]);
+        last_bar = &s_full[3 * t + s];
+        last_parity = (j / KS) & 1;
         return true;
       };
       // O_t += P_t(j) V(j): P read from tile t's S columns in TMEM; V is
-      // [keys x D], an MN-major operand (16 keys = 2048 bytes per K-step, the
-      // next 64 columns of D one box further)
+      // [keys x DV], an MN-major operand (16 keys = 2048 bytes per K-step, the
+      // next 64 columns of DV one box further)
       auto pv = [&](int t, int j) -> bool {
-        const int s = j % S;
+        const int s = j % VS;
         if (!mbar_wait(t == 0 ? &pa_full[j & 1] : &pb_full[j & 1], (j >> 1) & 1, abort_flag, p.status)) return false;
-        if ((t == 0 || j >= na) && !mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status)) return false;
+        if ((t == 0 || j >= na) && !mbar_wait(&v_full[s], (j / VS) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint64_t vd = vd0 + uint64_t(s) * kStageStep;
-        const uint32_t dst = tmem + C::kColO + t * D;
+        const uint64_t vd = vd0 + uint64_t(s) * kStepV;
+        const uint32_t dst = tmem + C::kColO + t * DV;
         const uint32_t pt = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
@@ -249,9 +284,9 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
             last_parity = 0;
           }
         } else {
-          mma_commit(&kv_free[s]);
-          last_bar = &kv_free[s];
-          last_parity = (j / S) & 1;
+          mma_commit(&v_free[s]);
+          last_bar = &v_free[s];
+          last_parity = (j / VS) & 1;
         }
         return true;
       };
@@ -277,7 +312,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     const int r = 32 * (warp & 3) + lane;
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
     const uint32_t col_s = t * 128;
-    const uint32_t col_o = C::kColO + t * D;
+    const uint32_t col_o = C::kColO + t * DV;
     const int n = t == 0 ? na : nb;
     const int tile_q0 = q0 + t * kTileM;
     const int i = tile_q0 + r;
@@ -334,7 +369,10 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         // the slot is read (mb depends on every byte): refill it with the next tile
         if (j + 1 < n) mask_fetch(j + 1);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, p.status))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[3 * t + j % KS], (j / KS) & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // S in two halves: the second half's load is in flight while the
       // first half is masked and reduced.
@@ -427,7 +465,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       // read, was issued after that P V on the same tensor pipe.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
+        for (int c = 0; c < DV / 16; ++c) {
           uint32_t u[16];
           tmem_ld16(tmem + lane_off + col_o + c * 16, u);
           tmem_wait_ld(u);
@@ -440,12 +478,12 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       // there but 0 * NaN is not, so they are cleared before the first P V that
       // reads this tile: tile A's if it uses the tile, else tile B's.
       if (ragged && (t == 0 || j >= na)) {
-        const int s = j % S;
-        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / S) & 1, abort_flag, p.status))) { ok = false; break; }
+        const int s = j % VS;
+        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / VS) & 1, abort_flag, p.status))) { ok = false; break; }
         if (r >= bi.kv_len - kv0) {
-          uint8_t* vs = smem + C::kOffV + s * C::kTileBytes;
+          uint8_t* vs = smem + C::kOffV + s * C::kTileV;
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
+          for (int c = 0; c < C::kChunksV; ++c)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
@@ -463,7 +501,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       const int jl = n - 1;
       ok = __all_sync(0xffffffffu, (t == 0 && nb > 0)
                                        ? mbar_wait(pva_done, 0, abort_flag, p.status)
-                                       : mbar_wait(&kv_free[jl % S], (jl / S) & 1, abort_flag, p.status));
+                                       : mbar_wait(&v_free[jl % VS], (jl / VS) & 1, abort_flag, p.status));
       tc_fence_after();
     }
     if (ok) {
@@ -475,7 +513,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
                                                        : int64_t(it.b) * p.out_sb + int64_t(i) * p.out_ss) +
                 int64_t(it.h) * p.out_sn;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t u[32];
         if (n > 0) {
           tmem_ld32(tmem + lane_off + col_o + c * 32, u);
@@ -515,12 +553,13 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
   }
 }
 
-template <int D, bool BF16, int MODE>
+template <int DQK, int DV, bool BF16, int MODE>
 cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
-  using C = PairCfg<D>;
-  auto k = prefill_pair_kernel<D, BF16, MODE>;
+  using C = PairCfg<DQK, DV>;
+  static_assert(MODE != kMask || C::kMaskFits, "mask slots do not fit beside the rings");
+  auto k = prefill_pair_kernel<DQK, DV, BF16, MODE>;
   constexpr int smem = MODE == kMask ? C::kSmemMask : C::kSmem;
-  cudaError_t e = set_smem_once<prefill_pair_kernel<D, BF16, MODE>>(smem);
+  cudaError_t e = set_smem_once<prefill_pair_kernel<DQK, DV, BF16, MODE>>(smem);
   if (e != cudaSuccess) return e;
   k<<<p.n_items, C::kThreads, smem, s>>>(p);
   return cudaGetLastError();
@@ -528,23 +567,36 @@ cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s) {
+cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int head_dim_v, bool bf16, int mode,
+                                cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
-#define FIA_PAIR_MODES(DD, BB)                                          \
-  switch (mode) {                                                       \
-    case kDense: return launch_pair_one<DD, BB, kDense>(p, s);          \
-    case kCausal: return launch_pair_one<DD, BB, kCausal>(p, s);        \
-    case kBand: return launch_pair_one<DD, BB, kBand>(p, s);            \
-    case kMask: return launch_pair_one<DD, BB, kMask>(p, s);            \
-    default: return cudaErrorInvalidValue;                              \
+#define FIA_PAIR_MODES(DQ, DV, BB)                                          \
+  switch (mode) {                                                           \
+    case kDense: return launch_pair_one<DQ, DV, BB, kDense>(p, s);          \
+    case kCausal: return launch_pair_one<DQ, DV, BB, kCausal>(p, s);        \
+    case kBand: return launch_pair_one<DQ, DV, BB, kBand>(p, s);            \
+    case kMask: return launch_pair_one<DQ, DV, BB, kMask>(p, s);            \
+    default: return cudaErrorInvalidValue;                                  \
   }
-  if (head_dim == 128) {
-    if (bf16) { FIA_PAIR_MODES(128, true) } else { FIA_PAIR_MODES(128, false) }
+  // MLA prefill (192 / 128) has no room for the mask slots
+#define FIA_PAIR_MODES_NOMASK(DQ, DV, BB)                                   \
+  switch (mode) {                                                           \
+    case kDense: return launch_pair_one<DQ, DV, BB, kDense>(p, s);          \
+    case kCausal: return launch_pair_one<DQ, DV, BB, kCausal>(p, s);        \
+    case kBand: return launch_pair_one<DQ, DV, BB, kBand>(p, s);            \
+    default: return cudaErrorInvalidValue;                                  \
   }
-  if (head_dim == 64) {
-    if (bf16) { FIA_PAIR_MODES(64, true) } else { FIA_PAIR_MODES(64, false) }
+  if (head_dim_qk == 128 && head_dim_v == 128) {
+    if (bf16) { FIA_PAIR_MODES(128, 128, true) } else { FIA_PAIR_MODES(128, 128, false) }
+  }
+  if (head_dim_qk == 64 && head_dim_v == 64) {
+    if (bf16) { FIA_PAIR_MODES(64, 64, true) } else { FIA_PAIR_MODES(64, 64, false) }
+  }
+  if (head_dim_qk == 192 && head_dim_v == 128) {
+    if (bf16) { FIA_PAIR_MODES_NOMASK(192, 128, true) } else { FIA_PAIR_MODES_NOMASK(192, 128, false) }
   }
 #undef FIA_PAIR_MODES
+#undef FIA_PAIR_MODES_NOMASK
   return cudaErrorInvalidValue;
 }
 

@@ -10,7 +10,8 @@ second (the K and V rows of every sequence, sum(L_b) * KV_N * D * 2 bytes * 2).
 
 The other hot-path workloads are measured in the same run under "sections":
 varlen TND causal prefill (TFLOP/s), the same with a 1024-key sliding window
-(sparse_mode 4), chunked prefill against a paged cache (TFLOP/s), block-sparse
+(sparse_mode 4), chunked prefill against a paged cache (TFLOP/s), MLA prefill
+(192 / 128, TFLOP/s), block-sparse
 prefill (TFLOP/s), MLA decode
 (cache GB/s), the headline decode with 4 new tokens per sequence (KV GB/s) and
 the small fp16 prefill.  Inputs are seeded synthetic tensors
@@ -321,6 +322,37 @@ def measure_chunked_prefill(torch, dev, timer, steps, warmup, pk, traffic):
                                  traffic.get("prefill_pair_kernel_chunked"))}
 
 
+def measure_mla_prefill(torch, dev, timer, steps, warmup, pk, traffic):
+    """MLA prefill, TND: the varlen prefill lengths, 32 heads, query/key D 192
+    (128 + 64 rope columns), value D 128, right-down causal."""
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    c = fia_inputs.workload_mla_prefill()
+    starts = [0] + c.actual_seq_qlen[:-1]
+    lens = [e - s0 for s0, e in zip(starts, c.actual_seq_qlen)]
+    flops = sum(L * (L + 1) // 2 for L in lens) * c.num_heads * 2 * (192 + 128)
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    out = torch.empty((q.shape[0], c.num_heads, 128), dtype=q.dtype, device=dev)
+    lse = torch.empty((q.shape[0], c.num_heads, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        fia.fia_prefill_mla(q, k, v, num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                            scale_value=c.scale, input_layout="TND", sparse_mode=3,
+                            actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
+                            softmax_lse_flag=True, out=out, softmax_lse=lse, workspace=ws)
+
+    call_ms, kern_ms = timer.run(call, steps, warmup, kernel_events=True)
+    km = statistics.mean(kern_ms)
+    return {"workload": "MLA prefill bf16, TND, 8 seqs U[256,4096], 32 heads, query/key D 192 (128 + 64 rope), "
+                        "value D 128, causal, LSE",
+            "metric": "prefill attention TFLOP/s", "unit": "TFLOP/s",
+            "value": round(flops / (statistics.mean(call_ms) * 1e-3) / 1e12, 2), "ms_per_call": statistics.mean(call_ms),
+            "kernel_ms": km, "flops": flops,
+            "roofline": roofline("tensor", flops / (km * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s",
+                                 traffic.get("prefill_pair_kernel_mla"))}
+
+
 def measure_bsa(torch, dev, timer, steps, warmup, pk, traffic):
     import attention_fia_prefill_gb300 as fia
     import fia_inputs
@@ -463,7 +495,7 @@ def run_ours(args):
     sections = {}
     if not args.headline_only:
         for name, fn in (("prefill_tnd", measure_prefill_tnd), ("prefill_band", measure_prefill_band),
-                         ("chunked_prefill", measure_chunked_prefill),
+                         ("chunked_prefill", measure_chunked_prefill), ("mla_prefill", measure_mla_prefill),
                          ("bsa", measure_bsa), ("mla_decode", measure_mla), ("decode_q4", measure_decode_tokens)):
             try:
                 sections[name] = fn(torch, dev, timer, args.steps, args.warmup, pk, traffic)

@@ -212,6 +212,54 @@ def workload_paged_gqa_decode(B=16, N1=32, N2=8, D=128, max_len=4096, workload=2
 
 
 # --------------------------------------------------------------------------------------
+# MLA prefill (scores over 192 columns, value 128)
+# --------------------------------------------------------------------------------------
+@dataclass
+class MLAPrefillCase:
+    q: torch.Tensor                   # (.., 192), or (.., 128) with q_rope (.., 64)
+    k: torch.Tensor
+    v: torch.Tensor                   # (.., 128)
+    q_rope: torch.Tensor | None
+    k_rope: torch.Tensor | None
+    num_heads: int
+    num_key_value_heads: int
+    scale: float
+    layout: str
+    actual_seq_qlen: list | None = None
+    actual_seq_kvlen: list | None = None
+
+
+def mla_prefill_case(lens_q, lens_kv, N1, N2, rope=True, dtype="bf16", layout="TND", workload=800) -> MLAPrefillCase:
+    """MLA prefill inputs: with rope, q/k of D 128 plus q_rope/k_rope of D 64,
+    else q/k of D 192; v of D 128; scale 1/sqrt(192).  TND takes cumulative
+    lists; the padded layouts take B = len(lens_q) and S = max length."""
+    dq = 128 if rope else 192
+
+    def shaped(n_heads, d, lens, tensor):
+        if layout == "TND":
+            return normal((sum(lens), n_heads, d), dtype, workload, tensor)
+        B, S = len(lens), max(lens) if lens else 0
+        shape = {"BNSD": (B, n_heads, S, d), "BSND": (B, S, n_heads, d), "BSH": (B, S, n_heads * d)}[layout]
+        return normal(shape, dtype, workload, tensor)
+
+    q, k, v = shaped(N1, dq, lens_q, 1), shaped(N2, dq, lens_kv, 2), shaped(N2, 128, lens_kv, 3)
+    qr = shaped(N1, 64, lens_q, 4) if rope else None
+    kr = shaped(N2, 64, lens_kv, 5) if rope else None
+    if layout == "TND":
+        aq, ak = cumsum_no_leading_zero(lens_q), cumsum_no_leading_zero(lens_kv)
+    else:
+        aq, ak = list(lens_q), list(lens_kv)
+    return MLAPrefillCase(q, k, v, qr, kr, N1, N2, 1.0 / math.sqrt(192), layout, aq, ak)
+
+
+def workload_mla_prefill(n_seq=8, lo=256, hi=4096, N=32, workload=3) -> MLAPrefillCase:
+    """MLA prefill bf16, TND: the varlen prefill lengths, 32 heads (MHA), query
+    and key D 192 (128 + 64 rope columns), value D 128, causal."""
+    lens = uniform_ints(lo, hi, n_seq, workload, 0)
+    return mla_prefill_case(lens, lens, N, N, rope=False, dtype="bf16", layout="TND", workload=810)
+
+
+# --------------------------------------------------------------------------------------
 # Prefill against a paged cache (chunked prefill)
 # --------------------------------------------------------------------------------------
 @dataclass

@@ -147,6 +147,29 @@ FIA_API fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, c
                        const fia_tensor* softmax_lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * fia_prefill_mla: MLA prefill (npu_fused_infer_attention_score_v2, query D
+ * not 512: "query, key, value D 128 with query_rope / key_rope D 64", or
+ * "query, key D 192, value D 128").  The score of a pair is
+ * scale_value * (q . k + q_rope . k_rope), the product over the 192-column
+ * concatenation; value and attention_out have D 128.
+ *   query / key: D 192 with query_rope = key_rope = NULL, or D 128 with both
+ *          rope tensors given (the query's / key's shape with D 64, same type).
+ *   value: key's shape with D 128.  attention_out: query's shape with D 128.
+ *   Layouts BSH/BSND/BNSD/TND (the pages list TND), f16 or bf16, GQA allowed.
+ *   sparse_mode 0, 2, 3, 4 as fia_prefill; an explicit atten_mask (mode 0 with
+ *   a mask, 1) returns FIA_ERR_UNSUPPORTED.  softmax_lse as fia_prefill.
+ * ------------------------------------------------------------------------ */
+FIA_API fia_status fia_prefill_mla_get_workspace_size(const fia_tensor* query, const fia_tensor* key,
+                                              const fia_tensor* value, const fia_tensor* query_rope,
+                                              const fia_tensor* key_rope, const fia_tensor* atten_mask,
+                                              const fia_params* params, const fia_tensor* attention_out,
+                                              const fia_tensor* softmax_lse, size_t* workspace_bytes);
+FIA_API fia_status fia_prefill_mla(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                           const fia_tensor* query_rope, const fia_tensor* key_rope, const fia_tensor* atten_mask,
+                           const fia_params* params, const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * fia_prefill_paged: fia_prefill with key/value in a paged cache (chunked
  * prefill: a chunk of new query tokens against a sequence's cached keys).
  *   npu_fused_infer_attention_score_v2, page attention: key j of batch b is

@@ -172,6 +172,30 @@ def test_paged_prefill_rules(lib):
     assert ws(qt, kp, t((3, 3), B.DTYPE_I32), layout="TND", ql=[300, 800]) == 7
 
 
+def test_mla_prefill_rules(lib):
+    """MLA prefill: query/key D 192 without rope tensors, or D 128 with both
+    (D 64); value and output D 128; no explicit mask."""
+    def ws(q, k, v, out, qr=None, kr=None, mask=None, mode=3):
+        prm = params(lib, num_heads=4, num_key_value_heads=2, input_layout="TND", sparse_mode=mode,
+                     actual_seq_qlen=[100, 300], actual_seq_kvlen=[100, 300])
+        w = ctypes.c_size_t(0)
+        ref = lambda d: ctypes.byref(d) if d is not None else None
+        return lib.fia_prefill_mla_get_workspace_size(ref(q), ref(k), ref(v), ref(qr), ref(kr), ref(mask),
+                                                      ctypes.byref(prm.p), ref(out), None, ctypes.byref(w))
+
+    q192, k192, v, out = t((300, 4, 192)), t((300, 2, 192)), t((300, 2, 128)), t((300, 4, 128))
+    q128, k128, qr, kr = t((300, 4, 128)), t((300, 2, 128)), t((300, 4, 64)), t((300, 2, 64))
+    assert ws(q192, k192, v, out) == 0
+    assert ws(q128, k128, v, out, qr, kr) == 0
+    assert ws(q128, k128, v, out) == 5                           # D 128 needs the rope tensors
+    assert ws(q192, k192, v, out, qr, kr) == 5                   # D 192 takes none
+    assert ws(q128, k128, v, out, qr, None) == 3                 # both or neither
+    assert ws(q192, k192, t((300, 2, 192)), out) == 5            # value D 128 only
+    assert ws(q192, k192, v, t((300, 4, 192))) == 3              # output has value's D
+    assert ws(q128, k128, v, out, t((300, 4, 32)), kr) == 3      # rope D 64
+    assert ws(q192, k192, v, out, mask=t((300, 300), B.DTYPE_U8), mode=1) == 5
+
+
 def test_shape_dtype_layout_errors(lib):
     q, k = t((1, 2, 8, 64)), t((1, 2, 9, 64))
     assert prefill_ws(lib, q, k, q, params(lib, num_heads=2, input_layout="BNSD"))[0] == 3      # k != v
