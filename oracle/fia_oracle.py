@@ -447,17 +447,40 @@ def _mask_for_batch_decode(mask, b: int):
 # ---------------------------------------------------------------------------
 def bsa_forward(q, k, v, block_sparse_mask, block_shape, *, num_heads: int, num_key_value_heads: int = 0,
                 scale_value: float = 1.0, input_layout: str = "BNSD",
-                actual_seq_qlen=None, actual_seq_kvlen=None, rows=None):
+                actual_seq_qlen=None, actual_seq_kvlen=None, rows=None,
+                q_dequant_scale=None, k_dequant_scale=None, v_dequant_scale=None):
+    """Block-sparse attention (aclnnBlockSparseAttentionV2, "计算公式").
+
+    FP8 inputs ("FP8特性说明"): q / k / v hold float8_e4m3fn values and the
+    dequant scales say what each block of rows is worth: row i of query head h
+    of batch b is q[i] * q_dequant_scale[b, h, i // X, 0], key / value row j
+    of kv head n is k[j] * k_dequant_scale[b, n, j // Y, 0] (and v with
+    v_dequant_scale), X / Y = block_shape (the pages tie the quantisation
+    blocks to block_shape: 128 query rows, 256 or 512 key rows).  Attention
+    then runs on the dequantised values."""
     X, Y = int(block_shape[0]), int(block_shape[1])
     M = np.asarray(block_sparse_mask.cpu().numpy() if hasattr(block_sparse_mask, "cpu") else block_sparse_mask)
     N1 = int(num_heads)
     N2 = int(num_key_value_heads) or N1
     g = N1 // N2
     Q, K, V = f64(q), f64(k), f64(v)
+    scales = (q_dequant_scale, k_dequant_scale, v_dequant_scale)
+    if any(x is not None for x in scales) and any(x is None for x in scales):
+        raise ValueError("FP8 needs all three dequant scales")
+    fp8 = q_dequant_scale is not None
+    if fp8:
+        QSC, KSC, VSC = (f64(x)[..., 0] for x in scales)   # (B, heads, blocks)
     if input_layout == "TND":
         qs, ql = tnd_lengths(actual_seq_qlen)
         ks, kl = tnd_lengths(actual_seq_kvlen)
         B = len(ql)
+        if fp8:
+            # step 0: dequantise every row by its block's scale
+            for b in range(B):
+                iq, jk = np.arange(ql[b]) // X, np.arange(kl[b]) // Y
+                Q[qs[b]:qs[b] + ql[b]] *= QSC[b][:, iq].T[:, :, None]
+                K[ks[b]:ks[b] + kl[b]] *= KSC[b][:, jk].T[:, :, None]
+                V[ks[b]:ks[b] + kl[b]] *= VSC[b][:, jk].T[:, :, None]
 
         def qrows(b, h): return Q[qs[b]:qs[b] + ql[b], h, :]
         def krows(b, h): return K[ks[b]:ks[b] + kl[b], h // g, :]
@@ -467,6 +490,13 @@ def bsa_forward(q, k, v, block_sparse_mask, block_shape, *, num_heads: int, num_
         B = Qb.shape[0]
         ql = resolve_lengths(actual_seq_qlen, B, Qb.shape[2])
         kl = resolve_lengths(actual_seq_kvlen, B, Kb.shape[2])
+        if fp8:
+            # step 0: dequantise every row by its block's scale (views of Q / K / V)
+            for b in range(B):
+                iq, jk = np.arange(ql[b]) // X, np.arange(kl[b]) // Y
+                Qb[b, :, :ql[b]] *= QSC[b][:, iq][:, :, None]
+                Kb[b, :, :kl[b]] *= KSC[b][:, jk][:, :, None]
+                Vb[b, :, :kl[b]] *= VSC[b][:, jk][:, :, None]
 
         def qrows(b, h): return Qb[b, h, :ql[b], :]
         def krows(b, h): return Kb[b, h // g, :kl[b], :]

@@ -398,6 +398,56 @@ def check_bsa(orc):
         assert np.allclose(o1[:, h:h + 1], o2, atol=ATOL) and np.allclose(l1[:, h:h + 1], l2), "BSA != expanded mask"
 
 
+def check_bsa_fp8_dequant(orc):
+    """FP8 block-sparse attention: dequant scales per block of X query rows and
+    Y key / value rows.  (a) A query block whose scale is 0 has all scores 0:
+    each of its rows is the plain mean of the dequantised value rows it may see
+    (closed form), and the rows of the other query block do not change.
+    (b) Output is linear in the value scales.  (c) Only the product of query
+    and key scales enters the scores.  (d) With unit scales the result is the
+    bf16 path's on the same values (e4m3 values are exact in bf16)."""
+    B, N1, N2, S, D, X, Y = 1, 2, 1, 10, 4, 4, 6
+    g = torch.Generator().manual_seed(150)
+    f8 = lambda shape: (torch.randn(shape, generator=g, dtype=torch.float64) * 4).clamp(-448, 448).to(
+        torch.float8_e4m3fn)
+    q, k, v = f8((B, N1, S, D)), f8((B, N2, S, D)), f8((B, N2, S, D))
+    nq, nk = -(-S // X), -(-S // Y)
+    m = np.ones((B, N1, nq, nk), np.uint8)
+    m[0, 1, 1, 1] = 0
+    pos = lambda shape, seed: torch.rand(shape, generator=torch.Generator().manual_seed(seed),
+                                         dtype=torch.float64) + 0.5
+    qs, ks, vs = pos((B, N1, nq, 1), 151).float(), pos((B, N2, nk, 1), 152).float(), pos((B, N2, nk, 1), 153).float()
+    run = lambda a, b, c: orc.bsa_forward(q, k, v, m, (X, Y), num_heads=N1, num_key_value_heads=N2, scale_value=0.3,
+                                          q_dequant_scale=a, k_dequant_scale=b, v_dequant_scale=c)
+    o, l = run(qs, ks, vs)
+    qz = qs.clone()
+    qz[0, :, 0] = 0
+    oz, lz = run(qz, ks, vs)
+    vdq = v.to(torch.float64).numpy()[0, 0] * np.repeat(vs.numpy()[0, 0, :, 0], Y)[:S, None]
+    for h in range(N1):
+        for i in range(X):
+            keep = np.repeat(m[0, h, i // X], Y)[:S] != 0
+            assert np.allclose(oz[0, h, i], vdq[keep].mean(axis=0), atol=1e-9), "zero query scale -> mean of V"
+            assert abs(lz[0, h, i, 0] - math.log(keep.sum())) < 1e-9, "zero query scale -> lse = ln(count)"
+    assert np.array_equal(oz[:, :, X:], o[:, :, X:]), "a query block's scale leaks into another block"
+    o2, _ = run(qs, ks, vs * 2)
+    assert np.allclose(o2, 2 * o, atol=1e-9), "output linear in the value scales"
+    o3, l3 = run(qs * 4, ks / 4, vs)
+    assert np.allclose(o3, o, atol=1e-9) and np.allclose(l3, l, atol=1e-9), "only q scale x k scale matters"
+    ones_q, ones_k = torch.ones_like(qs), torch.ones_like(ks)
+    o4, l4 = run(ones_q, ones_k, ones_k)
+    o5, l5 = orc.bsa_forward(q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), m, (X, Y),
+                             num_heads=N1, num_key_value_heads=N2, scale_value=0.3)
+    assert np.array_equal(o4, o5) and np.array_equal(l4, l5), "unit scales != bf16 path"
+    # TND: the same single sequence packed as (T, N, D) dequantises the same way
+    tnd = lambda x: x[0].transpose(0, 1).contiguous()
+    o6, l6 = orc.bsa_forward(tnd(q), tnd(k), tnd(v), m, (X, Y), num_heads=N1, num_key_value_heads=N2,
+                             scale_value=0.3, input_layout="TND", actual_seq_qlen=[S], actual_seq_kvlen=[S],
+                             q_dequant_scale=qs, k_dequant_scale=ks, v_dequant_scale=vs)
+    assert np.allclose(o6, o[0].transpose(1, 0, 2), atol=1e-12) and np.allclose(l6[:, :, 0], l[0, :, :, 0].T), \
+        "FP8 TND != BNSD"
+
+
 def check_lse_merge(orc):
     """Split the keys in two, attend to each half, merge by LSE: equals unsplit."""
     q, k, v = _rand((6, 4), 100).numpy(), _rand((10, 4), 101).numpy(), _rand((10, 3), 102).numpy()
@@ -427,6 +477,6 @@ ALL_CHECKS = [
     check_tnd_equals_per_sequence, check_actual_lengths_equal_truncation, check_paged_equals_contiguous,
     check_decode_equals_prefill_row, check_multitoken_decode_vs_library, check_paged_prefill_equals_contiguous,
     check_mla_prefill_vs_library, check_mla_equals_concatenated_attention,
-    check_bsa, check_lse_merge,
+    check_bsa, check_bsa_fp8_dequant, check_lse_merge,
     check_empty_rules,
 ]

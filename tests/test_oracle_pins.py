@@ -52,6 +52,13 @@ MUTATIONS = [
      "            K = np.concatenate([K, 0 * f64(key_rope)], axis=-1)", "MLA prefill rope term dropped"),
     ("            Q = np.concatenate([Q, f64(query_rope)], axis=-1)",
      "            Q = np.concatenate([f64(query_rope), Q], axis=-1)", "MLA prefill rope on the wrong side"),
+    ("                iq, jk = np.arange(ql[b]) // X, np.arange(kl[b]) // Y\n                Qb[",
+     "                iq, jk = np.arange(ql[b]) // Y, np.arange(kl[b]) // Y\n                Qb[",
+     "FP8 query blocks sized like key blocks"),
+    ("                Vb[b, :, :kl[b]] *= VSC[b][:, jk][:, :, None]", "                pass",
+     "FP8 value scales dropped"),
+    ("                K[ks[b]:ks[b] + kl[b]] *= KSC[b][:, jk].T[:, :, None]", "                pass",
+     "FP8 TND key scales dropped"),
 ]
 
 
