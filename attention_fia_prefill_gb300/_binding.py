@@ -21,13 +21,14 @@ STATUS_NAMES = {
     9: "FIA_ERR_CUDA", 10: "FIA_ERR_TIMEOUT", 11: "FIA_ERR_HEADS", 12: "FIA_ERR_SPARSE_MODE",
     13: "FIA_ERR_ALIGNMENT",
 }
-DTYPE_F16, DTYPE_BF16, DTYPE_F32, DTYPE_I32, DTYPE_I64, DTYPE_U8, DTYPE_BOOL, DTYPE_I8 = range(8)
+DTYPE_F16, DTYPE_BF16, DTYPE_F32, DTYPE_I32, DTYPE_I64, DTYPE_U8, DTYPE_BOOL, DTYPE_I8, DTYPE_F8E4M3 = range(9)
 
 # Every symbol include/fia.h declares.
 EXPORTS = [
     "fia_params_init", "fia_prefill_get_workspace_size", "fia_prefill", "fia_prefill_mla_get_workspace_size",
     "fia_prefill_mla", "fia_prefill_paged_get_workspace_size", "fia_prefill_paged", "fia_decode_get_workspace_size",
-    "fia_decode", "bsa_get_workspace_size", "bsa_forward", "fia_device_status", "fia_status_string",
+    "fia_decode", "bsa_get_workspace_size", "bsa_forward", "bsa_fp8_get_workspace_size", "bsa_forward_fp8",
+    "fia_device_status", "fia_status_string",
     "fia_last_error", "fia_profile_next_call", "fia_decode_no_alloc",
 ]
 
@@ -93,6 +94,11 @@ def load_library(path: str | None = None):
     lib.bsa_get_workspace_size.restype = st
     lib.bsa_forward.argtypes = [T, T, T, T, ctypes.POINTER(ctypes.c_int64), P, T, T, vp, ctypes.c_size_t, vp]
     lib.bsa_forward.restype = st
+    lib.bsa_fp8_get_workspace_size.argtypes = [T, T, T, T, ctypes.POINTER(ctypes.c_int64), T, T, T, P, T, T, sz]
+    lib.bsa_fp8_get_workspace_size.restype = st
+    lib.bsa_forward_fp8.argtypes = [T, T, T, T, ctypes.POINTER(ctypes.c_int64), T, T, T, P, T, T, vp,
+                                    ctypes.c_size_t, vp]
+    lib.bsa_forward_fp8.restype = st
     lib.fia_device_status.argtypes = [vp, vp]
     lib.fia_device_status.restype = st
     lib.fia_status_string.argtypes = [st]
@@ -112,7 +118,8 @@ def load_library(path: str | None = None):
 def _dtype_code(t) -> int:
     import torch
     m = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.int32: DTYPE_I32,
-         torch.int64: DTYPE_I64, torch.uint8: DTYPE_U8, torch.bool: DTYPE_BOOL, torch.int8: DTYPE_I8}
+         torch.int64: DTYPE_I64, torch.uint8: DTYPE_U8, torch.bool: DTYPE_BOOL, torch.int8: DTYPE_I8,
+         torch.float8_e4m3fn: DTYPE_F8E4M3}
     if t.dtype not in m:
         raise TypeError(f"unsupported dtype {t.dtype}")
     return m[t.dtype]
@@ -352,28 +359,42 @@ def fia_decode_no_alloc(query, key, value, *, out, softmax_lse=None, query_rope=
 
 def bsa_forward(query, key, value, block_sparse_mask, block_shape, *, actual_seq_qlen=None, actual_seq_kvlen=None,
                 num_heads=1, num_key_value_heads=0, scale_value=1.0, input_layout="BNSD", softmax_lse_flag=False,
-                out=None, softmax_lse=None, workspace=None):
-    """Block-sparse attention: each query block attends to the KV blocks its mask row keeps."""
+                out=None, softmax_lse=None, workspace=None, q_dequant_scale=None, k_dequant_scale=None,
+                v_dequant_scale=None):
+    """Block-sparse attention: each query block attends to the KV blocks its mask row keeps.
+    With float8 e4m3 query/key/value pass the three fp32 dequant scales (FP8
+    path, bf16 output)."""
     import torch
-    _require_cuda(query, key, value, block_sparse_mask)
+    fp8 = q_dequant_scale is not None or k_dequant_scale is not None or v_dequant_scale is not None
+    _require_cuda(query, key, value, block_sparse_mask, q_dequant_scale, k_dequant_scale, v_dequant_scale)
     lib = load_library()
     prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
                  input_layout=input_layout, actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen,
                  softmax_lse_flag=softmax_lse_flag)
     if out is None:
-        out = torch.empty_like(query)
+        out = torch.empty(query.shape, dtype=torch.bfloat16 if fp8 else query.dtype, device=query.device)
     if softmax_lse_flag and softmax_lse is None:
         softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
     shape = (ctypes.c_int64 * 2)(int(block_shape[0]), int(block_shape[1]))
     dq, dk, dv, dmask, do, dl = (tensor_desc(t) for t in (query, key, value, block_sparse_mask, out, softmax_lse))
     ws = ctypes.c_size_t(0)
-    check(lib.bsa_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do),
-                                     _ref(dl), ctypes.byref(ws)))
+    if fp8:
+        dsq, dsk, dsv = (_ref(tensor_desc(t)) for t in (q_dequant_scale, k_dequant_scale, v_dequant_scale))
+        check(lib.bsa_fp8_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, dsq, dsk, dsv,
+                                             ctypes.byref(prm.p), _ref(do), _ref(dl), ctypes.byref(ws)))
+    else:
+        check(lib.bsa_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p),
+                                         _ref(do), _ref(dl), ctypes.byref(ws)))
     if workspace is None or workspace.numel() < ws.value:
         workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
-    check(lib.bsa_forward(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do), _ref(dl),
-                          ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
-                          _stream_ptr(query.device)))
+    if fp8:
+        check(lib.bsa_forward_fp8(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, dsq, dsk, dsv,
+                                  ctypes.byref(prm.p), _ref(do), _ref(dl), ctypes.c_void_p(workspace.data_ptr()),
+                                  ctypes.c_size_t(workspace.numel()), _stream_ptr(query.device)))
+    else:
+        check(lib.bsa_forward(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do),
+                              _ref(dl), ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
+                              _stream_ptr(query.device)))
     return out, softmax_lse
 
 

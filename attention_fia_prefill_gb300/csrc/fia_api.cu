@@ -114,19 +114,21 @@ EncodeTiledFn encode_fn() {
 }
 
 // rank-d tiled map of 16-bit elements, 128-byte swizzle, box {64, box_rows, 1, ...}
+// Boxes of 128 bytes x box_rows: 64 16-bit elements, or 128 8-bit ones (u8).
 fia_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                    uint32_t box_rows) {
+                    uint32_t box_rows, bool u8 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(FIA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (no CUDA driver?)");
   cuuint64_t gd[5], gs[4];
   cuuint32_t box[5], es[5];
   for (int i = 0; i < rank; ++i) {
     gd[i] = dims[i];
-    box[i] = i == 0 ? 64 : (i == 1 ? box_rows : 1);
+    box[i] = i == 0 ? (u8 ? 128 : 64) : (i == 1 ? box_rows : 1);
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, rank, const_cast<void*>(base), gd, gs, box, es,
+  CUresult r = fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, rank,
+                  const_cast<void*>(base), gd, gs, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FIA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
@@ -211,6 +213,11 @@ struct Geometry {
   // prefill: 192 / 128, with the rope columns from qr / kr when given)
   int64_t Dqk = 0, Dv = 0;
   bool mla = false;
+  bool fp8 = false;   // FP8 block-sparse: e4m3 query / key / value, bf16 output
+  const float* fp8_q = nullptr;
+  const float* fp8_k = nullptr;
+  const float* fp8_v = nullptr;
+  int fp8_nqs = 0, fp8_nks = 0;
   const fia_tensor* qr = nullptr;
   const fia_tensor* kr = nullptr;
   // paged K/V (chunked prefill): pools (blocknum, KV_N, bs, D) or (blocknum, bs, KV_N*D)
@@ -313,7 +320,8 @@ fia_status paged_pools(const fia_tensor* k, const fia_tensor* v, const fia_tenso
 // plus query_rope / key_rope of D 64.
 fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_tensor* v, const fia_params* p,
                             const fia_tensor* out, bool bsa, Geometry& g, const fia_tensor* table = nullptr,
-                            bool mla = false, const fia_tensor* qr = nullptr, const fia_tensor* kr = nullptr) {
+                            bool mla = false, const fia_tensor* qr = nullptr, const fia_tensor* kr = nullptr,
+                            bool fp8 = false) {
   if (p != nullptr) {
     const int64_t lim = int64_t(1) << 30;
     g.band_pre = int(std::max(-lim, std::min(lim, p->pre_tokens)));
@@ -325,9 +333,16 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
   g.layout = parse_layout(p->input_layout);
   if (g.layout == L_BAD) return fail(FIA_ERR_LAYOUT, "input_layout '%s' not supported", p->input_layout);
   if (bsa && g.layout == L_BSH) return fail(FIA_ERR_LAYOUT, "block-sparse attention takes TND, BNSD or BSND");
-  if (!is_half(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype)
-    return fail(FIA_ERR_DTYPE, "query/key/value must share fp16 or bf16");
-  if (out->dtype != q->dtype) return fail(FIA_ERR_DTYPE, "attention_out must have the query's dtype");
+  if (fp8) {
+    if (q->dtype != FIA_DTYPE_F8E4M3 || k->dtype != q->dtype || v->dtype != q->dtype)
+      return fail(FIA_ERR_DTYPE, "FP8 attention takes float8 e4m3 query, key and value");
+    if (out->dtype != FIA_DTYPE_BF16) return fail(FIA_ERR_DTYPE, "FP8 attention writes a bf16 attention_out");
+  } else {
+    if (!is_half(q->dtype) || k->dtype != q->dtype || v->dtype != q->dtype)
+      return fail(FIA_ERR_DTYPE, "query/key/value must share fp16 or bf16");
+    if (out->dtype != q->dtype) return fail(FIA_ERR_DTYPE, "attention_out must have the query's dtype");
+  }
+  g.fp8 = fp8;
   fia_status st = resolve_heads(p, g.N1, g.N2);
   if (st != FIA_OK) return st;
   if (!mla && !same_shape(k, v)) return fail(FIA_ERR_SHAPE, "key and value shapes differ");
@@ -379,10 +394,11 @@ fia_status prefill_geometry(const fia_tensor* q, const fia_tensor* k, const fia_
   } else if (g.D != 64 && g.D != 128) {
     return fail(FIA_ERR_UNSUPPORTED, "head dim %lld (kernels take 64 or 128)", (long long)g.D);
   }
+  if (fp8 && g.D != 128) return fail(FIA_ERR_UNSUPPORTED, "FP8 attention takes D 128 (got %lld)", (long long)g.D);
   if (!(p->scale_value > 0.0) || !std::isfinite(p->scale_value))
     return fail(FIA_ERR_UNSUPPORTED, "scale_value must be finite and > 0");
   if (p->inner_precise < 0 || p->inner_precise > 4) return fail(FIA_ERR_UNSUPPORTED, "inner_precise %d", p->inner_precise);
-  g.bf16 = q->dtype == FIA_DTYPE_BF16;
+  g.bf16 = q->dtype == FIA_DTYPE_BF16 || fp8;
   if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(v->data) || !aligned16(out->data))
     return fail(FIA_ERR_ALIGNMENT, "query/key/value/attention_out must be 16-byte aligned");
   if (g.layout == L_TND) {
@@ -503,9 +519,10 @@ fia_status check_ws(void* ws, size_t have, size_t need) {
 }
 
 // Encode the (D, S, N, B) maps of a dense tensor (TND: (D, T, N, 1)).
-fia_status dense_map(CUtensorMap* m, const fia_tensor* t, Layout L, int64_t B, int64_t N, int64_t S, int64_t D) {
+fia_status dense_map(CUtensorMap* m, const fia_tensor* t, Layout L, int64_t B, int64_t N, int64_t S, int64_t D,
+                     bool u8 = false) {
   uint64_t dims[4], st[3];
-  const uint64_t e = 2;
+  const uint64_t e = u8 ? 1 : 2;
   if (L == L_BNSD) {
     dims[0] = D; dims[1] = S; dims[2] = N; dims[3] = B;
     st[0] = D * e; st[1] = S * D * e; st[2] = N * S * D * e;
@@ -516,7 +533,7 @@ fia_status dense_map(CUtensorMap* m, const fia_tensor* t, Layout L, int64_t B, i
     dims[0] = D; dims[1] = S; dims[2] = N; dims[3] = B;
     st[0] = N * D * e; st[1] = D * e; st[2] = S * N * D * e;
   }
-  return make_map(m, t->data, 4, dims, st, 128);
+  return make_map(m, t->data, 4, dims, st, 128, u8);
 }
 
 // Launch the prefill (dense/causal) or block-sparse kernels for a validated geometry.
@@ -526,7 +543,9 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
                        cudaStream_t stream) {
   std::vector<WorkItem> items;
   build_items(g, mode, causal_mode, items);
-  const size_t need = prefill_ws_bytes(g.batches.size(), items.size());
+  const size_t plan_bytes = prefill_ws_bytes(g.batches.size(), items.size());
+  // FP8: the value tensor converted to f16 once per call, after the plan
+  const size_t need = plan_bytes + (g.fp8 ? align_up(size_t(numel(v)) * 2, 256) : 0);
   fia_status st = check_ws(ws, ws_bytes, need);
   if (st != FIA_OK) return st;
   float* lse = (prm->softmax_lse_flag && present(lse_t)) ? static_cast<float*>(lse_t->data) : nullptr;
@@ -539,7 +558,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   else { ls[0] = g.N1 * g.S1; ls[1] = g.S1; ls[2] = 1; }
 
   // upload the plan
-  std::vector<uint8_t> plan(need - kHeader, 0);
+  std::vector<uint8_t> plan(plan_bytes - kHeader, 0);
   const size_t off_items = align_up(g.batches.size() * sizeof(BatchInfo), 256);
   memcpy(plan.data(), g.batches.data(), g.batches.size() * sizeof(BatchInfo));
   if (!items.empty()) memcpy(plan.data() + off_items, items.data(), items.size() * sizeof(WorkItem));
@@ -572,7 +591,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   PrefillParams pp;
   memset(&pp, 0, sizeof(pp));
   const int64_t Bmap = g.layout == L_TND ? 1 : g.B;
-  st = dense_map(&pp.tm_q, q, g.layout, Bmap, g.N1, g.S1, g.D);
+  st = dense_map(&pp.tm_q, q, g.layout, Bmap, g.N1, g.S1, g.D, g.fp8);
   if (st != FIA_OK) return st;
   if (g.paged) {
     // the pool as a (D, block_size, KV_N, blocknum) tensor: BNSD-like for
@@ -585,6 +604,17 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
     pp.block_table = g.table;
     pp.table_stride = g.table_stride;
     pp.block_size = int(g.bs);
+  } else if (g.fp8) {
+    st = dense_map(&pp.tm_k, k, g.layout, Bmap, g.N2, g.S2, g.D, true);
+    if (st != FIA_OK) return st;
+    // V as f16 (2^-8 of each e4m3 value) in the workspace, same layout
+    fia_tensor v16 = *v;
+    v16.data = base + plan_bytes;
+    v16.dtype = FIA_DTYPE_F16;
+    st = cuda_check(launch_e4m3_to_f16(v->data, v16.data, numel(v), sm_count(), stream), "value conversion");
+    if (st != FIA_OK) return st;
+    st = dense_map(&pp.tm_v, &v16, g.layout, Bmap, g.N2, g.S2, g.Dv);
+    if (st != FIA_OK) return st;
   } else {
     st = dense_map(&pp.tm_k, k, g.layout, Bmap, g.N2, g.S2, g.D);
     if (st != FIA_OK) return st;
@@ -624,9 +654,15 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.scale_log2 = float(prm->scale_value * 1.4426950408889634);
   pp.bsa_mask = bsa_mask;
   pp.bsa_nqb = nqb; pp.bsa_nkb = nkb; pp.bsa_x = bx; pp.bsa_y = by;
+  pp.fp8_qscale = g.fp8_q;
+  pp.fp8_kscale = g.fp8_k;
+  pp.fp8_vscale = g.fp8_v;
+  pp.fp8_nqs = g.fp8_nqs;
+  pp.fp8_nks = g.fp8_nks;
   pp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
   return cuda_check(profiled(stream,
                              [&] {
+                               if (g.fp8) return launch_bsa_fp8(pp, stream);
                                return mode == kBlockSparse ? launch_prefill(pp, int(g.D), g.bf16, mode, stream)
                                                            : launch_prefill_pair(pp, int(g.Dqk), int(g.Dv), g.bf16,
                                                                                  mode, stream);
@@ -858,10 +894,16 @@ fia_status fia_prefill_mla(const fia_tensor* query, const fia_tensor* key, const
 }
 
 // ------------------------------------------------------------ block-sparse
+// FP8 (q_scale non-NULL): e4m3 query / key / value with fp32 dequant scales
+// (BSA "FP8特性说明"): q_scale (B, N1, ceil(maxQS / 128), 1), k_scale and
+// v_scale (B, N2, ceil(maxKVS / Y), 1); block_shape X = 128, Y = 256 or 512.
 static fia_status bsa_validate(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
                                const fia_tensor* mask, const int64_t* block_shape, const fia_params* params,
-                               const fia_tensor* out, const fia_tensor* lse, Geometry& g, int& nqb, int& nkb) {
-  fia_status st = prefill_geometry(query, key, value, params, out, true, g);
+                               const fia_tensor* out, const fia_tensor* lse, Geometry& g, int& nqb, int& nkb,
+                               const fia_tensor* q_scale = nullptr, const fia_tensor* k_scale = nullptr,
+                               const fia_tensor* v_scale = nullptr) {
+  const bool fp8 = q_scale != nullptr || k_scale != nullptr || v_scale != nullptr;
+  fia_status st = prefill_geometry(query, key, value, params, out, true, g, nullptr, false, nullptr, nullptr, fp8);
   if (st != FIA_OK) return st;
   if (block_shape == nullptr) return fail(FIA_ERR_NULL, "block_shape is required");
   const int64_t X = block_shape[0], Y = block_shape[1];
@@ -877,6 +919,24 @@ static fia_status bsa_validate(const fia_tensor* query, const fia_tensor* key, c
   if (!(mask->ndim == 4 && mask->shape[0] == g.B && mask->shape[1] == g.N1 && mask->shape[2] == nqb && mask->shape[3] == nkb))
     return fail(FIA_ERR_SHAPE, "block_sparse_mask must be (B, N1, %d, %d)", nqb, nkb);
   if (params->sparse_mode != 0) return fail(FIA_ERR_SPARSE_MODE, "block-sparse attention takes no sparse_mode");
+  if (fp8) {
+    if (X != 128 || (Y != 256 && Y != 512))
+      return fail(FIA_ERR_SHAPE, "FP8 block_shape must be [128, 256] or [128, 512] (the quantisation blocks)");
+    const int64_t nqs = (maxq + 127) / 128, nks = (maxk + Y - 1) / Y;
+    auto scale_ok = [&](const fia_tensor* t, int64_t heads, int64_t blocks) {
+      return present(t) && t->dtype == FIA_DTYPE_F32 && t->ndim == 4 && t->shape[0] == g.B && t->shape[1] == heads &&
+             t->shape[2] == blocks && t->shape[3] == 1 && reinterpret_cast<uintptr_t>(t->data) % 4 == 0;
+    };
+    if (!scale_ok(q_scale, g.N1, nqs))
+      return fail(FIA_ERR_SHAPE, "q_dequant_scale must be fp32 (B, N1, %lld, 1)", (long long)nqs);
+    if (!scale_ok(k_scale, g.N2, nks) || !scale_ok(v_scale, g.N2, nks))
+      return fail(FIA_ERR_SHAPE, "k/v_dequant_scale must be fp32 (B, N2, %lld, 1)", (long long)nks);
+    g.fp8_q = static_cast<const float*>(q_scale->data);
+    g.fp8_k = static_cast<const float*>(k_scale->data);
+    g.fp8_v = static_cast<const float*>(v_scale->data);
+    g.fp8_nqs = int(nqs);
+    g.fp8_nks = int(nks);
+  }
   return check_lse(lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
 }
 
@@ -903,6 +963,45 @@ fia_status bsa_forward(const fia_tensor* query, const fia_tensor* key, const fia
   Geometry g;
   int nqb, nkb;
   fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse, g, nqb, nkb);
+  if (st != FIA_OK) return st;
+  return run_prefill(g, kBlockSparse, 0, query, key, value, attention_out, softmax_lse, params,
+                     static_cast<const uint8_t*>(block_sparse_mask->data), nqb, nkb, int(block_shape[0]),
+                     int(block_shape[1]), workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+fia_status bsa_fp8_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                      const fia_tensor* block_sparse_mask, const int64_t* block_shape,
+                                      const fia_tensor* q_dequant_scale, const fia_tensor* k_dequant_scale,
+                                      const fia_tensor* v_dequant_scale, const fia_params* params,
+                                      const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                                      size_t* workspace_bytes) {
+  if (workspace_bytes == nullptr) return fail(FIA_ERR_NULL, "workspace_bytes is NULL");
+  *workspace_bytes = kHeader;
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  if (q_dequant_scale == nullptr || k_dequant_scale == nullptr || v_dequant_scale == nullptr)
+    return fail(FIA_ERR_NULL, "FP8 attention needs all three dequant scales");
+  Geometry g;
+  int nqb, nkb;
+  fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse,
+                               g, nqb, nkb, q_dequant_scale, k_dequant_scale, v_dequant_scale);
+  if (st != FIA_OK) return st;
+  *workspace_bytes = prefill_ws_bytes(g.batches.size(), count_items(g)) + align_up(size_t(numel(value)) * 2, 256);
+  return FIA_OK;
+}
+
+fia_status bsa_forward_fp8(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                           const fia_tensor* block_sparse_mask, const int64_t* block_shape,
+                           const fia_tensor* q_dequant_scale, const fia_tensor* k_dequant_scale,
+                           const fia_tensor* v_dequant_scale, const fia_params* params,
+                           const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
+  if (q_dequant_scale == nullptr || k_dequant_scale == nullptr || v_dequant_scale == nullptr)
+    return fail(FIA_ERR_NULL, "FP8 attention needs all three dequant scales");
+  Geometry g;
+  int nqb, nkb;
+  fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse,
+                               g, nqb, nkb, q_dequant_scale, k_dequant_scale, v_dequant_scale);
   if (st != FIA_OK) return st;
   return run_prefill(g, kBlockSparse, 0, query, key, value, attention_out, softmax_lse, params,
                      static_cast<const uint8_t*>(block_sparse_mask->data), nqb, nkb, int(block_shape[0]),

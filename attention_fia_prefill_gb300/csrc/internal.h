@@ -76,6 +76,12 @@ struct PrefillParams {
   float scale_log2;               // scale * log2(e)
   const uint8_t* bsa_mask;        // [B, N1, nqb, nkb]
   int bsa_nqb, bsa_nkb, bsa_x, bsa_y;
+  // FP8 block-sparse: dequant scales [B, N1, fp8_nqs] (128 query rows per
+  // block) and [B, N2, fp8_nks] (bsa_y key rows per block) for K and V
+  const float* fp8_qscale;
+  const float* fp8_kscale;
+  const float* fp8_vscale;
+  int fp8_nqs, fp8_nks;
   DevStatus status;
 };
 
@@ -163,6 +169,10 @@ void set_last_error(int status, const char* message);
 cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int mode, cudaStream_t s);
 cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int head_dim_v, bool bf16, int mode,
                                 cudaStream_t s);
+cudaError_t launch_bsa_fp8(const PrefillParams& p, cudaStream_t s);
+// e4m3 bytes -> f16 holding 2^-8 of each value (the FP8 path's value tensor);
+// n_bytes a multiple of 16, both pointers 16-byte aligned.
+cudaError_t launch_e4m3_to_f16(const void* src, void* dst, int64_t n_bytes, int n_sm, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, bool bf16, cudaStream_t s);
 cudaError_t launch_mla(const MlaParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_fill_rows(void* out, bool half_type, float* lse, const int64_t* dims, const int64_t* out_strides,

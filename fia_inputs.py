@@ -399,6 +399,44 @@ def bsa_case(B, N1, N2, Sq, Skv, D, X=128, Y=128, keep=0.25, dtype="bf16", workl
     return BSACase(q, k, v, torch.from_numpy(m), (X, Y), N1, N2, 1.0 / math.sqrt(D), "BNSD")
 
 
+@dataclass
+class BSAFp8Case:
+    base: BSACase              # q / k / v float8 e4m3, the block mask, block_shape (128, Y)
+    q_scale: torch.Tensor      # fp32 (B, N1, ceil(Sq/128), 1)
+    k_scale: torch.Tensor      # fp32 (B, N2, ceil(Skv/Y), 1)
+    v_scale: torch.Tensor
+
+
+def fp8_e4m3(shape, workload: int, tensor: int, spread: float = 16.0) -> torch.Tensor:
+    """float8 e4m3 values: N(0,1) * spread, clipped to the format's +-448 and
+    rounded to nearest by torch."""
+    x = rng(workload, tensor).standard_normal(size=tuple(shape), dtype=np.float32) * spread
+    return torch.from_numpy(np.clip(x, -448.0, 448.0)).to(torch.float8_e4m3fn)
+
+
+def bsa_fp8_case(B, N1, N2, Sq, Skv, Y=256, keep=0.25, workload=600, layout="BNSD") -> BSAFp8Case:
+    """FP8 block-sparse inputs (D = 128): e4m3 q / k / v of spread 16, dequant
+    scales uniform on [0.5, 1.5] / 16 per block of 128 query rows / Y key rows,
+    the block mask of bsa_case (128 x Y blocks: diagonal + Bernoulli(keep))."""
+    c = bsa_case(B, N1, N2, Sq, Skv, 128, 128, Y, keep, "bf16", workload)
+    c.q, c.k, c.v = (fp8_e4m3(t.shape, workload, 20 + n) for n, t in enumerate((c.q, c.k, c.v)))
+    nq, nk = -(-Sq // 128), -(-Skv // Y)
+    g = rng(workload, 30)
+    qs = torch.from_numpy((g.random((B, N1, nq, 1)) + 0.5).astype(np.float32) / 16)
+    ks = torch.from_numpy((g.random((B, N2, nk, 1)) + 0.5).astype(np.float32) / 16)
+    vs = torch.from_numpy((g.random((B, N2, nk, 1)) + 0.5).astype(np.float32) / 16)
+    if layout == "BSND":
+        c.q, c.k, c.v = (t.transpose(1, 2).contiguous() for t in (c.q, c.k, c.v))
+        c.layout = "BSND"
+    return BSAFp8Case(c, qs, ks, vs)
+
+
 def workload_bsa(B=2, N1=32, N2=8, S=16384, D=128, workload=5) -> BSACase:
     """Block-sparse prefill bf16: 128x128 blocks, diagonal + ~25% of the rest."""
     return bsa_case(B, N1, N2, S, S, D, 128, 128, 0.25, "bf16", workload)
+
+
+def workload_bsa_fp8(B=2, N1=32, N2=8, S=16384, workload=5) -> BSAFp8Case:
+    """Block-sparse prefill FP8 e4m3 (D = 128): 128 x 256 blocks (the
+    quantisation blocks), diagonal + ~25% of the rest."""
+    return bsa_fp8_case(B, N1, N2, S, S, 256, 0.25, workload)

@@ -79,7 +79,8 @@ typedef enum fia_dtype {
   FIA_DTYPE_I64 = 4,
   FIA_DTYPE_U8 = 5,
   FIA_DTYPE_BOOL = 6,
-  FIA_DTYPE_I8 = 7
+  FIA_DTYPE_I8 = 7,
+  FIA_DTYPE_F8E4M3 = 8   /* float8 e4m3 (FN: no infinities), the FP8 block-sparse inputs */
 } fia_dtype;
 
 /* A contiguous row-major tensor.  ndim == 0 or data == NULL means "absent"
@@ -274,6 +275,34 @@ FIA_API fia_status bsa_forward(const fia_tensor* query, const fia_tensor* key, c
                        const fia_tensor* block_sparse_mask, const int64_t* block_shape, const fia_params* params,
                        const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * bsa_forward_fp8: FP8 block-sparse attention (aclnnBlockSparseAttentionV2,
+ * "FP8特性说明").  Row i of query head h is worth query[i] *
+ * q_dequant_scale[b][h][i / 128]; key / value row j of kv head n is worth
+ * key[j] * k_dequant_scale[b][n][j / Y] (value likewise).
+ *   query/key/value: float8 e4m3 (FIA_DTYPE_F8E4M3), D = 128, layouts as
+ *          bsa_forward.
+ *   block_shape: {128, 256} or {128, 512} (the quantisation blocks).
+ *   q_dequant_scale: fp32 (B, N1, ceil(maxQS/128), 1); k_dequant_scale and
+ *          v_dequant_scale: fp32 (B, N2, ceil(maxKVS/Y), 1); device memory;
+ *          positive (a scale <= 0 is taken as a tiny positive one).
+ *   attention_out: bf16, the query's shape.  softmax_lse as bsa_forward.
+ *   The scores run on the fp8 tensor cores; P V runs in bf16 with V
+ *   dequantised on chip.
+ * ------------------------------------------------------------------------ */
+FIA_API fia_status bsa_fp8_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                                      const fia_tensor* block_sparse_mask, const int64_t* block_shape,
+                                      const fia_tensor* q_dequant_scale, const fia_tensor* k_dequant_scale,
+                                      const fia_tensor* v_dequant_scale, const fia_params* params,
+                                      const fia_tensor* attention_out, const fia_tensor* softmax_lse,
+                                      size_t* workspace_bytes);
+FIA_API fia_status bsa_forward_fp8(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
+                           const fia_tensor* block_sparse_mask, const int64_t* block_shape,
+                           const fia_tensor* q_dequant_scale, const fia_tensor* k_dequant_scale,
+                           const fia_tensor* v_dequant_scale, const fia_params* params,
+                           const fia_tensor* attention_out, const fia_tensor* softmax_lse, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /* Waits for `stream`, then returns the device-side status recorded in a
  * workspace by the last call that used it (FIA_OK or FIA_ERR_TIMEOUT). */

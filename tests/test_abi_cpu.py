@@ -196,6 +196,36 @@ def test_mla_prefill_rules(lib):
     assert ws(q192, k192, v, out, mask=t((300, 300), B.DTYPE_U8), mode=1) == 5
 
 
+def test_bsa_fp8_rules(lib):
+    """FP8 block-sparse: e4m3 query/key/value, D 128, bf16 output, block shape
+    [128, 256 | 512], fp32 scales (B, N1, ceil(S1/128), 1) / (B, N2, ceil(S2/Y), 1)."""
+    F8, F32 = B.DTYPE_F8E4M3, B.DTYPE_F32
+    q, k = t((2, 4, 300, 128), F8), t((2, 2, 600, 128), F8)
+    out = t((2, 4, 300, 128), B.DTYPE_BF16)
+    mask = t((2, 4, 3, 3), B.DTYPE_U8)
+    qs, ks = t((2, 4, 3, 1), F32), t((2, 2, 3, 1), F32)
+
+    def ws(q=q, k=k, out=out, mask=mask, shape=(128, 256), qs=qs, ks=ks, vs=ks):
+        prm = params(lib, num_heads=4, num_key_value_heads=2, input_layout="BNSD")
+        w = ctypes.c_size_t(0)
+        bs = (ctypes.c_int64 * 2)(*shape)
+        ref = lambda d: ctypes.byref(d) if d is not None else None
+        return lib.bsa_fp8_get_workspace_size(ref(q), ref(k), ref(k), ref(mask), bs, ref(qs), ref(ks), ref(vs),
+                                              ctypes.byref(prm.p), ref(out), None, ctypes.byref(w))
+
+    assert ws() == 0
+    assert ws(mask=t((2, 4, 3, 2), B.DTYPE_U8), shape=(128, 512), ks=t((2, 2, 2, 1), F32),
+              vs=t((2, 2, 2, 1), F32)) == 0
+    assert ws(out=t((2, 4, 300, 128), B.DTYPE_F16)) == 2        # output bf16
+    assert ws(q=t((2, 4, 300, 128), B.DTYPE_BF16)) == 2         # all three e4m3
+    assert ws(shape=(128, 128), mask=t((2, 4, 3, 5), B.DTYPE_U8)) == 3   # Y 256 / 512 only
+    assert ws(qs=t((2, 4, 2, 1), F32)) == 3                     # query blocks of 128 rows
+    assert ws(ks=t((2, 2, 3, 1), B.DTYPE_F16)) == 3             # fp32 scales
+    assert ws(vs=None) == 1                                     # all three scales
+    q64, k64 = t((2, 4, 300, 64), F8), t((2, 2, 600, 64), F8)
+    assert ws(q=q64, k=k64, out=t((2, 4, 300, 64), B.DTYPE_BF16)) == 5   # D 128 only
+
+
 def test_shape_dtype_layout_errors(lib):
     q, k = t((1, 2, 8, 64)), t((1, 2, 9, 64))
     assert prefill_ws(lib, q, k, q, params(lib, num_heads=2, input_layout="BNSD"))[0] == 3      # k != v

@@ -63,3 +63,89 @@ def test_full_bsa_workload_sampled(fia):
             [0, 1, 127, 128, 8191, 16383] + list(rng.integers(16384, size=10))]
     ref = _oracle(c, rows=rows)
     assert_rows_close(out, lse, rows, ref, lambda r: (r[0], r[1], r[2]), torch.bfloat16)
+
+
+# ------------------------------------------------------------ FP8
+def _run_fp8(fia, f, **kw):
+    c = f.base
+    out, lse = fia.bsa_forward(c.q.cuda(), c.k.cuda(), c.v.cuda(), c.mask.cuda(), c.block_shape,
+                               num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                               scale_value=c.scale, input_layout=c.layout, softmax_lse_flag=True,
+                               actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
+                               q_dequant_scale=f.q_scale.cuda(), k_dequant_scale=f.k_scale.cuda(),
+                               v_dequant_scale=f.v_scale.cuda(), **kw)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.bfloat16
+    return out, lse
+
+
+def _fp8_atol(f, ref_absmax):
+    """Bound on |out - oracle| for the FP8 path, from its arithmetic: the
+    scores are exact (e4m3 products, fp32 sums); V enters exactly (e4m3 in
+    f16) and P times the value scale is rounded to f16 (2^-11 relative), so
+    out moves by at most 2^-11 * max|V| (2^-10 taken); the bf16 output adds
+    2^-9 * |out|; 2e-3 covers exp2 and fp32 sums.  Never below the bf16 bound."""
+    v_max = float(f.base.v.float().abs().max()) * float(f.v_scale.max())
+    return max(1.6e-2, 2.0 ** -9 * ref_absmax + 2.0 ** -10 * v_max + 2e-3)
+
+
+def _assert_fp8_close(f, out, ref):
+    ref = np.asarray(ref, dtype=np.float64)
+    g = out.float().cpu().numpy().astype(np.float64)
+    assert g.shape == ref.shape and np.all(np.isfinite(g))
+    tol = _fp8_atol(f, float(np.abs(ref).max()))
+    err = float(np.abs(g - ref).max())
+    assert err <= tol, f"FP8 attention_out: max abs err {err:.3e} > {tol:.3e}"
+
+
+def _oracle_fp8(f, rows=None):
+    c = f.base
+    return fia_oracle.bsa_forward(c.q, c.k, c.v, c.mask, c.block_shape, num_heads=c.num_heads,
+                                  num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                                  input_layout=c.layout, actual_seq_qlen=c.actual_seq_qlen,
+                                  actual_seq_kvlen=c.actual_seq_kvlen, rows=rows, q_dequant_scale=f.q_scale,
+                                  k_dequant_scale=f.k_scale, v_dequant_scale=f.v_scale)
+
+
+@pytest.mark.parametrize("Sq,Skv,Y,layout", [(300, 600, 256, "BNSD"), (384, 1100, 512, "BNSD"),
+                                             (257, 513, 256, "BSND")])
+def test_fp8_small(fia, Sq, Skv, Y, layout):
+    """FP8 e4m3 query/key/value with per-block dequant scales (128 query rows,
+    Y key rows): ragged query and key tails, both quantisation block sizes,
+    BNSD and BSND; the bf16 output within the bound the FP8 arithmetic
+    gives (_fp8_atol) of the oracle on the dequantised values."""
+    f = fia_inputs.bsa_fp8_case(2, 4, 2, Sq, Skv, Y, keep=0.4, workload=3500 + Sq + Y, layout=layout)
+    out, lse = _run_fp8(fia, f)
+    ro, rl = _oracle_fp8(f)
+    _assert_fp8_close(f, out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_fp8_tnd_varlen(fia):
+    """TND: per-sequence blocks of the scales and the mask, an empty sequence."""
+    lens = [1, 300, 0, 513]
+    T = sum(lens)
+    f = fia_inputs.bsa_fp8_case(4, 4, 2, max(lens), max(lens), 256, keep=0.5, workload=3600)
+    c = f.base
+    c.q = fia_inputs.fp8_e4m3((T, 4, 128), 3600, 40)
+    c.k = fia_inputs.fp8_e4m3((T, 2, 128), 3600, 41)
+    c.v = fia_inputs.fp8_e4m3((T, 2, 128), 3600, 42)
+    c.layout = "TND"
+    c.actual_seq_qlen = c.actual_seq_kvlen = fia_inputs.cumsum_no_leading_zero(lens)
+    out, lse = _run_fp8(fia, f)
+    ro, rl = _oracle_fp8(f)
+    _assert_fp8_close(f, out, ro)
+    assert_lse_close(lse, rl)
+
+
+def test_fp8_workload_sampled(fia):
+    """FP8 block-sparse workload (B=2, 32/8 heads, S=16384, 128 x 256 blocks,
+    diagonal + ~25%): sampled rows against the oracle."""
+    f = fia_inputs.workload_bsa_fp8()
+    out, lse = _run_fp8(fia, f)
+    rows = [(b, h, i) for b in (0, 1) for h in (0, 17, 31) for i in (0, 127, 128, 8191, 16383)]
+    ref = _oracle_fp8(f, rows=rows)
+    got = torch.stack([out[b, h, i] for (b, h, i) in rows])
+    _assert_fp8_close(f, got, np.stack([o for o, _ in ref]))
+    for (b, h, i), (_, l_ref) in zip(rows, ref):
+        assert abs(float(lse[b, h, i, 0]) - l_ref) <= 1e-3 * max(1.0, abs(l_ref)), (b, h, i)
