@@ -498,6 +498,28 @@ void build_items(const Geometry& g, int prefill_mode, int causal_mode, std::vect
   }
   // Longest first (an LPT order for the hardware block scheduler); ties keep
   // the heads of one GQA group next to each other for L2 reuse of K/V.
+  // When the keys and values the call reads are well beyond what L2 holds
+  // (MHA, long sequences), the items of one (batch, kv head) run back to back
+  // instead, so the CTAs reading the same K/V tiles are resident together:
+  // units by total cost, longest first, and LPT inside a unit.
+  double kv_bytes = 0.0;
+  for (const auto& bi : g.batches) kv_bytes += double(bi.kv_len) * double(g.N2) * double(g.Dqk + g.Dv) * 2.0;
+  constexpr double kL2Share = 48.0 * 1024 * 1024;   // about a third of the 126 MB L2
+  if (prefill_mode != kBlockSparse && kv_bytes > kL2Share) {
+    const int64_t group = g.N1 / g.N2;
+    std::vector<int64_t> unit_cost(size_t(g.B * g.N2), 0);
+    auto unit = [&](const WorkItem& w) { return int64_t(w.b) * g.N2 + w.h / group; };
+    for (const auto& w : items) unit_cost[size_t(unit(w))] += w.cost;
+    std::stable_sort(items.begin(), items.end(), [&](const WorkItem& a, const WorkItem& b) {
+      const int64_t ua = unit(a), ub = unit(b);
+      if (ua != ub) {
+        const int64_t ca = unit_cost[size_t(ua)], cb = unit_cost[size_t(ub)];
+        return ca != cb ? ca > cb : ua < ub;
+      }
+      return a.cost > b.cost;
+    });
+    return;
+  }
   std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) { return a.cost > b.cost; });
 }
 

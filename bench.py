@@ -650,6 +650,25 @@ def run_profile_target(args):
             fia.fia_decode(q, lat, lat, query_rope=qr, key_rope=rope, block_table=tb, block_size=c.block_size,
                            actual_seq_kvlen=c.kv_lens, num_heads=c.num_heads, num_key_value_heads=1,
                            scale_value=c.scale, input_layout="BSND", softmax_lse_flag=True)
+    elif name == "bsa_fp8":
+        f = fia_inputs.workload_bsa_fp8()
+        c = f.base
+        q, k, v, m = c.q.to(dev), c.k.to(dev), c.v.to(dev), c.mask.to(dev)
+        qs, ks, vs = f.q_scale.to(dev), f.k_scale.to(dev), f.v_scale.to(dev)
+
+        def call():
+            fia.bsa_forward(q, k, v, m, c.block_shape, num_heads=c.num_heads,
+                            num_key_value_heads=c.num_key_value_heads, scale_value=c.scale, input_layout="BNSD",
+                            softmax_lse_flag=True, q_dequant_scale=qs, k_dequant_scale=ks, v_dequant_scale=vs)
+    elif name == "mla_prefill":
+        c = fia_inputs.workload_mla_prefill()
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+
+        def call():
+            fia.fia_prefill_mla(q, k, v, num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                                scale_value=c.scale, input_layout="TND", sparse_mode=3,
+                                actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
+                                softmax_lse_flag=True)
     else:
         raise SystemExit(f"unknown profile target {name}")
     for _ in range(args.warmup + args.steps):
@@ -660,7 +679,7 @@ def run_profile_target(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, prefill_tnd, bsa, mla)")
+    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, prefill_tnd, bsa, bsa_fp8, mla, mla_prefill)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
