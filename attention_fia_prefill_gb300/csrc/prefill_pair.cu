@@ -120,7 +120,10 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     const int64_t hi = min(int64_t(bi.kv_len) - 1, last + band_d + p.band_next);
     const int n = hi < lo ? 0 : int(hi / kTileN - lo / kTileN + 1);
     jt0 = hi < lo ? 0 : int(lo / kTileN);
-    na = n;
+    // tile A's rows end earlier: it stops after its own last key's tile
+    const int64_t last_a = min(q0 + kTileM - 1, bi.q_len - 1);
+    const int64_t hi_a = min(int64_t(bi.kv_len) - 1, last_a + band_d + p.band_next);
+    na = (hi < lo || hi_a < lo) ? 0 : int(hi_a / kTileN - lo / kTileN + 1);
     nb = has_b ? n : 0;
   }
   const int nl = max(na, nb);
