@@ -37,6 +37,11 @@ Readings taken where the pages are silent, garbled or contradict each other
   * MLA: scores = scale * (q.k + q_rope.k_rope) over the 576-dim concatenation;
     the value is the 512-d latent.
   * blockSparseMask: nonzero keeps the (X x Y) block; head index is the query head.
+  * MLA prefill: the score is scale * (q.k + q_rope.k_rope), as for MLA decode.
+  * Prefill against a paged cache: actual_seq_kvlen holds per-batch key
+    counts, also for a TND query (the cache is paged, not packed).
+  * FP8 block-sparse: query rows dequantised per X-row block, key / value rows
+    per Y-row block (X = 128, Y = 256 or 512 on the pages).
 
 Parity is pinned by tests/test_oracle_pins.py (closed forms, a library softmax
 attention, invariants and the pages' empty-tensor rule).  No numeric output
