@@ -111,6 +111,18 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(vals, device=None):
+    """Max over ranks of a few host floats (the timed region is the slowest
+    rank's); the values themselves with one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
 class Timer:
     """Per-call CUDA-event timing with an L2 flush before each call."""
 
@@ -542,11 +554,7 @@ def run_ours(args):
             sections["prefill_small"] = {"error": repr(e)}
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    if ws_ > 1:
-        import torch.distributed as dist
-        t = torch.tensor([dec["call_ms"], dec["e2e_ms"]], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec["call_ms"], dec["e2e_ms"] = float(t[0]), float(t[1])
+    dec["call_ms"], dec["e2e_ms"] = max_over_ranks([dec["call_ms"], dec["e2e_ms"]], device=dev)
     if rank != 0:
         return
     value = ws_ * dec["kv_bytes"] / (dec["call_ms"] * 1e-3) / 1e9
