@@ -662,6 +662,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.batches = d_batches;
   pp.items = d_items;
   pp.n_items = int(items.size());
+  pp.prefetch_stride = sm_count();
   pp.num_heads = int(g.N1);
   pp.num_kv_heads = int(g.N2);
   pp.group = int(g.N1 / g.N2);

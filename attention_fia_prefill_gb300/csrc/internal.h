@@ -63,6 +63,7 @@ struct PrefillParams {
   const BatchInfo* batches;
   const WorkItem* items;
   int n_items;
+  int prefetch_stride;            // pair kernel: item blockIdx.x + stride gets its Q warmed in L2 (0: off)
   int num_heads, num_kv_heads, group;
   int is_tnd;
   int causal_offset_mode;         // 2: diagonal j <= i; 3: j <= i + kv_len - q_len

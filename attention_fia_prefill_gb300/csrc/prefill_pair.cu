@@ -215,6 +215,24 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         for (int c = 0; c < C::kChunksV; ++c)
           tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[sv], c * 64, kv_r, kvh, kv_b);
         nv = j + 1;
+        if (j == 0 && p.prefetch_stride > 0 && int(blockIdx.x) + p.prefetch_stride < p.n_items) {
+          // Q of the item that takes this CTA's place about one item from now
+          // (CTAs start in index order, one per SM): into L2, so its first
+          // loads do not wait on HBM
+          const WorkItem nx = p.items[blockIdx.x + p.prefetch_stride];
+          const BatchInfo nb_info = p.batches[nx.b];
+          const int nq0 = nx.q_tile * 2 * kTileM;
+          const int nrow = is_tnd ? nb_info.q_start + nq0 : nq0;
+          const int nbc = is_tnd ? 0 : nx.b;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int c = 0; c < C::kChunksQK; ++c) {
+              int col;
+              const CUtensorMap* m = qk_src(c, &p.tm_q, &p.tm_qr, col);
+              tma_prefetch_l2_4d(m, col, nrow + t * kTileM, nx.h, nbc);
+            }
+        }
       }
       if (*abort_flag) {
         // let every copy in flight land before the CTA exits
