@@ -1108,7 +1108,6 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
       g.kv_bnbd = false;
       if (k->shape[1] != g.bs || k->shape[2] != g.N2 * D)
         return fail(FIA_ERR_SHAPE, "paged key must be (blocknum, block_size, KV_N*D)");
-      if (g.layout == L_BNSD && false) return FIA_OK;
     } else {
       return fail(FIA_ERR_SHAPE, "paged key must be 3-D or 4-D");
     }

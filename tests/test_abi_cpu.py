@@ -226,6 +226,61 @@ def test_bsa_fp8_rules(lib):
     assert ws(q=q64, k=k64, out=t((2, 4, 300, 64), B.DTYPE_BF16)) == 5   # D 128 only
 
 
+def test_paged_prefill_with_mask_and_tnd_fp8_scales(lib):
+    """Paged prefill takes an explicit mask covering the per-batch lengths;
+    FP8 block-sparse in TND sizes its scale blocks by the longest sequence."""
+    q, kp, tab = t((2, 4, 300, 128)), t((9, 2, 256, 128)), t((2, 3), B.DTYPE_I32)
+
+    def ws_paged(mask, mode=1):
+        prm = params(lib, num_heads=4, num_key_value_heads=2, input_layout="BNSD", sparse_mode=mode, block_size=256,
+                     actual_seq_kvlen=[500, 300])
+        w = ctypes.c_size_t(0)
+        return lib.fia_prefill_paged_get_workspace_size(ctypes.byref(q), ctypes.byref(kp), ctypes.byref(kp),
+                                                        ctypes.byref(tab), ctypes.byref(mask) if mask else None,
+                                                        ctypes.byref(prm.p), ctypes.byref(q), None,
+                                                        ctypes.byref(w))
+
+    assert ws_paged(t((300, 512), B.DTYPE_U8)) == 0
+    assert ws_paged(t((300, 499), B.DTYPE_U8)) == 3       # shorter than the 500 keys of batch 0
+    assert ws_paged(None) == 12                           # mode 1 needs a mask
+
+    F8, F32 = B.DTYPE_F8E4M3, B.DTYPE_F32
+    # TND: sequences of 100 and 700 rows, so 6 query blocks and 3 key blocks at the longest
+    qt, kt = t((800, 4, 128), F8), t((800, 2, 128), F8)
+    out = t((800, 4, 128), B.DTYPE_BF16)
+    mask = t((2, 4, 6, 3), B.DTYPE_U8)                    # ceil(700/128) x ceil(700/256)
+
+    def ws_fp8(qs, ks):
+        prm = params(lib, num_heads=4, num_key_value_heads=2, input_layout="TND", actual_seq_qlen=[100, 800],
+                     actual_seq_kvlen=[100, 800])
+        w = ctypes.c_size_t(0)
+        bs = (ctypes.c_int64 * 2)(128, 256)
+        return lib.bsa_fp8_get_workspace_size(ctypes.byref(qt), ctypes.byref(kt), ctypes.byref(kt),
+                                              ctypes.byref(mask), bs, ctypes.byref(qs), ctypes.byref(ks),
+                                              ctypes.byref(ks), ctypes.byref(prm.p), ctypes.byref(out), None,
+                                              ctypes.byref(w))
+
+    assert ws_fp8(t((2, 4, 6, 1), F32), t((2, 2, 3, 1), F32)) == 0
+    assert ws_fp8(t((2, 4, 7, 1), F32), t((2, 2, 3, 1), F32)) == 3
+
+
+def test_mla_prefill_rejects_paged_and_masks(lib):
+    """MLA prefill runs on contiguous key/value only (its entry takes no block
+    table) and takes no explicit mask; causal and band modes are fine."""
+    q, k, v, out = t((300, 4, 192)), t((300, 2, 192)), t((300, 2, 128)), t((300, 4, 128))
+
+    def ws(mode, mask=None, **kw):
+        prm = params(lib, num_heads=4, num_key_value_heads=2, input_layout="TND", sparse_mode=mode,
+                     actual_seq_qlen=[300], actual_seq_kvlen=[300], **kw)
+        w = ctypes.c_size_t(0)
+        return lib.fia_prefill_mla_get_workspace_size(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), None, None,
+                                                      ctypes.byref(mask) if mask else None, ctypes.byref(prm.p),
+                                                      ctypes.byref(out), None, ctypes.byref(w))
+
+    assert ws(2) == 0 and ws(3) == 0 and ws(4, pre_tokens=64, next_tokens=0) == 0
+    assert ws(0, t((300, 300), B.DTYPE_BOOL)) == 5
+
+
 def test_shape_dtype_layout_errors(lib):
     q, k = t((1, 2, 8, 64)), t((1, 2, 9, 64))
     assert prefill_ws(lib, q, k, q, params(lib, num_heads=2, input_layout="BNSD"))[0] == 3      # k != v
