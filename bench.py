@@ -10,7 +10,8 @@ second (the K and V rows of every sequence, sum(L_b) * KV_N * D * 2 bytes * 2).
 
 The other hot-path workloads are measured in the same run under "sections":
 varlen TND causal prefill (TFLOP/s), the same with a 1024-key sliding window
-(sparse_mode 4), chunked prefill against a paged cache (TFLOP/s), MLA prefill
+(sparse_mode 4), the same with an explicit causal mask (sparse_mode 1), chunked prefill
+against a paged cache (TFLOP/s), MLA prefill
 (192 / 128, TFLOP/s), block-sparse
 prefill (TFLOP/s), MLA decode
 (cache GB/s), the headline decode with 4 new tokens per sequence (KV GB/s) and
@@ -303,6 +304,38 @@ def measure_prefill_band(torch, dev, timer, steps, warmup, pk, traffic):
                                  traffic.get("prefill_pair_kernel_band"))}
 
 
+def measure_prefill_mask(torch, dev, timer, steps, warmup, pk, traffic):
+    """The varlen TND workload with an explicit mask (sparse_mode 1): a uint8
+    lower-triangular (4096, 4096) mask, i.e. causal attention given as a mask.
+    An arbitrary mask cannot skip tiles, so every (row, key) tile of each
+    sequence is computed; flops count the allowed pairs only."""
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    c = fia_inputs.workload_tnd_varlen()
+    flops = prefill_tnd_flops(c)
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    mask = fia_inputs.atten_mask((4096, 4096), "causal").to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], c.num_heads, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        fia.fia_prefill(q, k, v, num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                        scale_value=c.scale, input_layout="TND", sparse_mode=1, atten_mask=mask,
+                        actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
+                        softmax_lse_flag=True, out=out, softmax_lse=lse, workspace=ws)
+
+    call_ms, kern_ms = timer.run(call, steps, warmup, kernel_events=True)
+    km = statistics.mean(kern_ms)
+    return {"workload": "varlen TND prefill bf16 with an explicit uint8 causal mask (sparse_mode 1, every tile "
+                        "computed), 8 seqs U[256,4096], Q_N=32, KV_N=8, D=128, LSE",
+            "metric": "prefill attention TFLOP/s", "unit": "TFLOP/s",
+            "value": round(flops / (statistics.mean(call_ms) * 1e-3) / 1e12, 2), "ms_per_call": statistics.mean(call_ms),
+            "kernel_ms": km, "flops": flops,
+            "roofline": roofline("tensor", flops / (km * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s",
+                                 traffic.get("prefill_pair_kernel_mask"))}
+
+
 def measure_chunked_prefill(torch, dev, timer, steps, warmup, pk, traffic):
     """Chunked prefill against a paged cache: 8 sequences, a 2048-token chunk
     after a cached context U[0, 14336], 256-token blocks, right-down causal."""
@@ -542,6 +575,7 @@ def run_ours(args):
     sections = {}
     if not args.headline_only:
         for name, fn in (("prefill_tnd", measure_prefill_tnd), ("prefill_band", measure_prefill_band),
+                         ("prefill_mask", measure_prefill_mask),
                          ("chunked_prefill", measure_chunked_prefill), ("mla_prefill", measure_mla_prefill),
                          ("bsa", measure_bsa), ("bsa_fp8", measure_bsa_fp8), ("mla_decode", measure_mla), ("decode_q4", measure_decode_tokens)):
             try:
