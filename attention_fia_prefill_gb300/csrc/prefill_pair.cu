@@ -372,6 +372,23 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       cp_async_commit();
     };
     if (mrow && n > 0) mask_fetch(0);
+    // Rows of V past the batch's keys may hold anything (even NaN); P is 0
+    // there but 0 * NaN is not, so they are cleared before the first P V that
+    // reads tile jj: tile A's if it uses the tile, else tile B's.
+    auto clear_v_tail = [&](int jj, int kv0j) -> bool {
+      const int s = jj % VS;
+      if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (jj / VS) & 1, abort_flag, p.status))) return false;
+      if (r >= bi.kv_len - kv0j) {
+        uint8_t* vs = smem + C::kOffV + s * C::kTileV;
+#pragma unroll
+        for (int c = 0; c < C::kChunksV; ++c)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      return true;
+    };
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -395,6 +412,25 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         break;
       }
       tc_fence_after();
+      if (MODE == kMask && __all_sync(0xffffffffu, (mb[0] & mb[1] & mb[2] & mb[3]) == 0xffffffffu)) {
+        // the mask hides every key of this tile from all of the warp's rows:
+        // P = 0, and the max, the sum and O stay as they are (what the full
+        // path computes, bit for bit, from a row of -inf)
+        uint32_t z[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(tmem + lane_off + col_s + c * 16, z);
+        const int kv0 = (jt0 + j) * kTileN;
+        if (kv0 + kTileN > bi.kv_len && (t == 0 || j >= na) && !clear_v_tail(j, kv0)) {
+          ok = false;
+          break;
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&my_pfull[j & 1]);
+        continue;
+      }
       // S in two halves: the second half's load is in flight while the
       // first half is masked and reduced.
       uint32_t su[4][32];
@@ -495,21 +531,9 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
           tmem_st16(tmem + lane_off + col_o + c * 16, u);
         }
       }
-      // Rows of V past the batch's keys may hold anything (even NaN); P is 0
-      // there but 0 * NaN is not, so they are cleared before the first P V that
-      // reads this tile: tile A's if it uses the tile, else tile B's.
-      if (ragged && (t == 0 || j >= na)) {
-        const int s = j % VS;
-        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (j / VS) & 1, abort_flag, p.status))) { ok = false; break; }
-        if (r >= bi.kv_len - kv0) {
-          uint8_t* vs = smem + C::kOffV + s * C::kTileV;
-#pragma unroll
-          for (int c = 0; c < C::kChunksV; ++c)
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(vs + c * C::kBoxBytes + r * 128 + q * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
+      if (ragged && (t == 0 || j >= na) && !clear_v_tail(j, kv0)) {
+        ok = false;
+        break;
       }
       tmem_wait_st();
       tc_fence_before();
