@@ -1,4 +1,5 @@
-// Prefill attention (dense and causal modes) with two query tiles per CTA.
+// Prefill attention with two query tiles per CTA: every sparse_mode, contiguous
+// or paged K/V, head dims 64/64, 128/128 and 192/128 (MLA prefill).
 //
 // Operation: as prefill.cu -- torch_npu.npu_prompt_flash_attention ("功能说明",
 // formula) and npu_fused_infer_attention_score_v2 (Q_S > 1, softmax_lse):
@@ -12,7 +13,9 @@
 // exponentiates S_A(j), the MMA warp runs P_B(j-1) V and Q_B K(j)^T, and the
 // other way round, so the softmax of one tile hides behind the products of the
 // other (one tile alone leaves the tensor core idle while its softmax runs).
-//   warp 0      TMA producer: Q_A and Q_B once, K/V tiles through a ring
+//   warp 0      TMA producer: Q_A and Q_B once, K and V tiles through rings
+//               of their own; after the first tile it warms L2 with the Q of
+//               the item that will take this CTA's SM about one item later
 //   warp 1      MMA issuer (one thread) and TMEM owner, in the order
 //                 P_A(j) V, Q_A K(j+1)^T, P_B(j) V, Q_B K(j+1)^T
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one thread
@@ -26,7 +29,8 @@
 // 128-key tile from its block (block_size is a multiple of 128).
 // Explicit mask: each softmax thread copies its row's 128 mask bytes for the
 // next K/V tile into its own 128-byte shared slot (cp.async, in flight while
-// the current tile is processed) and turns them into a 128-bit mask.
+// the current tile is processed) and turns them into a 128-bit mask; a warp
+// whose rows are all masked for a tile writes P = 0 and skips its softmax.
 #include "internal.h"
 #include "ptx.cuh"
 
