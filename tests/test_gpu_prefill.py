@@ -255,3 +255,32 @@ def test_mask_2k_full(fia):
     case = fia_inputs.prefill_case(1, 8, 2, 2048, 2048, 128, dtype="bf16", layout="BNSD", sparse_mode=1, workload=2400)
     mask = fia_inputs.atten_mask((2048, 2048), "blocks", workload=2401)
     _check_mask(fia, case, mask)
+
+
+def test_full_tnd_band_and_mask_workloads_sampled(fia):
+    """The varlen TND workload at full size with the band of the bench
+    (sparse_mode 4, pre_tokens 1024, next_tokens 0) and with an explicit
+    uint8 causal mask (sparse_mode 1, a (4096, 4096) mask): sampled rows
+    against the oracle."""
+    case = fia_inputs.workload_tnd_varlen()
+    lens = [b - a for a, b in zip([0] + case.actual_seq_qlen[:-1], case.actual_seq_qlen)]
+    starts = [0] + case.actual_seq_qlen[:-1]
+    rng = np.random.default_rng(7)
+    rows = []
+    for b in range(len(lens)):
+        for i in sorted({0, lens[b] - 1, int(rng.integers(lens[b])), 1024, 1100}):
+            if i < lens[b]:
+                rows.append((b, int(rng.integers(32)), i))
+    index = lambda r: (starts[r[0]] + r[2], r[1])
+    kw_oracle = dict(num_heads=case.num_heads, num_key_value_heads=case.num_key_value_heads, scale_value=case.scale,
+                     input_layout="TND", actual_seq_qlen=case.actual_seq_qlen, actual_seq_kvlen=case.actual_seq_kvlen,
+                     rows=rows)
+    case.sparse_mode = 4
+    out, lse = _run(fia, case, pre_tokens=1024, next_tokens=0)
+    ref = fia_oracle.fia_prefill(case.q, case.k, case.v, sparse_mode=4, pre_tokens=1024, next_tokens=0, **kw_oracle)
+    assert_rows_close(out, lse, rows, ref, index, torch.bfloat16)
+    mask = fia_inputs.atten_mask((4096, 4096), "causal")
+    case.sparse_mode = 1
+    out, lse = _run(fia, case, atten_mask=mask.cuda())
+    ref = fia_oracle.fia_prefill(case.q, case.k, case.v, sparse_mode=1, atten_mask=mask, **kw_oracle)
+    assert_rows_close(out, lse, rows, ref, index, torch.bfloat16)
