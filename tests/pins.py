@@ -149,6 +149,84 @@ def check_mask_modes_by_counting(orc):
         assert abs(lse[i] - math.log(hi - lo + 1)) < ATOL, "mode 0 window"
 
 
+def check_mask_shapes_by_counting(orc):
+    """atten_mask given per batch: the shapes (B,S1,S2) and (B,1,S1,S2) hold
+    one mask per batch, (1,S1,S2) and (1,1,S1,S2) one mask for all
+    (npu_fused_infer_attention_score_v2 / npu_prompt_flash_attention, parameter
+    atten_mask).  With K = 0 and V = identity, row i of batch b attends
+    uniformly to exactly the keys its own batch's mask leaves at 0, and
+    lse = ln(count): each batch's counts are set by hand below, different per
+    batch, so reading the wrong batch's mask changes the result."""
+    B, Sq, Skv = 3, 4, 6
+    q = _rand((B, 1, Sq, 4), 12)
+    k = torch.zeros((B, 1, Skv, 4), dtype=torch.float64)
+    v = torch.eye(Skv, dtype=torch.float64).reshape(1, 1, Skv, Skv).repeat(B, 1, 1, 1)
+    # batch b, row i: keys 0 .. (b + i) % Skv visible, the rest masked
+    per_batch = np.ones((B, Sq, Skv), dtype=np.uint8)
+    for b in range(B):
+        for i in range(Sq):
+            per_batch[b, i, :(b + i) % Skv + 1] = 0
+    forms = {"(B,S1,S2)": per_batch, "(B,1,S1,S2)": per_batch[:, None]}
+    for name, mask in forms.items():
+        out, lse = orc.fia_prefill(q, k, v, num_heads=1, scale_value=1.0, input_layout="BNSD", sparse_mode=1,
+                                   atten_mask=mask)
+        for b in range(B):
+            for i in range(Sq):
+                n = (b + i) % Skv + 1
+                want = np.zeros(Skv); want[:n] = 1.0 / n
+                assert np.allclose(out[b, 0, i], want, atol=ATOL), f"mask {name}: batch {b} row {i} set"
+                assert abs(lse[b, 0, i, 0] - math.log(n)) < ATOL, f"mask {name}: batch {b} row {i} count"
+    # one mask shared by every batch: batch 1's pattern for all
+    for name, mask in {"(1,S1,S2)": per_batch[1:2], "(1,1,S1,S2)": per_batch[1:2, None]}.items():
+        out, lse = orc.fia_prefill(q, k, v, num_heads=1, scale_value=1.0, input_layout="BNSD", sparse_mode=1,
+                                   atten_mask=mask)
+        for b in range(B):
+            for i in range(Sq):
+                n = (1 + i) % Skv + 1
+                assert abs(lse[b, 0, i, 0] - math.log(n)) < ATOL, f"mask {name}: broadcast to batch {b}"
+    # TND with a per-batch mask: rows and keys are batch-local
+    lens = [2, 4, 3]
+    cum = list(np.cumsum(lens))
+    qt = _rand((sum(lens), 1, 4), 13)
+    kt = torch.zeros((sum(lens), 1, 4), dtype=torch.float64)
+    vt = torch.eye(sum(lens), dtype=torch.float64)[:, None, :]
+    out, lse = orc.fia_prefill(qt, kt, vt, num_heads=1, scale_value=1.0, input_layout="TND", sparse_mode=1,
+                               atten_mask=per_batch, actual_seq_qlen=cum, actual_seq_kvlen=cum)
+    start = 0
+    for b, L in enumerate(lens):
+        for i in range(L):
+            n = min((b + i) % Skv + 1, L)
+            want = np.zeros(sum(lens)); want[start:start + n] = 1.0 / n
+            assert np.allclose(out[start + i, 0], want, atol=ATOL), f"TND mask batch {b} row {i}"
+        start += L
+
+
+def check_decode_mask_by_counting(orc):
+    """Decode atten_mask (B, KV_S), also as (B,1,KV_S) / (B,1,1,KV_S), one row
+    of keys per batch; (1, KV_S) is shared (npu_fused_infer_attention_score_v2,
+    atten_mask for Q_S = 1).  K = 0, V = identity: out is uniform over the
+    batch's unmasked keys and lse = ln(count), counts set by hand per batch."""
+    B, N, Skv = 3, 2, 5
+    q = _rand((B, N, 1, 4), 14)
+    k = torch.zeros((B, N, Skv, 4), dtype=torch.float64)
+    v = torch.eye(Skv, dtype=torch.float64).reshape(1, 1, Skv, Skv).repeat(B, N, 1, 1)
+    m = np.zeros((B, Skv), dtype=np.uint8)
+    m[0, 1] = 1                  # batch 0: keys {0, 2, 3, 4}
+    m[1, :3] = 1                 # batch 1: keys {3, 4}
+    m[2, [0, 2, 4]] = 1          # batch 2: keys {1, 3}
+    visible = [[0, 2, 3, 4], [3, 4], [1, 3]]
+    for name, mask in {"(B,KV_S)": m, "(B,1,KV_S)": m[:, None], "(B,1,1,KV_S)": m[:, None, None]}.items():
+        out, lse = orc.fia_decode(q, k, v, num_heads=N, input_layout="BNSD", atten_mask=mask)
+        for b in range(B):
+            want = np.zeros(Skv); want[visible[b]] = 1.0 / len(visible[b])
+            for h in range(N):
+                assert np.allclose(out[b, h, 0], want, atol=ATOL), f"decode mask {name}: batch {b}"
+                assert abs(lse[b, h, 0, 0] - math.log(len(visible[b]))) < ATOL, f"decode mask {name}: count"
+    out, lse = orc.fia_decode(q, k, v, num_heads=N, input_layout="BNSD", atten_mask=m[1:2])
+    for b in range(B):
+        assert abs(lse[b, 0, 0, 0] - math.log(2)) < ATOL, "decode mask (1, KV_S) broadcast"
+
+
 def check_softmax_rows_sum_to_one(orc):
     """With V = identity the output rows are the softmax probabilities."""
     q, k = _rand((1, 2, 5, 3), 20), _rand((1, 2, 7, 3), 21)
@@ -473,7 +551,8 @@ def check_empty_rules(orc):
 
 ALL_CHECKS = [
     check_rows_vs_library, check_prefill_causal_vs_library, check_gqa_vs_library, check_closed_forms,
-    check_mask_modes_by_counting, check_softmax_rows_sum_to_one, check_layouts_agree,
+    check_mask_modes_by_counting, check_mask_shapes_by_counting, check_decode_mask_by_counting,
+    check_softmax_rows_sum_to_one, check_layouts_agree,
     check_tnd_equals_per_sequence, check_actual_lengths_equal_truncation, check_paged_equals_contiguous,
     check_decode_equals_prefill_row, check_multitoken_decode_vs_library, check_paged_prefill_equals_contiguous,
     check_mla_prefill_vs_library, check_mla_equals_concatenated_attention,

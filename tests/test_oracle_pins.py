@@ -59,6 +59,12 @@ MUTATIONS = [
      "FP8 value scales dropped"),
     ("                K[ks[b]:ks[b] + kl[b]] *= KSC[b][:, jk].T[:, :, None]", "                pass",
      "FP8 TND key scales dropped"),
+    ("        return m[b if m.shape[0] > 1 else 0]\n", "        return m[0]\n", "3-D atten_mask reads batch 0"),
+    ("        return m[b if m.shape[0] > 1 else 0, 0]", "        return m[0, 0]", "4-D atten_mask reads batch 0"),
+    ("    return m.reshape(m.shape[0], -1)[b if m.shape[0] > 1 else 0]", "    return m.reshape(m.shape[0], -1)[0]",
+     "decode atten_mask reads batch 0"),
+    ("            ok = ok & (m[:kl[b]] == 0)[None, :]", "            ok = ok & (m[:kl[b]] != 0)[None, :]",
+     "decode atten_mask polarity"),
 ]
 
 
