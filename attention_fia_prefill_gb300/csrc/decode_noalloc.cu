@@ -18,46 +18,37 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "internal.h"
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-std::mutex g_setup_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  In host code
-// `g_decode_scratch` names a host-side stand-in, not device memory, so the
-// address must come from cudaGetSymbolAddress, once per device with that
-// device current.
-fia_status scratch_for_current_device(void** out) {
+// Device address of the scratch array in the calling thread's current
+// context.  In host code `g_decode_scratch` names a host-side stand-in, not
+// device memory, so the address must come from cudaGetSymbolAddress with the
+// target device current.  The address belongs to a CUDA context, not to a
+// device index: a host that makes another context current (driver API) or
+// resets the device gets a different one.  The lookup is therefore repeated
+// on every call (it allocates nothing); the first call in a context also loads
+// the library's kernels into it.
+fia_status scratch_for_current_context(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
     fia::set_last_error(FIA_ERR_CUDA, cudaGetErrorString(e));
     return FIA_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) {
-    fia::set_last_error(FIA_ERR_CUDA, "device index outside the scratch table");
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    fia::set_last_error(FIA_ERR_CUDA, e != cudaSuccess ? cudaGetErrorString(e) : "null scratch address");
     return FIA_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      fia::set_last_error(FIA_ERR_CUDA, e != cudaSuccess ? cudaGetErrorString(e) : "null scratch address");
-      return FIA_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return FIA_OK;
 }
 
@@ -80,7 +71,7 @@ extern "C" fia_status fia_decode_no_alloc(const fia_tensor* query, const fia_ten
     return FIA_ERR_WORKSPACE;
   }
   void* ws = nullptr;
-  st = scratch_for_current_device(&ws);
+  st = scratch_for_current_context(&ws);
   if (st != FIA_OK) return st;
   return fia_decode(query, key, value, query_rope, key_rope, block_table, atten_mask, params, attention_out,
                     softmax_lse, ws, kNoAllocScratchBytes, stream);

@@ -241,13 +241,20 @@ FIA_API fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, co
  *          held until the process exits).  A call whose workspace need
  *          (fia_decode_get_workspace_size) exceeds 16 MiB returns
  *          FIA_ERR_WORKSPACE before touching the device.
- *   Set-up: the first call on a device (with that device current) looks up the
- *          array's device address; make that first call before any stream
- *          capture.
+ *   Set-up: every call looks up the array's device address in the calling
+ *          thread's current CUDA context (the address belongs to a context:
+ *          another context made current through the driver API, or a device
+ *          reset, gives another one).  The first call in a context also loads
+ *          the library's kernels there; make that first call before any
+ *          stream capture.
  *   Sharing: every call uses the same array and leaves its contents behind.
  *          Calls that overlap on the GPU (other streams, other host threads)
  *          race on it; serialise them.  The device status word lives in the
- *          array and is cleared by each call; it is not exposed.
+ *          array and is not exposed: a device-side timeout of a call made
+ *          through this entry point cannot be read back.
+ *   Limit: MLA decode keeps two 256-wide partial outputs per query head and
+ *          plan slot, so MLA calls with many query heads do not fit (128 heads
+ *          never do, whatever the batch); they return FIA_ERR_WORKSPACE.
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  * ------------------------------------------------------------------------ */
 FIA_API fia_status fia_decode_no_alloc(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,

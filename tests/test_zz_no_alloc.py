@@ -57,6 +57,67 @@ def test_no_alloc_matches_fia_decode_twice():
             assert lerr <= LSE_REL, lerr
 
 
+def _mla_no_alloc(lib, c, dev, out, lse):
+    prm = B.Params(num_heads=c.num_heads, num_key_value_heads=1, scale_value=c.scale, input_layout="BSND",
+                   actual_seq_kvlen=c.kv_lens, block_size=c.block_size, softmax_lse_flag=lse is not None)
+    q, qr, lat, rope, tb = (t.to(dev) for t in (c.q, c.q_rope, c.latent, c.rope, c.block_table))
+    d = [B.tensor_desc(t) for t in (q, lat, qr, rope, tb, out, lse)]
+    st = lib.fia_decode_no_alloc(ctypes.byref(d[0]), ctypes.byref(d[1]), ctypes.byref(d[1]), ctypes.byref(d[2]),
+                                 ctypes.byref(d[3]), ctypes.byref(d[4]), None, ctypes.byref(prm.p),
+                                 ctypes.byref(d[5]), ctypes.byref(d[6]) if d[6] is not None else None,
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    return st
+
+
+def test_no_alloc_mla_matches_fia_decode_twice():
+    """The MLA branch (latent key = value, rope part) through the shared array,
+    twice in a row, equals fia_decode with a caller workspace."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_fia_prefill_gb300 as fia
+    lib = B.load_library()
+    dev = torch.device("cuda", 0)
+    c = fia_inputs.mla_decode_case(3, 16, [700, 33, 2100], workload=7200)
+    lat = c.latent.to(dev)
+    ref_o, ref_l = fia.fia_decode(c.q.to(dev), lat, lat, query_rope=c.q_rope.to(dev), key_rope=c.rope.to(dev),
+                                  block_table=c.block_table.to(dev), block_size=c.block_size,
+                                  actual_seq_kvlen=c.kv_lens, num_heads=c.num_heads, num_key_value_heads=1,
+                                  scale_value=c.scale, input_layout="BSND", softmax_lse_flag=True)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out = torch.full_like(ref_o, float("nan"))
+        lse = torch.full_like(ref_l, float("nan"))
+        st = _mla_no_alloc(lib, c, dev, out, lse)
+        assert st == 0, lib.fia_last_error().decode()
+        err = (out.float() - ref_o.float()).abs().max().item()
+        assert err <= OUT_TOL[torch.bfloat16], err
+        lerr = ((lse - ref_l).abs() / ref_l.abs().clamp_min(1.0)).max().item()
+        assert lerr <= LSE_REL, lerr
+
+
+def test_no_alloc_refuses_full_mla_workload():
+    """MLA decode with 128 query heads (B=32, latent 512 + rope 64, length
+    8192) needs more scratch than the built-in array holds: refused with
+    FIA_ERR_WORKSPACE before any device work."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = B.load_library()
+    P = 1 << 20
+    q = B.raw_desc(P, B.DTYPE_BF16, (32, 1, 128, 512))
+    qr = B.raw_desc(P, B.DTYPE_BF16, (32, 1, 128, 64))
+    lat = B.raw_desc(P, B.DTYPE_BF16, (2048, 128, 512))
+    rope = B.raw_desc(P, B.DTYPE_BF16, (2048, 128, 64))
+    table = B.raw_desc(P, B.DTYPE_I32, (32, 64))
+    prm = B.Params(num_heads=128, num_key_value_heads=1, input_layout="BSND", block_size=128,
+                   actual_seq_kvlen=[8192])
+    st = lib.fia_decode_no_alloc(ctypes.byref(q), ctypes.byref(lat), ctypes.byref(lat), ctypes.byref(qr),
+                                 ctypes.byref(rope), ctypes.byref(table), None, ctypes.byref(prm.p), ctypes.byref(q),
+                                 None, None)
+    assert st == 8, lib.fia_last_error().decode()
+    assert b"built-in maximum" in lib.fia_last_error()
+
+
 def test_no_alloc_rejects_oversized_call():
     """A call whose scratch need exceeds the built-in maximum is refused before
     any device work (here: 4096 batches x 8 KV heads of split partials)."""
