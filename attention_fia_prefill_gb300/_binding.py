@@ -29,7 +29,7 @@ EXPORTS = [
     "fia_prefill_mla", "fia_prefill_paged_get_workspace_size", "fia_prefill_paged", "fia_decode_get_workspace_size",
     "fia_decode", "bsa_get_workspace_size", "bsa_forward", "bsa_fp8_get_workspace_size", "bsa_forward_fp8",
     "fia_device_status", "fia_status_string",
-    "fia_last_error", "fia_profile_next_call", "fia_decode_no_alloc",
+    "fia_last_error", "fia_profile_next_call", "fia_debug_set_wait_limit_ns", "fia_decode_no_alloc",
 ]
 
 
@@ -107,6 +107,8 @@ def load_library(path: str | None = None):
     lib.fia_last_error.restype = ctypes.c_char_p
     lib.fia_profile_next_call.argtypes = [vp, vp]
     lib.fia_profile_next_call.restype = None
+    lib.fia_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.fia_debug_set_wait_limit_ns.restype = None
     lib.fia_decode_no_alloc.argtypes = [T, T, T, T, T, T, T, P, T, T, vp]
     lib.fia_decode_no_alloc.restype = st
     if path is None:
@@ -115,14 +117,21 @@ def load_library(path: str | None = None):
 
 
 # ------------------------------------------------------------------ marshalling
+_DTYPE_CODES = None
+_SHAPE5 = ctypes.c_int64 * 5
+
+
 def _dtype_code(t) -> int:
-    import torch
-    m = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.int32: DTYPE_I32,
-         torch.int64: DTYPE_I64, torch.uint8: DTYPE_U8, torch.bool: DTYPE_BOOL, torch.int8: DTYPE_I8,
-         torch.float8_e4m3fn: DTYPE_F8E4M3}
-    if t.dtype not in m:
+    global _DTYPE_CODES
+    if _DTYPE_CODES is None:
+        import torch
+        _DTYPE_CODES = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32,
+                        torch.int32: DTYPE_I32, torch.int64: DTYPE_I64, torch.uint8: DTYPE_U8, torch.bool: DTYPE_BOOL,
+                        torch.int8: DTYPE_I8, torch.float8_e4m3fn: DTYPE_F8E4M3}
+    code = _DTYPE_CODES.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    return m[t.dtype]
+    return code
 
 
 def tensor_desc(t) -> FiaTensor | None:
@@ -131,15 +140,10 @@ def tensor_desc(t) -> FiaTensor | None:
         return None
     if not t.is_contiguous():
         raise ValueError("tensors must be contiguous")
-    if t.dim() > 5:
+    shape = t.shape
+    if len(shape) > 5:
         raise ValueError("at most 5 dims")
-    d = FiaTensor()
-    d.data = t.data_ptr() if t.numel() > 0 else None
-    d.dtype = _dtype_code(t)
-    d.ndim = t.dim()
-    for i, s in enumerate(t.shape):
-        d.shape[i] = int(s)
-    return d
+    return FiaTensor(t.data_ptr() or None, _dtype_code(t), len(shape), _SHAPE5(*shape))
 
 
 def raw_desc(ptr: int | None, dtype: int, shape) -> FiaTensor:
@@ -163,29 +167,39 @@ class Params:
     def __init__(self, *, num_heads, num_key_value_heads=0, scale_value=1.0, input_layout="BSH", sparse_mode=0,
                  pre_tokens=INT32_MAX, next_tokens=INT32_MAX, actual_seq_qlen=None, actual_seq_kvlen=None,
                  block_size=0, softmax_lse_flag=False, inner_precise=0):
-        lib = load_library()
-        self.p = FiaParams()
-        lib.fia_params_init(ctypes.byref(self.p))
         self._layout = input_layout.encode()
-        self.p.num_heads = int(num_heads)
-        self.p.num_key_value_heads = int(num_key_value_heads)
-        self.p.scale_value = float(scale_value)
-        self.p.input_layout = self._layout
-        self.p.sparse_mode = int(sparse_mode)
-        self.p.pre_tokens = int(pre_tokens)
-        self.p.next_tokens = int(next_tokens)
         self._q = self._kv = None
+        nq = nkv = 0
         if actual_seq_qlen is not None:
-            self._q = (ctypes.c_int64 * len(actual_seq_qlen))(*[int(x) for x in actual_seq_qlen])
-            self.p.actual_seq_qlen = self._q
-            self.p.n_actual_seq_qlen = len(actual_seq_qlen)
+            nq = len(actual_seq_qlen)
+            self._q = (ctypes.c_int64 * nq)(*actual_seq_qlen)
         if actual_seq_kvlen is not None:
-            self._kv = (ctypes.c_int64 * len(actual_seq_kvlen))(*[int(x) for x in actual_seq_kvlen])
-            self.p.actual_seq_kvlen = self._kv
-            self.p.n_actual_seq_kvlen = len(actual_seq_kvlen)
-        self.p.block_size = int(block_size)
-        self.p.softmax_lse_flag = 1 if softmax_lse_flag else 0
-        self.p.inner_precise = int(inner_precise)
+            nkv = len(actual_seq_kvlen)
+            self._kv = (ctypes.c_int64 * nkv)(*actual_seq_kvlen)
+        I64P = ctypes.POINTER(ctypes.c_int64)
+        self.p = FiaParams(int(num_heads), int(num_key_value_heads), float(scale_value), self._layout,
+                           int(sparse_mode), int(pre_tokens), int(next_tokens),
+                           ctypes.cast(self._q, I64P) if self._q is not None else None, nq,
+                           ctypes.cast(self._kv, I64P) if self._kv is not None else None, nkv,
+                           int(block_size), 1 if softmax_lse_flag else 0, int(inner_precise))
+
+
+# The parameters of the last few calls, by value: a decode loop calls with the
+# same lengths for every layer of a step, so the struct is built once per step.
+_PARAMS_CACHE: dict = {}
+
+
+def _params(**kw) -> Params:
+    key = tuple((k, tuple(v) if isinstance(v, list) else v) for k, v in kw.items())
+    try:
+        prm = _PARAMS_CACHE.get(key)
+    except TypeError:   # unhashable argument (e.g. a tensor of lengths): no caching
+        return Params(**kw)
+    if prm is None:
+        if len(_PARAMS_CACHE) >= 16:
+            _PARAMS_CACHE.pop(next(iter(_PARAMS_CACHE)))
+        prm = _PARAMS_CACHE[key] = Params(**kw)
+    return prm
 
 
 def check(status: int):
@@ -197,6 +211,26 @@ def check(status: int):
 def _stream_ptr(device):
     import torch
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+FIA_ERR_WORKSPACE = 8
+
+
+def _run_with_workspace(size_fn, run_fn, args, workspace, device):
+    """Runs run_fn(*args, ws, ws_bytes, stream).  A caller workspace is tried
+    first (the call itself checks its size); otherwise, or when it is too
+    small, the size is queried and a workspace allocated with torch."""
+    stream = _stream_ptr(device)
+    if workspace is not None:
+        st = run_fn(*args, ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()), stream)
+        if st != FIA_ERR_WORKSPACE:
+            check(st)
+            return
+    import torch
+    ws = ctypes.c_size_t(0)
+    check(size_fn(*args, ctypes.byref(ws)))
+    workspace = torch.empty(max(ws.value, 1), dtype=torch.uint8, device=device)
+    check(run_fn(*args, ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()), stream))
 
 
 def _lse_shape(q, layout, num_heads):
@@ -222,7 +256,7 @@ def fia_prefill(query, key, value, *, atten_mask=None, actual_seq_qlen=None, act
     import torch
     _require_cuda(query, key, value, atten_mask)
     lib = load_library()
-    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+    prm = _params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
                  input_layout=input_layout, sparse_mode=sparse_mode, pre_tokens=pre_tokens, next_tokens=next_tokens,
                  actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen,
                  softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
@@ -231,14 +265,9 @@ def fia_prefill(query, key, value, *, atten_mask=None, actual_seq_qlen=None, act
     if softmax_lse_flag and softmax_lse is None:
         softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
     dq, dk, dv, dm, do, dl = (tensor_desc(t) for t in (query, key, value, atten_mask, out, softmax_lse))
-    ws = ctypes.c_size_t(0)
-    check(lib.fia_prefill_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dm), ctypes.byref(prm.p), _ref(do),
-                                             _ref(dl), ctypes.byref(ws)))
-    if workspace is None or workspace.numel() < ws.value:
-        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
-    check(lib.fia_prefill(_ref(dq), _ref(dk), _ref(dv), _ref(dm), ctypes.byref(prm.p), _ref(do), _ref(dl),
-                          ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
-                          _stream_ptr(query.device)))
+    _run_with_workspace(lib.fia_prefill_get_workspace_size, lib.fia_prefill,
+                        (_ref(dq), _ref(dk), _ref(dv), _ref(dm), ctypes.byref(prm.p), _ref(do), _ref(dl)),
+                        workspace, query.device)
     return out, softmax_lse
 
 
@@ -251,7 +280,7 @@ def fia_prefill_mla(query, key, value, *, query_rope=None, key_rope=None, atten_
     import torch
     _require_cuda(query, key, value, query_rope, key_rope, atten_mask)
     lib = load_library()
-    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+    prm = _params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
                  input_layout=input_layout, sparse_mode=sparse_mode, pre_tokens=pre_tokens, next_tokens=next_tokens,
                  actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen,
                  softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
@@ -265,14 +294,8 @@ def fia_prefill_mla(query, key, value, *, query_rope=None, key_rope=None, atten_
         softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
     descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, atten_mask, out, softmax_lse)]
     dq, dk, dv_, dqr, dkr, dm, do, dl = (_ref(d) for d in descs)
-    ws = ctypes.c_size_t(0)
-    check(lib.fia_prefill_mla_get_workspace_size(dq, dk, dv_, dqr, dkr, dm, ctypes.byref(prm.p), do, dl,
-                                                 ctypes.byref(ws)))
-    if workspace is None or workspace.numel() < ws.value:
-        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
-    check(lib.fia_prefill_mla(dq, dk, dv_, dqr, dkr, dm, ctypes.byref(prm.p), do, dl,
-                              ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
-                              _stream_ptr(query.device)))
+    _run_with_workspace(lib.fia_prefill_mla_get_workspace_size, lib.fia_prefill_mla,
+                        (dq, dk, dv_, dqr, dkr, dm, ctypes.byref(prm.p), do, dl), workspace, query.device)
     return out, softmax_lse
 
 
@@ -287,7 +310,7 @@ def fia_prefill_paged(query, key_cache, value_cache, block_table, *, block_size,
     import torch
     _require_cuda(query, key_cache, value_cache, block_table, atten_mask)
     lib = load_library()
-    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+    prm = _params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
                  input_layout=input_layout, sparse_mode=sparse_mode, pre_tokens=pre_tokens, next_tokens=next_tokens,
                  actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen, block_size=block_size,
                  softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
@@ -297,12 +320,8 @@ def fia_prefill_paged(query, key_cache, value_cache, block_table, *, block_size,
         softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
     descs = [tensor_desc(t) for t in (query, key_cache, value_cache, block_table, atten_mask, out, softmax_lse)]
     dq, dk, dv, dt, dm, do, dl = (_ref(d) for d in descs)
-    ws = ctypes.c_size_t(0)
-    check(lib.fia_prefill_paged_get_workspace_size(dq, dk, dv, dt, dm, ctypes.byref(prm.p), do, dl, ctypes.byref(ws)))
-    if workspace is None or workspace.numel() < ws.value:
-        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
-    check(lib.fia_prefill_paged(dq, dk, dv, dt, dm, ctypes.byref(prm.p), do, dl, ctypes.c_void_p(workspace.data_ptr()),
-                                ctypes.c_size_t(workspace.numel()), _stream_ptr(query.device)))
+    _run_with_workspace(lib.fia_prefill_paged_get_workspace_size, lib.fia_prefill_paged,
+                        (dq, dk, dv, dt, dm, ctypes.byref(prm.p), do, dl), workspace, query.device)
     return out, softmax_lse
 
 
@@ -316,7 +335,7 @@ def fia_decode(query, key, value, *, query_rope=None, key_rope=None, block_table
     import torch
     _require_cuda(query, key, value, query_rope, key_rope, block_table)
     lib = load_library()
-    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+    prm = _params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
                  input_layout=input_layout, sparse_mode=sparse_mode, actual_seq_kvlen=actual_seq_kvlen,
                  block_size=block_size, softmax_lse_flag=softmax_lse_flag, inner_precise=inner_precise)
     if out is None:
@@ -326,14 +345,9 @@ def fia_decode(query, key, value, *, query_rope=None, key_rope=None, block_table
     descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, block_table, atten_mask, out,
                                       softmax_lse)]
     dq, dk, dv, dqr, dkr, dbt, dm, do, dl = descs
-    ws = ctypes.c_size_t(0)
-    check(lib.fia_decode_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dqr), _ref(dkr), _ref(dbt), _ref(dm),
-                                            ctypes.byref(prm.p), _ref(do), _ref(dl), ctypes.byref(ws)))
-    if workspace is None or workspace.numel() < ws.value:
-        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
-    check(lib.fia_decode(_ref(dq), _ref(dk), _ref(dv), _ref(dqr), _ref(dkr), _ref(dbt), _ref(dm), ctypes.byref(prm.p),
-                         _ref(do), _ref(dl), ctypes.c_void_p(workspace.data_ptr()),
-                         ctypes.c_size_t(workspace.numel()), _stream_ptr(query.device)))
+    _run_with_workspace(lib.fia_decode_get_workspace_size, lib.fia_decode,
+                        (_ref(dq), _ref(dk), _ref(dv), _ref(dqr), _ref(dkr), _ref(dbt), _ref(dm), ctypes.byref(prm.p),
+                         _ref(do), _ref(dl)), workspace, query.device)
     return out, softmax_lse
 
 
@@ -346,7 +360,7 @@ def fia_decode_no_alloc(query, key, value, *, out, softmax_lse=None, query_rope=
     built-in array (see include/fia.h).  Nothing is allocated here."""
     _require_cuda(query, key, value, query_rope, key_rope, block_table, out, softmax_lse)
     lib = load_library()
-    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+    prm = _params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
                  input_layout=input_layout, sparse_mode=sparse_mode, actual_seq_kvlen=actual_seq_kvlen,
                  block_size=block_size, softmax_lse_flag=softmax_lse is not None, inner_precise=inner_precise)
     descs = [tensor_desc(t) for t in (query, key, value, query_rope, key_rope, block_table, atten_mask, out,
@@ -368,7 +382,7 @@ def bsa_forward(query, key, value, block_sparse_mask, block_shape, *, actual_seq
     fp8 = q_dequant_scale is not None or k_dequant_scale is not None or v_dequant_scale is not None
     _require_cuda(query, key, value, block_sparse_mask, q_dequant_scale, k_dequant_scale, v_dequant_scale)
     lib = load_library()
-    prm = Params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
+    prm = _params(num_heads=num_heads, num_key_value_heads=num_key_value_heads, scale_value=scale_value,
                  input_layout=input_layout, actual_seq_qlen=actual_seq_qlen, actual_seq_kvlen=actual_seq_kvlen,
                  softmax_lse_flag=softmax_lse_flag)
     if out is None:
@@ -377,24 +391,15 @@ def bsa_forward(query, key, value, block_sparse_mask, block_shape, *, actual_seq
         softmax_lse = torch.empty(_lse_shape(query, input_layout, num_heads), dtype=torch.float32, device=query.device)
     shape = (ctypes.c_int64 * 2)(int(block_shape[0]), int(block_shape[1]))
     dq, dk, dv, dmask, do, dl = (tensor_desc(t) for t in (query, key, value, block_sparse_mask, out, softmax_lse))
-    ws = ctypes.c_size_t(0)
     if fp8:
         dsq, dsk, dsv = (_ref(tensor_desc(t)) for t in (q_dequant_scale, k_dequant_scale, v_dequant_scale))
-        check(lib.bsa_fp8_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, dsq, dsk, dsv,
-                                             ctypes.byref(prm.p), _ref(do), _ref(dl), ctypes.byref(ws)))
+        _run_with_workspace(lib.bsa_fp8_get_workspace_size, lib.bsa_forward_fp8,
+                            (_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, dsq, dsk, dsv, ctypes.byref(prm.p),
+                             _ref(do), _ref(dl)), workspace, query.device)
     else:
-        check(lib.bsa_get_workspace_size(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p),
-                                         _ref(do), _ref(dl), ctypes.byref(ws)))
-    if workspace is None or workspace.numel() < ws.value:
-        workspace = torch.empty(ws.value, dtype=torch.uint8, device=query.device)
-    if fp8:
-        check(lib.bsa_forward_fp8(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, dsq, dsk, dsv,
-                                  ctypes.byref(prm.p), _ref(do), _ref(dl), ctypes.c_void_p(workspace.data_ptr()),
-                                  ctypes.c_size_t(workspace.numel()), _stream_ptr(query.device)))
-    else:
-        check(lib.bsa_forward(_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do),
-                              _ref(dl), ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()),
-                              _stream_ptr(query.device)))
+        _run_with_workspace(lib.bsa_get_workspace_size, lib.bsa_forward,
+                            (_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do),
+                             _ref(dl)), workspace, query.device)
     return out, softmax_lse
 
 

@@ -259,16 +259,22 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
     const int i = q0 + r;
     const float sl2_q = p.scale_log2 * q_scale;
+    // dequant scales must be positive: any other value (<= 0, NaN) is
+    // reported as FIA_ERR_UNSUPPORTED in the call's status word
+    if (r == 0 && !(q_scale > 0.f)) status_raise(p.status, 5u /* FIA_ERR_UNSUPPORTED */);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     int j = 0;
     for (int t = iter.next(-1); t >= 0; t = iter.next(t), ++j) {
       const int sb = j & 1;
       const int kv0 = t * kTileN;
-      // scales are positive; a zero one is kept just above 0 so that masked
-      // scores (-inf) times it stay -inf instead of NaN
-      const float sl2 = fmaxf(sl2_q * k_scales[kv0 / p.bsa_y], 1e-30f);
+      // a non-positive scale is an error (reported above or here); the
+      // factor is still kept above 0 so that masked scores (-inf) times it
+      // stay -inf instead of NaN and the kernel runs to its end
+      const float ks = k_scales[kv0 / p.bsa_y];
       const float vs = v_scales[kv0 / p.bsa_y];
+      if (r == 0 && !(ks > 0.f && vs > 0.f)) status_raise(p.status, 5u /* FIA_ERR_UNSUPPORTED */);
+      const float sl2 = fmaxf(sl2_q * ks, 1e-30f);
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t su[4][32];

@@ -59,6 +59,19 @@ constexpr size_t kHeader = 256;   // workspace bytes [0, 256): device status wor
 std::atomic<unsigned long long> g_epoch{0};
 unsigned long long next_epoch() { return g_epoch.fetch_add(1, std::memory_order_relaxed) + 1; }
 
+// Limit of the kernels' unwinding waits (fia_debug_set_wait_limit_ns; 0: the
+// default of kWaitLimitNs).
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+
+// A call's device status: the word at the start of its workspace, a fresh
+// epoch, and the wait limit.
+DevStatus make_status(void* workspace) {
+  DevStatus st{reinterpret_cast<unsigned long long*>(workspace), next_epoch()};
+  const unsigned long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+  if (lim != 0) st.limit_ns = lim;
+  return st;
+}
+
 // Status word for calls that launch no stamping kernel: cleared on the stream.
 fia_status clear_status(void* ws, cudaStream_t stream);
 constexpr int kMaxDecodeCtas = 256;   // decode CTAs per call (one per SM)
@@ -523,8 +536,42 @@ void build_items(const Geometry& g, int prefill_mode, int causal_mode, std::vect
   std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) { return a.cost > b.cost; });
 }
 
+constexpr int kMaxPairCtas = 256;   // persistent pair-kernel CTAs per call (one per SM)
+
 size_t prefill_ws_bytes(size_t n_batches, size_t n_items) {
-  return kHeader + align_up(n_batches * sizeof(BatchInfo), 256) + align_up(n_items * sizeof(WorkItem), 256);
+  return kHeader + align_up(n_batches * sizeof(BatchInfo), 256) + align_up(n_items * sizeof(WorkItem), 256) +
+         align_up((kMaxPairCtas + 1) * sizeof(int32_t), 256);
+}
+
+// Deals the items (in the order build_items chose) to n_cta persistent CTAs:
+// each item goes to the CTA with the least work so far (its cost in tile
+// products plus a fixed charge for the item's start and end), as the
+// hardware's block scheduler would; then the items are regrouped by CTA, each
+// CTA's in the order it received them.
+void deal_items(std::vector<WorkItem>& items, int n_cta, std::vector<int32_t>& cta_items) {
+  constexpr int64_t kItemCharge = 2;   // tile products' worth of an item's start and end
+  std::vector<std::pair<int64_t, int>> heap;   // (load, cta), a min-heap
+  heap.reserve(size_t(n_cta));
+  for (int c = 0; c < n_cta; ++c) heap.emplace_back(0, c);
+  auto cmp = [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) {
+    return a.first != b.first ? a.first > b.first : a.second > b.second;
+  };
+  std::vector<int> owner(items.size());
+  std::vector<int32_t> count(size_t(n_cta), 0);
+  for (size_t i = 0; i < items.size(); ++i) {
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    auto& top = heap.back();
+    owner[i] = top.second;
+    ++count[size_t(top.second)];
+    top.first += int64_t(items[i].cost) + kItemCharge;
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  cta_items.assign(size_t(n_cta) + 1, 0);
+  for (int c = 0; c < n_cta; ++c) cta_items[size_t(c) + 1] = cta_items[size_t(c)] + count[size_t(c)];
+  std::vector<WorkItem> out(items.size());
+  std::vector<int32_t> pos(cta_items.begin(), cta_items.end() - 1);
+  for (size_t i = 0; i < items.size(); ++i) out[size_t(pos[size_t(owner[i])]++)] = items[i];
+  items.swap(out);
 }
 
 size_t count_items(const Geometry& g) {
@@ -579,15 +626,23 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   if (g.layout == L_TND) { ls[0] = 0; ls[1] = 1; ls[2] = g.N1; }
   else { ls[0] = g.N1 * g.S1; ls[1] = g.S1; ls[2] = 1; }
 
+  // the two-tile kernel is persistent: deal its items to one CTA per SM
+  const bool pair = !g.fp8 && mode != kBlockSparse;
+  std::vector<int32_t> cta_items;
+  const int n_cta = pair ? int(std::min<size_t>(items.size(), size_t(std::min(sm_count(), kMaxPairCtas)))) : 0;
+  if (pair && n_cta > 0) deal_items(items, n_cta, cta_items);
   // upload the plan
   std::vector<uint8_t> plan(plan_bytes - kHeader, 0);
   const size_t off_items = align_up(g.batches.size() * sizeof(BatchInfo), 256);
+  const size_t off_cta = off_items + align_up(items.size() * sizeof(WorkItem), 256);
   memcpy(plan.data(), g.batches.data(), g.batches.size() * sizeof(BatchInfo));
   if (!items.empty()) memcpy(plan.data() + off_items, items.data(), items.size() * sizeof(WorkItem));
+  if (!cta_items.empty()) memcpy(plan.data() + off_cta, cta_items.data(), cta_items.size() * sizeof(int32_t));
   st = cuda_check(cudaMemcpyAsync(base + kHeader, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream), "plan upload");
   if (st != FIA_OK) return st;
   const BatchInfo* d_batches = reinterpret_cast<const BatchInfo*>(base + kHeader);
   const WorkItem* d_items = reinterpret_cast<const WorkItem*>(base + kHeader + off_items);
+  const int32_t* d_cta_items = reinterpret_cast<const int32_t*>(base + kHeader + off_cta);
 
   // rows that no CTA writes: padding rows of the padded layouts
   if (g.layout != L_TND) {
@@ -662,7 +717,8 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.batches = d_batches;
   pp.items = d_items;
   pp.n_items = int(items.size());
-  pp.prefetch_stride = sm_count();
+  pp.cta_items = d_cta_items;
+  pp.n_cta = n_cta;
   pp.num_heads = int(g.N1);
   pp.num_kv_heads = int(g.N2);
   pp.group = int(g.N1 / g.N2);
@@ -682,7 +738,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.fp8_vscale = g.fp8_v;
   pp.fp8_nqs = g.fp8_nqs;
   pp.fp8_nks = g.fp8_nks;
-  pp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
+  pp.status = make_status(base);
   return cuda_check(profiled(stream,
                              [&] {
                                if (g.fp8) return launch_bsa_fp8(pp, stream);
@@ -811,6 +867,8 @@ void fia_profile_next_call(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);
 }
+
+void fia_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
 
 fia_status fia_device_status(const void* workspace, void* stream) {
   if (workspace == nullptr) return fail(FIA_ERR_NULL, "workspace is NULL");
@@ -1164,6 +1222,9 @@ struct DecodePlan {
   int n_cta = 0, n_units = 0;
 };
 
+// How many stages ahead the decode producers warm L2 (0: off).
+int g_decode_l2_ahead = 0;
+
 // Charge, in stages, for every unit piece (segment) a CTA runs: the end of a
 // segment drains the pipeline (its last P V), sums and writes the partials.
 // Measured on the paged GQA decode kernel: ~1.4 us per 128-token stage and
@@ -1237,26 +1298,27 @@ void plan_decode(const DecodeGeometry& g, int n_sm, DecodePlan& pl, int stage_ke
 }
 
 struct DecodeWsLayout {
-  size_t off_ctr, off_segs, off_cta, off_units, off_len, off_po, off_pl, total;
+  size_t off_ctr, off_plan, off_po, off_pl, total;
 };
 
-// Workspace: status word | per-unit counters | (plan, when it does not fit in
-// the kernel parameters) | partial O | partial lse.
-DecodeWsLayout decode_ws_layout(size_t n_segs, size_t n_cta, size_t n_units, size_t B, size_t rows, size_t D,
-                                bool plan_in_ws) {
+// 32-bit plan words of a plan: cta_seg, segments (4 words), unit parts (2
+// words), kv lengths (1 word).
+size_t decode_plan_words(size_t n_segs, size_t n_cta, size_t n_units, size_t B) {
+  return align_up(n_cta + 1, 4) + 4 * n_segs + 2 * n_units + B + 2;
+}
+
+// Workspace: status word | per-unit counters | plan (used when it does not
+// fit in the kernel parameters) | partial O | partial lse.
+DecodeWsLayout decode_ws_layout(size_t n_segs, size_t n_cta, size_t n_units, size_t B, size_t rows, size_t D) {
   DecodeWsLayout w;
   size_t o = kHeader;
   w.off_ctr = o; o += align_up(n_units * sizeof(unsigned long long), 256);
-  w.off_segs = o; o += plan_in_ws ? align_up(n_segs * sizeof(DecodeSeg), 256) : 0;
-  w.off_cta = o; o += plan_in_ws ? align_up((n_cta + 1) * sizeof(int32_t), 256) : 0;
-  w.off_units = o; o += plan_in_ws ? align_up(n_units * sizeof(int2), 256) : 0;
-  w.off_len = o; o += plan_in_ws ? align_up(B * sizeof(int32_t), 256) : 0;
+  w.off_plan = o; o += align_up(decode_plan_words(n_segs, n_cta, n_units, B) * sizeof(int32_t), 256);
   w.off_po = o; o += align_up(n_segs * rows * D * sizeof(float), 256);
   w.off_pl = o; o += align_up(n_segs * rows * sizeof(float), 256);
   w.total = o;
   return w;
 }
-
 
 // Upper bound over every plan the call can make (at most kMaxDecodeCtas CTAs,
 // so at most n_units + kMaxDecodeCtas segments).
@@ -1264,7 +1326,60 @@ size_t decode_ws_bound(const DecodeGeometry& g) {
   const size_t n_units = size_t(g.B * g.N2);
   const size_t n_segs = n_units + kMaxDecodeCtas;
   const size_t rows = size_t(g.rows());
-  return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), rows, size_t(g.D), true).total;
+  return decode_ws_layout(n_segs, kMaxDecodeCtas, n_units, size_t(g.B), rows, size_t(g.D)).total;
+}
+
+// The decode plan as words (layout in internal.h): 16-bit words into the
+// kernel parameters when every value and the whole plan fit, else 32-bit
+// words for the workspace.  Returns true for the inline form.
+bool pack_decode_plan(const DecodePlan& pl, const std::vector<int32_t>& kv_len, DecodeParams& dp,
+                      std::vector<int32_t>& wide) {
+  const size_t n_cta = size_t(pl.n_cta), n_segs = pl.segs.size(), n_units = pl.unit_parts.size(), B = kv_len.size();
+  const int seg = int(align_up(n_cta + 1, 4));
+  const int unit = seg + int(4 * n_segs);
+  const int len = int(align_up(size_t(unit) + 2 * n_units, 2));
+  dp.plan_seg = seg;
+  dp.plan_unit = unit;
+  dp.plan_len = len;
+  bool fits = size_t(len) + 2 * B <= size_t(kDecodePlanInline) && n_segs <= 32767 && n_units <= 32767;
+  for (size_t i = 0; fits && i < n_segs; ++i) fits = pl.segs[i].stage_end <= 32767;
+  if (fits) {
+    int16_t* w = dp.plan_inline;
+    memset(w, 0, sizeof(dp.plan_inline));
+    for (size_t c = 0; c <= n_cta; ++c) w[c] = int16_t(pl.cta_seg[c]);
+    for (size_t i = 0; i < n_segs; ++i) {
+      const DecodeSeg& sg = pl.segs[i];
+      w[seg + 4 * i] = int16_t(sg.unit);
+      w[seg + 4 * i + 1] = int16_t(sg.stage_begin);
+      w[seg + 4 * i + 2] = int16_t(sg.stage_end);
+      w[seg + 4 * i + 3] = int16_t(sg.part);
+    }
+    for (size_t u = 0; u < n_units; ++u) {
+      w[unit + 2 * u] = int16_t(pl.unit_parts[u].x);
+      w[unit + 2 * u + 1] = int16_t(pl.unit_parts[u].y);
+    }
+    for (size_t b = 0; b < B; ++b) {
+      const uint32_t L = uint32_t(kv_len[b]);
+      w[len + 2 * b] = int16_t(uint16_t(L & 0xffffu));
+      w[len + 2 * b + 1] = int16_t(uint16_t(L >> 16));
+    }
+    return true;
+  }
+  wide.assign(size_t(len) + B, 0);
+  for (size_t c = 0; c <= n_cta; ++c) wide[c] = pl.cta_seg[c];
+  for (size_t i = 0; i < n_segs; ++i) {
+    const DecodeSeg& sg = pl.segs[i];
+    wide[seg + 4 * i] = sg.unit;
+    wide[seg + 4 * i + 1] = sg.stage_begin;
+    wide[seg + 4 * i + 2] = sg.stage_end;
+    wide[seg + 4 * i + 3] = sg.part;
+  }
+  for (size_t u = 0; u < n_units; ++u) {
+    wide[unit + 2 * u] = pl.unit_parts[u].x;
+    wide[unit + 2 * u + 1] = pl.unit_parts[u].y;
+  }
+  for (size_t b = 0; b < B; ++b) wide[len + b] = kv_len[b];
+  return false;
 }
 
 // MLA: stages of 32 keys, one plan slot per CTA pair, partials per output half.
@@ -1374,7 +1489,7 @@ fia_status run_mla(const DecodeGeometry& g, const fia_tensor* query, const fia_t
   mp.n_units = pl.n_units;
   mp.num_heads = int(g.N1);
   mp.scale_log2 = float(params->scale_value * 1.4426950408889634);
-  mp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
+  mp.status = make_status(base);
   return cuda_check(profiled(stream, [&] { return launch_mla(mp, g.bf16, stream); }), "MLA decode launch");
 }
 
@@ -1417,19 +1532,22 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   plan_decode(g, sm_count(), pl, 128, kDecodeSegmentCost);
   const size_t rows = size_t(g.rows());
   const DecodeWsLayout w = decode_ws_layout(pl.segs.size(), size_t(pl.n_cta), size_t(pl.n_units), size_t(g.B), rows,
-                                            size_t(g.D), true);
+                                            size_t(g.D));
   st = check_ws(workspace, workspace_bytes, w.total);
   if (st != FIA_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(workspace);
 
-  DecodeParams dp;
-  memset(&dp, 0, sizeof(dp));
-  st = upload_plan(pl, g.kv_len, base, w.off_segs, w.off_cta, w.off_units, w.off_len, w.off_po, stream_t);
-  if (st != FIA_OK) return st;
-  dp.segs = reinterpret_cast<const DecodeSeg*>(base + w.off_segs);
-  dp.cta_seg = reinterpret_cast<const int32_t*>(base + w.off_cta);
-  dp.unit_parts = reinterpret_cast<const int2*>(base + w.off_units);
-  dp.kv_len = reinterpret_cast<const int32_t*>(base + w.off_len);
+  // DecodeParams carries a 6 KB plan area: kept off the stack
+  thread_local DecodeParams dp;
+  memset(&dp, 0, offsetof(DecodeParams, plan_inline));
+  thread_local std::vector<int32_t> wide;
+  if (!pack_decode_plan(pl, g.kv_len, dp, wide)) {
+    st = cuda_check(cudaMemcpyAsync(base + w.off_plan, wide.data(), wide.size() * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, stream_t),
+                    "plan upload");
+    if (st != FIA_OK) return st;
+    dp.plan_ws = reinterpret_cast<const int32_t*>(base + w.off_plan);
+  }
   if (pl.n_cta > 0) {
     uint64_t dims[2], strides[1];
     if (g.paged) {
@@ -1481,7 +1599,8 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   dp.num_kv_heads = int(g.N2);
   dp.group = int(g.N1 / g.N2);
   dp.scale_log2 = float(params->scale_value * 1.4426950408889634);
-  dp.status = DevStatus{reinterpret_cast<unsigned long long*>(base), next_epoch()};
+  dp.l2_ahead = g_decode_l2_ahead;
+  dp.status = make_status(base);
   return cuda_check(profiled(stream_t, [&] { return launch_decode(dp, int(g.D), g.bf16, stream_t); }),
                     "decode launch");
 }

@@ -63,7 +63,9 @@ struct PrefillParams {
   const BatchInfo* batches;
   const WorkItem* items;
   int n_items;
-  int prefetch_stride;            // pair kernel: item blockIdx.x + stride gets its Q warmed in L2 (0: off)
+  // pair kernel (persistent): CTA c runs items [cta_items[c], cta_items[c + 1])
+  const int32_t* cta_items;
+  int n_cta;
   int num_heads, num_kv_heads, group;
   int is_tnd;
   int causal_offset_mode;         // 2: diagonal j <= i; 3: j <= i + kv_len - q_len
@@ -86,19 +88,22 @@ struct PrefillParams {
   DevStatus status;
 };
 
-// Paged / contiguous decode (Q_S = 1).  A unit is (batch, kv head).  Every
-// unit's keys are cut into 128-token stages; the stages of all units, in unit
-// order, are dealt out to the CTAs (one per SM), so a CTA may end one unit and
-// start the next: each such piece is a "segment", and each segment leaves one
-// partial (O / l, lse) per query head of the unit.
+// Paged / contiguous decode.  A unit is (batch, kv head).  Every unit's keys
+// are cut into 128-token stages; the stages of all units, in unit order, are
+// dealt out to the CTAs (one per SM), so a CTA may end one unit and start the
+// next: each such piece is a "segment", and each segment leaves one partial
+// (O / l, lse) per query row of the unit.
 struct DecodeSeg {
   int32_t unit, stage_begin, stage_end, part;   // part = global segment index
 };
 
-// The plan (segments, per-CTA segment ranges, per-unit {first segment,
-// segment count}, kv lengths) lives in the workspace, uploaded with the call:
-// every byte of the kernel parameter block is sent with each launch, and a
-// plan carried there (~9 KB) cost ~1 us per launch.
+// The plan travels in the kernel parameters when it fits (16-bit words, so
+// the launch needs no host-to-device copy and can overlap the previous kernel);
+// larger plans are copied into the workspace as 32-bit words.  Word layout:
+// cta_seg[n_cta + 1] at 0, segments (unit, stage_begin, stage_end, part) at
+// plan_seg, unit parts (first segment, count) at plan_unit, kv lengths at
+// plan_len (inline: low / high 16-bit halves; workspace: one word each).
+constexpr int kDecodePlanInline = 3072;   // 16-bit words (6 KB)
 
 struct DecodeParams {
   CUtensorMap tm_k, tm_v;         // 2-D maps (row width in elements, rows), box (64, box_rows)
@@ -126,11 +131,11 @@ struct DecodeParams {
   int n_cta, n_units;
   int batch, num_heads, num_kv_heads, group;
   float scale_log2;
+  int l2_ahead;                   // producers warm L2 with the tiles of the stage this many ahead (0: off)
   DevStatus status;
-  const DecodeSeg* segs;
-  const int32_t* cta_seg;
-  const int2* unit_parts;         // {first segment, number of segments} of every unit
-  const int32_t* kv_len;
+  const int32_t* plan_ws;         // the plan in the workspace (32-bit words), or nullptr: plan_inline
+  int plan_seg, plan_unit, plan_len;
+  alignas(16) int16_t plan_inline[kDecodePlanInline];
 };
 
 // MLA decode (latent D = 512 shared by key and value, plus a 64-d rope part of

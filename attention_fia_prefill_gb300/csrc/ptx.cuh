@@ -2,10 +2,10 @@
 // (tiled tensor and 1-D bulk copies), and the tcgen05 tensor-core family
 // (TMEM alloc/dealloc, MMA, commit, TMEM loads/stores, fences).
 //
-// Every wait in this library is bounded by a wall-clock limit read from
-// %globaltimer: a wait that runs out records FIA_ERR_TIMEOUT in the call's
-// device status word and returns false so the caller can unwind instead of
-// spinning forever.
+// Every wait in this library is bounded by a time limit (counted in SM clock
+// cycles): a wait that runs out records FIA_ERR_TIMEOUT in the call's device
+// status word and returns false so the caller can unwind instead of spinning
+// forever.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -14,6 +14,13 @@
 namespace fia {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+// Waits are timed with the SM's cycle counter (a register read; the global
+// nanosecond timer is far slower to read and sat on every wait's path).  The
+// limits are converted at kCyclesPerNs, above the 2.07 GHz maximum SM clock,
+// so a limit never expires early.
+constexpr uint64_t kCyclesPerNs = 3;
+__device__ __forceinline__ uint64_t cycles() { return static_cast<uint64_t>(clock64()); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -93,6 +100,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 struct DevStatus {
   unsigned long long* word;
   unsigned long long epoch;
+  // Limit of the waits that can give up (the ones that unwind a CTA); the
+  // waits that let in-flight copies and products finish before a CTA exits
+  // always use kWaitLimitNs.
+  unsigned long long limit_ns = kWaitLimitNs;
 };
 
 // Tag of a call in the high half of a per-unit completion counter.  The
@@ -106,12 +117,28 @@ __device__ __forceinline__ unsigned long long unit_tag(unsigned long long epoch)
   return (unsigned long long)(x | 0x80000000u) << 32;
 }
 
+// Both are compare-and-swap loops keyed on the epoch, so they may land in
+// either order: a stamp never clears a code this call already raised, and a
+// raise replaces whatever an earlier call (or uninitialised memory) left.
 __device__ __forceinline__ void status_stamp(const DevStatus& st) {
-  if (st.word != nullptr) atomicExch(st.word, st.epoch << 8);
+  if (st.word == nullptr) return;
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(st.word);
+  while ((cur >> 8) != st.epoch) {
+    const unsigned long long prev = atomicCAS(st.word, cur, st.epoch << 8);
+    if (prev == cur) break;
+    cur = prev;
+  }
 }
 
 __device__ __forceinline__ void status_raise(const DevStatus& st, unsigned code) {
-  if (st.word != nullptr) atomicMax(st.word, (st.epoch << 8) | code);
+  if (st.word == nullptr) return;
+  const unsigned long long want = (st.epoch << 8) | code;
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(st.word);
+  while (!((cur >> 8) == st.epoch && cur >= want)) {
+    const unsigned long long prev = atomicCAS(st.word, cur, want);
+    if (prev == cur) break;
+    cur = prev;
+  }
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns false
@@ -120,17 +147,31 @@ __device__ __forceinline__ void status_raise(const DevStatus& st, unsigned code)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           const DevStatus& status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const uint64_t t0 = cycles();
+  const uint64_t limit = (abort != nullptr ? status.limit_ns : kWaitLimitNs) * kCyclesPerNs;
   while (true) {
+    // back off between polls: a waiting warp leaves the issue slots of its
+    // scheduler to the warp it shares it with
+    __nanosleep(20);
     if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (cycles() - t0 > limit) {
       if (abort != nullptr) *abort = 1;
       status_raise(status, 10u /* FIA_ERR_TIMEOUT */);
       return false;
     }
   }
 }
+
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while the
+// kernel before it on the stream is still running: grid_dep_wait() blocks until
+// that kernel has completed and its writes are visible, so every read of an
+// input and every write of an output or of the workspace comes after it.
+// grid_dep_launch() lets the next such kernel start launching (its CTAs still
+// wait for this one to complete before touching memory).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
@@ -289,6 +330,20 @@ __device__ __forceinline__ void tmem_regs_after_wait(uint32_t (&r)[32]) {
         "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
         "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
         "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+// The same for smaller register sets (4, 8 or 16 columns).
+template <int N>
+__device__ __forceinline__ void tmem_regs_after_wait_n(uint32_t (&r)[N]) {
+  static_assert(N == 4 || N == 8 || N == 16, "column count");
+  if constexpr (N == 4) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
+  } else if constexpr (N == 8) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]));
+  } else {
+    asm volatile(""
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+          "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+  }
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

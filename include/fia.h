@@ -293,10 +293,15 @@ FIA_API fia_status bsa_forward(const fia_tensor* query, const fia_tensor* key, c
  *   block_shape: {128, 256} or {128, 512} (the quantisation blocks).
  *   q_dequant_scale: fp32 (B, N1, ceil(maxQS/128), 1); k_dequant_scale and
  *          v_dequant_scale: fp32 (B, N2, ceil(maxKVS/Y), 1); device memory;
- *          positive (a scale <= 0 is taken as a tiny positive one).
+ *          every scale must be positive.  The scales are read on the device
+ *          only: a scale <= 0 (or NaN) makes the kernel record
+ *          FIA_ERR_UNSUPPORTED in the call's status word (fia_device_status),
+ *          and the output of that call is unspecified.
  *   attention_out: bf16, the query's shape.  softmax_lse as bsa_forward.
- *   The scores run on the fp8 tensor cores; P V runs in bf16 with V
- *   dequantised on chip.
+ *   The scores run on the fp8 tensor cores (e4m3 x e4m3, fp32 accumulate).
+ *   V is first rewritten into the workspace as f16 by a separate pass (one
+ *   extra read of V and a write of twice its bytes); P V then runs on the
+ *   f16 tensor-core path, with P scaled by the tile's value scale.
  * ------------------------------------------------------------------------ */
 FIA_API fia_status bsa_fp8_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,
                                       const fia_tensor* block_sparse_mask, const int64_t* block_shape,
@@ -327,6 +332,16 @@ FIA_API const char* fia_last_error(void);
  * kernel alone with cudaEventElapsedTime.  Both are cudaEvent_t created by the
  * caller (either may be NULL); the request is consumed by that one call. */
 FIA_API void fia_profile_next_call(void* start_event, void* stop_event);
+
+/* Testing aid for the device-side failure path (FIA-v2 / FIA-V5 constraints
+ * list "aicore timeout or trap" among the operator's failures): every kernel
+ * wait that can give up does so after `ns` nanoseconds instead of the default
+ * 2 s, records FIA_ERR_TIMEOUT in the call's status word (fia_device_status),
+ * lets its in-flight copies and products finish, frees its tensor memory and
+ * returns.  Applies to calls launched afterwards from any thread; 0 restores
+ * the default.  A limit far below a kernel's run time makes its calls fail:
+ * meant only for tests of that path. */
+FIA_API void fia_debug_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -149,3 +149,24 @@ def test_fp8_workload_sampled(fia):
     _assert_fp8_close(f, got, np.stack([o for o, _ in ref]))
     for (b, h, i), (_, l_ref) in zip(rows, ref):
         assert abs(float(lse[b, h, i, 0]) - l_ref) <= 1e-3 * max(1.0, abs(l_ref)), (b, h, i)
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v"])
+def test_fp8_nonpositive_scale_reported(fia, which):
+    """A dequant scale that is not positive (BSA "FP8特性说明": the scales
+    describe what each block is worth) makes the call report
+    FIA_ERR_UNSUPPORTED through the device status word; a call with valid
+    scales on the same workspace afterwards reports FIA_OK."""
+    f = fia_inputs.bsa_fp8_case(1, 2, 1, 256, 512, 256, keep=1.0, workload=3600)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device="cuda")
+    bad = {"q": f.q_scale.clone(), "k": f.k_scale.clone(), "v": f.v_scale.clone()}
+    bad[which].view(-1)[0] = -1.0 if which != "v" else 0.0
+    c = f.base
+    dev = "cuda"
+    fia.bsa_forward(c.q.to(dev), c.k.to(dev), c.v.to(dev), c.mask.to(dev), c.block_shape, num_heads=c.num_heads,
+                    num_key_value_heads=c.num_key_value_heads, scale_value=c.scale, input_layout="BNSD",
+                    workspace=ws, q_dequant_scale=bad["q"].to(dev), k_dequant_scale=bad["k"].to(dev),
+                    v_dequant_scale=bad["v"].to(dev))
+    assert fia.fia_device_status(ws) == 5
+    _run_fp8(fia, f, workspace=ws)
+    assert fia.fia_device_status(ws) == 0

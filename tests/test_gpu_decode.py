@@ -209,3 +209,65 @@ def test_query_tokens_full_workload_sampled(fia):
     for (b, h), (ro, rl) in zip(rows, ref):
         assert_out_close(out[b, h], torch.from_numpy(ro), c.q.dtype)
         assert_lse_close(lse[b, h, :, 0], torch.from_numpy(rl))
+
+
+@pytest.mark.gpu
+def test_plan_in_workspace_wide(fia):
+    """A 700-batch plan (1400 units) is larger than the kernel parameters
+    carry: it goes to the workspace as 32-bit words."""
+    rng = np.random.default_rng(78)
+    lens = [int(x) for x in rng.integers(0, 260, size=700)]
+    c = fia_inputs.paged_decode_case(len(lens), 4, 2, 128, lens, block_size=128, workload=3150)
+    _check_paged(fia, c)
+
+
+def _check_rows(fia, c, rows, mode=0):
+    out, lse = _run_paged(fia, c, sparse_mode=mode)
+    ref = fia_oracle.fia_decode(c.q, c.k_pool, c.v_pool, num_heads=c.num_heads,
+                                num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                                input_layout="BNSD", actual_seq_kvlen=c.kv_lens, block_table=c.block_table,
+                                block_size=c.block_size, sparse_mode=mode, rows=rows)
+    for (b, h), (ro, rl) in zip(rows, ref):
+        if c.q.shape[2] == 1:
+            assert_out_close(out[b, h, 0], torch.from_numpy(ro), c.q.dtype)
+            assert_lse_close(lse[b, h, 0, 0], torch.tensor(rl))
+        else:
+            assert_out_close(out[b, h], torch.from_numpy(ro), c.q.dtype)
+            assert_lse_close(lse[b, h, :, 0], torch.from_numpy(rl))
+
+
+@pytest.mark.parametrize("B,n1,n2,L,qs", [(8, 32, 8, 16384, 1), (16, 64, 1, 9000, 1), (16, 16, 1, 9000, 4)])
+def test_long_segments_chunked(fia, B, n1, n2, L, qs):
+    """Segments longer than the S^T tiles TMEM holds at once (31 stages for up
+    to 16 rows, 7 for 64): the softmax runs chunk by chunk and rescales what
+    earlier chunks of the segment accumulated.  Sampled (batch, head) rows,
+    every row of batch 0's first kv head included."""
+    c = fia_inputs.paged_decode_case(B, n1, n2, 128, [L] * B, block_size=128, workload=3500 + n1 + qs,
+                                     q_tokens=qs)
+    rng = np.random.default_rng(n1)
+    rows = [(0, h) for h in range(n1 // n2)]
+    rows += [(int(b), int(h)) for b, h in zip(rng.integers(B, size=10), rng.integers(n1, size=10))]
+    _check_rows(fia, c, rows, mode=3 if qs > 1 else 0)
+
+
+def test_device_timeout_path(fia):
+    """The device-side failure path (the pages' "aicore timeout"): with a
+    test-only wait limit of 1 ns every kernel wait that can give up does so,
+    the call's status word reads FIA_ERR_TIMEOUT, and a normal call on the
+    same stream and workspace afterwards succeeds with the right result."""
+    from attention_fia_prefill_gb300 import _binding as B
+    lib = B.load_library()
+    c = fia_inputs.paged_decode_case(4, 8, 2, 128, [3000, 2000, 4000, 100], workload=3600)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device="cuda")
+    lib.fia_debug_set_wait_limit_ns(1)
+    try:
+        _run_paged(fia, c, workspace=ws)
+        status = fia.fia_device_status(ws)
+    finally:
+        lib.fia_debug_set_wait_limit_ns(0)
+    assert status == 10, status
+    out, lse = _run_paged(fia, c, workspace=ws)
+    assert fia.fia_device_status(ws) == 0
+    ro, rl = _oracle_paged(c)
+    assert_out_close(out, ro, c.q.dtype)
+    assert_lse_close(lse, rl)
