@@ -29,7 +29,7 @@ EXPORTS = [
     "fia_prefill_mla", "fia_prefill_paged_get_workspace_size", "fia_prefill_paged", "fia_decode_get_workspace_size",
     "fia_decode", "bsa_get_workspace_size", "bsa_forward", "bsa_fp8_get_workspace_size", "bsa_forward_fp8",
     "fia_device_status", "fia_status_string",
-    "fia_last_error", "fia_profile_next_call", "fia_debug_set_wait_limit_ns", "fia_decode_no_alloc",
+    "fia_last_error", "fia_profile_next_call", "fia_debug_set_wait_limit_ns", "fia_debug_set_decode_path", "fia_decode_no_alloc",
 ]
 
 
@@ -109,6 +109,8 @@ def load_library(path: str | None = None):
     lib.fia_profile_next_call.restype = None
     lib.fia_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.fia_debug_set_wait_limit_ns.restype = None
+    lib.fia_debug_set_decode_path.argtypes = [ctypes.c_int]
+    lib.fia_debug_set_decode_path.restype = None
     lib.fia_decode_no_alloc.argtypes = [T, T, T, T, T, T, T, P, T, T, vp]
     lib.fia_decode_no_alloc.restype = st
     if path is None:

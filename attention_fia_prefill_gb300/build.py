@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libfia.so")
-SOURCES = ["fia_api.cu", "prefill.cu", "prefill_pair.cu", "bsa_fp8.cu", "decode.cu", "decode_d64.cu", "decode_noalloc.cu",
+SOURCES = ["fia_api.cu", "prefill.cu", "prefill_pair.cu", "bsa_fp8.cu", "decode.cu", "decode_d64.cu", "decode_gqa.cu", "decode_noalloc.cu",
            "mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

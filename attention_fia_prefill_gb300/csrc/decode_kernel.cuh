@@ -161,8 +161,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // in the same segment, so a slot that frees up is refilled from L2.
 //
 // ql: the K producer's Q loader -- ql.issue(si, sg) starts the global loads
-// of segment si's Q rows just before its first copy, ql.commit(si, sg) lands
-// them in their tile just after (false: give up); the V producer passes a
+// of segment si's Q rows right after its first copies, ql.commit(si, sg)
+// lands them in their tile (false: give up); the V producer passes a
 // loader that does nothing.  Returns the number of stages whose copies it
 // issued.
 template <int TileBytes, int BoxBytes, int Chunks, int NS, int FN, typename QLoader>
@@ -212,7 +212,6 @@ __device__ __forceinline__ int decode_producer(const DecodeParams& p, const Deco
       const int nbox = (nvalid + p.box_rows - 1) / p.box_rows;
       uint8_t* dst = ring + s * TileBytes;
       const bool first = st == sg.stage_begin;
-      if (first) ql.issue(si - seg_begin, sg);   // in flight beside the page lookup and the copy
       const int64_t row0 = row_of(t0);
       if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(Chunks * nbox * p.box_rows * 128));
       for (int k = 0; k < nbox; ++k) {
@@ -224,6 +223,7 @@ __device__ __forceinline__ int decode_producer(const DecodeParams& p, const Deco
                         int(row));
         }
       }
+      if (first) ql.issue(si - seg_begin, sg);   // Q's loads in flight behind the stage's copies
       // warm L2 with a later stage of this segment (pages outside the lanes'
       // cached window are skipped rather than reloaded)
       const int st2 = st + p.l2_ahead;
@@ -470,6 +470,59 @@ struct NoQLoader {
   __device__ __forceinline__ bool commit(int, const DecodeSeg&) { return true; }
 };
 
+// Units without any key (kv length 0): attention_out = 0, lse = +inf, by
+// one warp per CTA.  Spread over the CTAs: a serial walk over every unit's
+// plan entry in one CTA would hold the whole launch back.
+template <int D, bool BF16>
+__device__ __forceinline__ void write_empty_units(const DecodeParams& p, const DecodePlanRef& pl, int lane) {
+  const int g = p.rows;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+    if (pl.unit_parts(u).y != 0) continue;
+    const int kvh = u % p.num_kv_heads, b = u / p.num_kv_heads;
+    for (int hh = 0; hh < g; ++hh) {
+      const int head = kvh * p.group + hh / p.q_tokens, tok = hh % p.q_tokens;
+      if (lane < D / 4) {
+        T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
+                  int64_t(tok) * p.out_ss + 4 * lane;
+        *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+      }
+      if (lane == 0 && p.lse != nullptr)
+        p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] = INFINITY;
+    }
+  }
+}
+
+// The merge warp: after each segment's partials are out (part_done, one
+// arrival per softmax warp), bump the unit's counter; the CTA that finishes
+// a unit merges it, off the softmax warps' path.  Then writes the units
+// without any key.
+template <int D, bool BF16>
+__device__ __forceinline__ void merge_warp(const DecodeParams& p, const DecodePlanRef& pl, uint64_t* part_done,
+                                           uint64_t* part_free, volatile int* abort_flag, int seg_begin, int nseg,
+                                           int lane) {
+  const int g = p.rows;
+  bool ok = true;
+  for (int segi = 0; segi < nseg && ok; ++segi) {
+    const DecodeSeg sg = pl.seg_at(seg_begin + segi);
+    if (!warp_wait(&part_done[segi & 3], (segi >> 2) & 1, abort_flag, p.status)) {
+      ok = false;
+      break;
+    }
+    if (lane == 0) mbar_arrive(&part_free[segi & 3]);   // the slot may take segment segi + 4
+    const int2 up = pl.unit_parts(sg.unit);
+    if (up.y == 1) continue;   // written directly by the softmax warps
+    __threadfence();
+    int last = 0;
+    if (lane == 0) last = int(tagged_increment(p.unit_counter + sg.unit, unit_tag(p.status.epoch))) == up.y;
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      __threadfence();
+      merge_unit<D, BF16>(p, sg.unit, up, lane);
+    }
+  }
+  if (ok) write_empty_units<D, BF16>(p, pl, lane);
+}
+
 template <int D, bool BF16, int GL>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, GL>;
@@ -671,57 +724,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
     __syncwarp();
   } else if (warp == 7) {
     // ------------------------------------------------------------ merge warp
-    // After each segment's partials are out, bump the unit's counter; the CTA
-    // that finishes a unit merges it here, off the softmax warps' path.
-    bool ok = true;
-    for (int segi = 0; segi < nseg && ok; ++segi) {
-      const DecodeSeg sg = pl.seg_at(seg_begin + segi);
-      if (!warp_wait(&bar->part_done[segi & 3], (segi >> 2) & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) mbar_arrive(&bar->part_free[segi & 3]);   // the slot may take segment segi + 4
-      const int2 up = pl.unit_parts(sg.unit);
-      if (up.y == 1) continue;   // written directly by the softmax warps
-      __threadfence();
-      int last = 0;
-      if (lane == 0) {
-        unsigned long long* ctr = p.unit_counter + sg.unit;
-        const unsigned long long tag = unit_tag(p.status.epoch);
-        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr), nxt, prev;
-        while (true) {
-          nxt = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : (tag | 1ull);
-          prev = atomicCAS(ctr, cur, nxt);
-          if (prev == cur) break;
-          cur = prev;
-        }
-        last = int(nxt & 0xffffffffull) == up.y;
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {
-        __threadfence();
-        merge_unit<D, BF16>(p, sg.unit, up, lane);
-      }
-    }
-    // Units without any key (kv length 0): attention_out = 0, lse = +inf.
-    // Spread over the CTAs: a serial walk over every unit's plan entry in
-    // one CTA would hold the whole launch back.
-    if (ok) {
-      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-        if (pl.unit_parts(u).y != 0) continue;
-        const int kvh = u % p.num_kv_heads, b = u / p.num_kv_heads;
-        for (int hh = 0; hh < g; ++hh) {
-          const int head = kvh * p.group + hh / p.q_tokens, tok = hh % p.q_tokens;
-          if (lane < D / 4) {
-            T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
-                      int64_t(tok) * p.out_ss + 4 * lane;
-            *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
-          }
-          if (lane == 0 && p.lse != nullptr)
-            p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] = INFINITY;
-        }
-      }
-    }
+    merge_warp<D, BF16>(p, pl, bar->part_done, bar->part_free, abort_flag, seg_begin, nseg, lane);
   } else {
     // ------------------------------------------------------------ softmax
     // Thread r owns key r of each stage (row r of S^T and of P^T) and element

@@ -62,6 +62,8 @@ unsigned long long next_epoch() { return g_epoch.fetch_add(1, std::memory_order_
 // Limit of the kernels' unwinding waits (fia_debug_set_wait_limit_ns; 0: the
 // default of kWaitLimitNs).
 std::atomic<unsigned long long> g_wait_limit_ns{0};
+// fia_debug_set_decode_path: 1 runs the tensor-core decode kernel for every unit
+std::atomic<int> g_decode_force_tc{0};
 
 // A call's device status: the word at the start of its workspace, a fresh
 // epoch, and the wait limit.
@@ -869,6 +871,7 @@ void fia_profile_next_call(void* start_event, void* stop_event) {
 }
 
 void fia_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
+void fia_debug_set_decode_path(int path) { g_decode_force_tc.store(path == 1 ? 1 : 0, std::memory_order_relaxed); }
 
 fia_status fia_device_status(const void* workspace, void* stream) {
   if (workspace == nullptr) return fail(FIA_ERR_NULL, "workspace is NULL");
@@ -1548,7 +1551,7 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
     if (st != FIA_OK) return st;
     dp.plan_ws = reinterpret_cast<const int32_t*>(base + w.off_plan);
   }
-  if (pl.n_cta > 0) {
+  if (!pl.segs.empty()) {
     uint64_t dims[2], strides[1];
     if (g.paged) {
       if (g.kv_bnbd) {
@@ -1600,6 +1603,7 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   dp.group = int(g.N1 / g.N2);
   dp.scale_log2 = float(params->scale_value * 1.4426950408889634);
   dp.l2_ahead = g_decode_l2_ahead;
+  dp.force_tc = g_decode_force_tc.load(std::memory_order_relaxed);
   dp.status = make_status(base);
   return cuda_check(profiled(stream_t, [&] { return launch_decode(dp, int(g.D), g.bf16, stream_t); }),
                     "decode launch");

@@ -385,18 +385,8 @@ __global__ void __launch_bounds__(256, 1) mla_kernel(const __grid_constant__ Mla
       if (up.y == 1) continue;   // written directly by the softmax warps
       __threadfence();
       int last = 0;
-      if (lane == 0) {
-        unsigned long long* ctr = p.unit_counter + sg.unit * 2 + half;
-        const unsigned long long tag = unit_tag(p.status.epoch);
-        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr), nxt, prev;
-        while (true) {
-          nxt = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : (tag | 1ull);
-          prev = atomicCAS(ctr, cur, nxt);
-          if (prev == cur) break;
-          cur = prev;
-        }
-        last = int(nxt & 0xffffffffull) == up.y;
-      }
+      if (lane == 0)
+        last = int(tagged_increment(p.unit_counter + sg.unit * 2 + half, unit_tag(p.status.epoch))) == up.y;
       if (__shfl_sync(0xffffffffu, last, 0)) {
         __threadfence();
         mla_merge<BF16>(p, sg.unit, half, up, lane);

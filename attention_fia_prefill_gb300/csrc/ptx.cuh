@@ -117,6 +117,26 @@ __device__ __forceinline__ unsigned long long unit_tag(unsigned long long epoch)
   return (unsigned long long)(x | 0x80000000u) << 32;
 }
 
+// Increments a counter word (tag << 32) | count that belongs to the call
+// with this tag (unit_tag of its epoch) and returns the new count.  A word
+// left by an earlier call, or any other bytes, is claimed for this call by the
+// first increment that sees it (the claim sets the count to 1); every other
+// increment is one atomic add, so many CTAs bumping one word at once cost
+// one round trip each, not a compare-and-swap retry each.
+__device__ __forceinline__ unsigned tagged_increment(unsigned long long* ctr, unsigned long long tag) {
+  unsigned long long old = atomicAdd(ctr, 1ull);
+  while ((old & 0xffffffff00000000ull) != tag) {
+    const unsigned long long prev = atomicCAS(ctr, old + 1ull, tag | 1ull);
+    if (prev == old + 1ull) return 1u;
+    if ((prev & 0xffffffff00000000ull) == tag) {
+      old = atomicAdd(ctr, 1ull);
+    } else {
+      old = prev - 1ull;   // another stale increment came in between: claim from its value
+    }
+  }
+  return unsigned(old & 0xffffffffull) + 1u;
+}
+
 // Both are compare-and-swap loops keyed on the epoch, so they may land in
 // either order: a stamp never clears a code this call already raised, and a
 // raise replaces whatever an earlier call (or uninitialised memory) left.
@@ -146,20 +166,22 @@ __device__ __forceinline__ void status_raise(const DevStatus& st, unsigned code)
 // CTA has already given up (*abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           const DevStatus& status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // a non-blocking test first: the limit is checked before the first
+  // try_wait, which may itself suspend the thread for a while
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = cycles();
   const uint64_t limit = (abort != nullptr ? status.limit_ns : kWaitLimitNs) * kCyclesPerNs;
   while (true) {
-    // back off between polls: a waiting warp leaves the issue slots of its
-    // scheduler to the warp it shares it with
-    __nanosleep(20);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (abort != nullptr && *abort) return false;
     if (cycles() - t0 > limit) {
       if (abort != nullptr) *abort = 1;
       status_raise(status, 10u /* FIA_ERR_TIMEOUT */);
       return false;
     }
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    // back off between polls: a waiting warp leaves the issue slots of its
+    // scheduler to the warp it shares it with
+    __nanosleep(20);
   }
 }
 

@@ -271,3 +271,62 @@ def test_device_timeout_path(fia):
     ro, rl = _oracle_paged(c)
     assert_out_close(out, ro, c.q.dtype)
     assert_lse_close(lse, rl)
+
+
+@pytest.fixture(params=[0, 1], ids=["cuda_core", "tensor_core"])
+def decode_path(request):
+    """Both kernels that serve units of at most 4 rows (head_dim 128): the
+    CUDA-core one (the default) and the tensor-core one of larger units."""
+    from attention_fia_prefill_gb300 import _binding as B
+    lib = B.load_library()
+    lib.fia_debug_set_decode_path(request.param)
+    yield request.param
+    lib.fia_debug_set_decode_path(0)
+
+
+@pytest.mark.parametrize("n1,n2,qs,mode,bs", [(8, 2, 1, 0, 128), (4, 4, 1, 0, 16), (6, 2, 1, 0, 64),
+                                              (4, 2, 1, 0, 256), (4, 2, 2, 3, 64), (1, 1, 4, 3, 128),
+                                              (2, 1, 2, 2, 128), (3, 1, 1, 0, 16)])
+def test_small_units_both_paths(fia, decode_path, n1, n2, qs, mode, bs):
+    """Units of 1..4 rows (heads per kv head x new tokens): ragged stages,
+    empty and one-key sequences, causal token limits, each block size."""
+    lens = [1, 0, 127, 128, 129, 700, 2049, 3]
+    c = fia_inputs.paged_decode_case(len(lens), n1, n2, 128, lens, block_size=bs,
+                                     workload=3700 + 10 * n1 + n2 + qs + bs, q_tokens=qs)
+    _check_tokens(fia, c, mode)
+
+
+def test_small_units_full_workload_both_paths(fia, decode_path):
+    """The headline paged workload on both kernels: every output."""
+    _check_paged(fia, fia_inputs.workload_paged_gqa_decode())
+
+
+def test_small_units_f16_long_split(fia, decode_path):
+    """fp16, sequences long enough to be split over many CTAs (merged
+    partials), sampled rows."""
+    c = fia_inputs.paged_decode_case(8, 32, 8, 128, [16384] * 8, block_size=128, workload=3800, dtype="f16")
+    rng = np.random.default_rng(5)
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, 8, 24), rng.integers(0, 32, 24))]
+    rows += [(0, h) for h in range(4)]
+    _check_rows(fia, c, rows)
+
+
+def test_small_units_timeout_path(fia):
+    """The CUDA-core kernel's waits give up under a 1 ns limit and report
+    FIA_ERR_TIMEOUT; the next call is correct."""
+    from attention_fia_prefill_gb300 import _binding as B
+    lib = B.load_library()
+    c = fia_inputs.paged_decode_case(4, 4, 1, 128, [3000, 2000, 4000, 100], workload=3610)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device="cuda")
+    lib.fia_debug_set_wait_limit_ns(1)
+    try:
+        _run_paged(fia, c, workspace=ws)
+        status = fia.fia_device_status(ws)
+    finally:
+        lib.fia_debug_set_wait_limit_ns(0)
+    assert status == 10, status
+    out, lse = _run_paged(fia, c, workspace=ws)
+    assert fia.fia_device_status(ws) == 0
+    ro, rl = _oracle_paged(c)
+    assert_out_close(out, ro, c.q.dtype)
+    assert_lse_close(lse, rl)
