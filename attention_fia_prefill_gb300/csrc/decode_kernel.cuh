@@ -147,7 +147,7 @@ __device__ __forceinline__ DecodePlanRef decode_plan(const DecodeParams& p) {
 }
 
 // Every lane waits; true only if all of them saw the phase complete.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const DevStatus& st) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, const DevStatus st) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, st));
 }
 

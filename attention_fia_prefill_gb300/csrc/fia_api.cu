@@ -68,10 +68,8 @@ std::atomic<int> g_decode_force_tc{0};
 // A call's device status: the word at the start of its workspace, a fresh
 // epoch, and the wait limit.
 DevStatus make_status(void* workspace) {
-  DevStatus st{reinterpret_cast<unsigned long long*>(workspace), next_epoch()};
   const unsigned long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
-  if (lim != 0) st.limit_ns = lim;
-  return st;
+  return DevStatus{reinterpret_cast<unsigned long long*>(workspace), next_epoch(), lim != 0 ? lim : kWaitLimitNs};
 }
 
 // Status word for calls that launch no stamping kernel: cleared on the stream.
@@ -538,42 +536,8 @@ void build_items(const Geometry& g, int prefill_mode, int causal_mode, std::vect
   std::stable_sort(items.begin(), items.end(), [](const WorkItem& a, const WorkItem& b) { return a.cost > b.cost; });
 }
 
-constexpr int kMaxPairCtas = 256;   // persistent pair-kernel CTAs per call (one per SM)
-
 size_t prefill_ws_bytes(size_t n_batches, size_t n_items) {
-  return kHeader + align_up(n_batches * sizeof(BatchInfo), 256) + align_up(n_items * sizeof(WorkItem), 256) +
-         align_up((kMaxPairCtas + 1) * sizeof(int32_t), 256);
-}
-
-// Deals the items (in the order build_items chose) to n_cta persistent CTAs:
-// each item goes to the CTA with the least work so far (its cost in tile
-// products plus a fixed charge for the item's start and end), as the
-// hardware's block scheduler would; then the items are regrouped by CTA, each
-// CTA's in the order it received them.
-void deal_items(std::vector<WorkItem>& items, int n_cta, std::vector<int32_t>& cta_items) {
-  constexpr int64_t kItemCharge = 2;   // tile products' worth of an item's start and end
-  std::vector<std::pair<int64_t, int>> heap;   // (load, cta), a min-heap
-  heap.reserve(size_t(n_cta));
-  for (int c = 0; c < n_cta; ++c) heap.emplace_back(0, c);
-  auto cmp = [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) {
-    return a.first != b.first ? a.first > b.first : a.second > b.second;
-  };
-  std::vector<int> owner(items.size());
-  std::vector<int32_t> count(size_t(n_cta), 0);
-  for (size_t i = 0; i < items.size(); ++i) {
-    std::pop_heap(heap.begin(), heap.end(), cmp);
-    auto& top = heap.back();
-    owner[i] = top.second;
-    ++count[size_t(top.second)];
-    top.first += int64_t(items[i].cost) + kItemCharge;
-    std::push_heap(heap.begin(), heap.end(), cmp);
-  }
-  cta_items.assign(size_t(n_cta) + 1, 0);
-  for (int c = 0; c < n_cta; ++c) cta_items[size_t(c) + 1] = cta_items[size_t(c)] + count[size_t(c)];
-  std::vector<WorkItem> out(items.size());
-  std::vector<int32_t> pos(cta_items.begin(), cta_items.end() - 1);
-  for (size_t i = 0; i < items.size(); ++i) out[size_t(pos[size_t(owner[i])]++)] = items[i];
-  items.swap(out);
+  return kHeader + align_up(n_batches * sizeof(BatchInfo), 256) + align_up(n_items * sizeof(WorkItem), 256);
 }
 
 size_t count_items(const Geometry& g) {
@@ -628,23 +592,15 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   if (g.layout == L_TND) { ls[0] = 0; ls[1] = 1; ls[2] = g.N1; }
   else { ls[0] = g.N1 * g.S1; ls[1] = g.S1; ls[2] = 1; }
 
-  // the two-tile kernel is persistent: deal its items to one CTA per SM
-  const bool pair = !g.fp8 && mode != kBlockSparse;
-  std::vector<int32_t> cta_items;
-  const int n_cta = pair ? int(std::min<size_t>(items.size(), size_t(std::min(sm_count(), kMaxPairCtas)))) : 0;
-  if (pair && n_cta > 0) deal_items(items, n_cta, cta_items);
   // upload the plan
   std::vector<uint8_t> plan(plan_bytes - kHeader, 0);
   const size_t off_items = align_up(g.batches.size() * sizeof(BatchInfo), 256);
-  const size_t off_cta = off_items + align_up(items.size() * sizeof(WorkItem), 256);
   memcpy(plan.data(), g.batches.data(), g.batches.size() * sizeof(BatchInfo));
   if (!items.empty()) memcpy(plan.data() + off_items, items.data(), items.size() * sizeof(WorkItem));
-  if (!cta_items.empty()) memcpy(plan.data() + off_cta, cta_items.data(), cta_items.size() * sizeof(int32_t));
   st = cuda_check(cudaMemcpyAsync(base + kHeader, plan.data(), plan.size(), cudaMemcpyHostToDevice, stream), "plan upload");
   if (st != FIA_OK) return st;
   const BatchInfo* d_batches = reinterpret_cast<const BatchInfo*>(base + kHeader);
   const WorkItem* d_items = reinterpret_cast<const WorkItem*>(base + kHeader + off_items);
-  const int32_t* d_cta_items = reinterpret_cast<const int32_t*>(base + kHeader + off_cta);
 
   // rows that no CTA writes: padding rows of the padded layouts
   if (g.layout != L_TND) {
@@ -719,8 +675,7 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.batches = d_batches;
   pp.items = d_items;
   pp.n_items = int(items.size());
-  pp.cta_items = d_cta_items;
-  pp.n_cta = n_cta;
+  pp.prefetch_stride = sm_count();
   pp.num_heads = int(g.N1);
   pp.num_kv_heads = int(g.N2);
   pp.group = int(g.N1 / g.N2);

@@ -63,9 +63,7 @@ struct PrefillParams {
   const BatchInfo* batches;
   const WorkItem* items;
   int n_items;
-  // pair kernel (persistent): CTA c runs items [cta_items[c], cta_items[c + 1])
-  const int32_t* cta_items;
-  int n_cta;
+  int prefetch_stride;            // pair kernel: item blockIdx.x + stride gets its Q warmed in L2 (0: off)
   int num_heads, num_kv_heads, group;
   int is_tnd;
   int causal_offset_mode;         // 2: diagonal j <= i; 3: j <= i + kv_len - q_len

@@ -7,20 +7,15 @@
 // causal modes 2 / 3 and the band mode 4 computed from indices, or an explicit
 // atten_mask (sparse_mode 0 with a mask, 1) read from memory.
 //
-// A work item is 256 query rows of one (batch, query head): tile A (rows
+// One CTA owns 256 query rows of one (batch, query head): tile A (rows
 // q0..q0+127) and tile B (q0+128..q0+255).  Both read every K/V tile the CTA
 // loads, and the tensor core alternates between them: while warpgroup A
 // exponentiates S_A(j), the MMA warp runs P_B(j-1) V and Q_B K(j)^T, and the
 // other way round, so the softmax of one tile hides behind the products of the
 // other (one tile alone leaves the tensor core idle while its softmax runs).
-// The grid is persistent: one CTA per SM runs the items the host dealt it
-// (longest first, each to the CTA with the least work so far), and the end of
-// one item overlaps the start of the next -- its Q and K/V tiles load while the
-// current item finishes, its first Q K^T runs during the current epilogue.
-//   warp 0      TMA producer: per item Q_A and Q_B (each once its tile's
-//               products of the previous item are done), K and V tiles
-//               through rings of their own; it warms L2 with the Q of its next
-//               item
+//   warp 0      TMA producer: Q_A and Q_B once, K and V tiles through rings
+//               of their own; after the first tile it warms L2 with the Q of
+//               the item that will take this CTA's SM about one item later
 //   warp 1      MMA issuer (one thread) and TMEM owner, in the order
 //                 P_A(j) V, Q_A K(j+1)^T, P_B(j) V, Q_B K(j+1)^T
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one thread
@@ -29,8 +24,7 @@
 //               by more than 2^8, epilogue O / l and LSE.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+DV), O_B [256+DV,
 // 256+2DV).  Causal: tile B needs the K/V tiles of tile A plus at most one; the
-// CTA walks tile B's range and tile A stops early.  A tile with no key tile
-// at all (no keys for its rows) is inactive: no loads or products, zeros out.
+// CTA walks tile B's range and tile A stops early.
 // Paged K/V (chunked prefill against a block table): the producer takes each
 // 128-key tile from its block (block_size is a multiple of 128).
 // Explicit mask: each softmax thread copies its row's 128 mask bytes for the
@@ -44,7 +38,8 @@ namespace fia {
 namespace {
 
 // DQK: head dim of the scores (Q and K; 192 = MLA's 128 + 64 rope columns),
-// DV: head dim of V and O.  K and V have rings of their own.
+// DV: head dim of V and O.  K and V have rings of their own: a K stage is free
+// once its last Q K^T is done, a V stage once its last P V is.
 template <int DQK, int DV>
 struct PairCfg {
   static constexpr int kChunksQK = DQK / 64;
@@ -80,58 +75,6 @@ __device__ __forceinline__ int tiles_for_rows(const BatchInfo& bi, int qa, int m
   return maxkey >= 0 ? maxkey / kTileN + 1 : 0;
 }
 
-// Geometry of one work item, computed alike by every role.
-struct PairItem {
-  WorkItem it;
-  BatchInfo bi;
-  int q0, kvh, diag_off;
-  int na, nb, nl;     // key tiles of tile A, of tile B (0: inactive), loaded by the CTA
-  int jt0;            // first key tile (band / explicit mask)
-  int64_t band_d;
-};
-
-template <int MODE>
-__device__ __forceinline__ PairItem pair_item(const PrefillParams& p, int idx) {
-  PairItem g;
-  g.it = p.items[idx];
-  g.bi = p.batches[g.it.b];
-  const BatchInfo& bi = g.bi;
-  g.q0 = g.it.q_tile * 2 * kTileM;
-  g.kvh = g.it.h / p.group;
-  g.diag_off = (MODE == kCausal && p.causal_offset_mode == 3) ? (bi.kv_len - bi.q_len) : 0;
-  g.na = tiles_for_rows(bi, g.q0, MODE, g.diag_off);
-  // Tile B walks at least tile A's range (its rows past the batch are computed
-  // but not written); a pair whose tile B starts past the batch runs tile A
-  // alone.  nl = tiles the CTA loads.
-  const bool has_b = g.q0 + kTileM < bi.q_len;
-  g.nb = has_b ? max(g.na, tiles_for_rows(bi, g.q0 + kTileM, MODE, g.diag_off)) : 0;
-  // sparse_mode 4 (band) and the explicit mask (band i - pre .. i + next): both
-  // tiles walk the K/V tiles of the union of their rows' bands, from tile jt0
-  // on; the softmax masks each row's edges.
-  g.jt0 = 0;
-  g.band_d = MODE == kBand ? int64_t(bi.kv_len) - bi.q_len : 0;
-  if (MODE == kBand || MODE == kMask) {
-    const int64_t last = min(g.q0 + 2 * kTileM - 1, bi.q_len - 1);
-    const int64_t lo = max(int64_t(0), g.q0 + g.band_d - p.band_pre);
-    const int64_t hi = min(int64_t(bi.kv_len) - 1, last + g.band_d + p.band_next);
-    const int n = hi < lo ? 0 : int(hi / kTileN - lo / kTileN + 1);
-    g.jt0 = hi < lo ? 0 : int(lo / kTileN);
-    // tile A's rows end earlier: it stops after its own last key's tile
-    const int64_t last_a = min(g.q0 + kTileM - 1, bi.q_len - 1);
-    const int64_t hi_a = min(int64_t(bi.kv_len) - 1, last_a + g.band_d + p.band_next);
-    g.na = (hi < lo || hi_a < lo) ? 0 : int(hi_a / kTileN - lo / kTileN + 1);
-    g.nb = has_b ? n : 0;
-  }
-  g.nl = max(g.na, g.nb);
-  return g;
-}
-
-// Arrivals a K/V stage release barrier takes per stage: one per tile that
-// reads the stage; a stage only one tile reads gets both from that tile.
-__device__ __forceinline__ void arrive_n(uint64_t* bar, uint32_t n) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
-}
-
 template <int DQK, int DV, bool BF16, int MODE>
 __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_constant__ PrefillParams p) {
   using C = PairCfg<DQK, DV>;
@@ -139,50 +82,73 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  // q_full[t]: Q_t of the tile's current item landed; q_free[t]: the item's
-  // last Q_t K^T is done (the softmax of tile t saw its last S)
-  uint64_t* q_full = bars + 0;     // [2]
-  uint64_t* q_free = bars + 2;     // [2]
-  uint64_t* k_full = bars + 4;     // [KS]
-  uint64_t* v_full = bars + 7;     // [VS]
-  // k_free / v_free[s]: both tiles are done with the K (V) tile of stage s:
-  // two arrivals from the softmax warpgroups (a stage one tile reads gets both
-  // from it) -- after its S is in for K, after its P V is done for V
-  uint64_t* k_free = bars + 10;    // [KS]
-  uint64_t* v_free = bars + 13;    // [VS]
-  // s_ready[t]: S_t of the tile's next product is in TMEM (one Q K^T in
-  // flight per tile: S_t is reused only after P_t V); pv_done[t]: a P_t V
-  // product finished (the epilogue waits for the item's last)
-  uint64_t* s_ready = bars + 16;   // [2]
-  uint64_t* pv_done = bars + 18;   // [2]
-  uint64_t* pa_full = bars + 20;   // [2] by the tile's P count parity: warpgroup A's P is in (4 warp arrivals)
-  uint64_t* pb_full = bars + 22;   // [2]
-  uint64_t* o_free = bars + 24;    // [2] the epilogue of tile t read O_t (4 warp arrivals)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 26);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 27);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;     // [KS]
+  uint64_t* v_full = bars + 4;     // [VS]
+  // v_free[s]: P_B V of the tile in V stage s is done (one commit per MMA
+  // group): the stage is free, and O_B holds it.
+  uint64_t* v_free = bars + 7;     // [VS]
+  // s_full[3 t + s]: S_t of the tile in K stage s is in TMEM.  The last one of
+  // a tile (S_B, or S_A when the pair has no tile B) also frees the K stage.
+  uint64_t* s_full = bars + 10;    // [2][3]
+  uint64_t* pa_full = bars + 16;   // [2] by tile parity: warpgroup A's P is in (4 warp arrivals)
+  uint64_t* pb_full = bars + 18;   // [2]
+  // pva_done: tile A's last P V is done (its epilogue may read O_A).  Earlier
+  // P_A V products need no commit of their own: each is followed on the
+  // tensor pipe by a Q K^T whose commit covers it.
+  uint64_t* pva_done = bars + 20;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 22);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i_begin = p.cta_items[blockIdx.x], i_end = p.cta_items[blockIdx.x + 1];
+  const WorkItem it = p.items[blockIdx.x];
+  const BatchInfo bi = p.batches[it.b];
+  const int q0 = it.q_tile * 2 * kTileM;
+  const int kvh = it.h / p.group;
+  const int diag_off = (MODE == kCausal && p.causal_offset_mode == 3) ? (bi.kv_len - bi.q_len) : 0;
+  int na = tiles_for_rows(bi, q0, MODE, diag_off);
+  // Tile B walks at least tile A's range (its rows past the batch are computed
+  // but not written); a pair whose tile B starts past the batch runs tile A
+  // alone.  nl = tiles the CTA loads; the last tile product of each K/V tile
+  // (tile B's when it has rows, else tile A's) releases the stage.
+  const bool has_b = q0 + kTileM < bi.q_len;
+  int nb = has_b ? max(na, tiles_for_rows(bi, q0 + kTileM, MODE, diag_off)) : 0;
+  // sparse_mode 4 (band) and the explicit mask (band i - pre .. i + next): both
+  // tiles walk the K/V tiles of the union of their rows' bands, from tile jt0
+  // on; the softmax masks each row's edges.
+  int jt0 = 0;
+  const int64_t band_d = MODE == kBand ? int64_t(bi.kv_len) - bi.q_len : 0;
+  if (MODE == kBand || MODE == kMask) {
+    const int64_t last = min(q0 + 2 * kTileM - 1, bi.q_len - 1);
+    const int64_t lo = max(int64_t(0), q0 + band_d - p.band_pre);
+    const int64_t hi = min(int64_t(bi.kv_len) - 1, last + band_d + p.band_next);
+    const int n = hi < lo ? 0 : int(hi / kTileN - lo / kTileN + 1);
+    jt0 = hi < lo ? 0 : int(lo / kTileN);
+    // tile A's rows end earlier: it stops after its own last key's tile
+    const int64_t last_a = min(q0 + kTileM - 1, bi.q_len - 1);
+    const int64_t hi_a = min(int64_t(bi.kv_len) - 1, last_a + band_d + p.band_next);
+    na = (hi < lo || hi_a < lo) ? 0 : int(hi_a / kTileN - lo / kTileN + 1);
+    nb = has_b ? n : 0;
+  }
+  const int nl = max(na, nb);
 
   if (threadIdx.x == 0) {
     if (blockIdx.x == 0) status_stamp(p.status);
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&q_full[t], 1);
-      mbar_init(&q_free[t], 1);
-      mbar_init(&s_ready[t], 1);
-      mbar_init(&pv_done[t], 1);
-      mbar_init(&pa_full[t], 4);
-      mbar_init(&pb_full[t], 4);
-      mbar_init(&o_free[t], 4);
-    }
+    mbar_init(q_full, 1);
     for (int s = 0; s < KS; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_free[s], 2);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_full[3 + s], 1);
     }
     for (int s = 0; s < VS; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_free[s], 2);
+      mbar_init(&v_free[s], 1);
     }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&pa_full[t], 4);
+      mbar_init(&pb_full[t], 4);
+    }
+    mbar_init(pva_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -194,7 +160,11 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+
   const bool is_tnd = p.is_tnd != 0;
+  const int q_row0 = is_tnd ? bi.q_start + q0 : q0;
+  const int kv_row0 = is_tnd && p.block_table == nullptr ? bi.kv_start : 0;
+  const int b_coord = is_tnd ? 0 : it.b;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -209,82 +179,68 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         col = c < 2 ? c * 64 : p.rope_col;
         return c < 2 ? m : mr;
       };
-      auto q_rows = [&](const PairItem& g, int& row0, int& bc) {
-        row0 = is_tnd ? g.bi.q_start + g.q0 : g.q0;
-        bc = is_tnd ? 0 : g.it.b;
-      };
-      int gs = 0;              // K/V stages loaded so far (all items): their ring slots and phases
-      int nq[2] = {0, 0};      // Q tiles loaded so far, per tile
-      int nk = 0, nv = 0;      // copies issued (for the drain after an abort)
-      bool ok = true;
-      for (int idx = i_begin; idx < i_end && ok; ++idx) {
-        const PairItem g = pair_item<MODE>(p, idx);
-        int q_row0, b_coord;
-        q_rows(g, q_row0, b_coord);
-        const int kv_row0 = is_tnd && p.block_table == nullptr ? g.bi.kv_start : 0;
-        // Q of each active tile, once the tile's previous item is done with it
-        for (int t = 0; t < 2 && ok; ++t) {
-          if ((t == 0 ? g.na : g.nb) == 0) continue;
-          if (nq[t] > 0 && !mbar_wait(&q_free[t], (nq[t] - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&q_full[t], C::kTileQK);
+      mbar_arrive_expect_tx(q_full, 2 * C::kTileQK);
 #pragma unroll
-          for (int c = 0; c < C::kChunksQK; ++c) {
-            int col;
-            const CUtensorMap* m = qk_src(c, &p.tm_q, &p.tm_qr, col);
-            tma_load_4d(smem + C::kOffQ + t * C::kTileQK + c * C::kBoxBytes, m, &q_full[t], col, q_row0 + t * kTileM,
-                        g.it.h, b_coord);
-          }
-          ++nq[t];
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < C::kChunksQK; ++c) {
+          int col;
+          const CUtensorMap* m = qk_src(c, &p.tm_q, &p.tm_qr, col);
+          tma_load_4d(smem + C::kOffQ + t * C::kTileQK + c * C::kBoxBytes, m, q_full, col, q_row0 + t * kTileM, it.h,
+                      b_coord);
         }
-        for (int j = 0; j < g.nl && ok; ++j) {
-          const int gj = gs + j;
-          const int sk = gj % KS, sv = gj % VS;
-          // K/V tile coordinates: (row, batch) of a contiguous tensor, or (row in
-          // block, block id) of a paged pool (the table read overlaps the wait)
-          const int key = (g.jt0 + j) * kTileN;
-          int kv_r = kv_row0 + key, kv_b = b_coord;
-          if (p.block_table != nullptr) {
-            kv_b = __ldg(p.block_table + int64_t(g.it.b) * p.table_stride + key / p.block_size);
-            kv_r = key % p.block_size;
-          }
-          if (gj >= KS && !mbar_wait(&k_free[sk], ((gj / KS) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-          uint8_t* ks = smem + C::kOffK + sk * C::kTileQK;
-          mbar_arrive_expect_tx(&k_full[sk], C::kTileQK);
-#pragma unroll
-          for (int c = 0; c < C::kChunksQK; ++c) {
-            int col;
-            const CUtensorMap* m = qk_src(c, &p.tm_k, &p.tm_kr, col);
-            tma_load_4d(ks + c * C::kBoxBytes, m, &k_full[sk], col, kv_r, g.kvh, kv_b);
-          }
-          nk = gj + 1;
-          if (gj >= VS && !mbar_wait(&v_free[sv], ((gj / VS) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-          uint8_t* vs = smem + C::kOffV + sv * C::kTileV;
-          mbar_arrive_expect_tx(&v_full[sv], C::kTileV);
-#pragma unroll
-          for (int c = 0; c < C::kChunksV; ++c)
-            tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[sv], c * 64, kv_r, g.kvh, kv_b);
-          nv = gj + 1;
-          if (j == 0 && idx + 1 < i_end) {
-            // Q of this CTA's next item into L2, so its loads do not wait on HBM
-            const PairItem nx = pair_item<MODE>(p, idx + 1);
-            int nrow, nbc;
-            q_rows(nx, nrow, nbc);
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-              for (int c = 0; c < C::kChunksQK; ++c) {
-                int col;
-                const CUtensorMap* m = qk_src(c, &p.tm_q, &p.tm_qr, col);
-                tma_prefetch_l2_4d(m, col, nrow + t * kTileM, nx.it.h, nbc);
-              }
-          }
+      // the Q K^T that frees a K stage: tile B's, or tile A's without a tile B
+      uint64_t* k_rel = s_full + (nb > 0 ? 3 : 0);
+      int j = 0, nk = 0, nv = 0;   // tiles loaded; K and V loads issued
+      for (; j < nl; ++j) {
+        const int sk = j % KS, sv = j % VS;
+        // K/V tile coordinates: (row, batch) of a contiguous tensor, or (row in
+        // block, block id) of a paged pool (the table read overlaps the wait)
+        const int key = (jt0 + j) * kTileN;
+        int kv_r = kv_row0 + key, kv_b = b_coord;
+        if (p.block_table != nullptr) {
+          kv_b = __ldg(p.block_table + int64_t(it.b) * p.table_stride + key / p.block_size);
+          kv_r = key % p.block_size;
         }
-        gs += g.nl;
+        if (j >= KS && !mbar_wait(&k_rel[sk], ((j / KS) - 1) & 1, abort_flag, p.status)) break;
+        uint8_t* ks = smem + C::kOffK + sk * C::kTileQK;
+        mbar_arrive_expect_tx(&k_full[sk], C::kTileQK);
+#pragma unroll
+        for (int c = 0; c < C::kChunksQK; ++c) {
+          int col;
+          const CUtensorMap* m = qk_src(c, &p.tm_k, &p.tm_kr, col);
+          tma_load_4d(ks + c * C::kBoxBytes, m, &k_full[sk], col, kv_r, kvh, kv_b);
+        }
+        nk = j + 1;
+        if (j >= VS && !mbar_wait(&v_free[sv], ((j / VS) - 1) & 1, abort_flag, p.status)) break;
+        uint8_t* vs = smem + C::kOffV + sv * C::kTileV;
+        mbar_arrive_expect_tx(&v_full[sv], C::kTileV);
+#pragma unroll
+        for (int c = 0; c < C::kChunksV; ++c)
+          tma_load_4d(vs + c * C::kBoxBytes, &p.tm_v, &v_full[sv], c * 64, kv_r, kvh, kv_b);
+        nv = j + 1;
+        if (j == 0 && p.prefetch_stride > 0 && int(blockIdx.x) + p.prefetch_stride < p.n_items) {
+          // Q of the item that takes this CTA's place about one item from now
+          // (CTAs start in index order, one per SM): into L2, so its first
+          // loads do not wait on HBM
+          const WorkItem nx = p.items[blockIdx.x + p.prefetch_stride];
+          const BatchInfo nb_info = p.batches[nx.b];
+          const int nq0 = nx.q_tile * 2 * kTileM;
+          const int nrow = is_tnd ? nb_info.q_start + nq0 : nq0;
+          const int nbc = is_tnd ? 0 : nx.b;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int c = 0; c < C::kChunksQK; ++c) {
+              int col;
+              const CUtensorMap* m = qk_src(c, &p.tm_q, &p.tm_qr, col);
+              tma_prefetch_l2_4d(m, col, nrow + t * kTileM, nx.h, nbc);
+            }
+        }
       }
       if (*abort_flag) {
         // let every copy in flight land before the CTA exits
-        for (int t = 0; t < 2; ++t)
-          if (nq[t] > 0) mbar_wait(&q_full[t], (nq[t] - 1) & 1, nullptr, p.status);
+        mbar_wait(q_full, 0, nullptr, p.status);
         for (int s = 0; s < KS && s < nk; ++s) {
           const int last = nk - 1 - ((nk - 1 - s) % KS);
           mbar_wait(&k_full[s], (last / KS) & 1, nullptr, p.status);
@@ -311,78 +267,65 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       constexpr uint64_t kStepK = C::kTileQK >> 4, kStepV = C::kTileV >> 4;
       uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
       uint32_t last_parity = 0;
-      int gs = 0;                     // K/V stages before this item (all items)
-      int nq[2] = {0, 0};             // active items so far, per tile (Q loads, epilogues)
-      int cp[2] = {0, 0};             // P V products so far, per tile
-      bool ok = true;
-      for (int idx = i_begin; idx < i_end && ok; ++idx) {
-        const PairItem g = pair_item<MODE>(p, idx);
-        const int na = g.na, nb = g.nb;
-        // S_t = Q_t K(j)^T.  A K/V stage is waited for once, by the first
-        // product that reads it (tile A's, unless the tile is past tile A's range).
-        auto qk = [&](int t, int j) -> bool {
-          const int gj = gs + j;
-          const int s = gj % KS;
-          if ((t == 0 || j >= na) && !mbar_wait(&k_full[s], (gj / KS) & 1, abort_flag, p.status)) return false;
-          tc_fence_after();
-          const uint64_t qd = t == 0 ? qd0 : qd1;
-          const uint64_t kd = kd0 + uint64_t(s) * kStepK;
-          const uint32_t dst = tmem + t * 128;
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      // A K/V stage is waited for once, by the first product that reads it
+      // (tile A's, unless the tile is past tile A's range).
+      // S_t = Q_t K(j)^T
+      auto qk = [&](int t, int j) -> bool {
+        const int s = j % KS;
+        if ((t == 0 || j >= na) && !mbar_wait(&k_full[s], (j / KS) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint64_t qd = t == 0 ? qd0 : qd1;
+        const uint64_t kd = kd0 + uint64_t(s) * kStepK;
+        const uint32_t dst = tmem + t * 128;
 #pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk) {
-            const uint64_t off = uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-            mma_ss(dst, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s_ready[t]);
-          last_bar = &s_ready[t];
-          last_parity = 0;   // set below by the caller's count
-          return true;
-        };
-        // O_t += P_t(j) V(j): P read from tile t's S columns in TMEM; V is
-        // [keys x DV], an MN-major operand (16 keys = 2048 bytes per K-step, the
-        // next 64 columns of DV one box further).  The item's first product
-        // overwrites O_t: the previous item's epilogue must have read it.
-        auto pv = [&](int t, int j) -> bool {
-          const int gj = gs + j;
-          const int s = gj % VS;
-          if (!mbar_wait(t == 0 ? &pa_full[cp[t] & 1] : &pb_full[cp[t] & 1], (cp[t] >> 1) & 1, abort_flag, p.status))
-            return false;
-          if ((t == 0 || j >= na) && !mbar_wait(&v_full[s], (gj / VS) & 1, abort_flag, p.status)) return false;
-          if (j == 0 && nq[t] > 1 && !mbar_wait(&o_free[t], (nq[t] - 2) & 1, abort_flag, p.status)) return false;
-          tc_fence_after();
-          const uint64_t vd = vd0 + uint64_t(s) * kStepV;
-          const uint32_t dst = tmem + C::kColO + t * DV;
-          const uint32_t pt = tmem + t * 128;
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint64_t off = uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
+          mma_ss(dst, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[3 * t + s]);
+        last_bar = &s_full[3 * t + s];
+        last_parity = (j / KS) & 1;
+        return true;
+      };
+      // O_t += P_t(j) V(j): P read from tile t's S columns in TMEM; V is
+      // [keys x DV], an MN-major operand (16 keys = 2048 bytes per K-step, the
+      // next 64 columns of DV one box further)
+      auto pv = [&](int t, int j) -> bool {
+        const int s = j % VS;
+        if (!mbar_wait(t == 0 ? &pa_full[j & 1] : &pb_full[j & 1], (j >> 1) & 1, abort_flag, p.status)) return false;
+        if ((t == 0 || j >= na) && !mbar_wait(&v_full[s], (j / VS) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint64_t vd = vd0 + uint64_t(s) * kStepV;
+        const uint32_t dst = tmem + C::kColO + t * DV;
+        const uint32_t pt = tmem + t * 128;
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ts(dst, pt + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&pv_done[t]);
-          last_bar = &pv_done[t];
-          last_parity = cp[t] & 1;
-          ++cp[t];
-          return true;
-        };
-        // Q of each active tile (every load is waited for, in order)
-        for (int t = 0; t < 2 && ok; ++t) {
-          if ((t == 0 ? na : nb) == 0) continue;
-          ok = mbar_wait(&q_full[t], nq[t] & 1, abort_flag, p.status);
-          ++nq[t];
-        }
-        // the S count parity of each commit: s_ready[t] completes once per
-        // Q_t K^T, i.e. once per P_t V that follows it
-        if (ok && na > 0) { ok = qk(0, 0); last_parity = cp[0] & 1; }
-        if (ok && nb > 0) { ok = qk(1, 0); last_parity = cp[1] & 1; }
-        for (int j = 0; j < g.nl && ok; ++j) {
-          if (j < na) {
-            ok = pv(0, j);
-            if (ok && j + 1 < na) { ok = qk(0, j + 1); last_parity = cp[0] & 1; }
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts(dst, pt + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        if (t == 0 && nb > 0) {
+          if (j == na - 1) {
+            mma_commit(pva_done);
+            last_bar = pva_done;
+            last_parity = 0;
           }
-          if (ok && j < nb) {
-            ok = pv(1, j);
-            if (ok && j + 1 < nb) { ok = qk(1, j + 1); last_parity = cp[1] & 1; }
-          }
+        } else {
+          mma_commit(&v_free[s]);
+          last_bar = &v_free[s];
+          last_parity = (j / VS) & 1;
         }
-        gs += g.nl;
+        return true;
+      };
+      if (ok && na > 0) ok = qk(0, 0);
+      if (ok && nb > 0) ok = qk(1, 0);
+      for (int j = 0; j < nl && ok; ++j) {
+        if (j < na) {
+          ok = pv(0, j);
+          if (ok && j + 1 < na) ok = qk(0, j + 1);
+        }
+        if (ok && j < nb) {
+          ok = pv(1, j);
+          if (ok && j + 1 < nb) ok = qk(1, j + 1);
+        }
       }
       // Every MMA issued has finished before TMEM goes: the latest commit
       // tracks them all (the one before it on the same barrier has completed).
@@ -395,21 +338,12 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
     const uint32_t col_s = t * 128;
     const uint32_t col_o = C::kColO + t * DV;
+    const int n = t == 0 ? na : nb;
+    const int tile_q0 = q0 + t * kTileM;
+    const int i = tile_q0 + r;
+    const int diag = i + diag_off;
     const float sl2 = p.scale_log2;
     uint64_t* my_pfull = t == 0 ? pa_full : pb_full;
-    int gs = 0;            // K/V stages before this item (all items)
-    int cp = 0;            // P tiles written so far (all items): s_ready / p_full / pv_done phases
-    bool ok = true;
-    for (int idx = i_begin; idx < i_end && ok; ++idx) {
-      const PairItem pi = pair_item<MODE>(p, idx);
-      const WorkItem it = pi.it;
-      const BatchInfo bi = pi.bi;
-      const int q0 = pi.q0, na = pi.na, nb = pi.nb, jt0 = pi.jt0, diag_off = pi.diag_off;
-      const int64_t band_d = pi.band_d;
-      const int n = t == 0 ? na : nb;
-      const int tile_q0 = q0 + t * kTileM;
-      const int i = tile_q0 + r;
-      const int diag = i + diag_off;
     // explicit mask: this row's bytes of K/V tile jj into the thread's slot
     const bool mrow = MODE == kMask && i < bi.q_len;
     const uint8_t* mask_row = MODE == kMask ? p.attn_mask + int64_t(it.b) * p.mask_sb + int64_t(i) * p.mask_ss : nullptr;
@@ -445,7 +379,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     // Rows of V past the batch's keys may hold anything (even NaN); P is 0
     // there but 0 * NaN is not, so they are cleared before the first P V that
     // reads tile jj: tile A's if it uses the tile, else tile B's.
-    auto clear_v_tail = [&](int jj, int kv0j) -> bool {   // jj: the stage (all items) of the tile
+    auto clear_v_tail = [&](int jj, int kv0j) -> bool {
       const int s = jj % VS;
       if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (jj / VS) & 1, abort_flag, p.status))) return false;
       if (r >= bi.kv_len - kv0j) {
@@ -460,8 +394,8 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       return true;
     };
     float m = -INFINITY, l = 0.f;
+    bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const int gj = gs + j;
       // mb: bit c of mb[c >> 5] set when atten_mask masks key kv0 + c
       uint32_t mb[4] = {0u, 0u, 0u, 0u};
       if (mrow) {
@@ -477,17 +411,9 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         // the slot is read (mb depends on every byte): refill it with the next tile
         if (j + 1 < n) mask_fetch(j + 1);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_ready[t], cp & 1, abort_flag, p.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[3 * t + j % KS], (j / KS) & 1, abort_flag, p.status))) {
         ok = false;
         break;
-      }
-      // S_t(j) in: K(j) no longer read by this tile, and P_t(j-1) V (before
-      // this Q K^T on the pipe) finished: V(j-1) no longer read either
-      if (r == 0) {
-        const bool both = j < na && j < nb;
-        arrive_n(&k_free[gj % KS], both ? 1u : 2u);
-        if (j > 0) arrive_n(&v_free[(gj - 1) % VS], (j - 1 < na && j - 1 < nb) ? 1u : 2u);
-        if (j == n - 1) mbar_arrive(&q_free[t]);   // the item's last Q_t K^T is done
       }
       tc_fence_after();
       if (MODE == kMask && __all_sync(0xffffffffu, (mb[0] & mb[1] & mb[2] & mb[3]) == 0xffffffffu)) {
@@ -500,14 +426,13 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_st16(tmem + lane_off + col_s + c * 16, z);
         const int kv0 = (jt0 + j) * kTileN;
-        if (kv0 + kTileN > bi.kv_len && (t == 0 || j >= na) && !clear_v_tail(gj, kv0)) {
+        if (kv0 + kTileN > bi.kv_len && (t == 0 || j >= na) && !clear_v_tail(j, kv0)) {
           ok = false;
           break;
         }
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(&my_pfull[cp & 1]);
-        ++cp;
+        warp_arrive(&my_pfull[j & 1]);
         continue;
       }
       // S in two halves: the second half's load is in flight while the
@@ -610,29 +535,27 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
           tmem_st16(tmem + lane_off + col_o + c * 16, u);
         }
       }
-      if (ragged && (t == 0 || j >= na) && !clear_v_tail(gj, kv0)) {
+      if (ragged && (t == 0 || j >= na) && !clear_v_tail(j, kv0)) {
         ok = false;
         break;
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(&my_pfull[cp & 1]);
-      ++cp;
+      warp_arrive(&my_pfull[j & 1]);
       m = m_use;
     }
     if (MODE == kMask) cp_async_wait_all();   // no copy into the slot outlives the loop
     // ------------------------------------------------------------ epilogue
-    // the item's last P_t V: then V(last) is free and O_t complete; O / l is
-    // read and stored 32 columns at a time (the stores do not wait), after
-    // which O_t may take the next item's first P_t V
-    const bool has = l > 0.f;
     if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (cp - 1) & 1, abort_flag, p.status));
+      const int jl = n - 1;
+      ok = __all_sync(0xffffffffu, (t == 0 && nb > 0)
+                                       ? mbar_wait(pva_done, 0, abort_flag, p.status)
+                                       : mbar_wait(&v_free[jl % VS], (jl / VS) & 1, abort_flag, p.status));
       tc_fence_after();
-      if (ok && r == 0) arrive_n(&v_free[(gs + n - 1) % VS], (n - 1 < na && n - 1 < nb) ? 1u : 2u);
     }
     if (ok) {
       const bool row_valid = i < bi.q_len;
+      const bool has = l > 0.f;
       const float inv_l = has ? 1.f / l : 0.f;
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* orow = reinterpret_cast<T*>(p.out) + (is_tnd ? int64_t(bi.q_start + i) * p.out_ss
@@ -661,11 +584,6 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
           }
         }
       }
-      if (n > 0) {
-        // O_t read: the next item's first P_t V may overwrite it
-        tc_fence_before();
-        warp_arrive(&o_free[t]);
-      }
       if (row_valid && p.lse != nullptr) {
         const float lse = has ? (m + __log2f(l)) * 0.69314718055994531f : INFINITY;
         float* lp = p.lse + (is_tnd ? int64_t(bi.q_start + i) * p.lse_ss
@@ -673,8 +591,6 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
                     int64_t(it.h) * p.lse_sn;
         *lp = lse;
       }
-    }
-    gs += pi.nl;
     }
   }
 
@@ -685,6 +601,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
+
 template <int DQK, int DV, bool BF16, int MODE>
 cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
   using C = PairCfg<DQK, DV>;
@@ -693,7 +610,7 @@ cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
   constexpr int smem = MODE == kMask ? C::kSmemMask : C::kSmem;
   cudaError_t e = set_smem_once<prefill_pair_kernel<DQK, DV, BF16, MODE>>(smem);
   if (e != cudaSuccess) return e;
-  k<<<p.n_cta, C::kThreads, smem, s>>>(p);
+  k<<<p.n_items, C::kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -701,7 +618,7 @@ cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
 
 cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int head_dim_v, bool bf16, int mode,
                                 cudaStream_t s) {
-  if (p.n_items == 0 || p.n_cta == 0) return cudaSuccess;
+  if (p.n_items == 0) return cudaSuccess;
 #define FIA_PAIR_MODES(DQ, DV, BB)                                          \
   switch (mode) {                                                           \
     case kDense: return launch_pair_one<DQ, DV, BB, kDense>(p, s);          \

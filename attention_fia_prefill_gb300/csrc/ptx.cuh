@@ -14,6 +14,7 @@
 namespace fia {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kShortestWaitLimitNs = 100000;   // limits below this (tests only) skip the blocking first try
 
 // Waits are timed with the SM's cycle counter (a register read; the global
 // nanosecond timer is far slower to read and sat on every wait's path).  The
@@ -102,8 +103,9 @@ struct DevStatus {
   unsigned long long epoch;
   // Limit of the waits that can give up (the ones that unwind a CTA); the
   // waits that let in-flight copies and products finish before a CTA exits
-  // always use kWaitLimitNs.
-  unsigned long long limit_ns = kWaitLimitNs;
+  // always use kWaitLimitNs.  (No default member initializer: the parameter
+  // structs that hold a DevStatus stay trivial types.)
+  unsigned long long limit_ns;
 };
 
 // Tag of a call in the high half of a per-unit completion counter.  The
@@ -137,9 +139,9 @@ __device__ __forceinline__ unsigned tagged_increment(unsigned long long* ctr, un
   return unsigned(old & 0xffffffffull) + 1u;
 }
 
-// Both are compare-and-swap loops keyed on the epoch, so they may land in
-// either order: a stamp never clears a code this call already raised, and a
-// raise replaces whatever an earlier call (or uninitialised memory) left.
+// The stamp is a compare-and-swap loop keyed on the epoch: it replaces
+// whatever an earlier call (or uninitialised memory) left, and never clears a
+// code this call has already raised.
 __device__ __forceinline__ void status_stamp(const DevStatus& st) {
   if (st.word == nullptr) return;
   unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(st.word);
@@ -150,27 +152,28 @@ __device__ __forceinline__ void status_stamp(const DevStatus& st) {
   }
 }
 
+// The stamp above has set the word to this call's epoch, so a raise is one
+// atomic maximum (the newest epoch's worst code wins).
 __device__ __forceinline__ void status_raise(const DevStatus& st, unsigned code) {
-  if (st.word == nullptr) return;
-  const unsigned long long want = (st.epoch << 8) | code;
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(st.word);
-  while (!((cur >> 8) == st.epoch && cur >= want)) {
-    const unsigned long long prev = atomicCAS(st.word, cur, want);
-    if (prev == cur) break;
-    cur = prev;
-  }
+  if (st.word != nullptr) atomicMax(st.word, (st.epoch << 8) | code);
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // (after recording FIA_ERR_TIMEOUT) if the limit passes or another role of the
 // CTA has already given up (*abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          const DevStatus& status) {
-  // a non-blocking test first: the limit is checked before the first
-  // try_wait, which may itself suspend the thread for a while
+                                          const DevStatus status) {
+  // The status comes by value: the call site copies it out of the kernel
+  // parameters into registers (constant-bank reads, hoisted out of loops).
+  // A reference into the parameters would make the limit a generic memory
+  // load on every wait.  The first probe does not block; then one try_wait
+  // that may suspend the thread until the phase completes -- skipped under a
+  // limit shorter than such a suspension (a test's), which is checked first.
   if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t limit_ns = abort != nullptr ? status.limit_ns : kWaitLimitNs;
+  if (limit_ns >= kShortestWaitLimitNs && mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = limit_ns * kCyclesPerNs;
   const uint64_t t0 = cycles();
-  const uint64_t limit = (abort != nullptr ? status.limit_ns : kWaitLimitNs) * kCyclesPerNs;
   while (true) {
     if (cycles() - t0 > limit) {
       if (abort != nullptr) *abort = 1;
@@ -179,9 +182,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
     if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    // back off between polls: a waiting warp leaves the issue slots of its
-    // scheduler to the warp it shares it with
-    __nanosleep(20);
   }
 }
 

@@ -129,9 +129,10 @@ class Timer:
     call and around its main kernel.
     back_to_back(): K calls in a row, call i running fns[i % len(fns)] over
     rotating input copies (so consecutive calls read inputs larger than L2);
-    the calls are queued behind ~1 ms of GPU work, so the GPU runs them back to
-    back whatever the host's pace, and one event pair brackets all K.  The
-    host's own time per call is measured around the enqueueing loop."""
+    the calls are queued behind GPU work longer than twice their enqueueing
+    time, so the GPU runs them back to back whatever the host's pace, and one
+    event pair brackets all K.  The host's own time per call is measured
+    around the enqueueing loop."""
 
     def __init__(self, torch, device):
         self.torch = torch
@@ -167,11 +168,16 @@ class Timer:
     def back_to_back(self, fns, steps, warmup):
         torch = self.torch
         n = len(fns)
+        t0 = time.perf_counter()
         for i in range(warmup):
             fns[i % n]()
+        host_us = (time.perf_counter() - t0) / max(warmup, 1) * 1e6
         torch.cuda.synchronize()
-        for _ in range(3):
-            self.flush()   # ~1 ms of queued GPU work; also leaves L2 cold
+        # queue the K calls behind GPU work that outlasts their enqueueing
+        # (each flush is a ~80 us write): the GPU then runs them back to back
+        # whatever the host's pace; the flush also leaves L2 cold
+        for _ in range(max(3, int(steps * host_us * 2 / 80) + 1)):
+            self.flush()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
         t0 = time.perf_counter()

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(128, 1) selftest_kernel(const __grid_constant_
   __syncthreads();
   if (threadIdx.x == 0) {
     tc_fence_after();
-    bool ok = mbar_wait(&bars[0], 0, abort_flag, DevStatus{status, 1});
+    bool ok = mbar_wait(&bars[0], 0, abort_flag, DevStatus{status, 1, kWaitLimitNs});
     if (ok) {
       tc_fence_after();
       const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(128, 1) selftest_kernel(const __grid_constant_
         }
       }
       mma_commit(&bars[1]);
-      mbar_wait(&bars[1], 0, abort_flag, DevStatus{status, 1});
+      mbar_wait(&bars[1], 0, abort_flag, DevStatus{status, 1, kWaitLimitNs});
     }
   }
   __syncthreads();
