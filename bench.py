@@ -273,7 +273,7 @@ def measure_decode(torch, dev, timer, steps, warmup, pk, traffic):
 
     res["e2e_ms"], _ = timer.back_to_back([e2e_call], steps, max(3, warmup // 2))
     res["roofline"] = roofline("hbm", kv_bytes / (step_ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s",
-                               traffic.get("decode_kernel"))
+                               traffic.get("decode_gqa_kernel"))
     return res, c
 
 
@@ -911,6 +911,26 @@ def run_profile_target(args):
                                 scale_value=c.scale, input_layout="TND", sparse_mode=3,
                                 actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
                                 softmax_lse_flag=True)
+    elif name == "decode_q4":
+        base = fia_inputs.workload_paged_gqa_decode()
+        c = fia_inputs.paged_decode_case(16, 32, 8, 128, base.kv_lens, block_size=128, workload=3400, q_tokens=4)
+        q, kp, vp, tb = c.q.to(dev), c.k_pool.to(dev), c.v_pool.to(dev), c.block_table.to(dev)
+
+        def call():
+            fia.fia_decode(q, kp, vp, block_table=tb, block_size=c.block_size, actual_seq_kvlen=c.kv_lens,
+                           num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                           input_layout="BNSD", sparse_mode=3, softmax_lse_flag=True)
+    elif name in ("prefill_band", "prefill_mask"):
+        c = fia_inputs.workload_tnd_varlen()
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        mask = fia_inputs.atten_mask((4096, 4096), "causal").to(dev) if name == "prefill_mask" else None
+        kw = (dict(sparse_mode=4, pre_tokens=1024, next_tokens=0) if name == "prefill_band"
+              else dict(sparse_mode=1, atten_mask=mask))
+
+        def call():
+            fia.fia_prefill(q, k, v, num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                            scale_value=c.scale, input_layout="TND", actual_seq_qlen=c.actual_seq_qlen,
+                            actual_seq_kvlen=c.actual_seq_kvlen, softmax_lse_flag=True, **kw)
     else:
         raise SystemExit(f"unknown profile target {name}")
     for _ in range(args.warmup + args.steps):
@@ -921,7 +941,7 @@ def run_profile_target(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, prefill_tnd, bsa, bsa_fp8, mla, mla_prefill)")
+    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, decode_q4, prefill_tnd, prefill_band, prefill_mask, bsa, bsa_fp8, mla, mla_prefill)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
