@@ -62,7 +62,7 @@ unsigned long long next_epoch() { return g_epoch.fetch_add(1, std::memory_order_
 // Limit of the kernels' unwinding waits (fia_debug_set_wait_limit_ns; 0: the
 // default of kWaitLimitNs).
 std::atomic<unsigned long long> g_wait_limit_ns{0};
-// fia_debug_set_decode_path: 1 runs the tensor-core decode kernel for every unit
+// fia_debug_set_decode_path: 1 runs the tcgen05 decode kernel for every unit
 std::atomic<int> g_decode_force_tc{0};
 
 // A call's device status: the word at the start of its workspace, a fresh

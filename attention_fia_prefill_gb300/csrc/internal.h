@@ -130,7 +130,7 @@ struct DecodeParams {
   int batch, num_heads, num_kv_heads, group;
   float scale_log2;
   int l2_ahead;                   // producers warm L2 with the tiles of the stage this many ahead (0: off)
-  int force_tc;                   // 1: the tensor-core kernel even for units of <= 4 rows (tests)
+  int force_tc;                   // 1: the tcgen05 kernel even for units of <= 16 rows (tests)
   DevStatus status;
   const int32_t* plan_ws;         // the plan in the workspace (32-bit words), or nullptr: plan_inline
   int plan_seg, plan_unit, plan_len;

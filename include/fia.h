@@ -343,11 +343,11 @@ FIA_API void fia_profile_next_call(void* start_event, void* stop_event);
  * meant only for tests of that path. */
 FIA_API void fia_debug_set_wait_limit_ns(uint64_t ns);
 
-/* Selects the decode kernel for units (batch, kv head) of at most 4 query
- * rows with head_dim 128: 0 (the default) the CUDA-core kernel, 1 the
- * tensor-core kernel that serves larger units.  Both compute the same
- * operation; applies to calls launched afterwards from any thread.  Meant
- * for tests that compare the two. */
+/* Selects the decode kernel for units (batch, kv head) of at most 16 query
+ * rows with head_dim 128: 0 (the default) the warp-level kernel (mma.sync per
+ * warp), 1 the tcgen05 kernel that serves larger units.  Both compute the
+ * same operation; applies to calls launched afterwards from any thread.
+ * Meant for tests that compare the two. */
 FIA_API void fia_debug_set_decode_path(int path);
 
 #ifdef __cplusplus

@@ -273,10 +273,11 @@ def test_device_timeout_path(fia):
     assert_lse_close(lse, rl)
 
 
-@pytest.fixture(params=[0, 1], ids=["cuda_core", "tensor_core"])
+@pytest.fixture(params=[0, 1], ids=["warp_mma", "tensor_core"])
 def decode_path(request):
-    """Both kernels that serve units of at most 4 rows (head_dim 128): the
-    CUDA-core one (the default) and the tensor-core one of larger units."""
+    """Both kernels that can serve units of at most 16 rows (head_dim 128):
+    the warp-level mma.sync one (the default) and the tcgen05 one of larger
+    units."""
     from attention_fia_prefill_gb300 import _binding as B
     lib = B.load_library()
     lib.fia_debug_set_decode_path(request.param)
@@ -286,10 +287,13 @@ def decode_path(request):
 
 @pytest.mark.parametrize("n1,n2,qs,mode,bs", [(8, 2, 1, 0, 128), (4, 4, 1, 0, 16), (6, 2, 1, 0, 64),
                                               (4, 2, 1, 0, 256), (4, 2, 2, 3, 64), (1, 1, 4, 3, 128),
-                                              (2, 1, 2, 2, 128), (3, 1, 1, 0, 16)])
+                                              (2, 1, 2, 2, 128), (3, 1, 1, 0, 16), (16, 2, 1, 0, 128),
+                                              (8, 1, 1, 0, 64), (8, 2, 4, 3, 128), (6, 1, 2, 2, 16),
+                                              (5, 1, 3, 3, 256), (32, 2, 1, 0, 128)])
 def test_small_units_both_paths(fia, decode_path, n1, n2, qs, mode, bs):
-    """Units of 1..4 rows (heads per kv head x new tokens): ragged stages,
-    empty and one-key sequences, causal token limits, each block size."""
+    """Units of 1..16 rows (heads per kv head x new tokens) on both decode
+    kernels: ragged stages, empty and one-key sequences, causal token limits,
+    each block size."""
     lens = [1, 0, 127, 128, 129, 700, 2049, 3]
     c = fia_inputs.paged_decode_case(len(lens), n1, n2, 128, lens, block_size=bs,
                                      workload=3700 + 10 * n1 + n2 + qs + bs, q_tokens=qs)
@@ -299,6 +303,17 @@ def test_small_units_both_paths(fia, decode_path, n1, n2, qs, mode, bs):
 def test_small_units_full_workload_both_paths(fia, decode_path):
     """The headline paged workload on both kernels: every output."""
     _check_paged(fia, fia_inputs.workload_paged_gqa_decode())
+
+
+def test_sixteen_row_units_full_workload_both_paths(fia, decode_path):
+    """The headline workload with 4 new tokens per sequence (16 rows per
+    unit, causal) on both kernels: sampled (batch, head) rows."""
+    base = fia_inputs.workload_paged_gqa_decode()
+    c = fia_inputs.paged_decode_case(16, 32, 8, 128, base.kv_lens, block_size=128, workload=3400, q_tokens=4)
+    rng = np.random.default_rng(11)
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, 16, 24), rng.integers(0, 32, 24))]
+    rows += [(12, h) for h in range(4)]
+    _check_rows(fia, c, rows, mode=3)
 
 
 def test_small_units_f16_long_split(fia, decode_path):
@@ -312,7 +327,7 @@ def test_small_units_f16_long_split(fia, decode_path):
 
 
 def test_small_units_timeout_path(fia):
-    """The CUDA-core kernel's waits give up under a 1 ns limit and report
+    """The warp-level kernel's waits give up under a 1 ns limit and report
     FIA_ERR_TIMEOUT; the next call is correct."""
     from attention_fia_prefill_gb300 import _binding as B
     lib = B.load_library()
