@@ -15,10 +15,14 @@
 //     the segment) and of every cache tile, which it alone reads.  Each
 //     computes its part of S = Q' K'^T for all heads (M = 128 head rows,
 //     N = 32 keys, 256 or 320 deep), sends the partial rows to the partner's
-//     shared memory (distributed shared memory, released by a cluster-scope
-//     barrier arrival) and adds the partner's: both CTAs then hold the same
-//     scores, run the same softmax, and accumulate O_h += P V_h over their
-//     own latent columns (N = 256), which are exactly the V half h needs;
+//     shared memory (distributed shared memory: asynchronous stores that
+//     complete on the partner's barrier) and adds the partner's: both CTAs
+//     then hold the same scores, run the same softmax, and accumulate
+//     O_h += P V_h over their own latent columns (N = 256), which are exactly
+//     the V half h needs.  The exchange moves 512 bytes per key each way,
+//     about as many as the pair reads from HBM, over a network measured at
+//     8-12 bytes per cycle per SM in both directions at once, under half an
+//     SM's share of HBM bandwidth: it, not HBM, sets this kernel's rate;
 //   * each segment leaves one partial (O_h / l, lse) per head; the CTA that
 //     completes a (unit, half) merges its partials in a fixed order on its
 //     merge warp; a unit held by one segment is written directly.
