@@ -35,6 +35,7 @@ constexpr int kGqaTile = 2 * 128 * 128;   // K (or V) of one 128-token stage, D 
 constexpr int kGqaBox = 128 * 128;
 constexpr int kGqaW = 8;                  // compute warps, 16 keys of a stage each
 constexpr int kGqaThreads = (kGqaW + 3) * 32;   // + K producer, V producer, merge
+constexpr int kGqaWarmStages = 4;          // stages warmed in L2 before the grid dependency resolves
 constexpr int kGqaBarBytes = 1024;
 
 // Shared memory of the kernel for units of kRows (4 or 16) rows: the K and V
@@ -133,6 +134,15 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
     fence_mbar_init();
   }
   __syncthreads();
+  // This CTA may start on an SM the previous kernel's CTA has just left while
+  // that kernel's other CTAs still run: the producers warm L2 with the first
+  // stages of the CTA's first segment meanwhile (a plan carried in the
+  // parameters only; one in the workspace is read after the wait).
+  if ((warp == kGqaW || warp == kGqaW + 1) && p.n_cta > 0 && p.plan_ws == nullptr) {
+    const int sb = pl.cta_seg(blockIdx.x);
+    if (sb < pl.cta_seg(blockIdx.x + 1))
+      l2_warm_segment<2>(p, pl, warp == kGqaW ? &p.tm_k : &p.tm_v, pl.seg_at(sb), kGqaWarmStages);
+  }
   grid_dep_wait();   // the previous kernel on the stream is complete from here on
   if (threadIdx.x == 0 && blockIdx.x == 0) status_stamp(p.status);
   const int seg_begin = p.n_cta > 0 ? pl.cta_seg(blockIdx.x) : 0;

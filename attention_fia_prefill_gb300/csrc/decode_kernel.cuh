@@ -257,6 +257,50 @@ __device__ __forceinline__ int decode_producer(const DecodeParams& p, const Deco
   return j;
 }
 
+// Warms L2 with the K (or V) boxes of the first `nst` stages of segment sg.
+// Run before griddepcontrol.wait, while the previous kernel on the stream may
+// still be running on other SMs: a prefetch hands nothing to the kernel, so a
+// block-table entry read here that the previous kernel later rewrites only
+// wastes the prefetch (the copies after the wait read the table again), and
+// L2 keeps lines that kernel writes coherent.  Coordinates past the pool are
+// not fetched (the tensor map bounds them).  The whole warp runs it.
+template <int Chunks>
+__device__ __forceinline__ void l2_warm_segment(const DecodeParams& p, const DecodePlanRef& pl, const CUtensorMap* tm,
+                                                const DecodeSeg& sg, int nst) {
+  const int lane = threadIdx.x & 31;
+  const int kvh = sg.unit % p.num_kv_heads;
+  const int b = sg.unit / p.num_kv_heads;
+  const int L = pl.kv_len(b);
+  const int st_end = min(sg.stage_end, sg.stage_begin + nst);
+  int page0 = 0;
+  int32_t blk_lane = 0;   // lane i: block_table[b][page0 + i]
+  if (p.block_table != nullptr) {
+    page0 = (sg.stage_begin * 128) / p.block_size;
+    const int e = page0 + lane;
+    blk_lane = e < p.table_stride ? p.block_table[int64_t(b) * p.table_stride + e] : 0;
+  }
+  for (int st = sg.stage_begin; st < st_end; ++st) {
+    const int t0 = st * 128;
+    const int nbox = (min(128, L - t0) + p.box_rows - 1) / p.box_rows;
+    for (int k = 0; k < nbox; ++k) {
+      const int tok = t0 + k * p.box_rows;
+      int64_t row;
+      if (p.block_table == nullptr) {
+        row = int64_t(b) * p.row_per_blk + int64_t(kvh) * p.row_per_head + tok;
+      } else {
+        const int page = tok / p.block_size;
+        if (page - page0 >= 32) return;   // past the lanes' window of table entries
+        const int64_t blk = __shfl_sync(0xffffffffu, blk_lane, page - page0);
+        row = blk * p.row_per_blk + int64_t(kvh) * p.row_per_head + (tok % p.block_size);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < Chunks; ++c) tma_prefetch_l2_2d(tm, kvh * p.col_per_head + c * 64, int(row));
+      }
+    }
+  }
+}
+
 // After an abort, lets the copies of the first `issued` stages land before the
 // CTA goes away (run once every role has stopped: a producer that finished
 // its walk before another role gave up still has copies in flight).
@@ -523,6 +567,8 @@ __device__ __forceinline__ void merge_warp(const DecodeParams& p, const DecodePl
   if (ok) write_empty_units<D, BF16>(p, pl, lane);
 }
 
+constexpr int kDecodeWarmStages = 4;   // stages warmed in L2 before the grid dependency resolves
+
 template <int D, bool BF16, int GL>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, GL>;
@@ -577,6 +623,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar->tmem_holder;
+  // L2 warm-up of the CTA's first stages while the previous kernel may still
+  // run (a plan carried in the parameters only)
+  if ((warp == 4 || warp == 6) && p.n_cta > 0 && p.plan_ws == nullptr) {
+    const int sb = pl.cta_seg(blockIdx.x);
+    if (sb < pl.cta_seg(blockIdx.x + 1))
+      l2_warm_segment<C::kChunks>(p, pl, warp == 4 ? &p.tm_k : &p.tm_v, pl.seg_at(sb), kDecodeWarmStages);
+  }
   grid_dep_wait();   // the previous kernel on the stream is complete from here on
   if (threadIdx.x == 0 && blockIdx.x == 0) status_stamp(p.status);
   // (a plan in the workspace was copied there on the stream: read it only now)
