@@ -491,12 +491,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
       if (lane == 0) mbar_arrive(&bar->part_free[segi & 3]);
       const int2 up = unit_parts[sg.unit];
       if (up.y == 1) continue;   // written directly by the softmax warps
-      __threadfence();
+      // the increment releases this segment's partials (written by the
+      // softmax warps before part_done) and, for the last one, acquires the
+      // others'; the warp barrier orders every lane's loads after it
       int last = 0;
       if (lane == 0)
-        last = int(tagged_increment(p.unit_counter + sg.unit * 2 + half, unit_tag(p.status.epoch))) == up.y;
+        last = int(tagged_increment_acq_rel(p.unit_counter + sg.unit * 2 + half, unit_tag(p.status.epoch))) == up.y;
       if (__shfl_sync(0xffffffffu, last, 0)) {
-        __threadfence();
+        __syncwarp();
         mla_merge<BF16>(p, sg.unit, half, up, lane);
       }
     }

@@ -139,6 +139,36 @@ __device__ __forceinline__ unsigned tagged_increment(unsigned long long* ctr, un
   return unsigned(old & 0xffffffffull) + 1u;
 }
 
+// tagged_increment with acquire-release semantics at device scope: the
+// increment publishes every write that happens before it (the partial
+// results other warps of the CTA handed over through a CTA barrier), and the
+// increment that sees the final count observes every earlier increment's
+// writes.  Lighter than a sequentially consistent fence on each side.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long atom_cas_acq_rel(unsigned long long* p, unsigned long long cmp,
+                                                               unsigned long long val) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(old) : "l"(p), "l"(cmp), "l"(val) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned tagged_increment_acq_rel(unsigned long long* ctr, unsigned long long tag) {
+  unsigned long long old = atom_add_acq_rel(ctr, 1ull);
+  while ((old & 0xffffffff00000000ull) != tag) {
+    const unsigned long long prev = atom_cas_acq_rel(ctr, old + 1ull, tag | 1ull);
+    if (prev == old + 1ull) return 1u;
+    if ((prev & 0xffffffff00000000ull) == tag) {
+      old = atom_add_acq_rel(ctr, 1ull);
+    } else {
+      old = prev - 1ull;   // another stale increment came in between: claim from its value
+    }
+  }
+  return unsigned(old & 0xffffffffull) + 1u;
+}
+
 // The stamp is a compare-and-swap loop keyed on the epoch: it replaces
 // whatever an earlier call (or uninitialised memory) left, and never clears a
 // code this call has already raised.
