@@ -221,6 +221,7 @@ struct Geometry {
   // explicit atten_mask (sparse_mode 0 with a mask, 1)
   const uint8_t* mask = nullptr;
   int64_t mask_sb = 0, mask_ss = 0;
+  int64_t mask_s1 = 0;               // rows of one mask slice (its key extent is mask_ss)
   int mask_cs = 1;
   // head dims the kernels run with: scores over Dqk, value / output Dv (MLA
   // prefill: 192 / 128, with the rope columns from qr / kr when given)
@@ -540,6 +541,14 @@ size_t prefill_ws_bytes(size_t n_batches, size_t n_items) {
   return kHeader + align_up(n_batches * sizeof(BatchInfo), 256) + align_up(n_items * sizeof(WorkItem), 256);
 }
 
+// Tile codes of an explicit mask (one byte per 128 x 128 tile of each mask
+// slice), kept in the workspace after the plan.
+size_t mask_tiles_bytes(const Geometry& g) {
+  if (g.mask == nullptr) return 0;
+  const size_t n_mb = g.mask_sb > 0 ? size_t(g.B) : 1;
+  return align_up(n_mb * size_t((g.mask_s1 + kTileM - 1) / kTileM) * size_t((g.mask_ss + kTileN - 1) / kTileN), 256);
+}
+
 size_t count_items(const Geometry& g) {
   size_t n = 0;
   for (const auto& bi : g.batches) n += size_t((bi.q_len + kTileM - 1) / kTileM) * size_t(g.N1);
@@ -579,8 +588,9 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   std::vector<WorkItem> items;
   build_items(g, mode, causal_mode, items);
   const size_t plan_bytes = prefill_ws_bytes(g.batches.size(), items.size());
-  // FP8: the value tensor converted to f16 once per call, after the plan
-  const size_t need = plan_bytes + (g.fp8 ? align_up(size_t(numel(v)) * 2, 256) : 0);
+  // FP8: the value tensor converted to f16 once per call, after the plan;
+  // an explicit mask's tile codes, after the plan
+  const size_t need = plan_bytes + (g.fp8 ? align_up(size_t(numel(v)) * 2, 256) : 0) + mask_tiles_bytes(g);
   fia_status st = check_ws(ws, ws_bytes, need);
   if (st != FIA_OK) return st;
   float* lse = (prm->softmax_lse_flag && present(lse_t)) ? static_cast<float*>(lse_t->data) : nullptr;
@@ -687,6 +697,17 @@ fia_status run_prefill(const Geometry& g, int mode, int causal_mode, const fia_t
   pp.mask_sb = g.mask_sb;
   pp.mask_ss = g.mask_ss;
   pp.mask_cs = g.mask_cs;
+  if (mode == kMask) {
+    // the tile codes, on the stream before the prefill kernel
+    uint8_t* codes = base + plan_bytes + (g.fp8 ? align_up(size_t(numel(v)) * 2, 256) : 0);
+    const int n_mb = g.mask_sb > 0 ? int(g.B) : 1;
+    st = cuda_check(launch_mask_tile_summary(g.mask, g.mask_s1, g.mask_ss, n_mb, g.mask_cs, codes, stream),
+                    "mask tile summary");
+    if (st != FIA_OK) return st;
+    pp.mask_tiles = codes;
+    pp.mask_nkt = int((g.mask_ss + kTileN - 1) / kTileN);
+    pp.mask_tiles_sb = g.mask_sb > 0 ? int64_t((g.mask_s1 + kTileM - 1) / kTileM) * pp.mask_nkt : 0;
+  }
   pp.scale_log2 = float(prm->scale_value * 1.4426950408889634);
   pp.bsa_mask = bsa_mask;
   pp.bsa_nqb = nqb; pp.bsa_nkb = nkb; pp.bsa_x = bx; pp.bsa_y = by;
@@ -729,6 +750,7 @@ fia_status explicit_mask(const fia_tensor* mask, Geometry& g) {
   if (ms1 * ms2 > 0 && mask->data == nullptr) return fail(FIA_ERR_NULL, "atten_mask data is NULL");
   g.mask = static_cast<const uint8_t*>(mask->data);
   g.mask_ss = ms2;
+  g.mask_s1 = ms1;
   g.mask_sb = mb > 1 ? ms1 * ms2 : 0;
   const uintptr_t a = reinterpret_cast<uintptr_t>(mask->data);
   g.mask_cs = 1;
@@ -872,7 +894,7 @@ fia_status fia_prefill_paged_get_workspace_size(const fia_tensor* query, const f
   if (st != FIA_OK) return st;
   st = check_lse(softmax_lse, params, g.layout, g.B, g.N1, g.S1, g.T1);
   if (st != FIA_OK) return st;
-  *workspace_bytes = prefill_ws_bytes(g.batches.size(), count_items(g));
+  *workspace_bytes = prefill_ws_bytes(g.batches.size(), count_items(g)) + mask_tiles_bytes(g);
   return FIA_OK;
 }
 

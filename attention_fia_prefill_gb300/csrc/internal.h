@@ -71,6 +71,12 @@ struct PrefillParams {
   const uint8_t* attn_mask;       // kMask: byte (i, j) of batch b at b * mask_sb + i * mask_ss + j
   int64_t mask_sb, mask_ss;       // mask_sb = 0 for a mask shared by all batches
   int mask_cs;                    // copy granule in bytes (16, 8, 4: alignment of base and rows; 1: plain loads)
+  // explicit mask: one code per 128 x 128 tile of the mask (0 no key masked,
+  // 1 some, 2 every one), [mask batches][mask_nqt][mask_nkt]; a batch's codes
+  // at b * mask_tiles_sb (0 for a mask shared by all batches)
+  const uint8_t* mask_tiles;
+  int mask_nkt;
+  int64_t mask_tiles_sb;
   const int32_t* block_table;     // paged K/V: [B, table_stride] block ids; nullptr = contiguous K/V
   int64_t table_stride;
   int block_size;                 // a multiple of 128: a 128-key tile lies in one block
@@ -175,6 +181,10 @@ cudaError_t launch_prefill(const PrefillParams& p, int head_dim, bool bf16, int 
 cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int head_dim_v, bool bf16, int mode,
                                 cudaStream_t s);
 cudaError_t launch_bsa_fp8(const PrefillParams& p, cudaStream_t s);
+// Tile codes of an explicit atten_mask (PrefillParams::mask_tiles): mask
+// [n_mb][s1][s2] bytes (n_mb slices s1 * s2 apart), codes [n_mb][nqt][nkt].
+cudaError_t launch_mask_tile_summary(const uint8_t* mask, int64_t s1, int64_t s2, int n_mb, int cs, uint8_t* codes,
+                                     cudaStream_t s);
 // e4m3 bytes -> f16 holding 2^-8 of each value (the FP8 path's value tensor);
 // n_bytes a multiple of 16, both pointers 16-byte aligned.
 cudaError_t launch_e4m3_to_f16(const void* src, void* dst, int64_t n_bytes, int n_sm, cudaStream_t s);

@@ -27,10 +27,13 @@
 // CTA walks tile B's range and tile A stops early.
 // Paged K/V (chunked prefill against a block table): the producer takes each
 // 128-key tile from its block (block_size is a multiple of 128).
-// Explicit mask: each softmax thread copies its row's 128 mask bytes for the
-// next K/V tile into its own 128-byte shared slot (cp.async, in flight while
-// the current tile is processed) and turns them into a 128-bit mask; a warp
-// whose rows are all masked for a tile writes P = 0 and skips its softmax.
+// Explicit mask: a summary pass first gives every 128 x 128 tile of the mask
+// a code (no key masked / some / all); a CTA walks only from its rows' first
+// to their last tile with a visible key.  For a tile with some keys masked
+// each softmax thread copies its row's 128 mask bytes into its own 128-byte
+// shared slot (cp.async, one tile ahead) and turns them into a 128-bit mask;
+// fully visible tiles need no bytes, and for a fully masked one (or a warp
+// whose rows are all masked) the warp writes P = 0 and skips its softmax.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -66,6 +69,39 @@ struct PairCfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kKStages <= 3 && kVStages <= 3, "barrier slots");
 };
+
+// Tile codes of an explicit atten_mask: one CTA per 128 x 128 tile of one
+// mask slice, code 0 when no byte of the tile is nonzero, 2 when every byte
+// is, 1 otherwise (rows and columns past the mask are left out).  Thread t
+// reads 64 bytes of row t / 2: four 16-byte loads when rows are 16-byte
+// aligned, single bytes otherwise.
+__global__ void __launch_bounds__(256) mask_tile_summary_kernel(const uint8_t* __restrict__ mask, int64_t s1,
+                                                                int64_t s2, int cs, uint8_t* __restrict__ codes) {
+  const int kt = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  const int64_t row = int64_t(qt) * kTileM + (threadIdx.x >> 1);
+  const int64_t c0 = int64_t(kt) * kTileN + (threadIdx.x & 1) * 64;
+  bool any = false, all = true;
+  if (row < s1 && c0 < s2) {
+    const uint8_t* src = mask + (int64_t(b) * s1 + row) * s2 + c0;
+    const int n = int(min(int64_t(64), s2 - c0));
+    if (cs == 16 && n == 64) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + q);
+        any |= (v.x | v.y | v.z | v.w) != 0u;
+        all &= (nonzero_bytes4(v.x) & nonzero_bytes4(v.y) & nonzero_bytes4(v.z) & nonzero_bytes4(v.w)) == 0xfu;
+      }
+    } else {
+      for (int c = 0; c < n; ++c) {
+        const bool nz = __ldg(src + c) != 0;
+        any |= nz;
+        all &= nz;
+      }
+    }
+  }
+  const int a = __syncthreads_or(any), l = __syncthreads_and(all);
+  if (threadIdx.x == 0) codes[(int64_t(b) * gridDim.y + qt) * gridDim.x + kt] = uint8_t(l ? 2 : (a ? 1 : 0));
+}
 
 // Key tiles needed by the query rows [qa, qa + 128) of a batch.
 __device__ __forceinline__ int tiles_for_rows(const BatchInfo& bi, int qa, int mode, int diag_off) {
@@ -129,6 +165,27 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     const int64_t hi_a = min(int64_t(bi.kv_len) - 1, last_a + band_d + p.band_next);
     na = (hi < lo || hi_a < lo) ? 0 : int(hi_a / kTileN - lo / kTileN + 1);
     nb = has_b ? n : 0;
+  }
+  // explicit mask: walk only from the first to the last tile in which some
+  // key of the tile's rows is visible (tile codes from the summary pass);
+  // all-masked tiles inside that range take the P = 0 path below
+  const uint8_t* mtc = MODE == kMask ? p.mask_tiles + int64_t(it.b) * p.mask_tiles_sb : nullptr;
+  const int qta = q0 / kTileM;   // row tile of tile A in the mask (tile B: qta + 1)
+  if (MODE == kMask && nb + na > 0) {
+    int fa = -1, la = -1, fb = -1, lb = -1;
+    for (int j = 0; j < na; ++j)
+      if (mtc[int64_t(qta) * p.mask_nkt + jt0 + j] != 2) { fa = fa < 0 ? j : fa; la = j; }
+    for (int j = 0; j < nb; ++j)
+      if (mtc[int64_t(qta + 1) * p.mask_nkt + jt0 + j] != 2) { fb = fb < 0 ? j : fb; lb = j; }
+    const int first = fa < 0 ? fb : (fb < 0 ? fa : min(fa, fb));
+    if (first < 0) {
+      na = nb = 0;
+    } else {
+      jt0 += first;
+      na = la < 0 ? 0 : la - first + 1;
+      // tile B releases every stage the CTA loads: it walks at least tile A's range
+      nb = has_b ? max(na, lb < 0 ? 0 : lb - first + 1) : 0;
+    }
   }
   const int nl = max(na, nb);
 
@@ -375,7 +432,9 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       }
       cp_async_commit();
     };
-    if (mrow && n > 0) mask_fetch(0);
+    // tile code of this tile's rows for K/V tile jj (explicit mask)
+    auto mcode = [&](int jj) -> int { return MODE == kMask ? mtc[int64_t(qta + t) * p.mask_nkt + jt0 + jj] : 0; };
+    if (mrow && n > 0 && mcode(0) == 1) mask_fetch(0);
     // Rows of V past the batch's keys may hold anything (even NaN); P is 0
     // there but 0 * NaN is not, so they are cleared before the first P V that
     // reads tile jj: tile A's if it uses the tile, else tile B's.
@@ -398,7 +457,13 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     for (int j = 0; j < n; ++j) {
       // mb: bit c of mb[c >> 5] set when atten_mask masks key kv0 + c
       uint32_t mb[4] = {0u, 0u, 0u, 0u};
-      if (mrow) {
+      const int code = mcode(j);
+      if (MODE == kMask && code == 2) {
+        mb[0] = mb[1] = mb[2] = mb[3] = 0xffffffffu;   // every key of the tile masked for every row
+        if (mrow && j + 1 < n && mcode(j + 1) == 1) mask_fetch(j + 1);
+      } else if (MODE == kMask && code == 0) {
+        if (mrow && j + 1 < n && mcode(j + 1) == 1) mask_fetch(j + 1);
+      } else if (mrow) {
         cp_async_wait_all();
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -409,7 +474,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
                   (nonzero_bytes4(a1.z) << 24) | (nonzero_bytes4(a1.w) << 28);
         }
         // the slot is read (mb depends on every byte): refill it with the next tile
-        if (j + 1 < n) mask_fetch(j + 1);
+        if (j + 1 < n && mcode(j + 1) == 1) mask_fetch(j + 1);
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[3 * t + j % KS], (j / KS) & 1, abort_flag, p.status))) {
         ok = false;
@@ -615,6 +680,15 @@ cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_mask_tile_summary(const uint8_t* mask, int64_t s1, int64_t s2, int n_mb, int cs, uint8_t* codes,
+                                     cudaStream_t s) {
+  const int64_t nqt = (s1 + kTileM - 1) / kTileM, nkt = (s2 + kTileN - 1) / kTileN;
+  if (nqt == 0 || nkt == 0 || n_mb == 0) return cudaSuccess;
+  if (nqt > 65535 || n_mb > 65535 || nkt > 0x7fffffff) return cudaErrorInvalidValue;
+  mask_tile_summary_kernel<<<dim3(unsigned(nkt), unsigned(nqt), unsigned(n_mb)), 256, 0, s>>>(mask, s1, s2, cs, codes);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int head_dim_v, bool bf16, int mode,
                                 cudaStream_t s) {

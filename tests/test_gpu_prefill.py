@@ -257,6 +257,23 @@ def test_mask_2k_full(fia):
     _check_mask(fia, case, mask)
 
 
+def test_mask_tile_codes_shape_the_walk(fia):
+    """Tile codes of the mask decide each pair's walk: a query tile with every
+    key masked (tile A of the first pair: no keys at all), a walk that starts
+    late (tile B's first visible tile is the fourth), fully masked tiles inside
+    a walk (P = 0 there), a tile B with every key masked (it still walks tile
+    A's range), and mixed tiles; fully masked rows give 0 and lse = +inf."""
+    S, T = 640, 128
+    case = fia_inputs.prefill_case(1, 4, 2, S, S, 128, dtype="bf16", layout="BNSD", sparse_mode=1, workload=2450)
+    g = np.random.default_rng(2451)
+    visible = {(1, 3): "all", (2, 1): "all", (2, 4): "mixed", (4, 0): "mixed", (4, 2): "all"}
+    m = np.ones((S, S), dtype=np.uint8)
+    for (qt, kt), kind in visible.items():
+        blk = np.zeros((T, T), dtype=np.uint8) if kind == "all" else (g.random((T, T)) < 0.5).astype(np.uint8)
+        m[qt * T:(qt + 1) * T, kt * T:(kt + 1) * T] = blk
+    _check_mask(fia, case, torch.from_numpy(m))
+
+
 def test_full_tnd_band_and_mask_workloads_sampled(fia):
     """The varlen TND workload at full size with the band of the bench
     (sparse_mode 4, pre_tokens 1024, next_tokens 0) and with an explicit
