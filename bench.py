@@ -300,7 +300,7 @@ def measure_decode_tokens(torch, dev, timer, steps, warmup, pk, traffic, pool):
     return section("paged GQA decode, 4 query tokens causal, B=16 32/8 heads D=128 U[1,4096]",
                    kv_bytes / (step_ms * 1e-3) / 1e9, "GB/s", step_ms,
                    roofline("hbm", kv_bytes / (step_ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s",
-                            traffic.get("decode_kernel_q4")), cpu)
+                            traffic.get("decode_gqa_kernel_q4")), cpu)
 
 
 def measure_mla(torch, dev, timer, steps, warmup, pk, traffic, pool):
