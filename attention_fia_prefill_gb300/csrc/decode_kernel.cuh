@@ -342,15 +342,19 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
 
 // One warp merges the partials of a finished unit, in part order:
 // lse = log sum_k exp(lse_k), out = sum_k exp(lse_k - lse) O_k.  Four rows at
-// a time, lanes over D / 4 float4 columns; the lse values and the O rows of
-// eight parts are loaded together, so a merge costs few L2 round trips.
+// a time, lanes over D / 4 float4 columns; the O rows of four parts are loaded
+// together, so a merge costs few L2 round trips.  Every lane reads the parts'
+// lse words of its four rows itself (the same words in all lanes: one
+// transaction each) and weighs the parts locally: no cross-lane reductions on
+// the merge's critical path.
 template <int D, bool BF16>
 __device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2 up, int lane) {
-  constexpr int KB = 8;   // parts per batch of loads
+  constexpr int KB = 4;   // parts per batch of loads
   const int g = p.rows;   // rows of the unit: heads x query tokens
   const int kvh = unit % p.num_kv_heads, b = unit / p.num_kv_heads;
   const int64_t s0 = up.x;
   const int ns = up.y;
+  const bool col = lane < D / 4;
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   for (int h0 = 0; h0 < g; h0 += 4) {
     float M[4], Ls[4];
@@ -363,43 +367,42 @@ __device__ __forceinline__ void merge_unit(const DecodeParams& p, int unit, int2
     }
     for (int k0 = 0; k0 < ns; k0 += KB) {
       const int kn = ns - k0 < KB ? ns - k0 : KB;
-      float lk[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        lk[t] = (h0 + t < g && lane < kn) ? __ldcg(p.part_lse + (s0 + k0 + lane) * g + h0 + t) : -INFINITY;
+      float lk[KB][4];
       float4 o[KB][4];
 #pragma unroll
       for (int k = 0; k < KB; ++k)
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          o[k][t] = (k < kn && h0 + t < g && lane < D / 4)
-                        ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + k0 + k) * g + h0 + t) * D) + lane)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-      // running max over the batches; rescale what is accumulated so far
-      float wl[4];
+        for (int t = 0; t < 4; ++t) {
+          const bool v = k < kn && h0 + t < g;
+          lk[k][t] = v ? __ldcg(p.part_lse + (s0 + k0 + k) * g + h0 + t) : -INFINITY;
+          o[k][t] = (v && col) ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((s0 + k0 + k) * g + h0 + t) * D) + lane)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const float m_new = fmaxf(M[t], warp_max(lk[t]));
+        float mb = lk[0][t];
+#pragma unroll
+        for (int k = 1; k < KB; ++k) mb = fmaxf(mb, lk[k][t]);
+        const float m_new = fmaxf(M[t], mb);
+        // rescale what is accumulated so far to the new maximum
         const float a = (m_new == -INFINITY) ? 1.f : __expf(M[t] - m_new);
         acc[t].x *= a; acc[t].y *= a; acc[t].z *= a; acc[t].w *= a;
-        M[t] = m_new;
-        wl[t] = (lk[t] == -INFINITY) ? 0.f : __expf(lk[t] - m_new);
-        Ls[t] = Ls[t] * a + warp_sum(wl[t]);
-      }
+        Ls[t] *= a;
 #pragma unroll
-      for (int k = 0; k < KB; ++k)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float w = __shfl_sync(0xffffffffu, wl[t], k);
+        for (int k = 0; k < KB; ++k) {
+          const float w = (lk[k][t] == -INFINITY) ? 0.f : __expf(lk[k][t] - m_new);
+          Ls[t] += w;
           acc[t].x += w * o[k][t].x; acc[t].y += w * o[k][t].y; acc[t].z += w * o[k][t].z; acc[t].w += w * o[k][t].w;
         }
+        M[t] = m_new;
+      }
     }
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int hh = h0 + t;
       if (hh >= g) break;
       const int head = kvh * p.group + hh / p.q_tokens, tok = hh % p.q_tokens;
-      if (lane < D / 4) {
+      if (col) {
         const float inv = Ls[t] > 0.f ? 1.f / Ls[t] : 0.f;
         T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
                   int64_t(tok) * p.out_ss + 4 * lane;

@@ -65,6 +65,9 @@ struct MlaBars {
   uint64_t part_done[4], part_free[4];
   uint32_t tmem_holder;
   int abort_flag;
+  // the CTA's last segment completed a unit: merged by every warp once the
+  // roles are done (-1: none)
+  int final_unit;
 };
 static_assert(sizeof(MlaBars) <= 512, "barrier area");
 static_assert(kMlaSmem <= 227 * 1024, "shared memory budget");
@@ -75,26 +78,20 @@ __device__ __forceinline__ const int32_t* mla_cta(const MlaParams& p) { return p
 __device__ __forceinline__ const int2* mla_units(const MlaParams& p) { return p.unit_parts; }
 __device__ __forceinline__ const int32_t* mla_kvlen(const MlaParams& p) { return p.kv_len; }
 
-__device__ __forceinline__ float mla_warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float mla_warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Merges the partials of (unit b, half) in part order (lanes over the 256
-// columns, two float4 each; four heads at a time; loads batched by 4 parts).
+// Merges the partials of (unit b, half) in part order: lanes over the 256
+// columns (two float4 each), four heads at a time, the O rows of four parts
+// loaded together.  Every lane reads the parts' lse words of its four heads
+// itself (the same words in all lanes: one transaction each) and weighs the
+// parts locally, so no cross-lane reduction sits on the merge's critical
+// path.  Head groups g0, g0 + gstep, ... of four heads: one warp takes them
+// all, or the CTA's warps share them.
 template <bool BF16>
-__device__ void mla_merge(const MlaParams& p, int b, int half, int2 up, int lane) {
+__device__ void mla_merge(const MlaParams& p, int b, int half, int2 up, int lane, int g0, int gstep) {
   constexpr int KB = 4;
   const int nh = p.num_heads;
   const float* po = p.part_o + half * p.part_stride_o;
   const float* pl = p.part_lse + half * p.part_stride_lse;
-  for (int h0 = 0; h0 < nh; h0 += 4) {
+  for (int h0 = 4 * g0; h0 < nh; h0 += 4 * gstep) {
     float M[4], Ls[4];
     float4 acc[4][2];
 #pragma unroll
@@ -105,45 +102,44 @@ __device__ void mla_merge(const MlaParams& p, int b, int half, int2 up, int lane
     }
     for (int k0 = 0; k0 < up.y; k0 += KB) {
       const int kn = up.y - k0 < KB ? up.y - k0 : KB;
-      float lk[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        lk[t] = (h0 + t < nh && lane < kn) ? __ldcg(pl + int64_t(up.x + k0 + lane) * nh + h0 + t) : -INFINITY;
+      float lk[KB][4];
       float4 o[KB][4][2];
 #pragma unroll
       for (int k = 0; k < KB; ++k)
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
+        for (int t = 0; t < 4; ++t) {
+          const bool v = k < kn && h0 + t < nh;
+          lk[k][t] = v ? __ldcg(pl + int64_t(up.x + k0 + k) * nh + h0 + t) : -INFINITY;
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            o[k][t][c] = (k < kn && h0 + t < nh)
-                             ? __ldcg(reinterpret_cast<const float4*>(po + (int64_t(up.x + k0 + k) * nh + h0 + t) * kHalf) +
-                                      c * 32 + lane)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      float wl[4];
+            o[k][t][c] = v ? __ldcg(reinterpret_cast<const float4*>(po + (int64_t(up.x + k0 + k) * nh + h0 + t) * kHalf) +
+                                    c * 32 + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const float m_new = fmaxf(M[t], mla_warp_max(lk[t]));
+        float mb = lk[0][t];
+#pragma unroll
+        for (int k = 1; k < KB; ++k) mb = fmaxf(mb, lk[k][t]);
+        const float m_new = fmaxf(M[t], mb);
         const float a = (m_new == -INFINITY) ? 1.f : __expf(M[t] - m_new);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           acc[t][c].x *= a; acc[t][c].y *= a; acc[t][c].z *= a; acc[t][c].w *= a;
         }
-        M[t] = m_new;
-        wl[t] = (lk[t] == -INFINITY) ? 0.f : __expf(lk[t] - m_new);
-        Ls[t] = Ls[t] * a + mla_warp_sum(wl[t]);
-      }
+        Ls[t] *= a;
 #pragma unroll
-      for (int k = 0; k < KB; ++k)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float w = __shfl_sync(0xffffffffu, wl[t], k);
+        for (int k = 0; k < KB; ++k) {
+          const float w = (lk[k][t] == -INFINITY) ? 0.f : __expf(lk[k][t] - m_new);
+          Ls[t] += w;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             acc[t][c].x += w * o[k][t][c].x; acc[t][c].y += w * o[k][t][c].y;
             acc[t][c].z += w * o[k][t][c].z; acc[t][c].w += w * o[k][t][c].w;
           }
         }
+        M[t] = m_new;
+      }
     }
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -275,6 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
       mbar_init(&bar->part_free[s], 1);
     }
     bar->abort_flag = 0;
+    bar->final_unit = -1;
     fence_mbar_init();
     // the exchange slots of stages 0 and 1 expect the partner's rows
     mbar_arrive_expect_tx(&bar->x_full[0], uint32_t(kXBytes));
@@ -499,7 +496,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
         last = int(tagged_increment_acq_rel(p.unit_counter + sg.unit * 2 + half, unit_tag(p.status.epoch))) == up.y;
       if (__shfl_sync(0xffffffffu, last, 0)) {
         __syncwarp();
-        mla_merge<BF16>(p, sg.unit, half, up, lane);
+        if (segi == nseg - 1) {
+          // the CTA's last segment: nothing follows it, so all eight warps
+          // share this merge after the roles end
+          if (lane == 0) bar->final_unit = sg.unit;
+        } else {
+          mla_merge<BF16>(p, sg.unit, half, up, lane, 0, 1);
+        }
       }
     }
     // batches without keys: attention_out = 0, lse = +inf (spread over the pairs)
@@ -707,6 +710,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // the last segment's merge (its counter's acquire, by the merge warp, is
+  // ordered before these loads by the CTA barrier above)
+  const int fu = bar->final_unit;
+  if (fu >= 0 && !*abort_flag) mla_merge<BF16>(p, fu, half, unit_parts[fu], lane, warp, 8);
   // neither CTA leaves while the other may still write to its shared memory
   cluster_sync_all();
 }
