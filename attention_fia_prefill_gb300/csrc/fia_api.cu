@@ -1206,13 +1206,15 @@ struct DecodePlan {
 int g_decode_l2_ahead = 0;
 
 // Charge, in stages, for every unit piece (segment) a CTA runs: the end of a
-// segment drains the pipeline (its last P V), sums and writes the partials.
-// Measured on the paged GQA decode kernel: ~1.4 us per 128-token stage and
-// ~3 us per segment, i.e. about two stages; planning with a charge of 2
-// instead of 1 cut the kernel from 42.5 to 38.5 us at B=16, U[1,4096].
-constexpr double kDecodeSegmentCost = 2.0;
-// MLA decode (32-token stages): the charge it was tuned with.
-constexpr double kMlaSegmentCost = 1.0;
+// segment drains the pipeline, sums and writes the partials, and a split
+// unit costs a merge at the end of the CTA that finishes it last.  Tuned on
+// the paged GQA decode kernel at B=16, U[1,4096] (same-box sweep, us per call
+// back to back): 1 -> 26.1, 2 -> 25.3, 3 -> 24.9, 4 -> 24.6, 5 -> 25.0,
+// 7 -> 25.6; the 4-token decode has its optimum between 3 and 5.
+constexpr double kDecodeSegmentCost = 4.0;
+// MLA decode (32-token stages; same-box sweep at B=32, L=8192, ms per call:
+// 1 -> 0.2470, 3 -> 0.2458, 8 -> 0.2495).
+constexpr double kMlaSegmentCost = 3.0;
 
 // Deals the stages of all units (unit order = batch-major, then kv head) to at
 // most n_sm CTAs so that every CTA carries about the same cost: one per stage
