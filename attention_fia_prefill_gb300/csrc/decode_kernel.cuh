@@ -277,7 +277,9 @@ __device__ __forceinline__ void l2_warm_segment(const DecodeParams& p, const Dec
   if (p.block_table != nullptr) {
     page0 = (sg.stage_begin * 128) / p.block_size;
     const int e = page0 + lane;
-    blk_lane = e < p.table_stride ? p.block_table[int64_t(b) * p.table_stride + e] : 0;
+    // through L2 only: a line of the table left in L1 here could be stale
+    // for the reads after the wait
+    blk_lane = e < p.table_stride ? __ldcg(p.block_table + int64_t(b) * p.table_stride + e) : 0;
   }
   for (int st = sg.stage_begin; st < st_end; ++st) {
     const int t0 = st * 128;
