@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
       int j = 0;
       for (int t = iter.next(-1); t >= 0; t = iter.next(t), ++j) {
         const int s = j % S;
-        if (j >= S && !mbar_wait(&pv_done[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
+        if (j >= S && !mbar_wait_lean(&pv_done[s], ((j / S) - 1) & 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&k_full[s], C::kTile8);
         tma_load_4d(smem + C::kOffK + s * C::kTile8, &p.tm_k, &k_full[s], 0, kv_row0 + t * kTileN, kvh, b_coord);
         mbar_arrive_expect_tx(&v_full[s], C::kTileV);
@@ -194,11 +194,11 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
       }
       // On an abort, let every copy already issued land before the CTA exits.
       if (*abort_flag) {
-        mbar_wait(q_full, 0, nullptr, p.status);
+        mbar_wait_lean(q_full, 0, nullptr, p.status);
         for (int s = 0; s < S && s < j; ++s) {
           const int last = j - 1 - ((j - 1 - s) % S);
-          mbar_wait(&k_full[s], (last / S) & 1, nullptr, p.status);
-          mbar_wait(&v_full[s], (last / S) & 1, nullptr, p.status);
+          mbar_wait_lean(&k_full[s], (last / S) & 1, nullptr, p.status);
+          mbar_wait_lean(&v_full[s], (last / S) & 1, nullptr, p.status);
         }
       }
     }
@@ -208,14 +208,14 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
       constexpr uint32_t idesc_qk = idesc_e4m3(128, 128);
       constexpr uint32_t idesc_pv = idesc_f16(128, 128, 0, 0, 1);   // f16 P and V
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      bool ok = mbar_wait_lean(q_full, 0, abort_flag, p.status);
       int j = 0;
       uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
       uint32_t last_parity = 0;
       auto issue_pv = [&](int jj) -> bool {
         const int s = jj % S;
-        if (!mbar_wait(&p_full[jj & 1], (jj >> 1) & 1, abort_flag, p.status)) return false;
-        if (!mbar_wait(&v_full[s], (jj / S) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait_lean(&p_full[jj & 1], (jj >> 1) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait_lean(&v_full[s], (jj / S) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t v_base = smem_u32(smem + C::kOffV + s * C::kTileV);
 #pragma unroll
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
         for (int t = iter.next(-1); t >= 0; t = iter.next(t), ++j) {
           const int s = j % S;
           const int sb = j & 1;
-          if (!mbar_wait(&k_full[s], (j / S) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait_lean(&k_full[s], (j / S) & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t k_base = smem_u32(smem + C::kOffK + s * C::kTile8);
           // 128 fp8 columns = one 128-byte swizzled row; a K-step is 32 of them
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
         }
         if (ok && j >= 1) issue_pv(j - 1);
       }
-      if (last_bar != nullptr) mbar_wait(last_bar, last_parity, nullptr, p.status);
+      if (last_bar != nullptr) mbar_wait_lean(last_bar, last_parity, nullptr, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
       const float vs = v_scales[kv0 / p.bsa_y];
       if (r == 0 && !(ks > 0.f && vs > 0.f)) status_raise(p.status, 5u /* FIA_ERR_UNSUPPORTED */);
       const float sl2 = fmaxf(sl2_q * ks, 1e-30f);
-      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!mbar_wait_lean(&s_full[sb], (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t su[4][32];
 #pragma unroll
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
         l = l * alpha + (s0 + s1);
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) % S], ((j - 1) / S) & 1, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_lean(&pv_done[(j - 1) % S], ((j - 1) / S) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
     }
     // ------------------------------------------------------------ epilogue
     if (ok && j > 0) {
-      ok = mbar_wait(&pv_done[(j - 1) % S], ((j - 1) / S) & 1, abort_flag, p.status);
+      ok = mbar_wait_lean(&pv_done[(j - 1) % S], ((j - 1) / S) & 1, abort_flag, p.status);
       tc_fence_after();
     }
     if (ok) {

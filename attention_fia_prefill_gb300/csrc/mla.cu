@@ -317,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
       };
       for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
         const int s = j % kKS;
-        if (j >= kKS && !__all_sync(0xffffffffu, mbar_wait(&bar->pv_done[s], uint32_t(j / kKS - 1) & 1u, abort_flag,
+        if (j >= kKS && !__all_sync(0xffffffffu, mbar_wait_lean(&bar->pv_done[s], uint32_t(j / kKS - 1) & 1u, abort_flag,
                                                            p.status))) {
           ok = false;
           break;
@@ -365,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
     if (lane == 0 && *abort_flag) {
       for (int s = 0; s < kKS && s < j; ++s) {
         const int last = j - 1 - ((j - 1 - s) % kKS);
-        mbar_wait(&bar->k_full[s], uint32_t(last / kKS) & 1u, nullptr, p.status);
+        mbar_wait_lean(&bar->k_full[s], uint32_t(last / kKS) & 1u, nullptr, p.status);
       }
     }
   } else if (warp == 6) {
@@ -379,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
       int issued = 0;
       for (int segi = 0; segi < nseg; ++segi) {
         const DecodeSeg sg = segs[seg_begin + segi];
-        if (segi > 0 && !mbar_wait(&bar->q_empty, uint32_t(segi - 1) & 1u, abort_flag, p.status)) break;
+        if (segi > 0 && !mbar_wait_lean(&bar->q_empty, uint32_t(segi - 1) & 1u, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&bar->q_full, uint32_t(nb * kQBox));
         const int row = sg.unit * nh;
         for (int bx = 0; bx < nb; ++bx) {
@@ -389,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
         }
         ++issued;
       }
-      if (*abort_flag && issued > 0) mbar_wait(&bar->q_full, uint32_t(issued - 1) & 1u, nullptr, p.status);
+      if (*abort_flag && issued > 0) mbar_wait_lean(&bar->q_full, uint32_t(issued - 1) & 1u, nullptr, p.status);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------- MMA issuer
@@ -408,9 +408,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
     auto issue_pv = [&](int jj, int first, int segi, int nvalid, bool seg_last) -> bool {
       const int s = jj % kKS, sb = jj % kNS;
       if (jj == first && segi > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(&bar->o_free, uint32_t(segi - 1) & 1u, abort_flag, p.status)))
+          !__all_sync(0xffffffffu, mbar_wait_lean(&bar->o_free, uint32_t(segi - 1) & 1u, abort_flag, p.status)))
         return false;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar->p_full[sb], uint32_t(jj / kNS) & 1u, abort_flag, p.status)))
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(&bar->p_full[sb], uint32_t(jj / kNS) & 1u, abort_flag, p.status)))
         return false;
       // every Q K'^T of the segment has completed once the softmax has its
       // last P: the Q' tile may be refilled
@@ -439,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
     for (int segi = 0; segi < nseg && ok; ++segi) {
       const DecodeSeg sg = segs[seg_begin + segi];
       const int L = kvlen[sg.unit];
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar->q_full, uint32_t(segi) & 1u, abort_flag, p.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(&bar->q_full, uint32_t(segi) & 1u, abort_flag, p.status))) {
         ok = false;
         break;
       }
@@ -453,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
           ++jp;
         }
         if (!ok) break;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar->k_full[s], uint32_t(j / kKS) & 1u, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_lean(&bar->k_full[s], uint32_t(j / kKS) & 1u, abort_flag, p.status))) {
           ok = false;
           break;
         }
@@ -473,14 +473,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
         ++jp;
       }
     }
-    if (last_bar != nullptr && lane == 0) mbar_wait(last_bar, last_parity, nullptr, p.status);
+    if (last_bar != nullptr && lane == 0) mbar_wait_lean(last_bar, last_parity, nullptr, p.status);
     __syncwarp();
   } else if (warp == 7) {
     // ------------------------------------------------------- merge warp
     bool ok = true;
     for (int segi = 0; segi < nseg && ok; ++segi) {
       const DecodeSeg sg = segs[seg_begin + segi];
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar->part_done[segi & 3], uint32_t(segi >> 2) & 1u, abort_flag,
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(&bar->part_done[segi & 3], uint32_t(segi >> 2) & 1u, abort_flag,
                                              p.status))) {
         ok = false;
         break;
@@ -582,7 +582,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
         if (js > first && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O_h holds P V up to stage js - 1 once that P V is done; the next
           // one waits for this stage's P
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar->pv_done[(js - 1) % kKS], uint32_t((js - 1) / kKS) & 1u,
+          if (!__all_sync(0xffffffffu, mbar_wait_lean(&bar->pv_done[(js - 1) % kKS], uint32_t((js - 1) / kKS) & 1u,
                                                  abort_flag, p.status)))
             return false;
           tc_fence_after();
@@ -609,7 +609,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
       for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
         const int sb = j % kNS, xs = j & 1;
         // ---- this stage's partial row: TMEM -> the partner's buffer
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar->qk_done[sb], uint32_t(j / kNS) & 1u, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_lean(&bar->qk_done[sb], uint32_t(j / kNS) & 1u, abort_flag, p.status))) {
           ok = false;
           break;
         }
@@ -642,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
         break;
       }
       // ---- segment epilogue: O_h / l and lse, as a partial or final
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar->pv_done[(j - 1) % kKS], uint32_t((j - 1) / kKS) & 1u, abort_flag,
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(&bar->pv_done[(j - 1) % kKS], uint32_t((j - 1) / kKS) & 1u, abort_flag,
                                              p.status))) {
         ok = false;
         break;
@@ -695,7 +695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mla_kernel(c
       }
       // hand the segment to the merge warp (4-slot ring); its fence before
       // the unit counter covers these writes (released by the arrival)
-      if (segi >= 4 && !__all_sync(0xffffffffu, mbar_wait(&bar->part_free[segi & 3], uint32_t((segi >> 2) - 1) & 1u,
+      if (segi >= 4 && !__all_sync(0xffffffffu, mbar_wait_lean(&bar->part_free[segi & 3], uint32_t((segi >> 2) - 1) & 1u,
                                                           abort_flag, p.status))) {
         ok = false;
         break;

@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
           kv_b = __ldg(p.block_table + int64_t(it.b) * p.table_stride + key / p.block_size);
           kv_r = key % p.block_size;
         }
-        if (j >= KS && !mbar_wait(&k_rel[sk], ((j / KS) - 1) & 1, abort_flag, p.status)) break;
+        if (j >= KS && !mbar_wait_lean(&k_rel[sk], ((j / KS) - 1) & 1, abort_flag, p.status)) break;
         uint8_t* ks = smem + C::kOffK + sk * C::kTileQK;
         mbar_arrive_expect_tx(&k_full[sk], C::kTileQK);
 #pragma unroll
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
           tma_load_4d(ks + c * C::kBoxBytes, m, &k_full[sk], col, kv_r, kvh, kv_b);
         }
         nk = j + 1;
-        if (j >= VS && !mbar_wait(&v_free[sv], ((j / VS) - 1) & 1, abort_flag, p.status)) break;
+        if (j >= VS && !mbar_wait_lean(&v_free[sv], ((j / VS) - 1) & 1, abort_flag, p.status)) break;
         uint8_t* vs = smem + C::kOffV + sv * C::kTileV;
         mbar_arrive_expect_tx(&v_full[sv], C::kTileV);
 #pragma unroll
@@ -297,14 +297,14 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       }
       if (*abort_flag) {
         // let every copy in flight land before the CTA exits
-        mbar_wait(q_full, 0, nullptr, p.status);
+        mbar_wait_lean(q_full, 0, nullptr, p.status);
         for (int s = 0; s < KS && s < nk; ++s) {
           const int last = nk - 1 - ((nk - 1 - s) % KS);
-          mbar_wait(&k_full[s], (last / KS) & 1, nullptr, p.status);
+          mbar_wait_lean(&k_full[s], (last / KS) & 1, nullptr, p.status);
         }
         for (int s = 0; s < VS && s < nv; ++s) {
           const int last = nv - 1 - ((nv - 1 - s) % VS);
-          mbar_wait(&v_full[s], (last / VS) & 1, nullptr, p.status);
+          mbar_wait_lean(&v_full[s], (last / VS) & 1, nullptr, p.status);
         }
       }
     }
@@ -324,13 +324,13 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       constexpr uint64_t kStepK = C::kTileQK >> 4, kStepV = C::kTileV >> 4;
       uint64_t* last_bar = nullptr;   // barrier and phase of the latest commit
       uint32_t last_parity = 0;
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      bool ok = mbar_wait_lean(q_full, 0, abort_flag, p.status);
       // A K/V stage is waited for once, by the first product that reads it
       // (tile A's, unless the tile is past tile A's range).
       // S_t = Q_t K(j)^T
       auto qk = [&](int t, int j) -> bool {
         const int s = j % KS;
-        if ((t == 0 || j >= na) && !mbar_wait(&k_full[s], (j / KS) & 1, abort_flag, p.status)) return false;
+        if ((t == 0 || j >= na) && !mbar_wait_lean(&k_full[s], (j / KS) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint64_t qd = t == 0 ? qd0 : qd1;
         const uint64_t kd = kd0 + uint64_t(s) * kStepK;
@@ -350,8 +350,8 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       // next 64 columns of DV one box further)
       auto pv = [&](int t, int j) -> bool {
         const int s = j % VS;
-        if (!mbar_wait(t == 0 ? &pa_full[j & 1] : &pb_full[j & 1], (j >> 1) & 1, abort_flag, p.status)) return false;
-        if ((t == 0 || j >= na) && !mbar_wait(&v_full[s], (j / VS) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait_lean(t == 0 ? &pa_full[j & 1] : &pb_full[j & 1], (j >> 1) & 1, abort_flag, p.status)) return false;
+        if ((t == 0 || j >= na) && !mbar_wait_lean(&v_full[s], (j / VS) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint64_t vd = vd0 + uint64_t(s) * kStepV;
         const uint32_t dst = tmem + C::kColO + t * DV;
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
       }
       // Every MMA issued has finished before TMEM goes: the latest commit
       // tracks them all (the one before it on the same barrier has completed).
-      if (last_bar != nullptr) mbar_wait(last_bar, last_parity, nullptr, p.status);
+      if (last_bar != nullptr) mbar_wait_lean(last_bar, last_parity, nullptr, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     // reads tile jj: tile A's if it uses the tile, else tile B's.
     auto clear_v_tail = [&](int jj, int kv0j) -> bool {
       const int s = jj % VS;
-      if (!__all_sync(0xffffffffu, mbar_wait(&v_full[s], (jj / VS) & 1, abort_flag, p.status))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(&v_full[s], (jj / VS) & 1, abort_flag, p.status))) return false;
       if (r >= bi.kv_len - kv0j) {
         uint8_t* vs = smem + C::kOffV + s * C::kTileV;
 #pragma unroll
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
         // the slot is read (mb depends on every byte): refill it with the next tile
         if (j + 1 < n && mcode(j + 1) == 1) mask_fetch(j + 1);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[3 * t + j % KS], (j / KS) & 1, abort_flag, p.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(&s_full[3 * t + j % KS], (j / KS) & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
@@ -614,8 +614,8 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
     if (ok && n > 0) {
       const int jl = n - 1;
       ok = __all_sync(0xffffffffu, (t == 0 && nb > 0)
-                                       ? mbar_wait(pva_done, 0, abort_flag, p.status)
-                                       : mbar_wait(&v_free[jl % VS], (jl / VS) & 1, abort_flag, p.status));
+                                       ? mbar_wait_lean(pva_done, 0, abort_flag, p.status)
+                                       : mbar_wait_lean(&v_free[jl % VS], (jl / VS) & 1, abort_flag, p.status));
       tc_fence_after();
     }
     if (ok) {
