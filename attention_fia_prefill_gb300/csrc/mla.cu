@@ -206,22 +206,21 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "memory");
   return ok != 0;
 }
-// mbar_wait with cluster-scope acquire (the phase is completed by the
-// partner CTA's arrivals, which release its writes to this CTA's memory).
+// mbar_wait_lean with cluster-scope acquire (the phase is completed by the
+// partner CTA's stores and arrivals).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  const DevStatus status) {
-  if (mbar_test_wait_cluster(bar, parity)) return true;
+                                                  const DevStatus& status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t limit_ns = status.limit_ns;
-  if (limit_ns >= kShortestWaitLimitNs && mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = cycles();
+  const uint64_t t0 = globaltimer();
   while (true) {
-    if (cycles() - t0 > limit_ns * kCyclesPerNs) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
       status_raise(status, 10u /* FIA_ERR_TIMEOUT */);
       return false;
     }
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort) return false;
   }
 }
 __device__ __forceinline__ void cluster_sync_all() {
