@@ -136,6 +136,12 @@ def _dtype_code(t) -> int:
     return code
 
 
+# Descriptors of recent tensors by (address, dtype, shape): a decode loop
+# passes the same buffers call after call, and building the ctypes struct is
+# most of a descriptor's cost.  The callee only reads a descriptor.
+_DESC_CACHE: dict = {}
+
+
 def tensor_desc(t) -> FiaTensor | None:
     """fia_tensor for a contiguous torch tensor (None stays None)."""
     if t is None:
@@ -143,9 +149,17 @@ def tensor_desc(t) -> FiaTensor | None:
     if not t.is_contiguous():
         raise ValueError("tensors must be contiguous")
     shape = t.shape
+    key = (t.data_ptr(), t.dtype, shape)
+    d = _DESC_CACHE.get(key)
+    if d is not None:
+        return d
     if len(shape) > 5:
         raise ValueError("at most 5 dims")
-    return FiaTensor(t.data_ptr() or None, _dtype_code(t), len(shape), _SHAPE5(*shape))
+    d = FiaTensor(key[0] or None, _dtype_code(t), len(shape), _SHAPE5(*shape))
+    if len(_DESC_CACHE) >= 64:
+        _DESC_CACHE.pop(next(iter(_DESC_CACHE)))
+    _DESC_CACHE[key] = d
+    return d
 
 
 def raw_desc(ptr: int | None, dtype: int, shape) -> FiaTensor:
@@ -210,8 +224,19 @@ def check(status: int):
         raise FIAError(status, lib.fia_last_error().decode(errors="replace"))
 
 
+_RAW_STREAM = None
+
+
 def _stream_ptr(device):
+    """The device's current CUDA stream (torch's raw accessor when it has one:
+    a tenth of the cost of building a torch.cuda.Stream object)."""
+    global _RAW_STREAM
     import torch
+    if _RAW_STREAM is None:
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _RAW_STREAM:
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        return ctypes.c_void_p(_RAW_STREAM(idx))
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
