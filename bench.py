@@ -920,6 +920,15 @@ def run_profile_target(args):
             fia.fia_decode(q, kp, vp, block_table=tb, block_size=c.block_size, actual_seq_kvlen=c.kv_lens,
                            num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
                            input_layout="BNSD", sparse_mode=3, softmax_lse_flag=True)
+    elif name == "chunked":
+        c = fia_inputs.workload_chunked_prefill()
+        q, kp, vp, tab = c.q.to(dev), c.k_pool.to(dev), c.v_pool.to(dev), c.block_table.to(dev)
+
+        def call():
+            fia.fia_prefill_paged(q, kp, vp, tab, block_size=c.block_size, actual_seq_kvlen=c.kv_lens,
+                                  actual_seq_qlen=c.actual_seq_qlen, num_heads=c.num_heads,
+                                  num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                                  input_layout="BNSD", sparse_mode=3, softmax_lse_flag=True)
     elif name in ("prefill_band", "prefill_mask"):
         c = fia_inputs.workload_tnd_varlen()
         q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
@@ -941,7 +950,7 @@ def run_profile_target(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, decode_q4, prefill_tnd, prefill_band, prefill_mask, bsa, bsa_fp8, mla, mla_prefill)")
+    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, decode_q4, prefill_tnd, prefill_band, prefill_mask, chunked, bsa, bsa_fp8, mla, mla_prefill)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
