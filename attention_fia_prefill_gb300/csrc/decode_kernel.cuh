@@ -550,7 +550,6 @@ template <int D, bool BF16>
 __device__ __forceinline__ void merge_warp(const DecodeParams& p, const DecodePlanRef& pl, uint64_t* part_done,
                                            uint64_t* part_free, volatile int* abort_flag, int seg_begin, int nseg,
                                            int lane) {
-  const int g = p.rows;
   bool ok = true;
   for (int segi = 0; segi < nseg && ok; ++segi) {
     const DecodeSeg sg = pl.seg_at(seg_begin + segi);

@@ -1009,7 +1009,7 @@ fia_status bsa_get_workspace_size(const fia_tensor* query, const fia_tensor* key
   *workspace_bytes = kHeader;
   if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
   Geometry g;
-  int nqb, nkb;
+  int nqb = 0, nkb = 0;
   fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse, g, nqb, nkb);
   if (st != FIA_OK) return st;
   *workspace_bytes = prefill_ws_bytes(g.batches.size(), count_items(g));
@@ -1022,7 +1022,7 @@ fia_status bsa_forward(const fia_tensor* query, const fia_tensor* key, const fia
                        size_t workspace_bytes, void* stream) {
   if (query != nullptr && query->ndim > 0 && numel(query) == 0) return FIA_OK;
   Geometry g;
-  int nqb, nkb;
+  int nqb = 0, nkb = 0;
   fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse, g, nqb, nkb);
   if (st != FIA_OK) return st;
   return run_prefill(g, kBlockSparse, 0, query, key, value, attention_out, softmax_lse, params,
@@ -1042,7 +1042,7 @@ fia_status bsa_fp8_get_workspace_size(const fia_tensor* query, const fia_tensor*
   if (q_dequant_scale == nullptr || k_dequant_scale == nullptr || v_dequant_scale == nullptr)
     return fail(FIA_ERR_NULL, "FP8 attention needs all three dequant scales");
   Geometry g;
-  int nqb, nkb;
+  int nqb = 0, nkb = 0;
   fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse,
                                g, nqb, nkb, q_dequant_scale, k_dequant_scale, v_dequant_scale);
   if (st != FIA_OK) return st;
@@ -1060,7 +1060,7 @@ fia_status bsa_forward_fp8(const fia_tensor* query, const fia_tensor* key, const
   if (q_dequant_scale == nullptr || k_dequant_scale == nullptr || v_dequant_scale == nullptr)
     return fail(FIA_ERR_NULL, "FP8 attention needs all three dequant scales");
   Geometry g;
-  int nqb, nkb;
+  int nqb = 0, nkb = 0;
   fia_status st = bsa_validate(query, key, value, block_sparse_mask, block_shape, params, attention_out, softmax_lse,
                                g, nqb, nkb, q_dequant_scale, k_dequant_scale, v_dequant_scale);
   if (st != FIA_OK) return st;
