@@ -19,8 +19,7 @@ step with numpy float64 (matrix products are the only library primitive used):
 Inputs arrive as torch tensors already rounded to fp16/bf16 and are upcast
 exactly to float64.  Outputs are float64 numpy arrays.
 
-Readings taken where the pages are silent, garbled or contradict each other
-(each is also listed in the design notes):
+Readings taken where the pages are silent, garbled or contradict each other:
   * GQA: query head h reads key/value head floor(h / (Q_N / KV_N)).
   * atten_mask: a nonzero / True element masks the pair (adds -inf).
   * sparse_mode 2: key j is allowed for query i iff j <= i (top-left aligned);

@@ -55,12 +55,17 @@ def test_all_ones_equals_dense(fia):
 
 def test_full_bsa_workload_sampled(fia):
     """Block-sparse prefill bf16: B=2, 32/8 heads, S=16384, D=128, 128x128
-    blocks, diagonal + ~25% -- at full size, sampled rows vs the oracle."""
+    blocks, diagonal + ~25% -- at full size, one row of every other work item
+    (one query block of one head: 4096 rows, the first, last and a random row
+    of the block in turn) vs the oracle."""
     c = fia_inputs.workload_bsa()
     out, lse = _run(fia, c)
     rng = np.random.default_rng(5)
-    rows = [(int(rng.integers(2)), int(rng.integers(32)), int(i)) for i in
-            [0, 1, 127, 128, 8191, 16383] + list(rng.integers(16384, size=10))]
+    rows = []
+    for b in range(2):
+        for h in range(32):
+            for qb in range((b + h) % 2, 128, 2):
+                rows.append((b, h, qb * 128 + (0, 127, int(rng.integers(128)))[(h + qb) % 3]))
     ref = _oracle(c, rows=rows)
     assert_rows_close(out, lse, rows, ref, lambda r: (r[0], r[1], r[2]), torch.bfloat16)
 

@@ -93,14 +93,17 @@ def test_paged_prefill_matches_contiguous(fia):
 
 def test_chunked_prefill_workload_sampled(fia):
     """The chunked-prefill workload (8 x 2048-token chunks after cached contexts
-    U[0, 14336], 32/8 heads, 256-token blocks): sampled rows against the oracle,
-    the first and last row and a tile edge of every sequence."""
+    U[0, 14336], 32/8 heads, 256-token blocks): 512 sampled rows against the
+    oracle, one of every (sequence, 256-row item, kv group)."""
     c = fia_inputs.workload_chunked_prefill()
     out, lse = _run(fia, c, 3)
+    # one row of every (sequence, 256-row item, kv group): its head cycling
+    # through the group, its position over the two tiles' edges
     rows = []
     for b in range(len(c.kv_lens)):
-        for h in (0, 31):
-            for i in (0, 128, 2047):
-                rows.append((b, h, i))
+        for q0 in range(0, 2048, 256):
+            for grp in range(8):
+                k = q0 // 256 + grp
+                rows.append((b, 4 * grp + k % 4, q0 + (0, 127, 128, 255)[k % 4]))
     ref = _oracle(c, 3, rows=rows)
     assert_rows_close(out, lse, rows, ref, lambda r: (r[0], r[1], r[2]), c.q.dtype)

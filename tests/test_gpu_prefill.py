@@ -143,17 +143,21 @@ def test_gqa_equals_repeated_heads(fia):
 
 def test_full_tnd_varlen_workload_sampled(fia):
     """Varlen TND bf16: 8 sequences with lengths uniform on [256, 4096], GQA
-    32/8, D=128, causal, LSE on -- at full size, sampled rows vs the oracle."""
+    32/8, D=128, causal, LSE on -- at full size, one row of every work item
+    (2272 rows) vs the oracle."""
     case = fia_inputs.workload_tnd_varlen()
     out, lse = _run(fia, case)
     lens = [b - a for a, b in zip([0] + case.actual_seq_qlen[:-1], case.actual_seq_qlen)]
     starts = [0] + case.actual_seq_qlen[:-1]
     rng = np.random.default_rng(0)
+    # one row of every work item (256 query rows of one head), its position
+    # cycling over the two tiles' first and last rows and a random one
     rows = []
     for b in range(len(lens)):
-        for i in sorted({0, lens[b] - 1, int(rng.integers(lens[b])), 127, 128}):
-            if i < lens[b]:
-                rows.append((b, int(rng.integers(32)), i))
+        for q0 in range(0, lens[b], 256):
+            for h in range(32):
+                pick = (q0, q0 + 127, q0 + 128, q0 + 255, q0 + int(rng.integers(256)))[(h + q0 // 256) % 5]
+                rows.append((b, h, min(pick, lens[b] - 1)))
     ref = _oracle(case, rows=rows)
     assert_rows_close(out, lse, rows, ref, lambda r: (starts[r[0]] + r[2], r[1]), torch.bfloat16)
     assert torch.isfinite(out.float()).all()
