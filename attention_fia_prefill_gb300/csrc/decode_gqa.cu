@@ -59,6 +59,8 @@ struct GqaBars {
   uint64_t k_free[kGqaKS], v_free[kGqaKS];   // every compute warp is done with the slot
   uint64_t esync, efree;                     // the warps' segment states are in / have been read
   uint64_t part_done[4], part_free[4];       // compute -> merge warp hand-off ring
+  uint64_t tail_in, tail_count;              // the last segment's partials are out / its unit is counted
+  int tail_last;                             // this CTA completed the last segment's unit
   int abort_flag;
 };
 static_assert(sizeof(GqaBars) <= kGqaBarBytes, "barrier area");
@@ -130,6 +132,9 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
       mbar_init(&bar->part_done[s], kGqaW);
       mbar_init(&bar->part_free[s], 1);
     }
+    mbar_init(&bar->tail_in, kGqaW);
+    mbar_init(&bar->tail_count, 1);
+    bar->tail_last = 0;
     bar->abort_flag = 0;
     fence_mbar_init();
   }
@@ -148,6 +153,10 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
   const int seg_begin = p.n_cta > 0 ? pl.cta_seg(blockIdx.x) : 0;
   const int seg_end = p.n_cta > 0 ? pl.cta_seg(blockIdx.x + 1) : 0;
   const int nseg = seg_end - seg_begin;
+  // The CTA's last segment, when its unit is split, is counted and merged by
+  // the compute warps themselves (it ends the CTA's walk: a hand-off to the
+  // merge warp would only add its latency); the merge warp takes the others.
+  const bool tail_split = nseg > 0 && pl.unit_parts(pl.seg_at(seg_end - 1).unit).y > 1;
 
   int issued = 0;
   if (warp == kGqaW) {
@@ -159,7 +168,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
     issued = decode_producer<kGqaTile, kGqaBox, 2, VS, VS>(p, pl, &p.tm_v, smem + C::kOffV, bar->v_full, bar->v_free,
                                                            abort_flag, seg_begin, seg_end, nq);
   } else if (warp == kGqaW + 2) {
-    merge_warp<D, BF16>(p, pl, bar->part_done, bar->part_free, abort_flag, seg_begin, nseg, lane);
+    merge_warp<D, BF16>(p, pl, bar->part_done, bar->part_free, abort_flag, seg_begin, nseg - int(tail_split), lane);
   } else {
     // ------------------------------------------------------------ compute
     // Warp-synchronous tensor-core products (mma.sync m16n8k16, fp32
@@ -395,9 +404,12 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
       // and softmax_lse when the unit lies in this segment alone.  4 rows:
       // warp w takes row w % 4, elements [64 (w / 4), + 64); 16 rows: rows
       // 2w and 2w + 1, all 128 elements.
-      const bool whole = pl.unit_parts(sg.unit).y == 1;
+      const int2 up = pl.unit_parts(sg.unit);
+      const bool whole = up.y == 1;
+      const bool tail = segi + 1 == nseg && !whole;
       constexpr int kRowsPerWarp = kTwo ? 2 : 1;
       constexpr int kCols = kTwo ? 4 : 2;   // elements per lane
+      float own_o[kRowsPerWarp][kCols], own_lse[kRowsPerWarp];   // this segment's partial of the warp's slice
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i) {
         const int r = kTwo ? 2 * w + i : (w & 3);
@@ -442,15 +454,107 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
         } else {
           const int64_t part = sg.part;
           float* prow = p.part_o + (part * g + r) * D + dcol;
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) own_o[i][c] = acc[c] * inv;
+          own_lse[i] = has ? lse : -INFINITY;
           if constexpr (kCols == 4) {
-            *reinterpret_cast<float4*>(prow) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<float4*>(prow) = make_float4(own_o[i][0], own_o[i][1], own_o[i][2], own_o[i][3]);
           } else {
-            *reinterpret_cast<float2*>(prow) = make_float2(acc[0] * inv, acc[1] * inv);
+            *reinterpret_cast<float2*>(prow) = make_float2(own_o[i][0], own_o[i][1]);
           }
-          if (lse_lane) p.part_lse[part * g + r] = has ? lse : -INFINITY;
+          if (lse_lane) p.part_lse[part * g + r] = own_lse[i];
         }
       }
       warp_arrive(&bar->efree);
+      if (tail) {
+        // count the unit's piece: warp 0 waits for every warp's partial
+        // (the arrivals release them within the CTA), a device-scope fence
+        // publishes them (cumulativity), one lane increments the counter
+        warp_arrive(&bar->tail_in);
+        if (w == 0) {
+          if (!warp_wait(&bar->tail_in, 0u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            __threadfence();
+            bar->tail_last = int(tagged_increment(p.unit_counter + sg.unit, unit_tag(p.status.epoch))) == up.y;
+            mbar_arrive(&bar->tail_count);
+          }
+        }
+        if (!warp_wait(&bar->tail_count, 0u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&bar->tail_last)) {
+          // every other piece is done: merge the warp's slice in part order,
+          // this piece from registers, with merge_unit's arithmetic (same
+          // bits whichever CTA completes the unit)
+          __threadfence();
+#pragma unroll
+          for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int r = kTwo ? 2 * w + i : (w & 3);
+            const int dcol = kTwo ? kCols * lane : 64 * (w >> 2) + kCols * lane;
+            if (r >= g) continue;
+            constexpr int KB = 4;
+            float M = -INFINITY, Ls = 0.f;
+            float a[kCols] = {};
+            for (int k0 = 0; k0 < up.y; k0 += KB) {
+              float lk[KB], o[KB][kCols];
+#pragma unroll
+              for (int k = 0; k < KB; ++k) {
+                const int part = up.x + k0 + k;
+                const bool v = k0 + k < up.y;
+                if (v && part == sg.part) {
+                  lk[k] = own_lse[i];
+#pragma unroll
+                  for (int c = 0; c < kCols; ++c) o[k][c] = own_o[i][c];
+                } else {
+                  lk[k] = v ? __ldcg(p.part_lse + int64_t(part) * g + r) : -INFINITY;
+                  const float* src = p.part_o + (int64_t(part) * g + r) * D + dcol;
+                  if constexpr (kCols == 4) {
+                    const float4 t4 = v ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    o[k][0] = t4.x; o[k][1] = t4.y; o[k][2] = t4.z; o[k][3] = t4.w;
+                  } else {
+                    const float2 t2 = v ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+                    o[k][0] = t2.x; o[k][1] = t2.y;
+                  }
+                }
+              }
+              float mb = lk[0];
+#pragma unroll
+              for (int k = 1; k < KB; ++k) mb = fmaxf(mb, lk[k]);
+              const float m_new = fmaxf(M, mb);
+              const float sc = (m_new == -INFINITY) ? 1.f : __expf(M - m_new);
+#pragma unroll
+              for (int c = 0; c < kCols; ++c) a[c] *= sc;
+              Ls *= sc;
+#pragma unroll
+              for (int k = 0; k < KB; ++k) {
+                const float wk = (lk[k] == -INFINITY) ? 0.f : __expf(lk[k] - m_new);
+                Ls += wk;
+#pragma unroll
+                for (int c = 0; c < kCols; ++c) a[c] += wk * o[k][c];
+              }
+              M = m_new;
+            }
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            const int head = kvh * p.group + r / p.q_tokens, tok = r % p.q_tokens;
+            T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
+                      int64_t(tok) * p.out_ss + dcol;
+            if constexpr (kCols == 4) {
+              *reinterpret_cast<uint2*>(orow) =
+                  make_uint2(pack2(a[0] * inv, a[1] * inv, BF16), pack2(a[2] * inv, a[3] * inv, BF16));
+            } else {
+              *reinterpret_cast<uint32_t*>(orow) = pack2(a[0] * inv, a[1] * inv, BF16);
+            }
+            if (lane == 0 && (kTwo || w < 4) && p.lse != nullptr)
+              p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] =
+                  Ls > 0.f ? M + __logf(Ls) : INFINITY;
+          }
+        }
+        continue;   // not handed to the merge warp
+      }
       // hand the segment to the merge warp (its 4-slot ring is reused only
       // after the merge warp took the segment 4 back).  No fence here: the
       // barrier arrival releases this warp's partial to the merge warp, whose
