@@ -266,6 +266,17 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
         const int t0 = st * 128;
         const int nvalid = min(128, L - t0);
         const int nvw = nvalid - 16 * w;   // valid keys of this warp (may be <= 0 or >= 16)
+        // atten_mask bytes of this lane's four keys (bit e: key e masked),
+        // read while the stage's copies land
+        uint32_t kmask = 0;
+        if (p.key_mask != nullptr) {
+          const uint8_t* mrow = p.key_mask + int64_t(b) * p.key_mask_sb + t0 + 16 * w;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int kl = 8 * (e >> 1) + 2 * ft + (e & 1);
+            if (kl < nvw && __ldg(mrow + kl) != 0) kmask |= 1u << e;
+          }
+        }
         if (!warp_wait(&bar->k_full[kslot], kpar, abort_flag, p.status)) {
           ok = false;
           break;
@@ -307,7 +318,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
           for (int e = 0; e < 4; ++e) {
             const int kl = 8 * (e >> 1) + 2 * ft + (e & 1);
             const int key = 16 * w + kl;
-            const bool on = live && kl < nvw && (!causal || t0 + key - klim <= tok);
+            const bool on = live && kl < nvw && (!causal || t0 + key - klim <= tok) && !((kmask >> e) & 1u);
             sv[e] = on ? sacc[e >> 1][2 * h + (e & 1)] * sl2 : -INFINITY;
           }
           float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));

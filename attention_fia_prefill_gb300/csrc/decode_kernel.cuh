@@ -968,8 +968,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
       // several query tokens: row h is token h % Q_S, which sees keys up to
       // klim + h % Q_S (sparse_mode 3: klim = S_kv - Q_S; 2: klim = 0)
       const int klim = p.q_causal == 3 ? L - p.q_tokens : 0;
+      const uint8_t* mrow = p.key_mask != nullptr
+                                ? p.key_mask + int64_t(sg.unit / p.num_kv_heads) * p.key_mask_sb : nullptr;
       for (int st = sg.stage_begin; st < sg.stage_end; ++st, ++j) {
         const int ps = j % VS, os = j % NO;
+        // this thread's key's atten_mask byte, read before the waits
+        const bool kmasked = mrow != nullptr && r < L - st * 128 && __ldg(mrow + st * 128 + r) != 0;
         // one O^T slot (64 rows): every stage shares the maxima slot, so the
         // stage before is folded first
         if (NO == 1 && jf < j && !fold()) {
@@ -989,7 +993,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const __grid_
         tmem_load_cols<GL>(tmem + lane_off + uint32_t(G) * uint32_t(j % NS), su);
         // every Q K^T of the segment has finished once its last S^T is in
         if (st + 1 == sg.stage_end && warp == 0 && lane == 0) mbar_arrive(&bar->q_free[segi % NQ]);
-        const bool valid = r < L - st * 128;
+        const bool valid = r < L - st * 128 && !kmasked;
         const bool causal = p.q_causal != 0 && st * 128 + 127 > klim;   // a key of this stage is past a limit
         const int kfrom = st * 128 + r - klim;
         uint8_t* pt = p_tiles + ps * C::kPBytes;

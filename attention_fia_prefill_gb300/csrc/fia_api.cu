@@ -771,7 +771,6 @@ fia_status prefill_mask_mode(const fia_params* p, const fia_tensor* mask, Geomet
       mode = kDense;   // no mask: pre_tokens / next_tokens are ignored
       return FIA_OK;
     }
-    if (g.mla) return fail(FIA_ERR_UNSUPPORTED, "an explicit atten_mask with MLA prefill is not implemented");
     fia_status st = explicit_mask(mask, g);
     if (st != FIA_OK) return st;
     // mode 0 keeps the band pre_tokens .. next_tokens around the diagonal;
@@ -1083,6 +1082,8 @@ struct DecodeGeometry {
   int64_t q_sb, q_sn, q_ss, o_sb, o_sn, o_ss;
   int64_t QS = 1;         // query tokens per sequence
   int q_causal = 0;       // with QS > 1: sparse_mode 0, 2 or 3
+  const uint8_t* key_mask = nullptr;   // atten_mask (Q_S = 1): one row of key bytes per batch
+  int64_t key_mask_sb = 0;             // 0: one row for every batch
   int64_t rows() const { return (N1 / N2) * QS; }
 };
 
@@ -1101,7 +1102,6 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
   g.mla = present(qr);
   fia_status st = resolve_heads(p, g.N1, g.N2, g.mla ? 128 : 64);
   if (st != FIA_OK) return st;
-  if (present(mask)) return fail(FIA_ERR_UNSUPPORTED, "atten_mask in decode is not implemented");
   if (!same_shape(q, out)) return fail(FIA_ERR_SHAPE, "attention_out must have the query's shape");
   int64_t Bq, Sq, D;
   st = dense_dims(q, g.layout, g.N1, Bq, Sq, D, "query");
@@ -1172,6 +1172,7 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
   }
   if (g.mla) {
     // MLA: key = value = the 512-d latent cache, plus a 64-d rope part of q and k
+    if (present(mask)) return fail(FIA_ERR_UNSUPPORTED, "atten_mask with MLA decode is not implemented");
     if (D != 512) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes a 512-d latent query (got %lld)", (long long)D);
     if (g.QS != 1) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes Q_S = 1");
     if (g.N2 != 1) return fail(FIA_ERR_UNSUPPORTED, "MLA decode takes num_key_value_heads = 1");
@@ -1190,6 +1191,30 @@ fia_status decode_geometry(const fia_tensor* q, const fia_tensor* k, const fia_t
   if (g.rows() > 64)
     return fail(FIA_ERR_UNSUPPORTED, "decode rows per KV head (Q_N / KV_N x Q_S = %lld) above 64", (long long)g.rows());
   g.Dv = D;
+  if (present(mask)) {
+    // the incremental case's atten_mask (npu_fused_infer_attention_score_v2,
+    // atten_mask with Q_S = 1): (B, KV_S), (B, 1, KV_S) or (B, 1, 1, KV_S),
+    // batch dim 1 broadcast; nonzero bytes mask their key
+    if (g.QS != 1) return fail(FIA_ERR_UNSUPPORTED, "decode atten_mask is taken with Q_S = 1 only");
+    if (mask->dtype != FIA_DTYPE_BOOL && mask->dtype != FIA_DTYPE_U8 && mask->dtype != FIA_DTYPE_I8)
+      return fail(FIA_ERR_DTYPE, "atten_mask must be bool, int8 or uint8");
+    const int n = mask->ndim;
+    if (n < 2 || n > 4) return fail(FIA_ERR_SHAPE, "decode atten_mask must be (B, KV_S), (B, 1, KV_S) or (B, 1, 1, KV_S)");
+    for (int i = 1; i < n - 1; ++i)
+      if (mask->shape[i] != 1)
+        return fail(FIA_ERR_SHAPE, "decode atten_mask must be (B, KV_S), (B, 1, KV_S) or (B, 1, 1, KV_S)");
+    const int64_t mb = mask->shape[0], ms = mask->shape[n - 1];
+    if (mb != 1 && mb != g.B)
+      return fail(FIA_ERR_SHAPE, "atten_mask batch dim %lld is neither 1 nor B=%lld", (long long)mb, (long long)g.B);
+    int64_t maxk = 0;
+    for (auto L : g.kv_len) maxk = std::max<int64_t>(maxk, L);
+    if (ms < maxk)
+      return fail(FIA_ERR_SHAPE, "atten_mask has %lld keys, below the longest sequence (%lld)", (long long)ms,
+                  (long long)maxk);
+    if (mb * ms > 0 && mask->data == nullptr) return fail(FIA_ERR_NULL, "atten_mask data is NULL");
+    g.key_mask = static_cast<const uint8_t*>(mask->data);
+    g.key_mask_sb = mb > 1 ? ms : 0;
+  }
   return FIA_OK;
 }
 
@@ -1570,6 +1595,8 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
   dp.lse_sb = g.N1 * g.QS; dp.lse_sn = g.QS; dp.lse_ss = 1;   // (B, N1, Q_S, 1)
   dp.q_tokens = int(g.QS);
   dp.q_causal = g.q_causal;
+  dp.key_mask = g.key_mask;
+  dp.key_mask_sb = g.key_mask_sb;
   dp.rows = int(g.rows());
   dp.part_o = reinterpret_cast<float*>(base + w.off_po);
   dp.part_lse = reinterpret_cast<float*>(base + w.off_pl);

@@ -128,6 +128,8 @@ struct DecodeParams {
   int64_t lse_sb, lse_sn, lse_ss;
   int q_tokens;                   // Q_S (1..16)
   int q_causal;                   // with Q_S > 1: 0 none, 2 key <= token, 3 key <= S_kv - Q_S + token
+  const uint8_t* key_mask;        // nullable: atten_mask of Q_S = 1, byte j of batch b at b * key_mask_sb + j
+  int64_t key_mask_sb;            // (nonzero: key j masked); 0 broadcasts one row to every batch
   int rows;                       // group * q_tokens (<= 64)
   float* part_o;                  // [n_segments, rows, D]
   float* part_lse;                // [n_segments, rows] natural log, -inf = empty

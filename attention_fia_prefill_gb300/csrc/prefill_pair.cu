@@ -42,15 +42,17 @@ namespace {
 
 // DQK: head dim of the scores (Q and K; 192 = MLA's 128 + 64 rope columns),
 // DV: head dim of V and O.  K and V have rings of their own: a K stage is free
-// once its last Q K^T is done, a V stage once its last P V is.
-template <int DQK, int DV>
+// once its last Q K^T is done, a V stage once its last P V is.  kM: the
+// explicit-mask layout, whose 32 KB of mask slots take, at DQK 192, one of
+// the two K stages.
+template <int DQK, int DV, bool kM = false>
 struct PairCfg {
   static constexpr int kChunksQK = DQK / 64;
   static constexpr int kChunksV = DV / 64;
   static constexpr int kBoxBytes = 128 * 128;
   static constexpr int kTileQK = kChunksQK * kBoxBytes;
   static constexpr int kTileV = kChunksV * kBoxBytes;
-  static constexpr int kKStages = DQK == 64 ? 3 : 2;
+  static constexpr int kKStages = DQK == 64 ? 3 : (DQK == 192 && kM) ? 1 : 2;
   static constexpr int kVStages = DQK == 64 ? 3 : DQK == 128 ? 2 : 1;
   static constexpr int kOffQ = 0;                                   // Q_A, Q_B
   static constexpr int kOffK = kOffQ + 2 * kTileQK;
@@ -113,7 +115,7 @@ __device__ __forceinline__ int tiles_for_rows(const BatchInfo& bi, int qa, int m
 
 template <int DQK, int DV, bool BF16, int MODE>
 __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_constant__ PrefillParams p) {
-  using C = PairCfg<DQK, DV>;
+  using C = PairCfg<DQK, DV, MODE == kMask>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -669,7 +671,7 @@ __global__ void __launch_bounds__(320, 1) prefill_pair_kernel(const __grid_const
 
 template <int DQK, int DV, bool BF16, int MODE>
 cudaError_t launch_pair_one(const PrefillParams& p, cudaStream_t s) {
-  using C = PairCfg<DQK, DV>;
+  using C = PairCfg<DQK, DV, MODE == kMask>;
   static_assert(MODE != kMask || C::kMaskFits, "mask slots do not fit beside the rings");
   auto k = prefill_pair_kernel<DQK, DV, BF16, MODE>;
   constexpr int smem = MODE == kMask ? C::kSmemMask : C::kSmem;
@@ -701,14 +703,6 @@ cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int hea
     case kMask: return launch_pair_one<DQ, DV, BB, kMask>(p, s);            \
     default: return cudaErrorInvalidValue;                                  \
   }
-  // MLA prefill (192 / 128) has no room for the mask slots
-#define FIA_PAIR_MODES_NOMASK(DQ, DV, BB)                                   \
-  switch (mode) {                                                           \
-    case kDense: return launch_pair_one<DQ, DV, BB, kDense>(p, s);          \
-    case kCausal: return launch_pair_one<DQ, DV, BB, kCausal>(p, s);        \
-    case kBand: return launch_pair_one<DQ, DV, BB, kBand>(p, s);            \
-    default: return cudaErrorInvalidValue;                                  \
-  }
   if (head_dim_qk == 128 && head_dim_v == 128) {
     if (bf16) { FIA_PAIR_MODES(128, 128, true) } else { FIA_PAIR_MODES(128, 128, false) }
   }
@@ -716,10 +710,9 @@ cudaError_t launch_prefill_pair(const PrefillParams& p, int head_dim_qk, int hea
     if (bf16) { FIA_PAIR_MODES(64, 64, true) } else { FIA_PAIR_MODES(64, 64, false) }
   }
   if (head_dim_qk == 192 && head_dim_v == 128) {
-    if (bf16) { FIA_PAIR_MODES_NOMASK(192, 128, true) } else { FIA_PAIR_MODES_NOMASK(192, 128, false) }
+    if (bf16) { FIA_PAIR_MODES(192, 128, true) } else { FIA_PAIR_MODES(192, 128, false) }
   }
 #undef FIA_PAIR_MODES
-#undef FIA_PAIR_MODES_NOMASK
   return cudaErrorInvalidValue;
 }
 

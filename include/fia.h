@@ -157,8 +157,8 @@ FIA_API fia_status fia_prefill(const fia_tensor* query, const fia_tensor* key, c
  *          rope tensors given (the query's / key's shape with D 64, same type).
  *   value: key's shape with D 128.  attention_out: query's shape with D 128.
  *   Layouts BSH/BSND/BNSD/TND (the pages list TND), f16 or bf16, GQA allowed.
- *   sparse_mode 0, 2, 3, 4 as fia_prefill; an explicit atten_mask (mode 0 with
- *   a mask, 1) returns FIA_ERR_UNSUPPORTED.  softmax_lse as fia_prefill.
+ *   sparse_mode 0 (with or without atten_mask), 1, 2, 3, 4 and atten_mask as
+ *   fia_prefill.  softmax_lse as fia_prefill.
  * ------------------------------------------------------------------------ */
 FIA_API fia_status fia_prefill_mla_get_workspace_size(const fia_tensor* query, const fia_tensor* key,
                                               const fia_tensor* value, const fia_tensor* query_rope,
@@ -217,7 +217,12 @@ FIA_API fia_status fia_prefill_paged(const fia_tensor* query, const fia_tensor* 
  *          N2 = 1, N1 in {1..128}, key = value = the 512-d latent cache
  *          (blocknum, block_size, 512), key_rope (blocknum, block_size, 64).
  *          scores = scale * (q . k + q_rope . k_rope).
- *   atten_mask: must be absent (masked decode is not implemented).
+ *   atten_mask: with Q_S = 1 (not MLA), bool / int8 / uint8 of shape (B, KV_S),
+ *          (B, 1, KV_S) or (B, 1, 1, KV_S), batch dim B or 1 (broadcast),
+ *          KV_S >= every actual_seq_kvlen, contiguous, device memory; a
+ *          nonzero byte masks its key.  A row whose keys are all masked gets
+ *          0 and softmax_lse +inf.  With Q_S > 1 or MLA it returns
+ *          FIA_ERR_UNSUPPORTED.
  *   attention_out: the query's shape; softmax_lse fp32 (B,N1,Q_S,1) if flagged.
  * ------------------------------------------------------------------------ */
 FIA_API fia_status fia_decode_get_workspace_size(const fia_tensor* query, const fia_tensor* key, const fia_tensor* value,

@@ -174,7 +174,8 @@ def test_paged_prefill_rules(lib):
 
 def test_mla_prefill_rules(lib):
     """MLA prefill: query/key D 192 without rope tensors, or D 128 with both
-    (D 64); value and output D 128; no explicit mask."""
+    (D 64); value and output D 128; an explicit mask is taken as for the
+    plain prefill (a mask too short for the keys is refused)."""
     def ws(q, k, v, out, qr=None, kr=None, mask=None, mode=3):
         prm = params(lib, num_heads=4, num_key_value_heads=2, input_layout="TND", sparse_mode=mode,
                      actual_seq_qlen=[100, 300], actual_seq_kvlen=[100, 300])
@@ -193,7 +194,9 @@ def test_mla_prefill_rules(lib):
     assert ws(q192, k192, t((300, 2, 192)), out) == 5            # value D 128 only
     assert ws(q192, k192, v, t((300, 4, 192))) == 3              # output has value's D
     assert ws(q128, k128, v, out, t((300, 4, 32)), kr) == 3      # rope D 64
-    assert ws(q192, k192, v, out, mask=t((300, 300), B.DTYPE_U8), mode=1) == 5
+    assert ws(q192, k192, v, out, mask=t((300, 300), B.DTYPE_U8), mode=1) == 0
+    assert ws(q128, k128, v, out, qr, kr, mask=t((2, 1, 300, 300), B.DTYPE_BOOL), mode=0) == 0
+    assert ws(q192, k192, v, out, mask=t((300, 150), B.DTYPE_U8), mode=1) != 0   # keys up to 200
 
 
 def test_bsa_fp8_rules(lib):
@@ -264,9 +267,10 @@ def test_paged_prefill_with_mask_and_tnd_fp8_scales(lib):
     assert ws_fp8(t((2, 4, 7, 1), F32), t((2, 2, 3, 1), F32)) == 3
 
 
-def test_mla_prefill_rejects_paged_and_masks(lib):
+def test_mla_prefill_modes_and_masks(lib):
     """MLA prefill runs on contiguous key/value only (its entry takes no block
-    table) and takes no explicit mask; causal and band modes are fine."""
+    table); causal and band modes and an explicit mask (modes 0 and 1) are
+    taken."""
     q, k, v, out = t((300, 4, 192)), t((300, 2, 192)), t((300, 2, 128)), t((300, 4, 128))
 
     def ws(mode, mask=None, **kw):
@@ -278,7 +282,8 @@ def test_mla_prefill_rejects_paged_and_masks(lib):
                                                       ctypes.byref(out), None, ctypes.byref(w))
 
     assert ws(2) == 0 and ws(3) == 0 and ws(4, pre_tokens=64, next_tokens=0) == 0
-    assert ws(0, t((300, 300), B.DTYPE_BOOL)) == 5
+    assert ws(0, t((300, 300), B.DTYPE_BOOL)) == 0 and ws(1, t((1, 300, 300), B.DTYPE_U8)) == 0
+    assert ws(1) != 0   # sparse_mode 1 needs the mask
 
 
 def test_shape_dtype_layout_errors(lib):
@@ -304,12 +309,43 @@ def test_workspace_too_small_rejected_before_launch(lib):
     assert r == 8
 
 
-def decode_ws(lib, q, k, v, prm, qr=None, kr=None, table=None, out=None):
+def decode_ws(lib, q, k, v, prm, qr=None, kr=None, table=None, out=None, mask=None):
     ws = ctypes.c_size_t(0)
     ref = lambda d: ctypes.byref(d) if d is not None else None
-    r = lib.fia_decode_get_workspace_size(ref(q), ref(k), ref(v), ref(qr), ref(kr), ref(table), None,
+    r = lib.fia_decode_get_workspace_size(ref(q), ref(k), ref(v), ref(qr), ref(kr), ref(table), ref(mask),
                                           ctypes.byref(prm.p), ref(out or q), None, ctypes.byref(ws))
     return r, ws.value
+
+
+def test_decode_mask_rules(lib):
+    """Decode atten_mask (Q_S = 1): (B, KV_S), (B, 1, KV_S), (B, 1, 1, KV_S),
+    batch dim B or 1, bool / int8 / uint8, at least the longest sequence's
+    keys; Q_S > 1 or MLA with a mask are not implemented."""
+    q = t((4, 8, 1, 128))
+    pool = t((40, 2, 128, 128))
+    table = t((4, 10), B.DTYPE_I32)
+    ok = params(lib, num_heads=8, num_key_value_heads=2, input_layout="BNSD", block_size=128,
+                actual_seq_kvlen=[100, 1000, 1, 1280])
+    w = lambda m, qq=q, prm=ok: decode_ws(lib, qq, pool, pool, prm, table=table, mask=m)[0]
+    assert w(t((4, 1280), B.DTYPE_U8)) == 0
+    assert w(t((4, 1, 1300), B.DTYPE_BOOL)) == 0
+    assert w(t((1, 1, 1, 1280), B.DTYPE_I8)) == 0
+    assert w(t((4, 1279), B.DTYPE_U8)) == 3                       # shorter than the longest sequence
+    assert w(t((3, 1280), B.DTYPE_U8)) == 3                       # batch dim neither B nor 1
+    assert w(t((4, 2, 1280), B.DTYPE_U8)) == 3                    # middle dims must be 1
+    assert w(t((4, 1, 1, 1, 1280), B.DTYPE_U8)) == 3              # at most 4-D
+    assert w(t((4, 1280), B.DTYPE_F16)) == 2                      # dtype
+    q3 = t((4, 8, 3, 128))
+    prm3 = params(lib, num_heads=8, num_key_value_heads=2, input_layout="BNSD", block_size=128, sparse_mode=3,
+                  actual_seq_kvlen=[100, 1000, 1, 1280])
+    assert w(t((4, 1280), B.DTYPE_U8), q3, prm3) == 5              # Q_S > 1
+    qm = t((2, 1, 128, 512))
+    lat = t((16, 128, 512))
+    prm = params(lib, num_heads=128, num_key_value_heads=1, input_layout="BSND", block_size=128,
+                 actual_seq_kvlen=[256])
+    r, _ = decode_ws(lib, qm, lat, lat, prm, qr=t((2, 1, 128, 64)), kr=t((16, 128, 64)),
+                     table=t((2, 2), B.DTYPE_I32), mask=t((2, 256), B.DTYPE_U8))
+    assert r == 5                                                  # MLA
 
 
 def test_decode_paged_rules(lib):

@@ -345,3 +345,55 @@ def test_small_units_timeout_path(fia):
     ro, rl = _oracle_paged(c)
     assert_out_close(out, ro, c.q.dtype)
     assert_lse_close(lse, rl)
+
+
+# ------------------------------------------------------------ atten_mask (Q_S = 1)
+def _mask_for(c, shape_kind, dtype, workload, pad=5, full_batch=1):
+    """A random key mask over max(kv_lens) + pad keys in the given form; one
+    batch's keys all masked (its rows give 0 and lse +inf)."""
+    B, S = len(c.kv_lens), max(c.kv_lens) + pad
+    shape = {"b": (B, S), "b1": (B, 1, S), "b11": (B, 1, 1, S), "1": (1, S)}[shape_kind]
+    m = fia_inputs.atten_mask(shape, "random", density=0.3, dtype=dtype, workload=workload)
+    if full_batch is not None and shape[0] > 1:
+        m[full_batch] = True if dtype == "bool" else 1
+    return m
+
+
+def _check_masked(fia, c, mask):
+    out, lse = _run_paged(fia, c, atten_mask=mask.cuda())
+    ro, rl = fia_oracle.fia_decode(c.q, c.k_pool, c.v_pool, num_heads=c.num_heads,
+                                   num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
+                                   input_layout="BNSD", actual_seq_kvlen=c.kv_lens, block_table=c.block_table,
+                                   block_size=c.block_size, atten_mask=mask)
+    assert_out_close(out, ro, c.q.dtype)
+    assert_lse_close(lse, rl)
+    return out, lse
+
+
+# (N1, N2, D, mask form, mask dtype, block size): 4-row and 16-row units on the
+# warp-level kernel, 32-row units and head_dim 64 on the tcgen05 kernel
+MASK_DECODE_CASES = [(32, 8, 128, "b", "u8", 128), (8, 1, 128, "b1", "bool", 64), (64, 2, 128, "b11", "i8", 16),
+                     (8, 2, 64, "1", "u8", 128), (4, 4, 128, "b", "bool", 256)]
+
+
+@pytest.mark.parametrize("n1,n2,D,form,mdtype,bs", MASK_DECODE_CASES)
+def test_decode_atten_mask(fia, n1, n2, D, form, mdtype, bs):
+    """atten_mask with one new token: every mask form and dtype, ragged and
+    empty sequences, a batch with every key masked, each kernel."""
+    lens = [1, 0, 127, 128, 129, 700, 2049, 3]
+    c = fia_inputs.paged_decode_case(len(lens), n1, n2, D, lens, block_size=bs, workload=4600 + n1 + D + bs)
+    _check_masked(fia, c, _mask_for(c, form, mdtype, 4700 + n1 + bs, full_batch=None if form == "1" else 5))
+
+
+def test_decode_atten_mask_both_paths_split(fia, decode_path):
+    """Long sequences split over many CTAs (merged partials, the tail merge)
+    with a key mask, on both kernels; an all-zero mask gives the unmasked
+    bits."""
+    lens = [16384, 9000, 5000, 1]
+    c = fia_inputs.paged_decode_case(len(lens), 32, 8, 128, lens, block_size=128, workload=4800)
+    _check_masked(fia, c, _mask_for(c, "b", "u8", 4801, full_batch=3))
+    zero = torch.zeros((len(lens), max(lens)), dtype=torch.uint8)
+    out_z, lse_z = _run_paged(fia, c, atten_mask=zero.cuda())
+    out_n, lse_n = _run_paged(fia, c)
+    assert torch.equal(out_z, out_n) and torch.equal(lse_z, lse_n)
+

@@ -13,10 +13,10 @@ pytestmark = pytest.mark.gpu
 INT32_MAX = 2147483647
 
 
-def _run(fia, c, mode, pre=INT32_MAX, nxt=INT32_MAX):
+def _run(fia, c, mode, pre=INT32_MAX, nxt=INT32_MAX, mask=None):
     cuda = lambda x: None if x is None else x.cuda()
     out, lse = fia.fia_prefill_mla(c.q.cuda(), c.k.cuda(), c.v.cuda(), query_rope=cuda(c.q_rope),
-                                   key_rope=cuda(c.k_rope), num_heads=c.num_heads,
+                                   key_rope=cuda(c.k_rope), atten_mask=cuda(mask), num_heads=c.num_heads,
                                    num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
                                    input_layout=c.layout, sparse_mode=mode, pre_tokens=pre, next_tokens=nxt,
                                    actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
@@ -25,8 +25,9 @@ def _run(fia, c, mode, pre=INT32_MAX, nxt=INT32_MAX):
     return out, lse
 
 
-def _oracle(c, mode, pre=INT32_MAX, nxt=INT32_MAX, rows=None):
-    return fia_oracle.fia_prefill(c.q, c.k, c.v, query_rope=c.q_rope, key_rope=c.k_rope, num_heads=c.num_heads,
+def _oracle(c, mode, pre=INT32_MAX, nxt=INT32_MAX, rows=None, mask=None):
+    return fia_oracle.fia_prefill(c.q, c.k, c.v, query_rope=c.q_rope, key_rope=c.k_rope, atten_mask=mask,
+                                  num_heads=c.num_heads,
                                   num_key_value_heads=c.num_key_value_heads, scale_value=c.scale,
                                   input_layout=c.layout, sparse_mode=mode, pre_tokens=pre, next_tokens=nxt,
                                   actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen, rows=rows)
@@ -58,6 +59,49 @@ def test_mla_prefill_padded_layouts(fia, layout, rope, mode):
                                     workload=4100 + mode)
     kw = {"pre": 100, "nxt": 20} if mode == 4 else {}
     _check(fia, c, mode, **kw)
+
+
+# (mode, layout, rope, dtype, mask shape, mask dtype, kind, pre, next): q lengths 300 / 129, key
+# lengths 260 / 400, so S1 = 300 and S2 = 400 (+ padding of the mask's key axis)
+MLA_MASK_CASES = [
+    (1, "BNSD", True, "bf16", (2, 300, 400), "u8", "random", None, None),
+    (1, "BSND", False, "f16", (300, 416), "bool", "blocks", None, None),
+    (0, "BSH", True, "bf16", (2, 1, 300, 401), "i8", "blocks", 100, 20),
+    (0, "BNSD", False, "bf16", (1, 300, 400), "u8", "random", 0, 300),
+]
+
+
+@pytest.mark.parametrize("mode,layout,rope,dtype,mshape,mdtype,kind,pre,nxt", MLA_MASK_CASES)
+def test_mla_prefill_explicit_mask(fia, mode, layout, rope, dtype, mshape, mdtype, kind, pre, nxt):
+    """An explicit atten_mask with MLA prefill (sparse_mode 1, and 0 with the
+    pre/next window): mask shapes and dtypes, ragged query and key tails,
+    fully masked rows, both input forms, element by element."""
+    c = fia_inputs.mla_prefill_case([300, 129], [260, 400], 4, 2, rope=rope, dtype=dtype, layout=layout,
+                                    workload=4300 + mode + mshape[-1])
+    mask = fia_inputs.atten_mask(mshape, kind, dtype=mdtype, workload=4400 + mshape[-1])
+    kw = {} if pre is None else {"pre": pre, "nxt": nxt}
+    out, lse = _run(fia, c, mode, mask=mask, **kw)
+    ref_o, ref_l = _oracle(c, mode, mask=mask, **kw)
+    assert_out_close(out, ref_o, c.q.dtype)
+    assert_lse_close(lse, ref_l)
+
+
+def test_mla_prefill_mask_tnd_and_causal_bits(fia):
+    """TND with a per-sequence mask indexed by each sequence's own rows and
+    keys, against the oracle; and a lower-triangular mask in sparse_mode 1
+    gives the same bits as sparse_mode 2 (the masked tiles only add zeros)."""
+    lens_q, lens_kv = [1, 127, 300, 0, 700, 129], [5, 127, 260, 3, 700, 200]
+    c = fia_inputs.mla_prefill_case(lens_q, lens_kv, 8, 2, rope=True, layout="TND", workload=4500)
+    mask = fia_inputs.atten_mask((6, 700, 704), "blocks", workload=4501)
+    out, lse = _run(fia, c, 1, mask=mask)
+    ref_o, ref_l = _oracle(c, 1, mask=mask)
+    assert_out_close(out, ref_o, c.q.dtype)
+    assert_lse_close(lse, ref_l)
+    c2 = fia_inputs.mla_prefill_case([700, 300], [700, 300], 4, 4, rope=False, layout="BNSD", workload=4502)
+    causal = fia_inputs.atten_mask((700, 704), "causal")
+    out_m, lse_m = _run(fia, c2, 1, mask=causal)
+    out_c, lse_c = _run(fia, c2, 2)
+    assert torch.equal(out_m, out_c) and torch.equal(lse_m, lse_c)
 
 
 def test_mla_prefill_forms_agree(fia):
