@@ -81,14 +81,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2_lo8(uint32_t w, bool hi) {
   return ((t << 7) & 0x3f803f80u) | ((t << 8) & 0x80008000u);
 }
 
-// Tiles one query tile visits: the mask row's kept 128-key tiles.
+// Tiles one query tile visits: the mask row's kept 128-key tiles (every
+// tile without a mask: dense FP8 attention).
 struct MaskIter {
   int n;
   const uint8_t* mrow;
   int y;
   __device__ __forceinline__ int next(int t) const {
     for (int u = t + 1; u < n; ++u)
-      if (mrow[(u * kTileN) / y] != 0) return u;
+      if (mrow == nullptr || mrow[(u * kTileN) / y] != 0) return u;
     return -1;
   }
 };
@@ -137,7 +138,9 @@ __global__ void __launch_bounds__(192, 1) bsa_fp8_kernel(const __grid_constant__
 
   MaskIter iter;
   iter.n = (bi.kv_len + kTileN - 1) / kTileN;
-  iter.mrow = p.bsa_mask + ((int64_t(it.b) * p.num_heads + it.h) * p.bsa_nqb + q0 / p.bsa_x) * p.bsa_nkb;
+  iter.mrow = p.bsa_mask != nullptr
+                  ? p.bsa_mask + ((int64_t(it.b) * p.num_heads + it.h) * p.bsa_nqb + q0 / p.bsa_x) * p.bsa_nkb
+                  : nullptr;
   iter.y = p.bsa_y;
   // dequant scales: the query block of this CTA, the key / value block of tile t
   const float q_scale = p.fp8_qscale[(int64_t(it.b) * p.num_heads + it.h) * p.fp8_nqs + q0 / kTileM];

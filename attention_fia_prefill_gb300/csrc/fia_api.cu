@@ -969,14 +969,17 @@ static fia_status bsa_validate(const fia_tensor* query, const fia_tensor* key, c
   const int64_t X = block_shape[0], Y = block_shape[1];
   if (X <= 0 || Y <= 0 || Y % 128 != 0) return fail(FIA_ERR_SHAPE, "block_shape [%lld,%lld]: X > 0 and Y a multiple of 128", (long long)X, (long long)Y);
   if (X % 128 != 0) return fail(FIA_ERR_UNSUPPORTED, "block_shape X=%lld: this library needs a multiple of 128", (long long)X);
-  if (!present(mask)) return fail(FIA_ERR_NULL, "block_sparse_mask is required");
-  if (mask->dtype != FIA_DTYPE_U8 && mask->dtype != FIA_DTYPE_BOOL) return fail(FIA_ERR_DTYPE, "block_sparse_mask must be uint8/bool");
+  // FP8 without a mask: every block kept (dense FP8 attention)
+  if (!present(mask) && !fp8) return fail(FIA_ERR_NULL, "block_sparse_mask is required");
+  if (present(mask) && mask->dtype != FIA_DTYPE_U8 && mask->dtype != FIA_DTYPE_BOOL)
+    return fail(FIA_ERR_DTYPE, "block_sparse_mask must be uint8/bool");
   int64_t maxq = 0, maxk = 0;
   for (const auto& bi : g.batches) { maxq = std::max<int64_t>(maxq, bi.q_len); maxk = std::max<int64_t>(maxk, bi.kv_len); }
   if (g.layout != L_TND && params->actual_seq_qlen == nullptr) { maxq = g.S1; maxk = g.S2; }
   nqb = int((maxq + X - 1) / X);
   nkb = int((maxk + Y - 1) / Y);
-  if (!(mask->ndim == 4 && mask->shape[0] == g.B && mask->shape[1] == g.N1 && mask->shape[2] == nqb && mask->shape[3] == nkb))
+  if (present(mask) &&
+      !(mask->ndim == 4 && mask->shape[0] == g.B && mask->shape[1] == g.N1 && mask->shape[2] == nqb && mask->shape[3] == nkb))
     return fail(FIA_ERR_SHAPE, "block_sparse_mask must be (B, N1, %d, %d)", nqb, nkb);
   if (params->sparse_mode != 0) return fail(FIA_ERR_SPARSE_MODE, "block-sparse attention takes no sparse_mode");
   if (fp8) {
@@ -1064,8 +1067,9 @@ fia_status bsa_forward_fp8(const fia_tensor* query, const fia_tensor* key, const
                                g, nqb, nkb, q_dequant_scale, k_dequant_scale, v_dequant_scale);
   if (st != FIA_OK) return st;
   return run_prefill(g, kBlockSparse, 0, query, key, value, attention_out, softmax_lse, params,
-                     static_cast<const uint8_t*>(block_sparse_mask->data), nqb, nkb, int(block_shape[0]),
-                     int(block_shape[1]), workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+                     present(block_sparse_mask) ? static_cast<const uint8_t*>(block_sparse_mask->data) : nullptr,
+                     nqb, nkb, int(block_shape[0]), int(block_shape[1]), workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

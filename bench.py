@@ -585,6 +585,40 @@ def measure_bsa_fp8(torch, dev, timer, steps, warmup, pk, traffic, pool):
                             peak=peak, extra={"peak_source": "measured bf16 x 4/3, derived (nominal fp8 = 2x bf16)"})
 
 
+def measure_fp8_dense(torch, dev, timer, steps, warmup, pk, traffic, pool):
+    """Dense FP8 prefill (the FP8 block-sparse call without a mask: every
+    key), B=2 32/8 heads S=4096 D=128, per-block scales; the same blended
+    peak as the block-sparse FP8 section."""
+    import numpy as np
+    import attention_fia_prefill_gb300 as fia
+    import fia_inputs
+    f = fia_inputs.workload_fp8_dense()
+    c = f.base
+    flops = bsa_flops(c)
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    qs, ks, vs = f.q_scale.to(dev), f.k_scale.to(dev), f.v_scale.to(dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q.shape[0], c.num_heads, q.shape[2], 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(16 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        fia.bsa_forward(q, k, v, None, c.block_shape, num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
+                        scale_value=c.scale, input_layout="BNSD", softmax_lse_flag=True, out=out, softmax_lse=lse,
+                        workspace=ws, q_dequant_scale=qs, k_dequant_scale=ks, v_dequant_scale=vs)
+
+    cpu = None
+    if pool:
+        rng = np.random.default_rng(8)
+        units = [(int(rng.integers(2)), int(rng.integers(32)), 4 * int(rng.integers(8))) for _ in range(pool.n)]
+        cpu = pool.run(oracle_tasks_bsa(c, units, 4, fp8=(f.q_scale, f.k_scale, f.v_scale)), 1e12, "TFLOP/s",
+                       f"{len(units)} runs of 4 query blocks of one (batch, head)")
+    peak = round(pk["bf16_tflops"] * 4 / 3, 1)
+    return _prefill_section("dense FP8 e4m3 prefill (per-block scales, no mask), B=2 32/8 heads S=4096, bf16 out",
+                            flops, call, timer, max(3, steps // 4), max(3, warmup), pk, "bsa_fp8_kernel_dense",
+                            traffic, cpu, peak=peak,
+                            extra={"peak_source": "measured bf16 x 4/3, derived (nominal fp8 = 2x bf16)"})
+
+
 def measure_small_prefill(torch, dev, timer, steps, warmup, pk, traffic, pool):
     import attention_fia_prefill_gb300 as fia
     import fia_inputs
@@ -772,7 +806,8 @@ def run_ours(args):
         pool = OraclePool()
     if not args.headline_only:
         # least important first: the driver keeps the tail of the line
-        for name, fn in (("prefill_small", measure_small_prefill), ("bsa_fp8", measure_bsa_fp8),
+        for name, fn in (("prefill_small", measure_small_prefill), ("fp8_dense", measure_fp8_dense),
+                         ("bsa_fp8", measure_bsa_fp8),
                          ("mla_prefill", measure_mla_prefill), ("prefill_band", measure_prefill_band),
                          ("prefill_mask", measure_prefill_mask), ("chunked_prefill", measure_chunked_prefill),
                          ("decode_q4", measure_decode_tokens), ("bsa", measure_bsa), ("mla_decode", measure_mla),
@@ -892,10 +927,11 @@ def run_profile_target(args):
             fia.fia_decode(q, lat, lat, query_rope=qr, key_rope=rope, block_table=tb, block_size=c.block_size,
                            actual_seq_kvlen=c.kv_lens, num_heads=c.num_heads, num_key_value_heads=1,
                            scale_value=c.scale, input_layout="BSND", softmax_lse_flag=True)
-    elif name == "bsa_fp8":
-        f = fia_inputs.workload_bsa_fp8()
+    elif name in ("bsa_fp8", "fp8_dense"):
+        f = fia_inputs.workload_bsa_fp8() if name == "bsa_fp8" else fia_inputs.workload_fp8_dense()
         c = f.base
-        q, k, v, m = c.q.to(dev), c.k.to(dev), c.v.to(dev), c.mask.to(dev)
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        m = c.mask.to(dev) if name == "bsa_fp8" else None
         qs, ks, vs = f.q_scale.to(dev), f.k_scale.to(dev), f.v_scale.to(dev)
 
         def call():
@@ -950,7 +986,7 @@ def run_profile_target(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, decode_q4, prefill_tnd, prefill_band, prefill_mask, chunked, bsa, bsa_fp8, mla, mla_prefill)")
+    ap.add_argument("--profile", default=None, help="only run plain calls of one workload (decode, decode_q4, prefill_tnd, prefill_band, prefill_mask, chunked, bsa, bsa_fp8, fp8_dense, mla, mla_prefill)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)

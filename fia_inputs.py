@@ -436,6 +436,16 @@ def workload_bsa(B=2, N1=32, N2=8, S=16384, D=128, workload=5) -> BSACase:
     return bsa_case(B, N1, N2, S, S, D, 128, 128, 0.25, "bf16", workload)
 
 
+def workload_fp8_dense(B=2, N1=32, N2=8, S=4096, workload=6) -> BSAFp8Case:
+    """Dense FP8 e4m3 prefill (D = 128, no mask: every key): B=2, 32/8 heads,
+    S=4096, per-block dequant scales of 128 query rows / 256 key rows.  The
+    case's block mask is all ones (what the oracle and the FLOP count take);
+    the call passes none."""
+    f = bsa_fp8_case(B, N1, N2, S, S, 256, 1.0, workload)
+    f.base.mask = torch.ones_like(f.base.mask)
+    return f
+
+
 def workload_bsa_fp8(B=2, N1=32, N2=8, S=16384, workload=5) -> BSAFp8Case:
     """Block-sparse prefill FP8 e4m3 (D = 128): 128 x 256 blocks (the
     quantisation blocks), diagonal + ~25% of the rest."""

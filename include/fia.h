@@ -296,6 +296,8 @@ FIA_API fia_status bsa_forward(const fia_tensor* query, const fia_tensor* key, c
  *   query/key/value: float8 e4m3 (FIA_DTYPE_F8E4M3), D = 128, layouts as
  *          bsa_forward.
  *   block_shape: {128, 256} or {128, 512} (the quantisation blocks).
+ *   block_sparse_mask: as bsa_forward, or NULL: every block kept, which is
+ *          dense (sparse_mode 0) FP8 prefill attention with the same scales.
  *   q_dequant_scale: fp32 (B, N1, ceil(maxQS/128), 1); k_dequant_scale and
  *          v_dequant_scale: fp32 (B, N2, ceil(maxKVS/Y), 1); device memory;
  *          every scale must be positive.  The scales are read on the device

@@ -227,6 +227,7 @@ def test_bsa_fp8_rules(lib):
     assert ws(vs=None) == 1                                     # all three scales
     q64, k64 = t((2, 4, 300, 64), F8), t((2, 2, 600, 64), F8)
     assert ws(q=q64, k=k64, out=t((2, 4, 300, 64), B.DTYPE_BF16)) == 5   # D 128 only
+    assert ws(mask=None) == 0                                   # no mask: dense FP8 attention
 
 
 def test_paged_prefill_with_mask_and_tnd_fp8_scales(lib):
@@ -407,8 +408,9 @@ def test_decode_query_token_limits(lib):
 def bsa_ws(lib, q, k, v, mask, shape, prm):
     ws = ctypes.c_size_t(0)
     s = (ctypes.c_int64 * 2)(*shape)
-    r = lib.bsa_get_workspace_size(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(mask), s,
-                                   ctypes.byref(prm.p), ctypes.byref(q), None, ctypes.byref(ws))
+    m = ctypes.byref(mask) if mask is not None else None
+    r = lib.bsa_get_workspace_size(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), m, s, ctypes.byref(prm.p),
+                                   ctypes.byref(q), None, ctypes.byref(ws))
     return r, ws.value
 
 
@@ -430,6 +432,7 @@ def test_bsa_rules(lib):
     q96 = t((2, 8, 1000, 96))
     assert bsa_ws(lib, q96, q96, q96, good_mask, (128, 128), params(lib, num_heads=8, input_layout="BNSD"))[0] == 5
     assert bsa_ws(lib, q, k, k, good_mask, (64, 128), prm)[0] == 5      # X not a multiple of 128 (library limit)
+    assert bsa_ws(lib, q, k, k, None, (128, 128), prm)[0] == 1          # the bf16 entry needs its mask
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

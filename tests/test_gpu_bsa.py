@@ -73,7 +73,8 @@ def test_full_bsa_workload_sampled(fia):
 # ------------------------------------------------------------ FP8
 def _run_fp8(fia, f, **kw):
     c = f.base
-    out, lse = fia.bsa_forward(c.q.cuda(), c.k.cuda(), c.v.cuda(), c.mask.cuda(), c.block_shape,
+    m = None if c.mask is None else c.mask.cuda()
+    out, lse = fia.bsa_forward(c.q.cuda(), c.k.cuda(), c.v.cuda(), m, c.block_shape,
                                num_heads=c.num_heads, num_key_value_heads=c.num_key_value_heads,
                                scale_value=c.scale, input_layout=c.layout, softmax_lse_flag=True,
                                actual_seq_qlen=c.actual_seq_qlen, actual_seq_kvlen=c.actual_seq_kvlen,
@@ -154,6 +155,25 @@ def test_fp8_workload_sampled(fia):
     _assert_fp8_close(f, got, np.stack([o for o, _ in ref]))
     for (b, h, i), (_, l_ref) in zip(rows, ref):
         assert abs(float(lse[b, h, i, 0]) - l_ref) <= 1e-3 * max(1.0, abs(l_ref)), (b, h, i)
+
+
+def test_fp8_dense_without_mask(fia):
+    """FP8 prefill without a block mask (every block kept, dense attention):
+    against the oracle with an all-ones mask, and the same bits as the call
+    given that all-ones mask."""
+    f = fia_inputs.bsa_fp8_case(2, 4, 2, 300, 600, 256, keep=0.4, workload=3650)
+    f.base.mask = torch.ones_like(f.base.mask)
+    out_m, lse_m = _run_fp8(fia, f)
+    ro, rl = _oracle_fp8(f)
+    _assert_fp8_close(f, out_m, ro)
+    assert_lse_close(lse_m, rl)
+    mask = f.base.mask
+    f.base.mask = None
+    try:
+        out_n, lse_n = _run_fp8(fia, f)
+    finally:
+        f.base.mask = mask
+    assert torch.equal(out_m, out_n) and torch.equal(lse_m, lse_n)
 
 
 @pytest.mark.parametrize("which", ["q", "k", "v"])
