@@ -30,6 +30,7 @@ EXPORTS = [
     "fia_decode", "bsa_get_workspace_size", "bsa_forward", "bsa_fp8_get_workspace_size", "bsa_forward_fp8",
     "fia_device_status", "fia_status_string",
     "fia_last_error", "fia_profile_next_call", "fia_debug_set_wait_limit_ns", "fia_debug_set_decode_path", "fia_decode_no_alloc",
+    "fia_debug_plan_decode",
 ]
 
 
@@ -113,6 +114,10 @@ def load_library(path: str | None = None):
     lib.fia_debug_set_decode_path.restype = None
     lib.fia_decode_no_alloc.argtypes = [T, T, T, T, T, T, T, P, T, T, vp]
     lib.fia_decode_no_alloc.restype = st
+    i32p, ip = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int)
+    lib.fia_debug_plan_decode.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, i32p,
+                                          ctypes.c_int, i32p, ctypes.c_int, ip, ip]
+    lib.fia_debug_plan_decode.restype = st
     if path is None:
         _lib = lib
     return lib
@@ -428,6 +433,25 @@ def bsa_forward(query, key, value, block_sparse_mask, block_shape, *, actual_seq
                             (_ref(dq), _ref(dk), _ref(dv), _ref(dmask), shape, ctypes.byref(prm.p), _ref(do),
                              _ref(dl)), workspace, query.device)
     return out, softmax_lse
+
+
+def debug_plan_decode(kv_len, num_key_value_heads, n_cta_max):
+    """The decode plan the library deals (host only): returns (cta_seg of
+    n_cta + 1 entries, segs as rows (unit, stage_begin, stage_end, part),
+    unit_parts as rows (first part, parts)) as lists."""
+    lib = load_library()
+    B, N2 = len(kv_len), int(num_key_value_heads)
+    n_units = B * N2
+    cap_cta, cap_segs = int(n_cta_max) + 1, 4 * (n_units + int(n_cta_max) + 1)
+    lens = (ctypes.c_int32 * max(B, 1))(*[int(x) for x in kv_len])
+    cta_seg = (ctypes.c_int32 * cap_cta)()
+    segs = (ctypes.c_int32 * cap_segs)()
+    parts = (ctypes.c_int32 * max(2 * n_units, 1))()
+    n_cta, n_segs = ctypes.c_int(0), ctypes.c_int(0)
+    check(lib.fia_debug_plan_decode(lens, B, N2, int(n_cta_max), cta_seg, cap_cta, segs, cap_segs, parts,
+                                    max(2 * n_units, 1), ctypes.byref(n_cta), ctypes.byref(n_segs)))
+    return (list(cta_seg[:n_cta.value + 1]), [tuple(segs[4 * i:4 * i + 4]) for i in range(n_segs.value)],
+            [tuple(parts[2 * u:2 * u + 2]) for u in range(n_units)])
 
 
 def profile_next_call(start_event, stop_event):

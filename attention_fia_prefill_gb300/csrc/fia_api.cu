@@ -1619,4 +1619,37 @@ fia_status fia_decode(const fia_tensor* query, const fia_tensor* key, const fia_
                     "decode launch");
 }
 
+
+fia_status fia_debug_plan_decode(const int32_t* kv_len, int B, int N2, int n_cta_max, int32_t* cta_seg,
+                                 int cta_seg_cap, int32_t* segs, int segs_cap, int32_t* unit_parts,
+                                 int unit_parts_cap, int* n_cta, int* n_segs) {
+  if (kv_len == nullptr || cta_seg == nullptr || segs == nullptr || unit_parts == nullptr || n_cta == nullptr ||
+      n_segs == nullptr)
+    return fail(FIA_ERR_NULL, "fia_debug_plan_decode: NULL argument");
+  if (B < 0 || N2 < 1 || n_cta_max < 1) return fail(FIA_ERR_SHAPE, "fia_debug_plan_decode: B >= 0, N2 >= 1, CTAs >= 1");
+  DecodeGeometry g;
+  g.B = B;
+  g.N2 = N2;
+  g.kv_len.assign(kv_len, kv_len + B);
+  DecodePlan pl;
+  plan_decode(g, n_cta_max, pl, 128, kDecodeSegmentCost);
+  if (int64_t(pl.n_cta) + 1 > cta_seg_cap || int64_t(pl.segs.size()) * 4 > segs_cap ||
+      int64_t(pl.n_units) * 2 > unit_parts_cap)
+    return fail(FIA_ERR_SHAPE, "fia_debug_plan_decode: output capacity too small");
+  for (int c = 0; c <= pl.n_cta; ++c) cta_seg[c] = pl.n_cta > 0 ? pl.cta_seg[size_t(c)] : 0;
+  for (size_t i = 0; i < pl.segs.size(); ++i) {
+    segs[4 * i] = pl.segs[i].unit;
+    segs[4 * i + 1] = pl.segs[i].stage_begin;
+    segs[4 * i + 2] = pl.segs[i].stage_end;
+    segs[4 * i + 3] = pl.segs[i].part;
+  }
+  for (int u = 0; u < pl.n_units; ++u) {
+    unit_parts[2 * u] = pl.unit_parts[size_t(u)].x;
+    unit_parts[2 * u + 1] = pl.unit_parts[size_t(u)].y;
+  }
+  *n_cta = pl.n_cta;
+  *n_segs = int(pl.segs.size());
+  return FIA_OK;
+}
+
 }  // extern "C"

@@ -357,6 +357,18 @@ FIA_API void fia_debug_set_wait_limit_ns(uint64_t ns);
  * Meant for tests that compare the two. */
 FIA_API void fia_debug_set_decode_path(int path);
 
+/* Test hook, host only (no device work): the plan fia_decode deals for
+ * per-batch lengths kv_len[0..B) (host memory) and N2 kv heads over at most
+ * n_cta_max CTAs, with the same per-segment charge as fia_decode.  Writes
+ * cta_seg[0..n_cta] (the first segment of each CTA, then the total),
+ * segs[4 i .. 4 i + 3] = (unit, first 128-key stage, end stage, part) for each
+ * segment in CTA order, unit_parts[2 u .. 2 u + 1] = (first part, parts) for
+ * each unit u = b * N2 + kv head, and the counts.  Returns FIA_ERR_SHAPE if a
+ * capacity is too small, FIA_ERR_NULL for a NULL pointer. */
+FIA_API fia_status fia_debug_plan_decode(const int32_t* kv_len, int B, int N2, int n_cta_max, int32_t* cta_seg,
+                                         int cta_seg_cap, int32_t* segs, int segs_cap, int32_t* unit_parts,
+                                         int unit_parts_cap, int* n_cta, int* n_segs);
+
 #ifdef __cplusplus
 }
 #endif
