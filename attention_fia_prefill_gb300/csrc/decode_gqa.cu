@@ -39,16 +39,18 @@ constexpr int kGqaWarmStages = 4;          // stages warmed in L2 before the gri
 constexpr int kGqaBarBytes = 1024;
 
 // Shared memory of the kernel for units of kRows (4 or 16) rows: the K and V
-// rings, each warp's O of a segment (its rows x 128, fp32) and (max, sum) per
-// row, the barriers.  With 16 rows the O buffer takes 64 KB, so the V ring
-// has two slots (a third slot hardly changes the streaming rate).
+// rings (three slots each), each warp's O of a segment (fp32, kERows x 128:
+// 16-row units go through it in two passes of 8 rows, which leaves the room
+// for the third V slot) and (max, sum) per row, the barriers.
 template <int kRows>
 struct GqaCfg {
-  static constexpr int kVS = kRows == 4 ? 3 : 2;
+  static constexpr int kVS = 3;
+  static constexpr int kERows = kRows == 16 ? 8 : kRows;   // rows per warp in one pass
+  static constexpr int kPasses = kRows / kERows;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kGqaKS * kGqaTile;
-  static constexpr int kOffE = kOffV + kVS * kGqaTile;             // [warp][kRows][128]
-  static constexpr int kOffML = kOffE + kGqaW * kRows * 128 * 4;   // [warp][kRows] (max, sum)
+  static constexpr int kOffE = kOffV + kVS * kGqaTile;              // [warp][kERows][128]
+  static constexpr int kOffML = kOffE + kGqaW * kERows * 128 * 4;   // [warp][kRows] (max, sum)
   static constexpr int kOffBar = kOffML + kGqaW * kRows * 8;
   static constexpr int kSmem = kOffBar + kGqaBarBytes + 1024;
   static_assert(kSmem <= kDecodeSmemMax, "shared memory budget");
@@ -384,99 +386,106 @@ __global__ void __launch_bounds__(kGqaThreads, 1) decode_gqa_kernel(const __grid
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
       }
-      // the buffers are free once every warp has read the previous segment's
-      if (segi > 0 && !warp_wait(&bar->efree, uint32_t(segi - 1) & 1u, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      if (ft == 0) {
-        if (ra < kRows) mlbuf[w * kRows + ra] = make_float2(m_run[0], l[0]);
-        if (kTwo) mlbuf[w * kRows + rb] = make_float2(m_run[1], l[1]);
-      }
-      if (kTwo || ft < 2) {
-#pragma unroll
-        for (int h = 0; h < NT; ++h) {
-          float* e0 = ebuf + (w * kRows + 8 * h + 2 * ft) * D + fg;   // row 2t (+ 8); row 2t + 1 is D further
+      // ---- the unit's rows: one partial (O / l, lse) each, or attention_out
+      // and softmax_lse when the unit lies in this segment alone.  4 rows:
+      // warp w takes row w % 4, elements [64 (w / 4), + 64); 16 rows: rows
+      // 2w and 2w + 1, all 128 elements, in the pass (of two, 8 rows each)
+      // that holds them.
+      const int2 up = pl.unit_parts(sg.unit);
+      const bool whole = up.y == 1;
+      const bool tail = segi + 1 == nseg && !whole;
+      constexpr int kRowsPerWarp = kTwo ? 2 : 1;
+      constexpr int kCols = kTwo ? 4 : 2;   // elements per lane
+      constexpr int NP = C::kPasses, ER = C::kERows;
+      float own_o[kRowsPerWarp][kCols], own_lse[kRowsPerWarp];   // this segment's partial of the warp's slice
+      for (int ps = 0; ps < NP; ++ps) {
+        const int pidx = segi * NP + ps;   // passes so far: the phase of esync / efree
+        // the buffers are free once every warp has read the previous pass's
+        if (pidx > 0 && !warp_wait(&bar->efree, uint32_t(pidx - 1) & 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        if (ps == 0 && ft == 0) {
+          if (ra < kRows) mlbuf[w * kRows + ra] = make_float2(m_run[0], l[0]);
+          if (kTwo) mlbuf[w * kRows + rb] = make_float2(m_run[1], l[1]);
+        }
+        if (kTwo || ft < 2) {
+          // rows 2t, 2t + 1 of the pass (row 2t + 1 is D further); 16 rows:
+          // O^T row tile ps
+          float* e0 = ebuf + (w * ER + 2 * ft) * D + fg;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
+            const int h = kTwo ? ps : 0;
             e0[16 * mt] = o[mt][h][0];
             e0[D + 16 * mt] = o[mt][h][1];
             e0[16 * mt + 8] = o[mt][h][2];
             e0[D + 16 * mt + 8] = o[mt][h][3];
           }
         }
-      }
-      warp_arrive(&bar->esync);
-      if (!warp_wait(&bar->esync, uint32_t(segi) & 1u, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      // ---- the unit's rows: one partial (O / l, lse) each, or attention_out
-      // and softmax_lse when the unit lies in this segment alone.  4 rows:
-      // warp w takes row w % 4, elements [64 (w / 4), + 64); 16 rows: rows
-      // 2w and 2w + 1, all 128 elements.
-      const int2 up = pl.unit_parts(sg.unit);
-      const bool whole = up.y == 1;
-      const bool tail = segi + 1 == nseg && !whole;
-      constexpr int kRowsPerWarp = kTwo ? 2 : 1;
-      constexpr int kCols = kTwo ? 4 : 2;   // elements per lane
-      float own_o[kRowsPerWarp][kCols], own_lse[kRowsPerWarp];   // this segment's partial of the warp's slice
+        warp_arrive(&bar->esync);
+        if (!warp_wait(&bar->esync, uint32_t(pidx) & 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int r = kTwo ? 2 * w + i : (w & 3);
-        const int dcol = kTwo ? kCols * lane : 64 * (w >> 2) + kCols * lane;
-        if (r >= g) continue;
-        float M = -INFINITY;
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          const int r = kTwo ? 2 * w + i : (w & 3);
+          const int dcol = kTwo ? kCols * lane : 64 * (w >> 2) + kCols * lane;
+          if (r >= g || (kTwo && (r >> 3) != ps)) continue;
+          const int er = r - ER * ps;   // the row's place in this pass
+          float M = -INFINITY;
 #pragma unroll
-        for (int x = 0; x < kGqaW; ++x) M = fmaxf(M, mlbuf[x * kRows + r].x);
-        const float Mo = M == -INFINITY ? 0.f : M;
-        float Ls = 0.f;
-        float acc[kCols] = {};
+          for (int x = 0; x < kGqaW; ++x) M = fmaxf(M, mlbuf[x * kRows + r].x);
+          const float Mo = M == -INFINITY ? 0.f : M;
+          float Ls = 0.f;
+          float acc[kCols] = {};
 #pragma unroll
-        for (int x = 0; x < kGqaW; ++x) {
-          const float2 ml = mlbuf[x * kRows + r];
-          const float wt = fast_exp2(ml.x - Mo);
-          Ls += ml.y * wt;
-          const float* src = ebuf + (x * kRows + r) * D + dcol;
-          if constexpr (kCols == 4) {
-            const float4 ov = *reinterpret_cast<const float4*>(src);
-            acc[0] += wt * ov.x; acc[1] += wt * ov.y; acc[2] += wt * ov.z; acc[3] += wt * ov.w;
+          for (int x = 0; x < kGqaW; ++x) {
+            const float2 ml = mlbuf[x * kRows + r];
+            const float wt = fast_exp2(ml.x - Mo);
+            Ls += ml.y * wt;
+            const float* src = ebuf + (x * ER + er) * D + dcol;
+            if constexpr (kCols == 4) {
+              const float4 ov = *reinterpret_cast<const float4*>(src);
+              acc[0] += wt * ov.x; acc[1] += wt * ov.y; acc[2] += wt * ov.z; acc[3] += wt * ov.w;
+            } else {
+              const float2 ov = *reinterpret_cast<const float2*>(src);
+              acc[0] += wt * ov.x; acc[1] += wt * ov.y;
+            }
+          }
+          const bool has = Ls > 0.f;
+          const float inv = has ? 1.f / Ls : 0.f;
+          const float lse = has ? (M + __log2f(Ls)) * 0.69314718055994531f : INFINITY;
+          const bool lse_lane = lane == 0 && (kTwo || w < 4);
+          if (whole) {
+            const int head = kvh * p.group + r / p.q_tokens, tok = r % p.q_tokens;
+            T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
+                      int64_t(tok) * p.out_ss + dcol;
+            if constexpr (kCols == 4) {
+              *reinterpret_cast<uint2*>(orow) =
+                  make_uint2(pack2(acc[0] * inv, acc[1] * inv, BF16), pack2(acc[2] * inv, acc[3] * inv, BF16));
+            } else {
+              *reinterpret_cast<uint32_t*>(orow) = pack2(acc[0] * inv, acc[1] * inv, BF16);
+            }
+            if (lse_lane && p.lse != nullptr)
+              p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] = lse;
           } else {
-            const float2 ov = *reinterpret_cast<const float2*>(src);
-            acc[0] += wt * ov.x; acc[1] += wt * ov.y;
+            const int64_t part = sg.part;
+            float* prow = p.part_o + (part * g + r) * D + dcol;
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) own_o[i][c] = acc[c] * inv;
+            own_lse[i] = has ? lse : -INFINITY;
+            if constexpr (kCols == 4) {
+              *reinterpret_cast<float4*>(prow) = make_float4(own_o[i][0], own_o[i][1], own_o[i][2], own_o[i][3]);
+            } else {
+              *reinterpret_cast<float2*>(prow) = make_float2(own_o[i][0], own_o[i][1]);
+            }
+            if (lse_lane) p.part_lse[part * g + r] = own_lse[i];
           }
         }
-        const bool has = Ls > 0.f;
-        const float inv = has ? 1.f / Ls : 0.f;
-        const float lse = has ? (M + __log2f(Ls)) * 0.69314718055994531f : INFINITY;
-        const bool lse_lane = lane == 0 && (kTwo || w < 4);
-        if (whole) {
-          const int head = kvh * p.group + r / p.q_tokens, tok = r % p.q_tokens;
-          T* orow = reinterpret_cast<T*>(p.out) + int64_t(b) * p.out_sb + int64_t(head) * p.out_sn +
-                    int64_t(tok) * p.out_ss + dcol;
-          if constexpr (kCols == 4) {
-            *reinterpret_cast<uint2*>(orow) =
-                make_uint2(pack2(acc[0] * inv, acc[1] * inv, BF16), pack2(acc[2] * inv, acc[3] * inv, BF16));
-          } else {
-            *reinterpret_cast<uint32_t*>(orow) = pack2(acc[0] * inv, acc[1] * inv, BF16);
-          }
-          if (lse_lane && p.lse != nullptr)
-            p.lse[int64_t(b) * p.lse_sb + int64_t(head) * p.lse_sn + int64_t(tok) * p.lse_ss] = lse;
-        } else {
-          const int64_t part = sg.part;
-          float* prow = p.part_o + (part * g + r) * D + dcol;
-#pragma unroll
-          for (int c = 0; c < kCols; ++c) own_o[i][c] = acc[c] * inv;
-          own_lse[i] = has ? lse : -INFINITY;
-          if constexpr (kCols == 4) {
-            *reinterpret_cast<float4*>(prow) = make_float4(own_o[i][0], own_o[i][1], own_o[i][2], own_o[i][3]);
-          } else {
-            *reinterpret_cast<float2*>(prow) = make_float2(own_o[i][0], own_o[i][1]);
-          }
-          if (lse_lane) p.part_lse[part * g + r] = own_lse[i];
-        }
+        warp_arrive(&bar->efree);
       }
-      warp_arrive(&bar->efree);
+      if (!ok) break;
       if (tail) {
         // count the unit's piece: warp 0 waits for every warp's partial
         // (the arrivals release them within the CTA), a device-scope fence
