@@ -4,8 +4,9 @@
 //
 // Operation: the IncreFlashAttention case of npu_fused_infer_attention_score
 // (as decode_kernel.cuh): out = softmax(scale * q K^T) V per (batch, head)
-// over a paged or contiguous cache, per-batch actual_seq_kvlen, GQA, and for
-// several new tokens the sparse_mode 2 / 3 limits.
+// over a paged or contiguous cache, per-batch actual_seq_kvlen, GQA, a
+// per-batch key mask with one new token, and for several new tokens the
+// sparse_mode 2 / 3 limits.
 //
 // With so few rows the two products of a 128-key stage are thin (at most
 // 16 x 128 x 128 multiply-adds each).  The tcgen05 form (decode_kernel.cuh)
@@ -17,7 +18,8 @@
 //     and row, merged in part order by the CTA that completes a unit;
 //   * warps 8 and 9 stream the K and V tiles of each stage into rings by TMA
 //     (128-byte swizzle, one 64-column box per 128 bytes of a row), warp 10
-//     merges finished units;
+//     merges finished units, except the unit of a CTA's last segment, which
+//     the compute warps count and merge themselves (it ends the CTA's walk);
 //   * compute warp w (0..7) owns keys [16 w, 16 w + 16) of every stage and
 //     keeps its own running maximum, sum and O^T for every row; the eight
 //     warps' states are combined once per segment with the exact LSE
