@@ -526,6 +526,34 @@ def check_bsa_fp8_dequant(orc):
         "FP8 TND != BNSD"
 
 
+def check_fp8_dense_vs_library(orc):
+    """Dense FP8 attention (every block kept): the oracle equals library
+    attention on the dequantised values, query row i scaled by its block's
+    q scale, key / value row j by its block's k / v scale (GQA, ragged last
+    blocks)."""
+    B, N1, N2, S, D, X, Y = 1, 4, 2, 11, 8, 4, 6
+    g = torch.Generator().manual_seed(160)
+    f8 = lambda shape: (torch.randn(shape, generator=g, dtype=torch.float64) * 4).clamp(-448, 448).to(
+        torch.float8_e4m3fn)
+    q, k, v = f8((B, N1, S, D)), f8((B, N2, S, D)), f8((B, N2, S, D))
+    nq, nk = -(-S // X), -(-S // Y)
+    pos = lambda shape, seed: (torch.rand(shape, generator=torch.Generator().manual_seed(seed),
+                                          dtype=torch.float64) + 0.5).float()
+    qs, ks, vs = pos((B, N1, nq, 1), 161), pos((B, N2, nk, 1), 162), pos((B, N2, nk, 1), 163)
+    m = np.ones((B, N1, nq, nk), np.uint8)
+    o, l = orc.bsa_forward(q, k, v, m, (X, Y), num_heads=N1, num_key_value_heads=N2, scale_value=0.25,
+                           q_dequant_scale=qs, k_dequant_scale=ks, v_dequant_scale=vs)
+    grp = N1 // N2
+    for h in range(N1):
+        qd = q.to(torch.float64).numpy()[0, h] * np.repeat(qs.double().numpy()[0, h, :, 0], X)[:S, None]
+        kd = k.to(torch.float64).numpy()[0, h // grp] * np.repeat(ks.double().numpy()[0, h // grp, :, 0], Y)[:S, None]
+        vd = v.to(torch.float64).numpy()[0, h // grp] * np.repeat(vs.double().numpy()[0, h // grp, :, 0], Y)[:S, None]
+        ref = _sdpa(qd, kd, vd, np.ones((S, S), bool), 0.25)
+        assert np.allclose(o[0, h], ref, atol=1e-9), "dense FP8 != library attention on dequantised values"
+        lref = logsumexp(0.25 * qd @ kd.T, axis=1)
+        assert np.allclose(l[0, h, :, 0], lref, atol=1e-9), "dense FP8 lse"
+
+
 def check_lse_merge(orc):
     """Split the keys in two, attend to each half, merge by LSE: equals unsplit."""
     q, k, v = _rand((6, 4), 100).numpy(), _rand((10, 4), 101).numpy(), _rand((10, 3), 102).numpy()
@@ -556,6 +584,6 @@ ALL_CHECKS = [
     check_tnd_equals_per_sequence, check_actual_lengths_equal_truncation, check_paged_equals_contiguous,
     check_decode_equals_prefill_row, check_multitoken_decode_vs_library, check_paged_prefill_equals_contiguous,
     check_mla_prefill_vs_library, check_mla_equals_concatenated_attention,
-    check_bsa, check_bsa_fp8_dequant, check_lse_merge,
+    check_bsa, check_bsa_fp8_dequant, check_fp8_dense_vs_library, check_lse_merge,
     check_empty_rules,
 ]
